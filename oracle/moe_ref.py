@@ -1,0 +1,300 @@
+"""Plain fp64 oracle of the fused MoE layer (TEST INFRASTRUCTURE ONLY).
+
+What the layer computes, step by step, in the order the Mixture-of-Kittens
+pages describe it: the router picks experts per token, the layout step counts
+tokens per expert and places each expert's tokens contiguously, the experts
+(SwiGLU FFNs) run, results return to their token, and a final weighted fusion
+sums them; backward runs the same chain in reverse.
+
+Sources (page title, section):
+* kucoin page "Cursor's MoK réalise une amélioration des performances de
+  2,37x sur NVIDIA GB300 NVL72", section 01 (router re-decides per step; count
+  tokens per expert, then place them contiguously for a grouped GEMM;
+  dispatch, combine, and two reverse steps in backward), section 02 (SwiGLU
+  with fused MXFP8; pull dispatch / push combine and their reverses),
+  section 03 (benchmarked layer = scheduler, routing, expert FFNs, combine,
+  final weighted fusion);
+* laura-martel.com blog on Mixture-of-Kittens, section "Le déterminisme est
+  la partie sous-estimée" (same inputs, same result).
+
+The pages never print the layer's formulas.  Readings used here (each one is
+listed with its reason in the design notes):
+* gate weights: softmax over the k selected logits (max-subtracted), which
+  equals a full softmax renormalised over the top-k; weights sum to 1;
+* top-k order: logit descending, ties to the lower expert id; slot j of a
+  token is its j-th choice;
+* layout: stable counting sort of the flat pair index t*k+j by expert;
+* expert: h = silu(x Wg^T) * (x Wu^T), y = h Wd^T, no biases;
+* combine: Y_t = sum_j w_tj y_tj;
+* backward: ordinary calculus of the above; the router-weight gradient is
+  dg_tj = <dY_t, y_tj> and dlogits is the softmax Jacobian applied to dg,
+  zero on experts that were not selected.
+
+Weights may be numpy arrays or any object whose ``[e]`` returns something
+``np.asarray`` turns into float64 (the tests pass a lazy per-expert converter
+for full-size layers, so one expert at a time is widened to fp64).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import mxfp8
+
+
+def _expert(W, e):
+    return np.asarray(W[e], dtype=np.float64)
+
+
+def sigmoid(a):
+    return 1.0 / (1.0 + np.exp(-a))
+
+
+def silu(a):
+    return a * sigmoid(a)
+
+
+# ----------------------------------------------------------------------------
+# 1. Router: top-k experts per token and their gate weights.
+# ----------------------------------------------------------------------------
+def route(logits, k):
+    """Top-k expert ids (logit descending, lower id on ties) and softmax-over-top-k weights.
+
+    logits: [T, E] (fp32 values widened exactly).  Returns idx [T, k] int64,
+    w [T, k] float64.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    if not np.all(np.isfinite(logits)):
+        raise ValueError("router logits must be finite")
+    T, E = logits.shape
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((ids, -logits), axis=-1)      # primary key -logit, then id
+    idx = order[:, :k].astype(np.int64)
+    sel = np.take_along_axis(logits, idx, axis=1)
+    z = np.exp(sel - sel[:, :1])                      # sel[:, 0] is the row maximum
+    w = z / z.sum(axis=1, keepdims=True)
+    return idx, w
+
+
+# ----------------------------------------------------------------------------
+# 2. Layout: per-expert counts, contiguous placement, stable permutation.
+# ----------------------------------------------------------------------------
+def layout(idx, E):
+    """Counts per expert, exclusive offsets, and the stable pair permutation.
+
+    perm_src[r] = flat pair index (t*k + j) placed at sorted row r;
+    dest[t, j]  = sorted row of pair (t, j).  Within one expert the pairs keep
+    ascending flat index order.
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    perm_src = np.argsort(flat, kind="stable").astype(np.int64)
+    dest = np.empty(T * k, dtype=np.int64)
+    dest[perm_src] = np.arange(T * k)
+    return {"counts": counts, "offsets": offsets, "perm_src": perm_src,
+            "dest": dest.reshape(T, k)}
+
+
+# ----------------------------------------------------------------------------
+# 3. Experts and 4. combine (forward).
+# ----------------------------------------------------------------------------
+def _q(v, axis, on):
+    return mxfp8.mx_fake_quant(v, axis) if on else v
+
+
+def _segment_rows(lay, e):
+    o = lay["offsets"]
+    return lay["perm_src"][o[e]:o[e + 1]]
+
+
+def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False):
+    """Layer forward.  Returns (Y [T, d] float64, ctx dict for :func:`backward`).
+
+    mx=True emulates the MXFP8 quantisation points: X, Wg, Wu along d;
+    h along F; Wd along F (each GEMM operand along that GEMM's K).
+    identity=True replaces every expert by y = x (plumbing check).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    T, d = X.shape
+    E = np.asarray(logits).shape[1]
+    idx, w = route(logits, k)
+    lay = layout(idx, E)
+    R = T * k
+    Xq = _q(X, 1, mx)
+    a_all = b_all = h_all = None
+    if not identity:
+        F = _expert(Wg, 0).shape[0]
+        a_all = np.zeros((R, F))
+        b_all = np.zeros((R, F))
+        h_all = np.zeros((R, F))
+    y_all = np.zeros((R, d))
+    for e in range(E):
+        rows = _segment_rows(lay, e)
+        if rows.size == 0:
+            continue
+        x = Xq[rows // k]
+        if identity:
+            y_all[rows] = X[rows // k]
+            continue
+        wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
+        a = x @ _q(wg, 1, mx).T
+        b = x @ _q(wu, 1, mx).T
+        h = silu(a) * b
+        y = _q(h, 1, mx) @ _q(wd, 1, mx).T
+        a_all[rows], b_all[rows], h_all[rows], y_all[rows] = a, b, h, y
+    Y = np.zeros((T, d))
+    for j in range(k):
+        Y += w[:, j:j + 1] * y_all[np.arange(T) * k + j]
+    ctx = {"idx": idx, "w": w, "layout": lay, "a": a_all, "b": b_all, "h": h_all,
+           "y": y_all, "k": k, "mx": mx}
+    return Y, ctx
+
+
+# ----------------------------------------------------------------------------
+# 5. Backward (reverse combine, expert backward, reverse dispatch, dW, router).
+# ----------------------------------------------------------------------------
+def backward(dY, X, logits, Wg, Wu, Wd, ctx):
+    """Gradients of L = <dY, Y>.  Returns dict dX, dWg, dWu, dWd, dg, dlogits.
+
+    MXFP8 emulation (ctx["mx"]): dY along d and Wd along d for u = Wd^T dY;
+    dA, dB along F and Wg, Wu along F for dX; for the weight gradients each
+    operand is quantised along the tokens of its expert (sorted order, padded
+    to a multiple of 32 with zeros): dY and w*h for dWd, dA/dB and x for dWg/dWu.
+    """
+    dY = np.asarray(dY, dtype=np.float64)
+    X = np.asarray(X, dtype=np.float64)
+    k, mx = ctx["k"], ctx["mx"]
+    idx, w, lay = ctx["idx"], ctx["w"], ctx["layout"]
+    T, d = X.shape
+    E = np.asarray(logits).shape[1]
+    F = _expert(Wg, 0).shape[0]
+    R = T * k
+    wflat = w.reshape(-1)
+    dYq = _q(dY, 1, mx)
+    dX = np.zeros((T, d))
+    dWg = np.zeros((E, F, d))
+    dWu = np.zeros((E, F, d))
+    dWd = np.zeros((E, d, F))
+    dg = np.zeros(R)
+    for e in range(E):
+        rows = _segment_rows(lay, e)
+        if rows.size == 0:
+            continue
+        tok = rows // k
+        wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
+        a, b, h = ctx["a"][rows], ctx["b"][rows], ctx["h"][rows]
+        wr = wflat[rows][:, None]
+        u = dYq[tok] @ _q(wd, 0, mx)                 # [m, F] = (Wd^T dY)^T, K = d
+        dg[rows] = np.sum(u * h, axis=1)            # <dY, y> = <Wd^T dY, h>
+        dh = wr * u
+        sa = sigmoid(a)
+        da = dh * b * sa * (1.0 + a * (1.0 - sa))
+        db = dh * silu(a)
+        dx = _q(da, 1, mx) @ _q(wg, 0, mx) + _q(db, 1, mx) @ _q(wu, 0, mx)
+        np.add.at(dX, tok, dx)
+        # weight gradients: K = the expert's tokens in sorted order
+        dWd[e] = _q(dY[tok], 0, mx).T @ _q(wr * h, 0, mx)
+        xs = _q(X[tok], 0, mx)
+        dWg[e] = _q(da, 0, mx).T @ xs
+        dWu[e] = _q(db, 0, mx).T @ xs
+    dg = dg.reshape(T, k)
+    s = np.sum(w * dg, axis=1, keepdims=True)
+    dsel = w * (dg - s)
+    dlogits = np.zeros((T, E))
+    np.put_along_axis(dlogits, idx, dsel, axis=1)
+    return {"dX": dX, "dWg": dWg, "dWu": dWu, "dWd": dWd, "dg": dg, "dlogits": dlogits}
+
+
+# ----------------------------------------------------------------------------
+# Sampled forms for full-size layers: the same arithmetic restricted to a
+# subset of tokens (per-token outputs) or of experts (per-expert dW).
+# ----------------------------------------------------------------------------
+def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False):
+    """Y, dX, dg, dlogits for the listed tokens only (BF16 arithmetic unless mx).
+
+    Routing and every per-token quantity depend on that token alone, so this
+    equals the corresponding rows of :func:`forward` / :func:`backward`.
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    logits = np.asarray(logits, dtype=np.float64)
+    idx, w = route(logits[tokens], k)
+    X = np.asarray(X, dtype=np.float64)[tokens]
+    dY = np.asarray(dY, dtype=np.float64)[tokens]
+    Xq, dYq = _q(X, 1, mx), _q(dY, 1, mx)
+    n, d = X.shape
+    E = logits.shape[1]
+    Y = np.zeros((n, d))
+    dX = np.zeros((n, d))
+    dg = np.zeros((n, k))
+    for e in np.unique(idx):
+        wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
+        for i, j in zip(*np.nonzero(idx == e)):
+            x = Xq[i]
+            a = _q(wg, 1, mx) @ x
+            b = _q(wu, 1, mx) @ x
+            h = silu(a) * b
+            if mx:  # h is quantised along F as one row
+                hq = _q(h[None, :], 1, True)[0]
+            else:
+                hq = h
+            y = _q(wd, 1, mx) @ hq
+            Y[i] += w[i, j] * y
+            u = _q(wd, 0, mx).T @ dYq[i]
+            dg[i, j] = u @ h
+            dh = w[i, j] * u
+            sa = sigmoid(a)
+            da = dh * b * sa * (1.0 + a * (1.0 - sa))
+            db = dh * silu(a)
+            if mx:
+                da, db = _q(da[None], 1, True)[0], _q(db[None], 1, True)[0]
+            dX[i] += _q(wg, 0, mx).T @ da + _q(wu, 0, mx).T @ db
+    s = np.sum(w * dg, axis=1, keepdims=True)
+    dlogits = np.zeros((n, E))
+    np.put_along_axis(dlogits, idx, w * (dg - s), axis=1)
+    return {"Y": Y, "dX": dX, "dg": dg, "dlogits": dlogits, "idx": idx, "w": w}
+
+
+def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False):
+    """dWg[e], dWu[e], dWd[e] over every token routed to expert e (sorted order)."""
+    idx, w = route(logits, k)
+    E = np.asarray(logits).shape[1]
+    lay = layout(idx, E)
+    rows = _segment_rows(lay, e)
+    wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
+    F, d = wg.shape
+    if rows.size == 0:
+        return np.zeros((F, d)), np.zeros((F, d)), np.zeros((d, F))
+    tok = rows // k
+    X = np.asarray(X, dtype=np.float64)[tok]
+    dY = np.asarray(dY, dtype=np.float64)[tok]
+    wr = w.reshape(-1)[rows][:, None]
+    Xq, dYq = _q(X, 1, mx), _q(dY, 1, mx)
+    a = Xq @ _q(wg, 1, mx).T
+    b = Xq @ _q(wu, 1, mx).T
+    h = silu(a) * b
+    u = dYq @ _q(wd, 0, mx)
+    dh = wr * u
+    sa = sigmoid(a)
+    da = dh * b * sa * (1.0 + a * (1.0 - sa))
+    db = dh * silu(a)
+    dWd = _q(dY, 0, mx).T @ _q(wr * h, 0, mx)
+    xs = _q(X, 0, mx)
+    return _q(da, 0, mx).T @ xs, _q(db, 0, mx).T @ xs, dWd
+
+
+# ----------------------------------------------------------------------------
+# Minibatch floor (host heuristic), restated for the oracle's own pins.
+# ----------------------------------------------------------------------------
+def minibatch_floor(num_sms, tile_m, tile_n, n_out, waves=2):
+    """Smallest minibatch (rows) whose grouped GEMM covers `waves` full waves.
+
+    One wave gives every SM one tile; a minibatch of m rows yields
+    (m / tile_m) * (n_out / tile_n) tiles, so m >= waves * S * tile_m * tile_n / n_out.
+    (fluidifia page "Cursor ouvre MoK, un mégakernel qui accélère
+    l'entraînement MoE", section "Comment MoK tente de gratter des
+    millisecondes partout"; kucoin page, section 02.)
+    """
+    return waves * num_sms * tile_m * tile_n // n_out
