@@ -1,0 +1,158 @@
+/*
+ * moe.h -- C ABI of the fused Mixture-of-Experts layer (router top-k,
+ * stable token permutation, gather, grouped SwiGLU expert GEMMs, weighted
+ * combine; forward and backward) on one GB300 (sm_103a).
+ *
+ * The operation is the MoE layer benchmarked by the Mixture-of-Kittens pages:
+ * "scheduler, routing, expert FFNs, combine and final weighted fusion"
+ * (kucoin page "Cursor's MoK réalise une amélioration des performances de
+ * 2,37x sur NVIDIA GB300 NVL72", section 03), with its backward pass
+ * ("two more communication steps in the reverse direction", same page,
+ * section 01).  The pages give no formulas; this library computes, per token
+ * t with router logits l_t:
+ *
+ *   idx_t = top-k experts of l_t (logit descending, ties to the lower id)
+ *   w_tj  = exp(l_t[idx_tj] - max) / sum_i exp(l_t[idx_ti] - max)
+ *   a = x_t Wg[e]^T, b = x_t Wu[e]^T, h = silu(a) * b, y_tj = h Wd[e]^T
+ *   Y_t   = sum_j w_tj y_tj            (j ascending, fp32, one bf16 rounding)
+ *
+ * and the gradients of L = <dY, Y>.  The plain fp64 statement of the same
+ * arithmetic is the CPU oracle the test suite checks against.
+ *
+ * Conventions for every entry point below:
+ *  - All tensor arguments are DEVICE pointers to row-major, contiguous,
+ *    16-byte aligned buffers owned by the caller (e.g. torch tensors).
+ *    bf16 buffers are passed as void*.
+ *  - Weights use the nn.Linear [out, in] convention:
+ *      Wg, Wu: [E, F, d] bf16;  Wd: [E, d, F] bf16.
+ *  - The plan owns all device workspace; it is allocated once in moe_plan.
+ *    moe_forward / moe_backward never allocate and never synchronise with
+ *    the host: they enqueue kernels on `stream` and return.
+ *  - Argument / shape errors return synchronously and enqueue nothing.
+ *    Errors detected on the device (a bounded wait that ran out) are written
+ *    to the plan's device status word and reported by moe_device_status.
+ *  - No C++ exception crosses this ABI.  One stream per plan at a time.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, T > T_max, bad config value */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape outside the supported set (see moe_plan) */
+  MOE_ERR_OOM = 3,          /* workspace allocation failed in moe_plan */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed */
+  MOE_ERR_TIMEOUT = 5,      /* a device-side bounded wait expired */
+  MOE_ERR_INTERNAL = 6
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision_t;
+
+/* debug_flags bits */
+#define MOE_DEBUG_IDENTITY_EXPERTS 0x1u /* experts return their input (y = x); GEMMs skipped */
+#define MOE_DEBUG_TIMING 0x2u           /* bracket each kernel with CUDA events (moe_kernel_times) */
+
+typedef struct {
+  int64_t T_max;          /* largest token count a call may pass */
+  int32_t d;              /* hidden size; multiple of 256 */
+  int32_t F;              /* expert FFN width; multiple of 256 */
+  int32_t E;              /* experts, k <= E <= 1024 */
+  int32_t k;              /* experts per token, 1 <= k <= 32 */
+  int32_t prec;           /* moe_precision_t; only MOE_BF16 is implemented */
+  int32_t minibatch_rows; /* rows per ring slot; 0 = two-wave floor (moe_minibatch_floor) */
+  int32_t ring_slots;     /* ring buffer slots; 0 = default */
+  int32_t mover_ctas;     /* CTAs that gather (data movers); 0 = default */
+  int64_t wait_timeout_ns;/* bound on every device-side wait; 0 = 2e9 (2 s) */
+  uint32_t debug_flags;   /* MOE_DEBUG_* */
+  int32_t device;         /* CUDA device ordinal the plan binds to */
+} moe_config_t;
+
+typedef struct moe_plan_s* moe_plan_t;
+
+/* Create a plan: validates `cfg`, binds `cfg->device`, allocates all device
+ * workspace for T <= T_max, and returns it in *out (caller frees with
+ * moe_plan_destroy).  Supported: d % 256 == 0, F % 256 == 0, 1 <= k <= 32,
+ * k <= E <= 1024, 1 <= T_max <= 2^20, prec == MOE_BF16.  Otherwise
+ * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG; allocation failure MOE_ERR_OOM. */
+moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out);
+
+/* Free the plan's workspace (synchronises its device first). NULL is a no-op. */
+moe_status_t moe_plan_destroy(moe_plan_t plan);
+
+/* Bytes of the caller-owned "saved" context a forward of T tokens writes and
+ * the matching backward reads (routing, permutation, tile table and the
+ * gate/up pre-activations A|B).  The caller allocates it (256-byte aligned). */
+moe_status_t moe_saved_bytes(moe_plan_t plan, int64_t T, size_t* bytes);
+
+/* Forward of T tokens (0 <= T <= T_max; T == 0 is a no-op).
+ *   X      [T, d] bf16      tokens
+ *   logits [T, E] fp32      router logits (finite)
+ *   Wg, Wu [E, F, d] bf16, Wd [E, d, F] bf16
+ *   Y      [T, d] bf16      output (written)
+ *   saved  moe_saved_bytes(T) bytes, written; pass it unchanged to moe_backward.
+ * Enqueued on `stream`; bitwise deterministic for identical inputs. */
+moe_status_t moe_forward(moe_plan_t plan, int64_t T, const void* X, const float* logits,
+                         const void* Wg, const void* Wu, const void* Wd, void* Y,
+                         void* saved, moe_stream_t stream);
+
+/* Backward of the forward that wrote `saved` (same T, X and weights).
+ *   dY [T, d] bf16 upstream gradient
+ *   dX [T, d] bf16; dWg, dWu [E, F, d] bf16; dWd [E, d, F] bf16 (overwritten,
+ *      experts that received no token get zeros)
+ *   dg      [T, k] fp32  gradient of the gate weights w (written)
+ *   dlogits [T, E] fp32  gradient of the router logits, or NULL to skip
+ * Every reduction runs in a fixed order: bitwise deterministic. */
+moe_status_t moe_backward(moe_plan_t plan, int64_t T, const void* dY, const void* X,
+                          const void* Wg, const void* Wu, const void* Wd, const void* saved,
+                          void* dX, void* dWg, void* dWu, void* dWd, float* dg, float* dlogits,
+                          moe_stream_t stream);
+
+/* Copy the routing a forward stored in `saved` into caller device buffers
+ * (any pointer may be NULL to skip it):
+ *   idx [T, k] int32, w [T, k] fp32, counts [E] int32, offsets [E+1] int32
+ *   (unpadded exclusive prefix of counts), perm_src [T*k] int32 (flat pair
+ *   index t*k+j at each sorted row, padding removed), dest [T, k] int32
+ *   (unpadded sorted row of each pair).  Enqueued on `stream`. */
+moe_status_t moe_get_routing(moe_plan_t plan, int64_t T, const void* saved, int32_t* idx,
+                             float* w, int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                             int32_t* dest, moe_stream_t stream);
+
+/* Synchronise `stream`, read the plan's device status word into *status
+ * (a moe_status_t value; MOE_OK if no device error), and clear it. */
+moe_status_t moe_device_status(moe_plan_t plan, moe_stream_t stream, int32_t* status);
+
+/* Per-kernel device times of the calls made since the last read, when the
+ * plan was created with MOE_DEBUG_TIMING.  Synchronises the device.  Writes
+ * up to `cap` entries: names[i] (static strings), total_ms[i] and launches[i];
+ * *n receives the number of distinct kernels.  Resets the accumulators. */
+moe_status_t moe_kernel_times(moe_plan_t plan, const char** names, double* total_ms,
+                              int64_t* launches, int32_t cap, int32_t* n);
+
+/* Two-wave minibatch floor: the smallest row count m for which a grouped
+ * GEMM of output width n_out cut into tile_m x tile_n tiles gives `waves`
+ * full waves on `num_sms` SMs: m = ceil(waves * num_sms * tile_m * tile_n / n_out).
+ * Pure host function (fluidifia page "Cursor ouvre
+ * MoK, un mégakernel qui accélère l'entraînement MoE", section "Comment MoK
+ * tente de gratter des millisecondes partout"; kucoin page, section 02). */
+moe_status_t moe_minibatch_floor(int32_t num_sms, int32_t tile_m, int32_t tile_n, int32_t n_out,
+                                 int32_t waves, int64_t* rows);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t s);
+
+/* Human-readable detail of the last error returned on the calling thread. */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,597 @@
+// api.cu -- the C ABI (include/moe.h): plan / workspace, argument checks,
+// tensor-map encoding and the kernel sequence of forward and backward.
+//
+// Forward  (one stream, no host sync, no allocation):
+//   router+histogram -> scan -> stable permute -> gather X into sorted rows
+//   -> [a|b] GEMM + SwiGLU -> down GEMM -> fixed-order weighted combine.
+// Backward:
+//   gather dY and X -> u GEMM + SwiGLU backward -> dx GEMM -> per-token dx
+//   reduce -> router gradient -> dWd GEMM -> dWg/dWu GEMM.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "gemm.cuh"
+#include "kernels.h"
+#include "moe.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+moe_status_t cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return MOE_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] buffer.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in, uint32_t box_out,
+               CUtensorMapSwizzle sw) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_in, box_out};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+// The three shapes the GEMMs use.
+bool map_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows = BM) {
+  return encode_2d(m, b, inner, outer, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_mnmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return encode_2d(m, b, inner, outer, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_store(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return encode_2d(m, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+struct SavedLayout {
+  size_t idx, w, dest, counts, offsets, poff, mtile, totals, perm, ab, total;
+  int64_t rows;  // padded sorted-row capacity for this T
+};
+
+SavedLayout saved_layout(const moe_config_t& c, int64_t T) {
+  SavedLayout L{};
+  const int64_t R = T * c.k;
+  L.rows = ((R + (int64_t)c.E * (kTileRows - 1)) + kTileRows - 1) / kTileRows * kTileRows;
+  size_t o = 0;
+  L.idx = o;     o += align256(R * 4);
+  L.w = o;       o += align256(R * 4);
+  L.dest = o;    o += align256(R * 4);
+  L.counts = o;  o += align256(c.E * 4);
+  L.offsets = o; o += align256((c.E + 1) * 4);
+  L.poff = o;    o += align256((c.E + 1) * 4);
+  L.mtile = o;   o += align256((c.E + 1) * 4);
+  L.totals = o;  o += align256(16);
+  L.perm = o;    o += align256(L.rows * 4);
+  L.ab = o;      o += align256((size_t)L.rows * 2 * c.F * 2);
+  L.total = o;
+  return L;
+}
+
+RoutingPtrs routing_ptrs(const SavedLayout& L, void* saved) {
+  char* b = static_cast<char*>(saved);
+  RoutingPtrs rp;
+  rp.idx = reinterpret_cast<int32_t*>(b + L.idx);
+  rp.w = reinterpret_cast<float*>(b + L.w);
+  rp.dest = reinterpret_cast<int32_t*>(b + L.dest);
+  rp.counts = reinterpret_cast<int32_t*>(b + L.counts);
+  rp.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  rp.poff = reinterpret_cast<int32_t*>(b + L.poff);
+  rp.mtile_off = reinterpret_cast<int32_t*>(b + L.mtile);
+  rp.totals = reinterpret_cast<int32_t*>(b + L.totals);
+  rp.perm_src = reinterpret_cast<int32_t*>(b + L.perm);
+  return rp;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceGuard {
+  int old = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&old) != cudaSuccess) old = -1;
+    if (old != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (old >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != old) cudaSetDevice(old);
+  }
+};
+
+struct TimedLaunch {
+  const char* name;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct moe_plan_s {
+  moe_config_t cfg;
+  int num_sms = 0;
+  int64_t Rpm = 0;  // padded row capacity at T_max
+  void* ws = nullptr;
+  int32_t* chunk_hist = nullptr;
+  int32_t* chunk_base = nullptr;
+  int32_t* status = nullptr;
+  void *Xg = nullptr, *H = nullptr, *Ys = nullptr, *dYg = nullptr, *dAB = nullptr, *wH = nullptr;
+  float* dgp = nullptr;
+  // workspace tensor maps
+  CUtensorMap m_Xg_k, m_Xg_mn, m_H_k, m_H_st, m_Ys_st, m_dYg_k, m_dYg_mn, m_dAB_k, m_dAB_mn, m_dAB_st, m_wH_mn,
+      m_wH_st;
+  // caller-pointer tensor maps, re-encoded when a pointer changes
+  const void *p_wg = nullptr, *p_wu = nullptr, *p_wd = nullptr;
+  CUtensorMap m_Wg_k, m_Wu_k, m_Wd_k, m_Wg_mn, m_Wu_mn, m_Wd_mn;
+  const void *p_dwg = nullptr, *p_dwu = nullptr, *p_dwd = nullptr;
+  CUtensorMap m_dWg_st, m_dWu_st, m_dWd_st;
+  // timing (MOE_DEBUG_TIMING)
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> spare_events;
+};
+
+namespace {
+
+cudaEvent_t take_event(moe_plan_s* p) {
+  if (!p->spare_events.empty()) {
+    cudaEvent_t e = p->spare_events.back();
+    p->spare_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch `fn` on `st`; in timing mode bracket it with a pair of events.
+template <class Fn>
+cudaError_t timed_launch(moe_plan_s* p, const char* name, cudaStream_t st, Fn&& fn) {
+  if (!(p->cfg.debug_flags & MOE_DEBUG_TIMING)) return fn();
+  TimedLaunch t{name, take_event(p), take_event(p)};
+  cudaEventRecord(t.a, st);
+  cudaError_t e = fn();
+  cudaEventRecord(t.b, st);
+  p->timed.push_back(t);
+  return e;
+}
+
+bool ensure_weight_maps(moe_plan_s* p, const void* Wg, const void* Wu, const void* Wd) {
+  const moe_config_t& c = p->cfg;
+  const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
+  if (Wg != p->p_wg) {
+    if (!map_kmajor(&p->m_Wg_k, Wg, c.d, EF) || !map_mnmajor(&p->m_Wg_mn, Wg, c.d, EF)) return false;
+    p->p_wg = Wg;
+  }
+  if (Wu != p->p_wu) {
+    if (!map_kmajor(&p->m_Wu_k, Wu, c.d, EF) || !map_mnmajor(&p->m_Wu_mn, Wu, c.d, EF)) return false;
+    p->p_wu = Wu;
+  }
+  if (Wd != p->p_wd) {
+    if (!map_kmajor(&p->m_Wd_k, Wd, c.F, Ed, BN) || !map_mnmajor(&p->m_Wd_mn, Wd, c.F, Ed)) return false;
+    p->p_wd = Wd;
+  }
+  return true;
+}
+
+GemmArgs base_args(moe_plan_s* p, const RoutingPtrs& rp) {
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.poff = rp.poff;
+  a.mtile_off = rp.mtile_off;
+  a.status = p->status;
+  a.timeout_ns = (uint64_t)p->cfg.wait_timeout_ns;
+  a.E = p->cfg.E;
+  a.d = p->cfg.d;
+  a.F = p->cfg.F;
+  return a;
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case MOE_ERR_OOM: return "device memory allocation failed";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_INTERNAL: return "internal error";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status_t moe_minibatch_floor(int32_t num_sms, int32_t tile_m, int32_t tile_n, int32_t n_out, int32_t waves,
+                                 int64_t* rows) {
+  if (!rows || num_sms <= 0 || tile_m <= 0 || tile_n <= 0 || n_out <= 0 || waves <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "moe_minibatch_floor: all arguments must be positive");
+  const int64_t num = (int64_t)waves * num_sms * tile_m * tile_n;
+  *rows = (num + n_out - 1) / n_out;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
+  if (!cfg || !out) return fail(MOE_ERR_INVALID_ARG, "moe_plan: null argument");
+  *out = nullptr;
+  const moe_config_t c = *cfg;
+  if (c.T_max < 1 || c.T_max > (1 << 20)) return fail(MOE_ERR_INVALID_ARG, "moe_plan: T_max must be in [1, 2^20]");
+  if (c.k < 1 || c.k > 32 || c.E < c.k || c.E > 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: need 1 <= k <= 32 and k <= E <= 1024");
+  if (c.d <= 0 || c.F <= 0 || c.d % BN || c.F % BN)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: d and F must be positive multiples of 256");
+  if (c.prec != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "moe_plan: only MOE_BF16 is implemented");
+  if ((int64_t)c.E * c.F * c.d >= (int64_t)1 << 40)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: weight tensor too large");
+  if (!encode_fn()) return fail(MOE_ERR_CUDA, "moe_plan: cuTensorMapEncodeTiled unavailable");
+
+  DeviceGuard guard(c.device);
+  if (!guard.ok) return fail(MOE_ERR_CUDA, "moe_plan: cudaSetDevice failed");
+  cudaDeviceProp prop;
+  cudaError_t err = cudaGetDeviceProperties(&prop, c.device);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_plan: cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: this library is built for sm_103a (GB300) only; device is sm_" +
+                                         std::to_string(prop.major) + std::to_string(prop.minor));
+
+  moe_plan_s* p = new (std::nothrow) moe_plan_s();
+  if (!p) return fail(MOE_ERR_OOM, "moe_plan: host allocation failed");
+  p->cfg = c;
+  if (p->cfg.wait_timeout_ns <= 0) p->cfg.wait_timeout_ns = 2000000000LL;
+  p->num_sms = prop.multiProcessorCount;
+  const SavedLayout L = saved_layout(c, c.T_max);
+  p->Rpm = L.rows;
+  const int nch = route_chunks((int)c.T_max);
+
+  size_t o = 0;
+  const size_t o_hist = o;  o += align256((size_t)nch * c.E * 4);
+  const size_t o_base = o;  o += align256((size_t)nch * c.E * 4);
+  const size_t o_stat = o;  o += 256;
+  const size_t o_xg = o;    o += align256((size_t)p->Rpm * c.d * 2);
+  const size_t o_h = o;     o += align256((size_t)p->Rpm * c.F * 2);
+  const size_t o_ys = o;    o += align256((size_t)p->Rpm * c.d * 2);
+  const size_t o_dyg = o;   o += align256((size_t)p->Rpm * c.d * 2);
+  const size_t o_dab = o;   o += align256((size_t)p->Rpm * 2 * c.F * 2);
+  const size_t o_wh = o;    o += align256((size_t)p->Rpm * c.F * 2);
+  const size_t o_dgp = o;   o += align256((size_t)p->Rpm * (c.F / BN) * 4);
+  err = cudaMalloc(&p->ws, o);
+  if (err != cudaSuccess) {
+    delete p;
+    return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of workspace failed: ") + cudaGetErrorString(err));
+  }
+  char* b = static_cast<char*>(p->ws);
+  p->chunk_hist = reinterpret_cast<int32_t*>(b + o_hist);
+  p->chunk_base = reinterpret_cast<int32_t*>(b + o_base);
+  p->status = reinterpret_cast<int32_t*>(b + o_stat);
+  p->Xg = b + o_xg;
+  p->H = b + o_h;
+  p->Ys = b + o_ys;
+  p->dYg = b + o_dyg;
+  p->dAB = b + o_dab;
+  p->wH = b + o_wh;
+  p->dgp = reinterpret_cast<float*>(b + o_dgp);
+  err = cudaMemset(p->status, 0, 256);
+  if (err != cudaSuccess) {
+    cudaFree(p->ws);
+    delete p;
+    return cuda_fail(err, "moe_plan: cudaMemset");
+  }
+  const uint64_t R = p->Rpm;
+  bool ok = map_kmajor(&p->m_Xg_k, p->Xg, c.d, R) && map_mnmajor(&p->m_Xg_mn, p->Xg, c.d, R) &&
+            map_kmajor(&p->m_H_k, p->H, c.F, R) && map_store(&p->m_H_st, p->H, c.F, R) &&
+            map_store(&p->m_Ys_st, p->Ys, c.d, R) && map_kmajor(&p->m_dYg_k, p->dYg, c.d, R) &&
+            map_mnmajor(&p->m_dYg_mn, p->dYg, c.d, R) && map_kmajor(&p->m_dAB_k, p->dAB, 2 * c.F, R) &&
+            map_mnmajor(&p->m_dAB_mn, p->dAB, 2 * c.F, R) && map_store(&p->m_dAB_st, p->dAB, 2 * c.F, R) &&
+            map_mnmajor(&p->m_wH_mn, p->wH, c.F, R) && map_store(&p->m_wH_st, p->wH, c.F, R);
+  if (!ok) {
+    cudaFree(p->ws);
+    delete p;
+    return fail(MOE_ERR_CUDA, "moe_plan: tensor map encoding failed");
+  }
+  for (int kind = 0; kind < 6; ++kind) {
+    err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
+    if (err != cudaSuccess) {
+      cudaFree(p->ws);
+      delete p;
+      return cuda_fail(err, "moe_plan: cudaFuncSetAttribute");
+    }
+  }
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan_destroy(moe_plan_t p) {
+  if (!p) return MOE_OK;
+  DeviceGuard guard(p->cfg.device);
+  cudaDeviceSynchronize();
+  for (auto& t : p->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : p->spare_events) cudaEventDestroy(e);
+  cudaError_t err = cudaFree(p->ws);
+  delete p;
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
+}
+
+moe_status_t moe_saved_bytes(moe_plan_t p, int64_t T, size_t* bytes) {
+  if (!p || !bytes) return fail(MOE_ERR_INVALID_ARG, "moe_saved_bytes: null argument");
+  if (T < 0 || T > p->cfg.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_saved_bytes: T outside [0, T_max]");
+  *bytes = saved_layout(p->cfg, T).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* logits, const void* Wg,
+                         const void* Wu, const void* Wd, void* Y, void* saved, moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_forward: null plan");
+  const moe_config_t& c = p->cfg;
+  if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_forward: T outside [0, T_max]");
+  if (T == 0) return MOE_OK;
+  const bool ident = (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS) != 0;
+  if (!X || !logits || !Y || !saved || (!ident && (!Wg || !Wu || !Wd)))
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward: null tensor pointer");
+  if (!aligned16(X) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(saved) & 255u) ||
+      (!ident && (!aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))) ||
+      (reinterpret_cast<uintptr_t>(logits) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward: misaligned pointer (16 B tensors, 256 B saved)");
+  DeviceGuard guard(c.device);
+  if (!guard.ok) return fail(MOE_ERR_CUDA, "moe_forward: cudaSetDevice failed");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const SavedLayout L = saved_layout(c, T);
+  const RoutingPtrs rp = routing_ptrs(L, saved);
+  const int Ti = (int)T;
+  cudaError_t err;
+
+  if (!ident && !ensure_weight_maps(p, Wg, Wu, Wd)) return fail(MOE_ERR_CUDA, "moe_forward: weight tensor maps");
+  CUtensorMap m_ab_st;
+  if (!ident && !map_store(&m_ab_st, static_cast<char*>(saved) + L.ab, 2 * c.F, L.rows))
+    return fail(MOE_ERR_CUDA, "moe_forward: saved tensor map");
+
+  err = timed_launch(p, "router_topk_hist", st,
+                     [&] { return launch_router(logits, Ti, c.E, c.k, p->chunk_hist, rp, st); });
+  if (err == cudaSuccess)
+    err = timed_launch(p, "layout_scan", st,
+                       [&] { return launch_scan(Ti, c.E, p->chunk_hist, p->chunk_base, rp, st); });
+  if (err == cudaSuccess)
+    err = timed_launch(p, "layout_permute", st,
+                       [&] { return launch_permute(Ti, c.E, c.k, p->chunk_base, rp, st); });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward: routing launch");
+  err = timed_launch(p, "gather", st, [&] {
+    return launch_gather(X, nullptr, rp.perm_src, rp.totals, c.k, c.d, p->Xg, nullptr, p->num_sms * 8, st);
+  });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
+  const void* ys = p->Xg;
+  if (!ident) {
+    GemmArgs a = base_args(p, rp);
+    a.mapA = p->m_Xg_k;
+    a.mapB0 = p->m_Wg_k;
+    a.mapB1 = p->m_Wu_k;
+    a.mapO0 = m_ab_st;
+    a.mapO1 = p->m_H_st;
+    err = timed_launch(p, "gemm_up_swiglu", st, [&] { return launch_gemm_fwd(kUp, a, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: up GEMM launch");
+    GemmArgs b = base_args(p, rp);
+    b.mapA = p->m_H_k;
+    b.mapB0 = p->m_Wd_k;
+    b.mapO0 = p->m_Ys_st;
+    err = timed_launch(p, "gemm_down", st, [&] { return launch_gemm_fwd(kDown, b, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: down GEMM launch");
+    ys = p->Ys;
+  }
+  const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
+  err = timed_launch(p, "combine", st,
+                     [&] { return launch_combine(ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X, const void* Wg, const void* Wu,
+                          const void* Wd, const void* saved, void* dX, void* dWg, void* dWu, void* dWd, float* dg,
+                          float* dlogits, moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_backward: null plan");
+  const moe_config_t& c = p->cfg;
+  if (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_backward: identity-expert debug mode has no backward");
+  if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_backward: T outside [0, T_max]");
+  if (!dWg || !dWu || !dWd || !Wg || !Wu || !Wd)
+    return fail(MOE_ERR_INVALID_ARG, "moe_backward: null weight or weight-gradient pointer");
+  if (T > 0 && (!dY || !X || !saved || !dX || !dg))
+    return fail(MOE_ERR_INVALID_ARG, "moe_backward: null tensor pointer");
+  if ((T > 0 && (!aligned16(dY) || !aligned16(X) || !aligned16(dX) ||
+                 (reinterpret_cast<uintptr_t>(saved) & 255u))) ||
+      !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(dWg) || !aligned16(dWu) ||
+      !aligned16(dWd))
+    return fail(MOE_ERR_INVALID_ARG, "moe_backward: misaligned pointer");
+  DeviceGuard guard(c.device);
+  if (!guard.ok) return fail(MOE_ERR_CUDA, "moe_backward: cudaSetDevice failed");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (T == 0) {  // no tokens: every expert's weight gradient is zero
+    const size_t wbytes = (size_t)c.E * c.F * c.d * 2;
+    if ((err = cudaMemsetAsync(dWg, 0, wbytes, st)) != cudaSuccess ||
+        (err = cudaMemsetAsync(dWu, 0, wbytes, st)) != cudaSuccess ||
+        (err = cudaMemsetAsync(dWd, 0, wbytes, st)) != cudaSuccess)
+      return cuda_fail(err, "moe_backward: memset");
+    return MOE_OK;
+  }
+  const SavedLayout L = saved_layout(c, T);
+  const RoutingPtrs rp = routing_ptrs(L, const_cast<void*>(saved));
+  const int Ti = (int)T;
+  if (!ensure_weight_maps(p, Wg, Wu, Wd)) return fail(MOE_ERR_CUDA, "moe_backward: weight tensor maps");
+  const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
+  if (dWg != p->p_dwg) {
+    if (!map_store(&p->m_dWg_st, dWg, c.d, EF)) return fail(MOE_ERR_CUDA, "moe_backward: dWg map");
+    p->p_dwg = dWg;
+  }
+  if (dWu != p->p_dwu) {
+    if (!map_store(&p->m_dWu_st, dWu, c.d, EF)) return fail(MOE_ERR_CUDA, "moe_backward: dWu map");
+    p->p_dwu = dWu;
+  }
+  if (dWd != p->p_dwd) {
+    if (!map_store(&p->m_dWd_st, dWd, c.F, Ed)) return fail(MOE_ERR_CUDA, "moe_backward: dWd map");
+    p->p_dwd = dWd;
+  }
+  const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(saved) + L.ab);
+
+  err = timed_launch(p, "gather_bwd", st, [&] {
+    return launch_gather(dY, X, rp.perm_src, rp.totals, c.k, c.d, p->dYg, p->Xg, p->num_sms * 8, st);
+  });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_backward: gather launch");
+  {
+    GemmArgs a = base_args(p, rp);
+    a.mapA = p->m_dYg_k;
+    a.mapB0 = p->m_Wd_mn;
+    a.mapO0 = p->m_dAB_st;
+    a.mapO1 = p->m_wH_st;
+    a.ab = ab;
+    a.perm_src = rp.perm_src;
+    a.wts = rp.w;
+    a.dgp = p->dgp;
+    err = timed_launch(p, "gemm_bwd_u_swiglu", st, [&] { return launch_gemm_bwd(kBwdU, a, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: u GEMM launch");
+  }
+  {
+    GemmArgs a = base_args(p, rp);
+    a.mapA = p->m_dAB_k;
+    a.mapB0 = p->m_Wg_mn;
+    a.mapB1 = p->m_Wu_mn;
+    a.mapO0 = p->m_Ys_st;
+    err = timed_launch(p, "gemm_bwd_dx", st, [&] { return launch_gemm_bwd(kBwdX, a, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx GEMM launch");
+  }
+  const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
+  err = timed_launch(p, "reduce_dx", st,
+                     [&] { return launch_combine(p->Ys, rp.dest, nullptr, Ti, c.k, c.d, dX, cgrid, st); });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx reduce launch");
+  const int rgrid = (int)std::min<int64_t>((T + 7) / 8, (int64_t)p->num_sms * 8);
+  err = timed_launch(p, "router_grad", st, [&] {
+    return launch_router_grad(p->dgp, rp.dest, rp.idx, rp.w, Ti, c.k, c.E, c.F / BN, dg, dlogits, rgrid, st);
+  });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_backward: router gradient launch");
+  {
+    GemmArgs a = base_args(p, rp);
+    a.mapA = p->m_dYg_mn;
+    a.mapB0 = p->m_wH_mn;
+    a.mapO0 = p->m_dWd_st;
+    err = timed_launch(p, "gemm_wgrad_down", st, [&] { return launch_gemm_bwd(kWgradD, a, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dWd GEMM launch");
+  }
+  {
+    GemmArgs a = base_args(p, rp);
+    a.mapA = p->m_dAB_mn;
+    a.mapB0 = p->m_Xg_mn;
+    a.mapO0 = p->m_dWg_st;
+    a.mapO1 = p->m_dWu_st;
+    err = timed_launch(p, "gemm_wgrad_gate_up", st, [&] { return launch_gemm_bwd(kWgradGU, a, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dWg/dWu GEMM launch");
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_get_routing(moe_plan_t p, int64_t T, const void* saved, int32_t* idx, float* w, int32_t* counts,
+                             int32_t* offsets, int32_t* perm_src, int32_t* dest, moe_stream_t stream) {
+  if (!p || !saved) return fail(MOE_ERR_INVALID_ARG, "moe_get_routing: null argument");
+  const moe_config_t& c = p->cfg;
+  if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_get_routing: T outside [0, T_max]");
+  if (T == 0) return MOE_OK;
+  DeviceGuard guard(c.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const SavedLayout L = saved_layout(c, T);
+  const RoutingPtrs rp = routing_ptrs(L, const_cast<void*>(saved));
+  const size_t R = (size_t)T * c.k;
+  cudaError_t err = cudaSuccess;
+  if (idx && err == cudaSuccess) err = cudaMemcpyAsync(idx, rp.idx, R * 4, cudaMemcpyDeviceToDevice, st);
+  if (w && err == cudaSuccess) err = cudaMemcpyAsync(w, rp.w, R * 4, cudaMemcpyDeviceToDevice, st);
+  if (counts && err == cudaSuccess) err = cudaMemcpyAsync(counts, rp.counts, c.E * 4, cudaMemcpyDeviceToDevice, st);
+  if (offsets && err == cudaSuccess)
+    err = cudaMemcpyAsync(offsets, rp.offsets, (c.E + 1) * 4, cudaMemcpyDeviceToDevice, st);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_get_routing: copy");
+  if (perm_src || dest) {
+    err = launch_unpad_routing(rp, (int)R, perm_src, dest, st);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_get_routing: unpad launch");
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_device_status(moe_plan_t p, moe_stream_t stream, int32_t* status) {
+  if (!p || !status) return fail(MOE_ERR_INVALID_ARG, "moe_device_status: null argument");
+  DeviceGuard guard(p->cfg.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaStreamSynchronize(st);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_device_status: stream synchronize");
+  int32_t v = 0;
+  err = cudaMemcpy(&v, p->status, 4, cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_device_status: read");
+  if (v != 0) cudaMemset(p->status, 0, 4);
+  *status = v;
+  return MOE_OK;
+}
+
+moe_status_t moe_kernel_times(moe_plan_t p, const char** names, double* total_ms, int64_t* launches, int32_t cap,
+                              int32_t* n) {
+  if (!p || !n) return fail(MOE_ERR_INVALID_ARG, "moe_kernel_times: null argument");
+  DeviceGuard guard(p->cfg.device);
+  cudaError_t err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return cuda_fail(err, "moe_kernel_times: synchronize");
+  std::vector<const char*> nm;
+  std::vector<double> ms;
+  std::vector<int64_t> cnt;
+  for (auto& t : p->timed) {
+    float x = 0.f;
+    cudaEventElapsedTime(&x, t.a, t.b);
+    size_t i = 0;
+    while (i < nm.size() && strcmp(nm[i], t.name) != 0) ++i;
+    if (i == nm.size()) {
+      nm.push_back(t.name);
+      ms.push_back(0.0);
+      cnt.push_back(0);
+    }
+    ms[i] += x;
+    cnt[i] += 1;
+    p->spare_events.push_back(t.a);
+    p->spare_events.push_back(t.b);
+  }
+  p->timed.clear();
+  *n = (int32_t)nm.size();
+  for (int32_t i = 0; i < *n && i < cap; ++i) {
+    if (names) names[i] = nm[i];
+    if (total_ms) total_ms[i] = ms[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

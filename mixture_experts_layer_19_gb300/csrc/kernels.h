@@ -1,0 +1,49 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernels (routing.cu, gemm_*.cu).  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kTileRows = 128;  // expert segments are padded to this many sorted rows
+
+// Device pointers of the routing state a forward writes into the caller's
+// saved context (all int32 unless noted).
+struct RoutingPtrs {
+  int32_t* idx;        // [T*k] expert of each pair
+  float* w;            // [T*k] gate weight of each pair (fp32)
+  int32_t* dest;       // [T*k] padded sorted row of each pair
+  int32_t* counts;     // [E]
+  int32_t* offsets;    // [E+1] unpadded exclusive prefix of counts
+  int32_t* poff;       // [E+1] padded segment starts
+  int32_t* mtile_off;  // [E+1] prefix of 128-row tiles
+  int32_t* totals;     // [4]: padded rows in use, routed pairs
+  int32_t* perm_src;   // [R_pad] flat pair index of each padded sorted row, -1 = padding
+};
+
+int route_chunks(int T);
+cudaError_t launch_router(const float* logits, int T, int E, int k, int32_t* chunk_hist, const RoutingPtrs& rp,
+                          cudaStream_t st);
+cudaError_t launch_scan(int T, int E, const int32_t* chunk_hist, int32_t* chunk_base, const RoutingPtrs& rp,
+                        cudaStream_t st);
+cudaError_t launch_permute(int T, int E, int k, const int32_t* chunk_base, const RoutingPtrs& rp, cudaStream_t st);
+cudaError_t launch_gather(const void* X0, const void* X1, const int32_t* perm_src, const int32_t* totals, int k,
+                          int d, void* G0, void* G1, int grid, cudaStream_t st);
+cudaError_t launch_combine(const void* S, const int32_t* dest, const float* w, int T, int k, int d, void* Y,
+                           int grid, cudaStream_t st);
+cudaError_t launch_router_grad(const float* dgp, const int32_t* dest, const int32_t* idx, const float* w, int T,
+                               int k, int E, int ntu, float* dg, float* dlogits, int grid, cudaStream_t st);
+cudaError_t launch_unpad_routing(const RoutingPtrs& rp, int R, int32_t* perm_out, int32_t* dest_out,
+                                 cudaStream_t st);
+
+struct GemmArgs;
+// kind: 0 up (+SwiGLU), 1 down (gemm_fwd.cu); 2 bwd-u (+SwiGLU backward), 3 bwd-x, 4 wgrad down,
+// 5 wgrad gate/up (gemm_bwd.cu).  prepare_* raises the dynamic shared-memory limit.
+cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t prepare_gemm_fwd(int kind);
+cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t prepare_gemm_bwd(int kind);
+
+}  // namespace moe

@@ -1,0 +1,363 @@
+// routing.cu -- router top-k + softmax weights, per-chunk expert histogram,
+// scan to padded expert segments, stable permutation, row gathers (pull
+// dispatch and its backward residue), fixed-order weighted combine, and the
+// router-weight gradient.
+//
+// Mixture-of-Kittens pages: the router re-decides each token's experts at
+// every step, then the layout step counts tokens per expert and places each
+// expert's tokens contiguously so one grouped GEMM can consume them (kucoin
+// page "Cursor's MoK réalise une amélioration des performances de 2,37x sur
+// NVIDIA GB300 NVL72", section 01); dispatch is a pull by source position and
+// combine a push to the token's home (same page, section 02); the final
+// weighted fusion belongs to the layer (section 03); results are the same run
+// to run (laura-martel.com blog, section "Le déterminisme est la partie
+// sous-estimée") -- here every reduction has one fixed order and the only
+// atomics are integer histogram increments.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kRouteChunk = 64;   // tokens per router block / permutation chunk
+constexpr int kRouteThreads = 256;
+
+// -----------------------------------------------------------------------------
+// S1: one warp per token.  Lane l holds logits l, l+32, ...; k rounds of a
+// warp arg-max (larger logit wins, lower id on ties) pick the experts in
+// descending order; weights are the softmax over the k picked logits, taken
+// relative to the first (largest) one.  The block also histograms its chunk.
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRouteThreads) router_kernel(const float* __restrict__ logits, int T, int E,
+                                                                 int k, int32_t* __restrict__ idx,
+                                                                 float* __restrict__ w,
+                                                                 int32_t* __restrict__ chunk_hist) {
+  __shared__ int hist[1024];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int nper = (E + 31) >> 5;
+  for (int tt = warp; tt < kRouteChunk; tt += kRouteThreads / 32) {
+    const int t = blockIdx.x * kRouteChunk + tt;
+    if (t >= T) break;
+    const float* row = logits + (size_t)t * E;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (i < nper && e < E) ? __ldg(row + e) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_val = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float best = -INFINITY;
+      int bid = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        if (i < nper && e < E && !((taken >> i) & 1u)) {
+          if (v[i] > best || (v[i] == best && e < bid)) {
+            best = v[i];
+            bid = e;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bid, off);
+        if (ob > best || (ob == best && oi < bid)) {
+          best = ob;
+          bid = oi;
+        }
+      }
+      if (bid == 0x7fffffff) bid = 0;  // only reachable with NaN logits (outside the contract)
+      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+      if (lane == j) {
+        my_id = bid;
+        my_val = best;
+      }
+    }
+    const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
+    const float z = lane < k ? expf(my_val - vmax) : 0.0f;
+    float sum = z;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      idx[(size_t)t * k + lane] = my_id;
+      w[(size_t)t * k + lane] = z / sum;
+      atomicAdd(&hist[my_id], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// -----------------------------------------------------------------------------
+// S2a: per-expert running sums over chunks (chunk bases), per-expert counts,
+// exclusive scans of counts (unpadded offsets) and of counts rounded up to
+// the 128-row tile (padded segment starts), tile prefix, padding markers.
+// One block of 1024 threads; thread e owns expert e.
+// -----------------------------------------------------------------------------
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    warp_tot[lane] = s;  // inclusive
+    if (lane == 31) *total = s;
+  }
+  __syncthreads();
+  const int res = x - v + (warp > 0 ? warp_tot[warp - 1] : 0);
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_hist,
+                                                      int32_t* __restrict__ chunk_base, int nchunks, int E,
+                                                      RoutingPtrs rp) {
+  __shared__ int warp_tot[32];
+  __shared__ int tot0, tot1;
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      chunk_base[(size_t)c * E + e] = cnt;
+      cnt += chunk_hist[(size_t)c * E + e];
+    }
+  }
+  const int padded = (cnt + kTileRows - 1) / kTileRows * kTileRows;
+  const int off = block_excl_scan(cnt, warp_tot, &tot0);
+  const int poff = block_excl_scan(padded, warp_tot, &tot1);
+  if (e < E) {
+    rp.counts[e] = cnt;
+    rp.offsets[e] = off;
+    rp.poff[e] = poff;
+    rp.mtile_off[e] = poff / kTileRows;
+    for (int r = poff + cnt; r < poff + padded; ++r) rp.perm_src[r] = -1;
+  }
+  if (threadIdx.x == 0) {
+    rp.offsets[E] = tot0;
+    rp.poff[E] = tot1;
+    rp.mtile_off[E] = tot1 / kTileRows;
+    rp.totals[0] = tot1;  // padded rows in use
+    rp.totals[1] = tot0;  // routed pairs
+  }
+}
+
+// -----------------------------------------------------------------------------
+// S2b: stable placement.  One warp per chunk walks its pairs in flat order,
+// 32 at a time; lanes with the same expert get consecutive slots in lane
+// order (match_any + popc), so within an expert the flat index increases.
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(32) permute_kernel(const int32_t* __restrict__ chunk_base, int T, int E, int k,
+                                                     RoutingPtrs rp) {
+  extern __shared__ int cursor[];
+  const int lane = threadIdx.x;
+  const int c = blockIdx.x;
+  for (int e = lane; e < E; e += 32) cursor[e] = rp.poff[e] + chunk_base[(size_t)c * E + e];
+  __syncwarp();
+  const int p0 = c * kRouteChunk * k;
+  const int p1 = min(T, (c + 1) * kRouteChunk) * k;
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    const bool valid = p < p1;
+    const int e = valid ? rp.idx[p] : -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(grp & ((1u << lane) - 1u));
+    int slot = 0;
+    if (valid) slot = cursor[e];
+    __syncwarp();
+    if (valid && rank == 0) cursor[e] = slot + __popc(grp);
+    __syncwarp();
+    if (valid) {
+      const int dst = slot + rank;
+      rp.dest[p] = dst;
+      rp.perm_src[dst] = p;
+    }
+  }
+}
+
+// -----------------------------------------------------------------------------
+// S4 (pull dispatch residue): sorted row r <- token row X[perm_src[r] / k];
+// padding rows are zero.  One warp per row, 16-byte vectors.  With two
+// sources (backward) the same rows of a second tensor are gathered too.
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ X0, const uint4* __restrict__ X1,
+                                                     const int32_t* __restrict__ perm_src,
+                                                     const int32_t* __restrict__ totals, int k, int d,
+                                                     uint4* __restrict__ G0, uint4* __restrict__ G1) {
+  const int rows = totals[0];
+  const int nvec = d / 8;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps_total) {
+    const int src = perm_src[r];
+    uint4* g0 = G0 + (size_t)r * nvec;
+    uint4* g1 = G1 ? G1 + (size_t)r * nvec : nullptr;
+    if (src < 0) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int i = lane; i < nvec; i += 32) {
+        g0[i] = z;
+        if (g1) g1[i] = z;
+      }
+    } else {
+      const size_t t = (size_t)(src / k);
+      const uint4* x0 = X0 + t * nvec;
+      const uint4* x1 = X1 ? X1 + t * nvec : nullptr;
+      for (int i = lane; i < nvec; i += 32) {
+        g0[i] = __ldg(x0 + i);
+        if (g1) g1[i] = __ldg(x1 + i);
+      }
+    }
+  }
+}
+
+// -----------------------------------------------------------------------------
+// S7 / B4: Y[t] = sum_j w[t,j] * S[dest[t,j]] in slot order j = 0..k-1 as an
+// fp32 fmaf chain, one rounding to bf16 (w == nullptr: plain sum, for dX).
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ S, const int32_t* __restrict__ dest,
+                                                      const float* __restrict__ w, int T, int k, int d,
+                                                      uint4* __restrict__ Y) {
+  const int nvec = d / 8;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int r = __ldg(dest + (size_t)t * k + j);
+        const float wj = w ? __ldg(w + (size_t)t * k + j) : 1.0f;
+        const uint4 v = __ldg(S + (size_t)r * nvec + i);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]));
+          acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
+          acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+        }
+      }
+      uint4 o;
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4], acc[5]);
+      __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6], acc[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&b0);
+      o.y = *reinterpret_cast<uint32_t*>(&b1);
+      o.z = *reinterpret_cast<uint32_t*>(&b2);
+      o.w = *reinterpret_cast<uint32_t*>(&b3);
+      Y[(size_t)t * nvec + i] = o;
+    }
+  }
+}
+
+// -----------------------------------------------------------------------------
+// B6: dg[t,j] = sum over N tiles of the partial <u, h> (tile order), then
+// dlogits[t, idx[t,j]] = w_j (dg_j - sum_i w_i dg_i), zero elsewhere.
+// One warp per token.
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_grad_kernel(const float* __restrict__ dgp,
+                                                          const int32_t* __restrict__ dest,
+                                                          const int32_t* __restrict__ idx,
+                                                          const float* __restrict__ w, int T, int k, int E,
+                                                          int ntu, float* __restrict__ dg,
+                                                          float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps_total) {
+    float g = 0.0f, wj = 0.0f;
+    int e = 0;
+    if (lane < k) {
+      const int r = dest[(size_t)t * k + lane];
+      for (int n = 0; n < ntu; ++n) g += dgp[(size_t)r * ntu + n];
+      wj = w[(size_t)t * k + lane];
+      e = idx[(size_t)t * k + lane];
+      dg[(size_t)t * k + lane] = g;
+    }
+    float s = wj * g;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (dlogits) {
+      float* row = dlogits + (size_t)t * E;
+      for (int i = lane; i < E; i += 32) row[i] = 0.0f;
+      __syncwarp();
+      if (lane < k) row[e] = wj * (g - s);
+    }
+  }
+}
+
+// -----------------------------------------------------------------------------
+// moe_get_routing helper: padded sorted rows -> unpadded rows.
+// -----------------------------------------------------------------------------
+__global__ void unpad_routing_kernel(RoutingPtrs rp, int R, int32_t* __restrict__ perm_out,
+                                     int32_t* __restrict__ dest_out) {
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < R; p += gridDim.x * blockDim.x) {
+    const int e = rp.idx[p];
+    const int u = rp.dest[p] - rp.poff[e] + rp.offsets[e];
+    if (dest_out) dest_out[p] = u;
+    if (perm_out) perm_out[u] = p;
+  }
+}
+
+// ============================================================================ launchers
+cudaError_t launch_router(const float* logits, int T, int E, int k, int32_t* chunk_hist, const RoutingPtrs& rp,
+                          cudaStream_t st) {
+  router_kernel<<<route_chunks(T), kRouteThreads, 0, st>>>(logits, T, E, k, rp.idx, rp.w, chunk_hist);
+  return cudaGetLastError();
+}
+cudaError_t launch_scan(int T, int E, const int32_t* chunk_hist, int32_t* chunk_base, const RoutingPtrs& rp,
+                        cudaStream_t st) {
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, chunk_base, route_chunks(T), E, rp);
+  return cudaGetLastError();
+}
+cudaError_t launch_permute(int T, int E, int k, const int32_t* chunk_base, const RoutingPtrs& rp, cudaStream_t st) {
+  permute_kernel<<<route_chunks(T), 32, E * sizeof(int), st>>>(chunk_base, T, E, k, rp);
+  return cudaGetLastError();
+}
+
+int route_chunks(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
+
+cudaError_t launch_gather(const void* X0, const void* X1, const int32_t* perm_src, const int32_t* totals, int k,
+                          int d, void* G0, void* G1, int grid, cudaStream_t st) {
+  gather_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(X0), reinterpret_cast<const uint4*>(X1),
+                                      perm_src, totals, k, d, reinterpret_cast<uint4*>(G0),
+                                      reinterpret_cast<uint4*>(G1));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* S, const int32_t* dest, const float* w, int T, int k, int d, void* Y,
+                           int grid, cudaStream_t st) {
+  combine_kernel<<<grid, 128, 0, st>>>(reinterpret_cast<const uint4*>(S), dest, w, T, k, d,
+                                       reinterpret_cast<uint4*>(Y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_grad(const float* dgp, const int32_t* dest, const int32_t* idx, const float* w, int T,
+                               int k, int E, int ntu, float* dg, float* dlogits, int grid, cudaStream_t st) {
+  router_grad_kernel<<<grid, 256, 0, st>>>(dgp, dest, idx, w, T, k, E, ntu, dg, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpad_routing(const RoutingPtrs& rp, int R, int32_t* perm_out, int32_t* dest_out,
+                                 cudaStream_t st) {
+  unpad_routing_kernel<<<(R + 255) / 256, 256, 0, st>>>(rp, R, perm_out, dest_out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,247 @@
+"""Thin Python binding of the C ABI in include/moe.h (ctypes).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+of libmoe.so.  The library must be built (``__graft_entry__.build()`` or
+``python -m mixture_experts_layer_19_gb300.build``); importing this module
+without it raises ImportError -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+MOE_OK = 0
+MOE_BF16 = 0
+MOE_MXFP8 = 1
+MOE_DEBUG_IDENTITY_EXPERTS = 0x1
+MOE_DEBUG_TIMING = 0x2
+
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_INTERNAL"}
+
+# Every symbol include/moe.h declares (the test suite checks the library exports them).
+EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "moe_backward",
+            "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
+            "moe_status_string", "moe_last_error")
+
+
+class moe_config_t(ctypes.Structure):
+    _fields_ = [("T_max", ctypes.c_int64), ("d", ctypes.c_int32), ("F", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("prec", ctypes.c_int32),
+                ("minibatch_rows", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
+                ("mover_ctas", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_int64),
+                ("debug_flags", ctypes.c_uint32), ("device", ctypes.c_int32)]
+
+
+def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libmoe.so not built ({path}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P, I64, I32, VP, FP = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
+    sig = {
+        "moe_plan": [ctypes.POINTER(moe_config_t), ctypes.POINTER(P)],
+        "moe_plan_destroy": [P],
+        "moe_saved_bytes": [P, I64, ctypes.POINTER(ctypes.c_size_t)],
+        "moe_forward": [P, I64, VP, FP, VP, VP, VP, VP, VP, P],
+        "moe_backward": [P, I64, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, FP, FP, P],
+        "moe_get_routing": [P, I64, VP, VP, VP, VP, VP, VP, VP, P],
+        "moe_device_status": [P, P, ctypes.POINTER(I32)],
+        "moe_kernel_times": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                             ctypes.POINTER(I64), I32, ctypes.POINTER(I32)],
+        "moe_minibatch_floor": [I32, I32, I32, I32, I32, ctypes.POINTER(I64)],
+        "moe_status_string": [I32],
+        "moe_last_error": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name in ("moe_status_string", "moe_last_error") else ctypes.c_int
+    return lib
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load_library()
+    return _lib
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        detail = lib().moe_last_error().decode()
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({detail})")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoEError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def minibatch_floor(num_sms: int, tile_m: int, tile_n: int, n_out: int, waves: int = 2) -> int:
+    out = ctypes.c_int64()
+    _check(lib().moe_minibatch_floor(num_sms, tile_m, tile_n, n_out, waves, ctypes.byref(out)),
+           "moe_minibatch_floor")
+    return out.value
+
+
+@dataclass
+class Config:
+    T_max: int
+    d: int
+    F: int
+    E: int
+    k: int
+    prec: int = MOE_BF16
+    minibatch_rows: int = 0
+    ring_slots: int = 0
+    mover_ctas: int = 0
+    wait_timeout_ns: int = 0
+    debug_flags: int = 0
+    device: int = 0
+
+    def to_c(self) -> moe_config_t:
+        return moe_config_t(self.T_max, self.d, self.F, self.E, self.k, self.prec, self.minibatch_rows,
+                            self.ring_slots, self.mover_ctas, self.wait_timeout_ns, self.debug_flags,
+                            self.device)
+
+
+class Plan:
+    """One moe_plan_t: owns the device workspace for tokens T <= T_max."""
+
+    def __init__(self, cfg: Config):
+        self.cfg = cfg
+        self._c = cfg.to_c()
+        h = ctypes.c_void_p()
+        _check(lib().moe_plan(ctypes.byref(self._c), ctypes.byref(h)), "moe_plan")
+        self.handle = h
+        self.device = torch.device("cuda", cfg.device)
+
+    def close(self):
+        if self.handle:
+            lib().moe_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def saved_bytes(self, T: int) -> int:
+        n = ctypes.c_size_t()
+        _check(lib().moe_saved_bytes(self.handle, T, ctypes.byref(n)), "moe_saved_bytes")
+        return n.value
+
+    def new_saved(self, T: int) -> torch.Tensor:
+        return torch.empty(self.saved_bytes(T), dtype=torch.uint8, device=self.device)
+
+    def forward(self, X, logits, Wg, Wu, Wd, Y=None, saved=None, stream=None):
+        T = X.shape[0]
+        if Y is None:
+            Y = torch.empty((T, self.cfg.d), dtype=torch.bfloat16, device=self.device)
+        if saved is None:
+            saved = self.new_saved(T)
+        _check(lib().moe_forward(self.handle, T, _ptr(X), _ptr(logits), _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                                 _ptr(Y), _ptr(saved), _stream(stream)), "moe_forward")
+        return Y, saved
+
+    def backward(self, dY, X, Wg, Wu, Wd, saved, out=None, want_dlogits=True, stream=None):
+        T, c = X.shape[0], self.cfg
+        dev = self.device
+        if out is None:
+            out = {
+                "dX": torch.empty((T, c.d), dtype=torch.bfloat16, device=dev),
+                "dWg": torch.empty((c.E, c.F, c.d), dtype=torch.bfloat16, device=dev),
+                "dWu": torch.empty((c.E, c.F, c.d), dtype=torch.bfloat16, device=dev),
+                "dWd": torch.empty((c.E, c.d, c.F), dtype=torch.bfloat16, device=dev),
+                "dg": torch.empty((T, c.k), dtype=torch.float32, device=dev),
+                "dlogits": torch.empty((T, c.E), dtype=torch.float32, device=dev) if want_dlogits else None,
+            }
+        _check(lib().moe_backward(self.handle, T, _ptr(dY), _ptr(X), _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                                  _ptr(saved), _ptr(out["dX"]), _ptr(out["dWg"]), _ptr(out["dWu"]),
+                                  _ptr(out["dWd"]), _ptr(out["dg"]), _ptr(out.get("dlogits")),
+                                  _stream(stream)), "moe_backward")
+        return out
+
+    def routing(self, saved, T, stream=None):
+        c, dev = self.cfg, self.device
+        R = T * c.k
+        out = {
+            "idx": torch.empty((T, c.k), dtype=torch.int32, device=dev),
+            "w": torch.empty((T, c.k), dtype=torch.float32, device=dev),
+            "counts": torch.empty((c.E,), dtype=torch.int32, device=dev),
+            "offsets": torch.empty((c.E + 1,), dtype=torch.int32, device=dev),
+            "perm_src": torch.empty((R,), dtype=torch.int32, device=dev),
+            "dest": torch.empty((T, c.k), dtype=torch.int32, device=dev),
+        }
+        _check(lib().moe_get_routing(self.handle, T, _ptr(saved), _ptr(out["idx"]), _ptr(out["w"]),
+                                     _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm_src"]),
+                                     _ptr(out["dest"]), _stream(stream)), "moe_get_routing")
+        return out
+
+    def device_status(self, stream=None) -> int:
+        st = ctypes.c_int32()
+        _check(lib().moe_device_status(self.handle, _stream(stream), ctypes.byref(st)), "moe_device_status")
+        return st.value
+
+    def kernel_times(self):
+        cap = 64
+        names = (ctypes.c_char_p * cap)()
+        ms = (ctypes.c_double * cap)()
+        cnt = (ctypes.c_int64 * cap)()
+        n = ctypes.c_int32()
+        _check(lib().moe_kernel_times(self.handle, names, ms, cnt, cap, ctypes.byref(n)), "moe_kernel_times")
+        return {names[i].decode(): (ms[i], cnt[i]) for i in range(min(n.value, cap))}
+
+
+class _MoEFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, plan: Plan, X, logits, Wg, Wu, Wd):
+        Y, saved = plan.forward(X.contiguous(), logits.contiguous(), Wg, Wu, Wd)
+        ctx.plan = plan
+        ctx.save_for_backward(X, Wg, Wu, Wd, saved)
+        return Y
+
+    @staticmethod
+    def backward(ctx, dY):
+        X, Wg, Wu, Wd, saved = ctx.saved_tensors
+        g = ctx.plan.backward(dY.contiguous(), X, Wg, Wu, Wd, saved, want_dlogits=True)
+        return None, g["dX"], g["dlogits"], g["dWg"], g["dWu"], g["dWd"]
+
+
+class MoELayer(torch.nn.Module):
+    """Fused MoE layer over bf16 expert weights; router logits are an input."""
+
+    def __init__(self, d: int, F: int, E: int, k: int, T_max: int, device=0, debug_flags: int = 0):
+        super().__init__()
+        dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        self.plan = Plan(Config(T_max=T_max, d=d, F=F, E=E, k=k, device=dev.index or 0,
+                                debug_flags=debug_flags))
+        self.Wg = torch.nn.Parameter(torch.empty((E, F, d), dtype=torch.bfloat16, device=dev))
+        self.Wu = torch.nn.Parameter(torch.empty((E, F, d), dtype=torch.bfloat16, device=dev))
+        self.Wd = torch.nn.Parameter(torch.empty((E, d, F), dtype=torch.bfloat16, device=dev))
+
+    def forward(self, X, logits):
+        return _MoEFunction.apply(self.plan, X, logits, self.Wg, self.Wu, self.Wd)

@@ -1,0 +1,88 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every entry point include/moe.h declares, the pure-host minibatch floor
+reproduces the figure the pages print, and argument errors come back
+synchronously as status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+GOLDEN_FLOOR = os.path.join(ROOT, "tests", "golden", "minibatch_floor.txt")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_19_gb300 import build as b
+    b.build()
+    from mixture_experts_layer_19_gb300 import moe
+    return moe.load_library()
+
+
+def _declared_symbols():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from mixture_experts_layer_19_gb300 import moe
+    declared = _declared_symbols()
+    assert declared, "no declarations parsed"
+    assert set(declared) == set(moe.EXPORTED), (declared, moe.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_minibatch_floor_matches_pages(lib):
+    for line in open(GOLDEN_FLOOR, encoding="utf-8"):
+        if line.startswith("#") or not line.strip():
+            continue
+        hidden, ffn, waves, sms, tm, tn, expect = map(int, line.split())
+        out = ctypes.c_int64()
+        assert lib.moe_minibatch_floor(sms, tm, tn, ffn, waves, ctypes.byref(out)) == 0
+        assert out.value == expect
+    out = ctypes.c_int64()
+    assert lib.moe_minibatch_floor(0, 128, 128, 2048, 2, ctypes.byref(out)) == 1
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.moe_status_string(s)
+    assert lib.moe_status_string(5).decode() == "device-side wait timed out"
+
+
+def test_plan_rejects_bad_configs_without_touching_a_gpu(lib):
+    from mixture_experts_layer_19_gb300 import moe
+    h = ctypes.c_void_p()
+    assert lib.moe_plan(None, ctypes.byref(h)) == 1
+    bad = [
+        dict(T_max=0, d=256, F=256, E=8, k=2),          # T_max out of range
+        dict(T_max=16, d=200, F=256, E=8, k=2),         # d not a multiple of 256
+        dict(T_max=16, d=256, F=384, E=8, k=2),         # F not a multiple of 256
+        dict(T_max=16, d=256, F=256, E=2, k=4),         # k > E
+        dict(T_max=16, d=256, F=256, E=2048, k=4),      # E > 1024
+        dict(T_max=16, d=256, F=256, E=8, k=33),        # k > 32
+        dict(T_max=16, d=256, F=256, E=8, k=2, prec=7),  # unknown precision
+    ]
+    for kw in bad:
+        c = moe.Config(**kw).to_c()
+        st = lib.moe_plan(ctypes.byref(c), ctypes.byref(h))
+        assert st in (1, 2), (kw, st)
+        assert lib.moe_last_error()
+    # null-plan calls are argument errors, not crashes
+    assert lib.moe_forward(None, 4, None, None, None, None, None, None, None, None) == 1
+    n = ctypes.c_size_t()
+    assert lib.moe_saved_bytes(None, 4, ctypes.byref(n)) == 1
+    assert lib.moe_plan_destroy(None) == 0
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding refuses to run without the compiled library."""
+    from mixture_experts_layer_19_gb300 import moe
+    with pytest.raises(ImportError):
+        moe.load_library("/nonexistent/libmoe.so")
+    src = open(os.path.join(ROOT, "mixture_experts_layer_19_gb300", "moe.py"), encoding="utf-8").read()
+    assert "oracle" not in src.replace("no fallback", "")

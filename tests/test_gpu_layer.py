@@ -1,0 +1,171 @@
+"""GPU parity of the fused MoE layer against the fp64 CPU oracle, through
+the C ABI.  Routing, histograms and the permutation are compared bit for
+bit; floating-point outputs within max|err| / max|ref| <= 2e-2 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_19_gb300 import moe
+from oracle import moe_ref
+from tests.util import BF16_TOL, cpu_and_gpu_inputs, rel_err
+
+pytestmark = pytest.mark.gpu
+
+# (T, d, F, E, k, alpha): tiny config, a mid config spanning several tiles in
+# every dimension with ragged expert segments, and skewed routing.
+CASES = [
+    (128, 256, 512, 8, 2, 0.0),
+    (512, 1024, 512, 32, 4, 1.1),
+    (300, 512, 768, 16, 3, 1.5),
+]
+
+
+def _plan(T, d, F, E, k, flags=0):
+    return moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, debug_flags=flags))
+
+
+def _check_routing(plan, saved, T, k, E, L):
+    r = plan.routing(saved, T)
+    torch.cuda.synchronize()
+    idx_ref, w_ref = moe_ref.route(L, k)
+    lay = moe_ref.layout(idx_ref, E)
+    assert np.array_equal(r["idx"].cpu().numpy(), idx_ref)
+    assert np.array_equal(r["counts"].cpu().numpy(), lay["counts"])
+    assert np.array_equal(r["offsets"].cpu().numpy(), lay["offsets"])
+    assert np.array_equal(r["perm_src"].cpu().numpy(), lay["perm_src"])
+    assert np.array_equal(r["dest"].cpu().numpy(), lay["dest"])
+    w = r["w"].cpu().double().numpy()
+    assert np.abs(w - w_ref).max() <= 1e-6
+    assert np.abs(w.sum(1) - 1.0).max() <= 4 * 2.0 ** -23 * k
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_forward_backward_parity(case):
+    T, d, F, E, k, alpha = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=1, alpha=alpha)
+    plan = _plan(T, d, F, E, k)
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    _check_routing(plan, saved, T, k, E, h["logits"])
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    errs = {"Y": rel_err(Y, Yr)}
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        errs[key] = rel_err(out[key], gr[key])
+    assert all(v <= BF16_TOL for v in errs.values()), errs
+
+
+def test_identity_experts_top1_returns_input_bitwise():
+    T, d, F, E, k = 257, 512, 256, 16, 1
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=4, alpha=1.5)
+    plan = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_IDENTITY_EXPERTS)
+    Y, _ = plan.forward(g["X"], g["logits"], None, None, None)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, g["X"])
+    plan3 = _plan(T, d, F, E, 3, flags=moe.MOE_DEBUG_IDENTITY_EXPERTS)
+    Y3, _ = plan3.forward(g["X"], g["logits"], None, None, None)
+    torch.cuda.synchronize()
+    assert rel_err(Y3, g["X"].double().cpu().numpy()) <= 2 ** -8
+
+
+@pytest.mark.parametrize("T", [1, 3, 127, 129])
+def test_ragged_token_counts(T):
+    d, F, E, k = 256, 256, 8, 2
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=T)
+    plan = _plan(256, d, F, E, k)
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    _check_routing(plan, saved, T, k, E, h["logits"])
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    assert rel_err(Y, Yr) <= BF16_TOL
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        assert rel_err(out[key], gr[key]) <= BF16_TOL, key
+
+
+def test_all_tokens_to_same_experts_and_empty_experts():
+    T, d, F, E, k = 300, 256, 256, 12, 2
+    bias = torch.zeros(E)
+    bias[5], bias[9] = 40.0, 30.0  # every token picks experts 5 then 9; the other ten get nothing
+
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=8, logits_fn=lambda L: L + bias[None, :])
+    plan = _plan(T, d, F, E, k)
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    _check_routing(plan, saved, T, k, E, h["logits"])
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    assert rel_err(Y, Yr) <= BF16_TOL
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        assert rel_err(out[key], gr[key]) <= BF16_TOL, key
+    empty = [e for e in range(E) if e not in (5, 9)]
+    for key in ("dWg", "dWu", "dWd"):
+        assert torch.count_nonzero(out[key][empty]).item() == 0
+
+
+def test_k_equals_E():
+    T, d, F, E, k = 64, 256, 256, 4, 4
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=9)
+    plan = _plan(T, d, F, E, k)
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    _check_routing(plan, saved, T, k, E, h["logits"])
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    assert rel_err(Y, Yr) <= BF16_TOL
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        assert rel_err(out[key], gr[key]) <= BF16_TOL, key
+
+
+def test_bitwise_deterministic_over_10_runs():
+    T, d, F, E, k = 512, 512, 512, 16, 4
+    for alpha in (0.0, 1.1, 1.5):
+        g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=12, alpha=alpha)
+        plan = _plan(T, d, F, E, k)
+        ref = None
+        for _ in range(10):
+            Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+            out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+            r = plan.routing(saved, T)
+            cur = [Y.clone()] + [out[n].clone() for n in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")] + \
+                  [r[n].clone() for n in ("idx", "w", "perm_src", "dest")]
+            if ref is None:
+                ref = cur
+            else:
+                for a, b in zip(ref, cur):
+                    assert torch.equal(a, b)
+
+
+def test_zero_tokens_is_noop_and_zero_weight_grads():
+    d, F, E, k = 256, 256, 4, 2
+    plan = _plan(16, d, F, E, k)
+    dev = torch.device("cuda", 0)
+    X = torch.empty((0, d), dtype=torch.bfloat16, device=dev)
+    L = torch.empty((0, E), dtype=torch.float32, device=dev)
+    W = torch.randn((E, F, d), device=dev).to(torch.bfloat16)
+    Wd = torch.randn((E, d, F), device=dev).to(torch.bfloat16)
+    Y, saved = plan.forward(X, L, W, W, Wd)
+    out = plan.backward(X, X, W, W, Wd, saved)
+    torch.cuda.synchronize()
+    assert Y.shape == (0, d)
+    for key in ("dWg", "dWu", "dWd"):
+        assert torch.count_nonzero(out[key]).item() == 0
+
+
+def test_argument_errors_are_synchronous():
+    T, d, F, E, k = 32, 256, 256, 4, 2
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=2)
+    plan = _plan(T, d, F, E, k)
+    with pytest.raises(moe.MoEError) as ei:
+        plan.forward(torch.cat([g["X"], g["X"]]), torch.cat([g["logits"], g["logits"]]), g["Wg"], g["Wu"], g["Wd"])
+    assert ei.value.status == 1  # T > T_max
+    bad = torch.empty(g["X"].numel() * 2 + 8, dtype=torch.uint8, device=g["X"].device)[8:].view(torch.bfloat16)
+    Xmis = bad[: g["X"].numel()].view(T, d)
+    with pytest.raises(moe.MoEError):
+        plan.forward(Xmis, g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    assert plan.device_status() == 0
