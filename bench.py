@@ -1,0 +1,421 @@
+"""Benchmark of the fused MoE layer (forward + backward, BF16) on GB300.
+
+One step = one forward and one backward of the whole layer (router top-k,
+layout, gather, [a|b] GEMM + SwiGLU, down GEMM, combine; gather, u GEMM +
+SwiGLU backward, dx GEMM, dx reduce, router gradient, dWd and dWg/dWu GEMMs)
+over T=4096 tokens, hidden 7168, expert width 2048, 256 experts, top-8, with
+Zipf(1.1) routing skew (synthetic seeded inputs; random weights).
+
+Prints one JSON line.  Under torchrun every rank runs its own copy of the
+workload (token-parallel replicas: no data-path collective); timing is the
+maximum over ranks.  `--impl reference` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_19_gb300.workload import LayerShape, make_inputs  # noqa: E402
+
+METRIC = "MoE layer tokens/s fwd+bwd (BF16, MXFP8) on 1 GB300; % of roofline"
+SHAPE = dict(T=4096, d=7168, F=2048, E=256, k=8)
+ALPHA = 1.1
+SEED = 0
+WORKLOAD = "moe_layer_fwd_bwd_bf16_T4096_d7168_F2048_E256_top8_zipf1.1"
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws: int):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """Largest value of x over all ranks (host-side timing exchange only)."""
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- roofline bookkeeping
+def algorithmic_bytes(shape, R: int):
+    """Compulsory HBM bytes per launch of each kernel (bf16 = 2 B): the weights
+    it must stream once plus the rows it must read and write (R routed rows,
+    padding excluded)."""
+    d, F, E = shape["d"], shape["F"], shape["E"]
+    W = E * F * d * 2          # one weight tensor
+    return {
+        "gemm_up_swiglu": 2 * W + R * d * 2 + R * 3 * F * 2,
+        "gemm_down": W + R * F * 2 + R * d * 2,
+        "gemm_bwd_u_swiglu": W + R * d * 2 + R * 2 * F * 2 + R * 3 * F * 2,
+        "gemm_bwd_dx": 2 * W + R * 2 * F * 2 + R * d * 2,
+        "gemm_wgrad_down": W + R * d * 2 + R * F * 2,
+        "gemm_wgrad_gate_up": 2 * W + R * 2 * F * 2 + R * d * 2,
+    }
+
+
+def layer_roofline(shape, peaks):
+    """Roofline time of one fwd+bwd: max(FLOPs / bf16 peak, compulsory bytes / HBM peak)."""
+    T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
+    R = T * k
+    flops = 18.0 * R * d * F
+    W = 3.0 * E * F * d * 2
+    act = T * d * 2 * 4 + T * E * 4 * 2   # X, dY in; Y, dX out; logits in, dlogits out
+    byts = 2 * W + W + act                # weights read fwd + bwd, weight grads written
+    t_tc = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    return {"flops": flops, "bytes": byts, "t_ms": max(t_tc, t_hbm) * 1e3,
+            "bound": "hbm" if t_hbm >= t_tc else "tensor"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+class _HostWeights:
+    """Per-expert host copies (float32, exact widening of bf16) of device weights."""
+
+    def __init__(self, W, experts):
+        self.cache = {int(e): W[int(e)].float().cpu().numpy() for e in experts}
+
+    def __getitem__(self, e):
+        return self.cache[int(e)]
+
+
+def oracle_sample(inp, tokens, k):
+    """Prepare the oracle's inputs for a sub-batch of tokens (host copies)."""
+    from oracle import moe_ref
+    tokens = torch.as_tensor(np.asarray(tokens), device=inp.X.device)
+    logits = inp.logits[tokens].double().cpu().numpy()
+    idx, _ = moe_ref.route(logits, k)
+    experts = sorted(set(idx.reshape(-1).tolist()) | {0})
+    return {
+        "X": inp.X[tokens].double().cpu().numpy(), "logits": logits,
+        "dY": inp.dY[tokens].double().cpu().numpy(),
+        "Wg": _HostWeights(inp.Wg, experts), "Wu": _HostWeights(inp.Wu, experts),
+        "Wd": _HostWeights(inp.Wd, experts), "n": int(tokens.numel()), "experts": len(experts) - 1,
+    }
+
+
+def run_oracle(s, k):
+    from oracle import moe_ref
+    Y, ctx = moe_ref.forward(s["X"], s["logits"], s["Wg"], s["Wu"], s["Wd"], k)
+    g = moe_ref.backward(s["dY"], s["X"], s["logits"], s["Wg"], s["Wu"], s["Wd"], ctx, sparse_dw=True)
+    return Y, g
+
+
+def cpu_cores():
+    return len(os.sched_getaffinity(0))
+
+
+def set_blas_threads(n):
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(n)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- main arms
+def bench_gpu(args):
+    from mixture_experts_layer_19_gb300 import moe
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    shape = dict(SHAPE)
+    if args.experts:
+        shape["E"] = args.experts   # smaller layer for profiler captures only
+    T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
+    inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED + rank, alpha=ALPHA, device=dev)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, device=local, debug_flags=moe.MOE_DEBUG_TIMING))
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    grads = {
+        "dX": torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+        "dWg": torch.empty((E, F, d), dtype=torch.bfloat16, device=dev),
+        "dWu": torch.empty((E, F, d), dtype=torch.bfloat16, device=dev),
+        "dWd": torch.empty((E, d, F), dtype=torch.bfloat16, device=dev),
+        "dg": torch.empty((T, k), dtype=torch.float32, device=dev),
+        "dlogits": torch.empty((T, E), dtype=torch.float32, device=dev),
+    }
+    stream = torch.cuda.current_stream(dev)
+
+    def step(X, logits, dY):
+        plan.forward(X, logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        plan.backward(dY, X, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+
+    for _ in range(args.warmup):
+        step(inp.X, inp.logits, inp.dY)
+    torch.cuda.synchronize(dev)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    plan.kernel_times()  # discard warm-up records
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(inp.X, inp.logits, inp.dY)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    ktimes = plan.kernel_times()
+    status = plan.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after timed region")
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = ws * T * args.steps / (elapsed_ms / 1e3)
+
+    # ---- roofline of the dominant kernel (largest share of device time)
+    peaks = load_peaks()
+    R = T * k
+    ab = algorithmic_bytes(shape, R)
+    gemm_names = [n for n in ktimes if n in ab]
+    dom = max(gemm_names, key=lambda n: ktimes[n][0])
+    dom_ms = ktimes[dom][0] / ktimes[dom][1]
+    achieved = ab[dom] / (dom_ms / 1e3) / 1e9
+    roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "peak_source": peaks["source"] + " hbm_gbs (STREAM copy)",
+            "algorithmic_bytes": ab[dom], "avg_launch_ms": round(dom_ms, 4)}
+    total_dev = sum(v[0] for v in ktimes.values())
+    kernels = {n: {"ms_per_step": round(v[0] / args.steps, 4), "launches": v[1],
+                   "share": round(v[0] / total_dev, 4)} for n, v in sorted(ktimes.items(), key=lambda x: -x[1][0])}
+    launches = int(sum(v[1] for v in ktimes.values()))
+    lr = layer_roofline(shape, peaks)
+
+    # ---- end-to-end through the public API with host buffers
+    e2e = None if args.no_e2e else bench_e2e(args, plan, inp, Y, saved, grads, stream, dev, ws)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD if not args.experts else f"profile_E{E}", "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
+                   "seed": SEED, "tokens_per_gpu": T, "parallelism": f"replicas{ws}",
+                   "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass, 129 MB L2)"},
+        "roofline": roof,
+        "layer_roofline": {"bound": lr["bound"], "t_ms": round(lr["t_ms"], 4),
+                           "frac": round(lr["t_ms"] / ms_per_step, 4),
+                           "note": "max(18*R*d*F / sustained bf16 peak, weights read twice + dW written + I/O / HBM peak)"},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(inp, k, args.cpu_tokens)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_e2e(args, plan, inp, Y, saved, grads, stream, dev, ws):
+    """Same fwd+bwd through the public API with pinned HOST inputs and results:
+    each step copies X, logits, dY host->device and Y, dX device->host."""
+    hX = inp.X.cpu().pin_memory()
+    hL = inp.logits.cpu().pin_memory()
+    hdY = inp.dY.cpu().pin_memory()
+    hY = torch.empty_like(hX).pin_memory()
+    hdX = torch.empty_like(hX).pin_memory()
+    dX_in = torch.empty_like(inp.X)
+    dL_in = torch.empty_like(inp.logits)
+    ddY_in = torch.empty_like(inp.dY)
+
+    def step():
+        dX_in.copy_(hX, non_blocking=True)
+        dL_in.copy_(hL, non_blocking=True)
+        ddY_in.copy_(hdY, non_blocking=True)
+        plan.forward(dX_in, dL_in, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        plan.backward(ddY_in, dX_in, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+        hY.copy_(Y, non_blocking=True)
+        hdX.copy_(grads["dX"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        step()
+    torch.cuda.synchronize(dev)
+    plan.kernel_times()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    el = time.perf_counter() - t0
+    plan.kernel_times()
+    el = max_over_ranks(el, ws, dev)
+    T = inp.X.shape[0]
+    h2d = hX.numel() * 2 + hL.numel() * 4 + hdY.numel() * 2
+    d2h = hY.numel() * 2 + hdX.numel() * 2
+    return {"value": round(ws * T * args.steps / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def cpu_baseline(inp, k, n_tokens):
+    cores = cpu_cores()
+    lim = set_blas_threads(cores)
+    toks = np.arange(n_tokens)
+    s = oracle_sample(inp, toks, k)
+    t0 = time.perf_counter()
+    run_oracle(s, k)
+    el = time.perf_counter() - t0
+    del lim
+    return {"value": round(n_tokens / el, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of the first {n_tokens} tokens of the same workload as one batch "
+                      f"({s['experts']} experts touched; {el:.1f} s)"}
+
+
+def bench_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    shape = dict(SHAPE)
+    T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=ALPHA, device=dev)
+    cores = cpu_cores()
+    set_blas_threads(cores)
+    per = args.ref_tokens
+    samples = [oracle_sample(inp, np.arange(i * per, (i + 1) * per) % T, k)
+               for i in range(args.warmup + args.steps)]
+    for s in samples[:args.warmup]:
+        run_oracle(s, k)
+    t0 = time.perf_counter()
+    for s in samples[args.warmup:]:
+        run_oracle(s, k)
+    el = time.perf_counter() - t0
+    value = per * args.steps / el
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
+                   "seed": SEED, "tokens_per_step": per},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle fwd+bwd of {per} consecutive tokens of the workload"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=48, help="tokens in the timed CPU-oracle sample")
+    ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

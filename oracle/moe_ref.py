@@ -156,8 +156,12 @@ def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False):
 # ----------------------------------------------------------------------------
 # 5. Backward (reverse combine, expert backward, reverse dispatch, dW, router).
 # ----------------------------------------------------------------------------
-def backward(dY, X, logits, Wg, Wu, Wd, ctx):
+def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
     """Gradients of L = <dY, Y>.  Returns dict dX, dWg, dWu, dWd, dg, dlogits.
+
+    sparse_dw=True stores the weight gradients as {expert: array} for the
+    experts that received tokens (others are zero) instead of dense [E, ...]
+    arrays -- storage only, for full-size layers on a sub-batch of tokens.
 
     MXFP8 emulation (ctx["mx"]): dY along d and Wd along d for u = Wd^T dY;
     dA, dB along F and Wg, Wu along F for dX; for the weight gradients each
@@ -175,9 +179,12 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx):
     wflat = w.reshape(-1)
     dYq = _q(dY, 1, mx)
     dX = np.zeros((T, d))
-    dWg = np.zeros((E, F, d))
-    dWu = np.zeros((E, F, d))
-    dWd = np.zeros((E, d, F))
+    if sparse_dw:
+        dWg, dWu, dWd = {}, {}, {}
+    else:
+        dWg = np.zeros((E, F, d))
+        dWu = np.zeros((E, F, d))
+        dWd = np.zeros((E, d, F))
     dg = np.zeros(R)
     for e in range(E):
         rows = _segment_rows(lay, e)
