@@ -146,6 +146,33 @@ moe_status_t moe_kernel_times(moe_plan_t plan, const char** names, double* total
 moe_status_t moe_minibatch_floor(int32_t num_sms, int32_t tile_m, int32_t tile_n, int32_t n_out,
                                  int32_t waves, int64_t* rows);
 
+/* Routing without any device allocation.  The Mixture-of-Kittens pages have
+ * no counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc -- e.g. code running inside a host framework whose allocator has
+ * already reserved the device memory, or latency-critical paths that cannot
+ * afford an allocation (which may synchronise the device).  moe_plan
+ * allocates, so those callers cannot reach moe_forward's routing.
+ *
+ * Computes on the current device, enqueued on `stream`, exactly the routing
+ * moe_forward stores and moe_get_routing returns (same kernels, same
+ * results): idx [T, k] int32, w [T, k] fp32, counts [E] int32, offsets [E+1]
+ * int32, perm_src [T*k] int32 and dest [T, k] int32, all caller-owned device
+ * buffers.  logits [T, E] fp32.  Requires 1 <= k <= 32, k <= E <= 1024.
+ *
+ * Scratch lives in one fixed 4 MiB device array inside the library, which
+ * every GPU that loads the library keeps until the process exits.  A call
+ * needs about 4*(2*ceil(T/64)*E + 2*T*k + 128*E) bytes of it; larger calls
+ * return MOE_ERR_UNSUPPORTED (see moe_last_error) and enqueue nothing.  The
+ * first call on each device looks up the array's device address; make that
+ * first call outside any stream capture.  All calls share the array and it
+ * keeps the previous call's contents (each call writes every entry it reads,
+ * so nothing needs clearing).  Calls that overlap on the GPU -- e.g. on two
+ * streams without ordering between them -- race on the array.  Never calls
+ * cudaMalloc, cudaFree or any allocating routine. */
+moe_status_t moe_route_noalloc(int64_t T, int32_t E, int32_t k, const float* logits, int32_t* idx, float* w,
+                               int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* dest,
+                               moe_stream_t stream);
+
 /* Static description of a status code. */
 const char* moe_status_string(moe_status_t s);
 

@@ -217,6 +217,8 @@ GemmArgs base_args(moe_plan_s* p, const RoutingPtrs& rp) {
 
 }  // namespace
 
+void moe::set_error_detail(const char* msg) { g_last_error = msg ? msg : ""; }
+
 // ============================================================================ C ABI
 extern "C" {
 

@@ -46,4 +46,7 @@ cudaError_t prepare_gemm_fwd(int kind);
 cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_gemm_bwd(int kind);
 
+// Record the detail string moe_last_error() returns on this thread.
+void set_error_detail(const char* msg);
+
 }  // namespace moe

@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares (the test suite checks the library exports them).
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "moe_backward",
             "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
-            "moe_status_string", "moe_last_error")
+            "moe_status_string", "moe_last_error", "moe_route_noalloc")
 
 
 class moe_config_t(ctypes.Structure):
@@ -57,6 +57,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_minibatch_floor": [I32, I32, I32, I32, I32, ctypes.POINTER(I64)],
         "moe_status_string": [I32],
         "moe_last_error": [],
+        "moe_route_noalloc": [I64, I32, I32, FP, VP, VP, VP, VP, VP, VP, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
