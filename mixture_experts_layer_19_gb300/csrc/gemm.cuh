@@ -1,12 +1,13 @@
 // gemm.cuh -- persistent tcgen05 grouped GEMM for the MoE expert contractions.
 //
-// One CTA per SM (192 threads):
+// One CTA per SM (192 or 320 threads):
 //   warp 0      TMA producer: streams 64-deep K slices of A and B into a
 //               4-stage shared-memory ring (128-byte swizzle).
 //   warp 1      TMEM owner + single-thread UMMA issuer (tcgen05.mma
 //               kind::f16, M=128, N=256, K=16, fp32 accumulate in TMEM).
-//   warps 2..5  epilogue: TMEM -> registers -> fused math -> bf16 ->
-//               64-byte-swizzled staging -> TMA store.
+//   warps 2..   epilogue (4 warps, or 8 for single-output kinds: two per TMEM
+//               lane quadrant, each on half the columns): TMEM -> registers
+//               -> fused math -> bf16 -> 64-byte-swizzled staging -> TMA store.
 // Two 256-column TMEM accumulators let the epilogue of tile i overlap the
 // main loop of tile i+1.  Tiles are handed out statically (tile = CTA id +
 // j * gridDim.x), every tile accumulates its K range in one fixed order, so
@@ -29,7 +30,7 @@ constexpr int BM = 128;           // tile rows (UMMA M)
 constexpr int BN = 256;           // tile cols (UMMA N)
 constexpr int BK = 64;            // K slice per pipeline stage (128 bytes of bf16)
 constexpr int kStages = 4;
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreadsMax = 320;  // 2 control warps + up to 8 epilogue warps
 constexpr int kABytes = BM * BK * 2;             // 16 KB
 constexpr int kBBytes = BN * BK * 2;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
@@ -44,8 +45,13 @@ struct KindTraits {
   static constexpr bool grouped = (KIND <= kBwdX);          // tiles follow expert segments
   static constexpr int n_out = (KIND == kUp || KIND == kBwdU) ? 3 : 1;
   static constexpr int n_buf = (n_out == 3) ? 1 : 2;
+  // single-output epilogues are store-bound (weight gradients write 64 KB per
+  // tile): two warps per TMEM lane quadrant, each taking half of the columns
+  static constexpr int epi_warps = (n_out == 1) ? 8 : 4;
+  static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int staging_per_warp = n_out * n_buf * kStageChunk;
-  static constexpr int smem_bytes = kStages * kStageBytes + 4 * staging_per_warp + 1024 /*align*/ + 256 /*bars*/;
+  static constexpr int smem_bytes =
+      kStages * kStageBytes + epi_warps * staging_per_warp + 1024 /*align*/ + 256 /*bars*/;
 };
 
 struct GemmArgs {
@@ -208,13 +214,13 @@ __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + __ex
 // The kernel.
 // ----------------------------------------------------------------------------
 template <int KIND>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs g) {
+__global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(const __grid_constant__ GemmArgs g) {
   using TR = KindTraits<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
   uint8_t* staging_base = smem + kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(staging_base + 4 * TR::staging_per_warp);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging_base + TR::epi_warps * TR::staging_per_warp);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], TR::epi_warps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -424,14 +430,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           om = up ? &g.mapO1 : &g.mapO0;
           orow = t.e * g.F + (up ? t.row0 - g.F : t.row0) + 32 * q;
         }
+        constexpr int kChunks = 8 / (TR::epi_warps / 4);   // 32-column chunks per warp
+        const int c0 = ((warp - 2) >> 2) * kChunks;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c0; c < c0 + kChunks; ++c) {
           float v[32];
           if (has_acc) {
             uint32_t rv[32];
             tmem_ld32(tbase + c * 32, rv);
             tmem_ld_wait();
-            if (c == 7) {
+            if (c == c0 + kChunks - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&tempty[acc]);

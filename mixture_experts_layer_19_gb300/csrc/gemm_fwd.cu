@@ -10,7 +10,7 @@ namespace moe {
 
 template <int KIND>
 static cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t st) {
-  gemm_kernel<KIND><<<grid, kGemmThreads, KindTraits<KIND>::smem_bytes, st>>>(a);
+  gemm_kernel<KIND><<<grid, KindTraits<KIND>::threads, KindTraits<KIND>::smem_bytes, st>>>(a);
   return cudaGetLastError();
 }
 template <int KIND>
