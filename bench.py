@@ -216,6 +216,8 @@ def bench_gpu(args):
     shape = dict(SHAPE)
     if args.experts:
         shape["E"] = args.experts   # smaller layer for profiler captures only
+    if args.tokens:
+        shape["T"] = args.tokens
     T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED + rank, alpha=ALPHA, device=dev)
     plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, device=local, debug_flags=moe.MOE_DEBUG_TIMING))
@@ -289,7 +291,7 @@ def bench_gpu(args):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if not args.experts else f"profile_E{E}", "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
+        "config": {"workload": WORKLOAD if not (args.experts or args.tokens) else f"profile_T{T}_E{E}", "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
                    "seed": SEED, "tokens_per_gpu": T, "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass, 129 MB L2)"},
         "roofline": roof,
@@ -408,6 +410,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
