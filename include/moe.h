@@ -67,7 +67,7 @@ typedef struct {
   int32_t F;              /* expert FFN width; multiple of 256 */
   int32_t E;              /* experts, k <= E <= 1024 */
   int32_t k;              /* experts per token, 1 <= k <= 32 */
-  int32_t prec;           /* moe_precision_t; only MOE_BF16 is implemented */
+  int32_t prec;           /* moe_precision_t; MOE_MXFP8: forward only (see moe_quantize_weights) */
   int32_t minibatch_rows; /* rows per ring slot; 0 = two-wave floor (moe_minibatch_floor) */
   int32_t ring_slots;     /* ring buffer slots; 0 = default */
   int32_t mover_ctas;     /* CTAs that gather (data movers); 0 = default */
@@ -81,7 +81,9 @@ typedef struct moe_plan_s* moe_plan_t;
 /* Create a plan: validates `cfg`, binds `cfg->device`, allocates all device
  * workspace for T <= T_max, and returns it in *out (caller frees with
  * moe_plan_destroy).  Supported: d % 256 == 0, F % 256 == 0, 1 <= k <= 32,
- * k <= E <= 1024, 1 <= T_max <= 2^20, prec == MOE_BF16.  Otherwise
+ * k <= E <= 1024, 1 <= T_max <= 2^20, prec MOE_BF16 or MOE_MXFP8 (an MXFP8
+ * plan also holds E4M3 copies of the weights; its moe_backward returns
+ * MOE_ERR_UNSUPPORTED).  Otherwise
  * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG; allocation failure MOE_ERR_OOM. */
 moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out);
 
@@ -115,6 +117,28 @@ moe_status_t moe_backward(moe_plan_t plan, int64_t T, const void* dY, const void
                           const void* Wg, const void* Wu, const void* Wd, const void* saved,
                           void* dX, void* dWg, void* dWu, void* dWd, float* dg, float* dlogits,
                           moe_stream_t stream);
+
+/* MXFP8 plans only: quantise the bf16 expert weights into the plan's E4M3
+ * copies (once per optimiser step, outside the layer's timing).  Wg, Wu are
+ * quantised along d and Wd along F, each in blocks of 32 with one E8M0 scale
+ * (the layout of moe_mx_quantize).  Must precede moe_forward on an MXFP8
+ * plan (moe_forward then reads the plan's copies; the bf16 pointers it is
+ * given are not read).  Enqueued on `stream`.  MXFP8 activation quantisation
+ * is fused into the dispatch / GEMM / SwiGLU datapaths (kucoin page "Cursor's
+ * MoK réalise une amélioration des performances de 2,37x sur NVIDIA GB300
+ * NVL72", section 02); the format itself is OCP Microscaling v1.0 MXFP8. */
+moe_status_t moe_quantize_weights(moe_plan_t plan, const void* Wg, const void* Wu, const void* Wd,
+                                  moe_stream_t stream);
+
+/* Quantise a bf16 row-major [rows, K] device matrix to MXFP8 along K
+ * (K % 128 == 0): q [rows, K] E4M3 bytes; sf the E8M0 scale bytes
+ * (X + 127 with X = floor(log2 amax) - 8 clamped to [-127, 127], all-zero
+ * block -> 0) arranged in 512-byte atoms: rows [128 i, 128 i + 128) and
+ * blocks [4 j, 4 j + 4) form atom i * (K / 128) + j, and row r / block b sits
+ * at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + b % 4 of its atom.  sf must hold
+ * ceil(rows / 128) * (K / 128) * 512 bytes.  Elements round to nearest even
+ * and saturate at +-448.  The same kernel quantises the weights. */
+moe_status_t moe_mx_quantize(const void* src, int64_t rows, int64_t K, void* q, void* sf, moe_stream_t stream);
 
 /* Copy the routing a forward stored in `saved` into caller device buffers
  * (any pointer may be NULL to skip it):

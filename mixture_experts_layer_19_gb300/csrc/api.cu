@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "gemm.cuh"
+#include "gemm_mx.cuh"
 #include "kernels.h"
 #include "moe.h"
 
@@ -50,19 +51,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] buffer.
+// 2-D tensor map over a row-major [outer, inner] buffer of bf16 (esize 2) or
+// bytes (esize 1, E4M3 data).
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in, uint32_t box_out,
-               CUtensorMapSwizzle sw) {
+               CUtensorMapSwizzle sw, int esize = 2) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * (uint64_t)esize};
   cuuint32_t box[2] = {box_in, box_out};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+// E4M3 operand loads: 128-byte K slices, 128 (or 256) rows, 128-byte swizzle.
+bool map_fp8_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows = BM) {
+  return encode_2d(m, b, inner, outer, 128, rows, CU_TENSOR_MAP_SWIZZLE_128B, 1);
+}
+// E4M3 stores of 32 rows x 32 bytes, no swizzle.
+bool map_fp8_store(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return encode_2d(m, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE, 1);
 }
 // The three shapes the GEMMs use.
 bool map_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows = BM) {
@@ -154,6 +164,13 @@ struct moe_plan_s {
   CUtensorMap m_Wg_k, m_Wu_k, m_Wd_k, m_Wg_mn, m_Wu_mn, m_Wd_mn;
   const void *p_dwg = nullptr, *p_dwu = nullptr, *p_dwd = nullptr;
   CUtensorMap m_dWg_st, m_dWu_st, m_dWd_st;
+  // MXFP8 (prec == MOE_MXFP8): E4M3 weights + scale atoms (filled by
+  // moe_quantize_weights), E4M3 gathered activations and h with their scales
+  void* mx_ws = nullptr;
+  uint8_t *Wgq = nullptr, *Wuq = nullptr, *Wdq = nullptr, *Wgs = nullptr, *Wus = nullptr, *Wds = nullptr;
+  uint8_t *Xq = nullptr, *Xs = nullptr, *Hq = nullptr, *Hs = nullptr;
+  bool weights_quantized = false;
+  CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
   // timing (MOE_DEBUG_TIMING)
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
@@ -255,7 +272,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: need 1 <= k <= 32 and k <= E <= 1024");
   if (c.d <= 0 || c.F <= 0 || c.d % BN || c.F % BN)
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: d and F must be positive multiples of 256");
-  if (c.prec != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "moe_plan: only MOE_BF16 is implemented");
+  if (c.prec != MOE_BF16 && c.prec != MOE_MXFP8)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: prec must be MOE_BF16 or MOE_MXFP8");
   if ((int64_t)c.E * c.F * c.d >= (int64_t)1 << 40)
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: weight tensor too large");
   if (!encode_fn()) return fail(MOE_ERR_CUDA, "moe_plan: cuTensorMapEncodeTiled unavailable");
@@ -325,10 +343,46 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   }
   for (int kind = 0; kind < 6; ++kind) {
     err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
+    if (err == cudaSuccess && kind < 2 && c.prec == MOE_MXFP8) err = prepare_gemm_mx(kind);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
       delete p;
       return cuda_fail(err, "moe_plan: cudaFuncSetAttribute");
+    }
+  }
+  if (c.prec == MOE_MXFP8) {
+    const size_t wbytes = (size_t)c.E * c.F * c.d;  // E4M3 bytes of one weight tensor
+    size_t m = 0;
+    const size_t o_wgq = m; m += align256(wbytes);
+    const size_t o_wuq = m; m += align256(wbytes);
+    const size_t o_wdq = m; m += align256(wbytes);
+    const size_t o_wgs = m; m += align256(wbytes / 32);
+    const size_t o_wus = m; m += align256(wbytes / 32);
+    const size_t o_wds = m; m += align256(wbytes / 32);
+    const size_t o_xq = m;  m += align256((size_t)R * c.d);
+    const size_t o_xs = m;  m += align256((size_t)R * c.d / 32);
+    const size_t o_hq = m;  m += align256((size_t)R * c.F);
+    const size_t o_hs = m;  m += align256((size_t)R * c.F / 32);
+    err = cudaMalloc(&p->mx_ws, m);
+    if (err != cudaSuccess) {
+      cudaFree(p->ws);
+      delete p;
+      return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of MXFP8 workspace failed: ") +
+                                   cudaGetErrorString(err));
+    }
+    uint8_t* mb = static_cast<uint8_t*>(p->mx_ws);
+    p->Wgq = mb + o_wgq; p->Wuq = mb + o_wuq; p->Wdq = mb + o_wdq;
+    p->Wgs = mb + o_wgs; p->Wus = mb + o_wus; p->Wds = mb + o_wds;
+    p->Xq = mb + o_xq; p->Xs = mb + o_xs; p->Hq = mb + o_hq; p->Hs = mb + o_hs;
+    const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
+    ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, c.d, EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, c.d, EF) &&
+         map_fp8_kmajor(&p->m_Wdq, p->Wdq, c.F, Ed, BN) && map_fp8_kmajor(&p->m_Xq, p->Xq, c.d, R) &&
+         map_fp8_kmajor(&p->m_Hq_k, p->Hq, c.F, R) && map_fp8_store(&p->m_Hq_st, p->Hq, c.F, R);
+    if (!ok) {
+      cudaFree(p->mx_ws);
+      cudaFree(p->ws);
+      delete p;
+      return fail(MOE_ERR_CUDA, "moe_plan: MXFP8 tensor map encoding failed");
     }
   }
   *out = p;
@@ -344,6 +398,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
     cudaEventDestroy(t.b);
   }
   for (auto e : p->spare_events) cudaEventDestroy(e);
+  if (p->mx_ws) cudaFree(p->mx_ws);
   cudaError_t err = cudaFree(p->ws);
   delete p;
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
@@ -377,6 +432,9 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   const int Ti = (int)T;
   cudaError_t err;
 
+  const bool mx = c.prec == MOE_MXFP8 && !ident;
+  if (mx && !p->weights_quantized)
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward: MXFP8 plan needs moe_quantize_weights before the forward");
   if (!ident && !ensure_weight_maps(p, Wg, Wu, Wd)) return fail(MOE_ERR_CUDA, "moe_forward: weight tensor maps");
   CUtensorMap m_ab_st;
   if (!ident && !map_store(&m_ab_st, static_cast<char*>(saved) + L.ab, 2 * c.F, L.rows))
@@ -391,6 +449,47 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     err = timed_launch(p, "layout_permute", st,
                        [&] { return launch_permute(Ti, c.E, c.k, p->chunk_base, rp, st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: routing launch");
+  if (mx) {
+    // MXFP8: gather + quantise X along d, block-scaled [a|b] GEMM with SwiGLU and
+    // h re-quantised along F in its epilogue, block-scaled down GEMM.
+    err = timed_launch(p, "gather_quant", st, [&] {
+      return launch_gather_quant(X, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
+    MxArgs a;
+    memset(&a, 0, sizeof(a));
+    a.poff = rp.poff;
+    a.mtile_off = rp.mtile_off;
+    a.status = p->status;
+    a.timeout_ns = (uint64_t)c.wait_timeout_ns;
+    a.E = c.E;
+    a.d = c.d;
+    a.F = c.F;
+    MxArgs b = a;
+    a.mapA = p->m_Xq;
+    a.mapB0 = p->m_Wgq;
+    a.mapB1 = p->m_Wuq;
+    a.mapO0 = m_ab_st;
+    a.mapO1 = p->m_Hq_st;
+    a.sfA = p->Xs;
+    a.sfB0 = p->Wgs;
+    a.sfB1 = p->Wus;
+    a.sfO = p->Hs;
+    err = timed_launch(p, "gemm_mx_up_swiglu", st, [&] { return launch_gemm_mx(kUp, a, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 up GEMM launch");
+    b.mapA = p->m_Hq_k;
+    b.mapB0 = p->m_Wdq;
+    b.mapO0 = p->m_Ys_st;
+    b.sfA = p->Hs;
+    b.sfB0 = p->Wds;
+    err = timed_launch(p, "gemm_mx_down", st, [&] { return launch_gemm_mx(kDown, b, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 down GEMM launch");
+    const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
+    err = timed_launch(p, "combine", st,
+                       [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
+    return MOE_OK;
+  }
   err = timed_launch(p, "gather", st, [&] {
     return launch_gather(X, nullptr, rp.perm_src, rp.totals, c.k, c.d, p->Xg, nullptr, p->num_sms * 8, st);
   });
@@ -427,6 +526,8 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   const moe_config_t& c = p->cfg;
   if (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)
     return fail(MOE_ERR_UNSUPPORTED, "moe_backward: identity-expert debug mode has no backward");
+  if (c.prec == MOE_MXFP8)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_backward: the MXFP8 backward is not built; use a MOE_BF16 plan");
   if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_backward: T outside [0, T_max]");
   if (!dWg || !dWu || !dWd || !Wg || !Wu || !Wd)
     return fail(MOE_ERR_INVALID_ARG, "moe_backward: null weight or weight-gradient pointer");
@@ -545,6 +646,41 @@ moe_status_t moe_get_routing(moe_plan_t p, int64_t T, const void* saved, int32_t
     err = launch_unpad_routing(rp, (int)R, perm_src, dest, st);
     if (err != cudaSuccess) return cuda_fail(err, "moe_get_routing: unpad launch");
   }
+  return MOE_OK;
+}
+
+moe_status_t moe_mx_quantize(const void* src, int64_t rows, int64_t K, void* q, void* sf, moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 128 != 0 || rows * K >= ((int64_t)1 << 40))
+    return fail(MOE_ERR_INVALID_ARG, "moe_mx_quantize: need K a positive multiple of 128 and rows >= 0");
+  if (rows == 0) return MOE_OK;
+  if (!src || !q || !sf || !aligned16(src) || !aligned16(q) || !aligned16(sf))
+    return fail(MOE_ERR_INVALID_ARG, "moe_mx_quantize: null or misaligned pointer");
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t err = launch_quant_rows(src, rows, (int)K, q, sf, std::max(1, sms) * 8,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_mx_quantize: launch");
+}
+
+moe_status_t moe_quantize_weights(moe_plan_t p, const void* Wg, const void* Wu, const void* Wd, moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: null plan");
+  const moe_config_t& c = p->cfg;
+  if (c.prec != MOE_MXFP8) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: plan is not MOE_MXFP8");
+  if (!Wg || !Wu || !Wd || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: null or misaligned weight pointer");
+  DeviceGuard guard(c.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t EF = (int64_t)c.E * c.F, Ed = (int64_t)c.E * c.d;
+  const int grid = p->num_sms * 8;
+  cudaError_t err = timed_launch(p, "quant_weights", st, [&] {
+    cudaError_t e = launch_quant_rows(Wg, EF, c.d, p->Wgq, p->Wgs, grid, st);
+    if (e == cudaSuccess) e = launch_quant_rows(Wu, EF, c.d, p->Wuq, p->Wus, grid, st);
+    if (e == cudaSuccess) e = launch_quant_rows(Wd, Ed, c.F, p->Wdq, p->Wds, grid, st);
+    return e;
+  });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_quantize_weights: launch");
+  p->weights_quantized = true;
   return MOE_OK;
 }
 

@@ -79,33 +79,35 @@ struct Tile {
   int kbase;       // first sorted row of the K range (wgrad)
 };
 
-template <int KIND>
-__device__ __forceinline__ int n_tiles_n(const GemmArgs& g) {
+// The helpers below take any argument struct with E, d, F, poff, mtile_off
+// (GemmArgs here, MxArgs for the MXFP8 kernel).
+template <int KIND, class G>
+__device__ __forceinline__ int n_tiles_n(const G& g) {
   if (KIND == kUp) return g.F / 128;
   if (KIND == kDown || KIND == kBwdX) return g.d / BN;
   if (KIND == kBwdU) return g.F / BN;
   if (KIND == kWgradD) return g.F / BN;
   return g.d / BN;  // kWgradGU
 }
-template <int KIND>
-__device__ __forceinline__ int n_tiles_m_wgrad(const GemmArgs& g) {
+template <int KIND, class G>
+__device__ __forceinline__ int n_tiles_m_wgrad(const G& g) {
   return KIND == kWgradD ? g.d / BM : (2 * g.F) / BM;
 }
-template <int KIND>
-__device__ __forceinline__ int k_blocks_grouped(const GemmArgs& g) {
+template <int KIND, class G>
+__device__ __forceinline__ int k_blocks_grouped(const G& g) {
   if (KIND == kUp || KIND == kBwdU) return g.d / BK;
   if (KIND == kDown) return g.F / BK;
   return (2 * g.F) / BK;  // kBwdX
 }
 
-template <int KIND>
-__device__ __forceinline__ int total_tiles(const GemmArgs& g) {
+template <int KIND, class G>
+__device__ __forceinline__ int total_tiles(const G& g) {
   if (KindTraits<KIND>::grouped) return g.mtile_off[g.E] * n_tiles_n<KIND>(g);
   return g.E * n_tiles_m_wgrad<KIND>(g) * n_tiles_n<KIND>(g);
 }
 
-template <int KIND>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& g, int tile) {
+template <int KIND, class G>
+__device__ __forceinline__ Tile decode_tile(const G& g, int tile) {
   Tile t;
   const int NT = n_tiles_n<KIND>(g);
   if (KindTraits<KIND>::grouped) {

@@ -1,0 +1,281 @@
+// gemm_mx.cuh -- persistent block-scaled (MXFP8) grouped GEMM for the
+// forward expert contractions:
+//   kUp    [a|b] = Xq . [Wgq;Wuq]^T   epilogue: a|b bf16 (saved), h = silu(a) b
+//                                     re-quantised to MXFP8 along F (fused)
+//   kDown  Ys    = Hq . Wdq^T         epilogue: bf16 rows
+// (MXFP8 quantisation fused into the grouped-GEMM and SwiGLU datapaths:
+// kucoin page "Cursor's MoK réalise une amélioration des performances de
+// 2,37x sur NVIDIA GB300 NVL72", section 02.)
+//
+// Same structure as the bf16 kernel (gemm.cuh): warp 0 streams 128-byte K
+// slices (128 E4M3 values = 4 scale blocks) of A and B with TMA plus their
+// scale atoms with 1-D bulk copies; one thread of warp 1 copies the stage's
+// scale atoms into TMEM (tcgen05.cp 32x128b.warpx4) and issues four
+// tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256, K=32), the scale
+// byte of each picked by the instruction's scale-factor id.  TMEM holds one
+// 256-column fp32 accumulator plus a 16-column scale slot per stage, so the
+// eight epilogue warps first drain the whole accumulator into registers
+// (128 columns each), release it, and only then do the math and the stores.
+#pragma once
+#include "gemm.cuh"
+#include "mx.cuh"
+
+namespace moe {
+
+constexpr int kMxBK = 128;  // bytes (= E4M3 values) of K per stage
+
+template <int KIND>
+struct MxTraits {
+  static constexpr int stages = (KIND == kUp) ? 3 : 4;
+  static constexpr int epi_warps = 8;
+  static constexpr int threads = 64 + 32 * epi_warps;
+  static constexpr int sf_stage = 1536;  // A atom + two B atoms
+  static constexpr int staging_per_warp = (KIND == kUp) ? (2 * 2048 + 1024) : 2048;
+  static constexpr int staging_off = (stages * (kStageBytes + sf_stage) + 1023) / 1024 * 1024;
+  static constexpr int smem_bytes = staging_off + epi_warps * staging_per_warp + 1024 + 256;
+};
+
+struct MxArgs {
+  CUtensorMap mapA;   // E4M3 activations [rows, K]
+  CUtensorMap mapB0;  // E4M3 weights (Wg / Wd)
+  CUtensorMap mapB1;  // E4M3 weights (Wu) for kUp
+  CUtensorMap mapO0;  // bf16 stores (a|b for kUp, Ys for kDown)
+  CUtensorMap mapO1;  // kUp: E4M3 h stores
+  const uint8_t* sfA;   // scale atoms of A (rows = sorted padded rows)
+  const uint8_t* sfB0;  // scale atoms of B0
+  const uint8_t* sfB1;  // scale atoms of B1
+  uint8_t* sfO;         // kUp: scale atoms of h
+  const int32_t* poff;
+  const int32_t* mtile_off;
+  int32_t* status;
+  uint64_t timeout_ns;
+  int E, d, F;
+};
+
+template <int KIND>
+__device__ __forceinline__ void mx_load_stage(const MxArgs& g, const Tile& t, int kb, uint8_t* sa, uint8_t* sb,
+                                              uint8_t* ssf, uint64_t* bar, uint64_t pol_w, uint64_t pol_a) {
+  const int k0 = kb * kMxBK;
+  if (KIND == kUp) {
+    const int kg = g.d / kMxBK;  // scale atoms per 128-row block
+    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
+    const int brow = t.e * g.F + t.nt * 128;
+    tma_load_2d(sb, &g.mapB0, k0, brow, bar, pol_w);
+    tma_load_2d(sb + kBBytes / 2, &g.mapB1, k0, brow, bar, pol_w);
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + kb) * 512, 512, bar);
+    bulk_load_1d(ssf + 512, g.sfB0 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
+    bulk_load_1d(ssf + 1024, g.sfB1 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
+  } else {  // kDown
+    const int kg = g.F / kMxBK;
+    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
+    const int brow = t.e * g.d + t.nt * BN;
+    tma_load_2d(sb, &g.mapB0, k0, brow, bar, pol_w);
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + kb) * 512, 512, bar);
+    bulk_load_1d(ssf + 512, g.sfB0 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
+    bulk_load_1d(ssf + 1024, g.sfB0 + ((size_t)((brow >> 7) + 1) * kg + kb) * 512, 512, bar);
+  }
+}
+
+// 32 fp32 -> 32 E4M3 bytes of one row into an unswizzled 32x32-byte staging tile.
+__device__ __forceinline__ void stage_row_fp8(uint8_t* buf, int lane, const uint32_t (&q)[8]) {
+  uint4* p = reinterpret_cast<uint4*>(buf + lane * 32);
+  p[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  p[1] = make_uint4(q[4], q[5], q[6], q[7]);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(const __grid_constant__ MxArgs g) {
+  using TR = MxTraits<KIND>;
+  constexpr int S = TR::stages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  uint8_t* sf_base = smem + S * kStageBytes;
+  uint8_t* staging_base = smem + TR::staging_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging_base + TR::epi_warps * TR::staging_per_warp);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, TR::epi_warps);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&g.mapA);
+    tma_prefetch_desc(&g.mapB0);
+    if (KIND == kUp) tma_prefetch_desc(&g.mapB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  WaitCtl wc{g.status, abort_flag, g.timeout_ns};
+  const int ntiles = total_tiles<KIND>(g);
+  const int nkb = (KIND == kUp ? g.d : g.F) / kMxBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t s = 0, ph = 0, issued_mask = 0, last_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const Tile t = decode_tile<KIND>(g, tile);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kStageBytes + TR::sf_stage);
+          uint8_t* sa = stage_base + s * kStageBytes;
+          mx_load_stage<KIND>(g, t, kb, sa, sa + kABytes, sf_base + s * TR::sf_stage, &full[s], pol_w, pol_a);
+          issued_mask |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+          if (++s == S) { s = 0; ph ^= 1; }
+        }
+      }
+      if (!ok) {  // abort: let issued copies land before the CTA may exit
+        for (int st = 0; st < S; ++st) {
+          if (!(issued_mask & (1u << st))) continue;
+          const uint32_t par = (last_par >> st) & 1u;
+          for (uint64_t t0 = globaltimer_ns(); !mbar_try_wait(&full[st], par);)
+            if (globaltimer_ns() - t0 > 50000000ull) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t s = 0, ph = 0, aph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(tempty, aph ^ 1, wc)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stage_base + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint32_t ssf = smem_u32(sf_base + s * TR::sf_stage);
+          const uint32_t sfa_t = tmem_base + BN + s * 16;  // 4 columns
+          const uint32_t sfb_t = sfa_t + 8;                // 8 columns
+          tmem_cp_32x128_x4(sfa_t, sdesc_plain(ssf));
+          tmem_cp_32x128_x4(sfb_t, sdesc_plain(ssf + 512));
+          tmem_cp_32x128_x4(sfb_t + 4, sdesc_plain(ssf + 1024));
+#pragma unroll
+          for (int kk = 0; kk < kMxBK / 32; ++kk) {
+            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_mxf8(tmem_base, ad, bd, idesc_mxf8(BM, BN, 0, 0, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+          if (++s == S) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(tfull);
+        aph ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;            // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
+    uint8_t* stg = staging_base + (warp - 2) * TR::staging_per_warp;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const Tile t = decode_tile<KIND>(g, tile);
+      if (!mbar_wait(tfull, aph, wc)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16);
+      const int rowq = t.row0 + 32 * q;
+      uint32_t acc[4][32];
+      if (KIND == kUp) {  // a cols [64 half, +64), b cols 128 + [64 half, +64)
+        tmem_ld32(tb + half * 64, acc[0]);
+        tmem_ld32(tb + half * 64 + 32, acc[1]);
+        tmem_ld32(tb + 128 + half * 64, acc[2]);
+        tmem_ld32(tb + 128 + half * 64 + 32, acc[3]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tb + half * 128 + c * 32, acc[c]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      aph ^= 1;
+      if (KIND == kUp) {
+        uint32_t sfw = 0;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float a[32], b[32], h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            a[i] = __uint_as_float(acc[c2][i]);
+            b[i] = __uint_as_float(acc[2 + c2][i]);
+            h[i] = a[i] * sigmoidf_(a[i]) * b[i];
+          }
+          const int X = mx_block_exponent(amax32(h));
+          uint32_t hq[8];
+          mx_encode32(h, X, hq);
+          sfw |= (uint32_t)(X + 127) << (8 * c2);
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          stage_row(stg, lane, a);
+          stage_row(stg + kStageChunk, lane, b);
+          stage_row_fp8(stg + 2 * kStageChunk, lane, hq);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int col = t.nt * 128 + half * 64 + c2 * 32;
+            tma_store_2d(&g.mapO0, stg, col, rowq);
+            tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
+            tma_store_2d(&g.mapO1, stg + 2 * kStageChunk, col, rowq);
+            bulk_commit();
+          }
+        }
+        // two consecutive scale bytes of this row (blocks 4 nt + 2 half, +1)
+        const int r = rowq + lane;
+        const int kb = t.nt * 4 + half * 2;
+        *reinterpret_cast<uint16_t*>(g.sfO + sf_atom_offset(r, kb, g.F / 32)) = (uint16_t)sfw;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[c][i]);
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          stage_row(stg, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&g.mapO0, stg, t.nt * BN + half * 128 + c * 32, rowq);
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace moe

@@ -46,6 +46,14 @@ cudaError_t prepare_gemm_fwd(int kind);
 cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_gemm_bwd(int kind);
 
+// MXFP8 (mx_quant.cu, gemm_mx.cu)
+cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st);
+cudaError_t launch_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d, void* q,
+                                void* sf, int grid, cudaStream_t st);
+struct MxArgs;
+cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st);  // kind 0 up, 1 down
+cudaError_t prepare_gemm_mx(int kind);
+
 // Record the detail string moe_last_error() returns on this thread.
 void set_error_detail(const char* msg);
 

@@ -1,0 +1,94 @@
+// mx_quant.cu -- MXFP8 quantisers.
+//
+//  * quant_rows_kernel: a bf16 row-major [rows, K] matrix -> E4M3 [rows, K] +
+//    scale atoms, blocks of 32 along K (the expert weights once per optimiser
+//    step, and the public moe_mx_quantize utility).
+//  * gather_quant_kernel: the forward gather with the quantisation fused in
+//    (MXFP8 activation quantisation inside the dispatch datapath: kucoin page
+//    "Cursor's MoK réalise une amélioration des performances de 2,37x sur
+//    NVIDIA GB300 NVL72", section 02): sorted row r <- MXFP8(X[perm_src[r]/k]),
+//    padding rows -> zero bytes and zero scales.
+// One thread per 32-element block: 64 contiguous input bytes, 32 output bytes.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "mx.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 q = __ldg(s + c);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      v[8 * c + 2 * i] = f.x;
+      v[8 * c + 2 * i + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void quant_block_store(const float* v, uint8_t* q, uint8_t* sfp) {
+  const int X = mx_block_exponent(amax32(v));
+  uint32_t o[8];
+  mx_encode32(v, X, o);
+  uint4* dq = reinterpret_cast<uint4*>(q);
+  dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  *sfp = (uint8_t)(X + 127);
+}
+
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int K,
+                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int kblocks = K >> 5;
+  const int64_t total = rows * kblocks;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / kblocks;
+    const int kb = (int)(i - r * kblocks);
+    float v[32];
+    load_bf16x32_f(src + r * K + kb * 32, v);
+    quant_block_store(v, q + r * K + kb * 32, sf + sf_atom_offset(r, kb, kblocks));
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16* __restrict__ X,
+                                                           const int32_t* __restrict__ perm_src,
+                                                           const int32_t* __restrict__ totals, int k, int d,
+                                                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int kblocks = d >> 5;
+  const int64_t total = (int64_t)totals[0] * kblocks;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / kblocks;
+    const int kb = (int)(i - r * kblocks);
+    const int src = perm_src[r];
+    uint8_t* dq = q + r * d + kb * 32;
+    if (src < 0) {
+      reinterpret_cast<uint4*>(dq)[0] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(dq)[1] = make_uint4(0, 0, 0, 0);
+      sf[sf_atom_offset(r, kb, kblocks)] = 0;
+      continue;
+    }
+    float v[32];
+    load_bf16x32_f(X + (int64_t)(src / k) * d + kb * 32, v);
+    quant_block_store(v, dq, sf + sf_atom_offset(r, kb, kblocks));
+  }
+}
+
+cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st) {
+  quant_rows_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), rows, K,
+                                          reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d, void* q,
+                                void* sf, int grid, cudaStream_t st) {
+  gather_quant_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), perm_src, totals, k, d,
+                                            reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

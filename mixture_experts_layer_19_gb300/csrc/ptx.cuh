@@ -197,6 +197,48 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- block-scaled (MXFP8) pieces
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// Descriptor of a 32-row x 16-byte shared-memory block without swizzle (one
+// scale-factor atom): 8-row core matrices of 128 contiguous bytes.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128 >> 4) << 16;   // leading byte offset (unused: one core matrix along K)
+  d |= (uint64_t)(128 >> 4) << 32;   // stride byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;
+  return d;                          // layout 0: no swizzle
+}
+// Copy one 32x128-bit block from shared memory into TMEM at `taddr`,
+// replicated into all four 32-lane quadrants.
+__device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Instruction descriptor, kind::mxf8f6f4 with E4M3 A/B, fp32 D, UE8M0 scales;
+// sf_id selects which byte of each scale word this MMA's K block uses.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_mn, int b_mn, int sf_id) {
+  return ((uint32_t)sf_id << 4)                 // B scale-factor id
+         | (0u << 7) | (0u << 10)              // A, B format: E4M3
+         | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         (1u << 23)                            // scale format: UE8M0
+         | ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);   // A scale-factor id
+}
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Named barrier over `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares (the test suite checks the library exports them).
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "moe_backward",
             "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
-            "moe_status_string", "moe_last_error", "moe_route_noalloc")
+            "moe_status_string", "moe_last_error", "moe_route_noalloc", "moe_quantize_weights",
+            "moe_mx_quantize")
 
 
 class moe_config_t(ctypes.Structure):
@@ -58,6 +59,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_status_string": [I32],
         "moe_last_error": [],
         "moe_route_noalloc": [I64, I32, I32, FP, VP, VP, VP, VP, VP, VP, P],
+        "moe_quantize_weights": [P, VP, VP, VP, P],
+        "moe_mx_quantize": [VP, I64, I64, VP, VP, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -105,6 +108,25 @@ def minibatch_floor(num_sms: int, tile_m: int, tile_n: int, n_out: int, waves: i
     _check(lib().moe_minibatch_floor(num_sms, tile_m, tile_n, n_out, waves, ctypes.byref(out)),
            "moe_minibatch_floor")
     return out.value
+
+
+def mx_quantize(src: torch.Tensor, stream=None):
+    """MXFP8 of a bf16 [rows, K] CUDA tensor along K: (E4M3 bytes [rows, K] uint8,
+    scale atoms uint8 [ceil(rows/128) * K/128 * 512]) -- layout in include/moe.h."""
+    rows, K = src.shape
+    q = torch.empty((rows, K), dtype=torch.uint8, device=src.device)
+    sf = torch.empty(((rows + 127) // 128) * (K // 128) * 512, dtype=torch.uint8, device=src.device)
+    _check(lib().moe_mx_quantize(_ptr(src), rows, K, _ptr(q), _ptr(sf), _stream(stream)), "moe_mx_quantize")
+    return q, sf
+
+
+def sf_atom_index(rows: int, K: int):
+    """Host copy of the scale-atom layout: flat offsets [rows, K/32] into the sf buffer."""
+    import numpy as np
+    r = np.arange(rows)[:, None]
+    b = np.arange(K // 32)[None, :]
+    atom = (r >> 7) * (K // 128) + (b >> 2)
+    return atom * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3)
 
 
 @dataclass
@@ -201,6 +223,11 @@ class Plan:
                                      _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm_src"]),
                                      _ptr(out["dest"]), _stream(stream)), "moe_get_routing")
         return out
+
+    def quantize_weights(self, Wg, Wu, Wd, stream=None):
+        """MXFP8 plans: fill the plan's E4M3 weight copies (once per weight update)."""
+        _check(lib().moe_quantize_weights(self.handle, _ptr(Wg), _ptr(Wu), _ptr(Wd), _stream(stream)),
+               "moe_quantize_weights")
 
     def device_status(self, stream=None) -> int:
         st = ctypes.c_int32()
