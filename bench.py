@@ -32,6 +32,7 @@ from mixture_experts_layer_19_gb300.workload import LayerShape, make_inputs  # n
 
 METRIC = "MoE layer tokens/s fwd+bwd (BF16, MXFP8) on 1 GB300; % of roofline"
 SHAPE = dict(T=4096, d=7168, F=2048, E=256, k=8)
+MX_SHAPE = dict(T=16384)   # the MXFP8 forward configuration: same layer, 16384 tokens
 ALPHA = 1.1
 SEED = 0
 WORKLOAD = "moe_layer_fwd_bwd_bf16_T4096_d7168_F2048_E256_top8_zipf1.1"
@@ -305,10 +306,72 @@ def bench_gpu(args):
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, k, args.cpu_tokens)
+    if not args.no_mx:
+        del plan, inp, grads, saved, Y
+        torch.cuda.empty_cache()
+        out["mxfp8_forward"] = [bench_mx_forward(args, dev, ws, peaks, alpha) for alpha in (0.0, ALPHA)]
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def bench_mx_forward(args, dev, ws, peaks, alpha):
+    """MXFP8 forward of the layer at T=16384 (uniform or Zipf routing): E4M3
+    gather, block-scaled [a|b] GEMM + SwiGLU + h re-quantisation, block-scaled
+    down GEMM, combine.  Weight quantisation (once per optimiser step) is timed
+    on its own and is not part of the step."""
+    from mixture_experts_layer_19_gb300 import moe
+    T, d, F, E, k = MX_SHAPE["T"], SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
+    inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, device=dev.index,
+                               debug_flags=moe.MOE_DEBUG_TIMING))
+    stream = torch.cuda.current_stream(dev)
+    plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
+    wq = plan.kernel_times()
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+    torch.cuda.synchronize(dev)
+    plan.kernel_times()
+    barrier(ws)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status set in the MXFP8 forward")
+    el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+    kt = plan.kernel_times()
+    R = T * k
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # nominal fp8/bf16 dense ratio x measured bf16
+    up_ms = kt["gemm_mx_up_swiglu"][0] / kt["gemm_mx_up_swiglu"][1]
+    dn_ms = kt["gemm_mx_down"][0] / kt["gemm_mx_down"][1]
+    up_tf = 4.0 * R * d * F / (up_ms / 1e3) / 1e12
+    dn_tf = 2.0 * R * d * F / (dn_ms / 1e3) / 1e12
+    ms = el / args.steps
+    t_tc = 6.0 * R * d * F / (fp8_peak * 1e12) * 1e3
+    t_hbm = (3.0 * E * F * d * (1 + 1 / 32) + T * d * 2 * 2 + T * E * 4) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    res = {
+        "workload": f"moe_layer_fwd_mxfp8_T{T}_d{d}_F{F}_E{E}_top{k}_zipf{alpha:g}",
+        "value": round(ws * T * args.steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+        "dtype": "e4m3+e8m0 (fp32 accumulate, bf16 out)",
+        "roofline": {"kernel": "gemm_mx_up_swiglu", "bound": "tensor", "achieved": round(up_tf, 1),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(up_tf / fp8_peak, 4),
+                     "traffic": None,
+                     "peak_source": peaks["source"] + " bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"},
+        "down_gemm": {"achieved": round(dn_tf, 1), "unit": "TFLOP/s", "frac": round(dn_tf / fp8_peak, 4)},
+        "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
+                           "frac": round(max(t_tc, t_hbm) / ms, 4)},
+        "kernels": {n: {"ms_per_step": round(v[0] / args.steps, 4), "launches": v[1]} for n, v in kt.items()},
+        "weight_quant_ms": round(wq.get("quant_weights", (0.0, 0))[0], 3),
+    }
+    del plan, inp, saved, Y
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_e2e(args, plan, inp, Y, saved, grads, stream, dev, ws):
@@ -405,12 +468,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=48, help="tokens in the timed CPU-oracle sample")
+    ap.add_argument("--cpu-tokens", type=int, default=128, help="tokens in the timed CPU-oracle sample")
     ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
