@@ -18,6 +18,7 @@
 #include "gemm.cuh"
 #include "gemm_mx.cuh"
 #include "kernels.h"
+#include "megakernel.cuh"
 #include "moe.h"
 
 using namespace moe;
@@ -171,6 +172,14 @@ struct moe_plan_s {
   uint8_t *Xq = nullptr, *Xs = nullptr, *Hq = nullptr, *Hs = nullptr;
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
+  // ring-buffer forward megakernel (BF16): ring slots of X and h rows, GPU-local
+  // hand-off counters, minibatch table
+  void* ring_ws = nullptr;
+  void *ring_x = nullptr, *ring_h = nullptr;
+  int* counters = nullptr;  // claim | gathered[NM] | mb_done[NM] | g1_done[NM]
+  int32_t *mb_start = nullptr, *phase_start = nullptr, *n_mb = nullptr;
+  int movers = 0, slots = 0, mbt = 0, cap = 0, nm_max = 0;
+  CUtensorMap m_ring_x, m_ring_h, m_ring_h_st;
   // timing (MOE_DEBUG_TIMING)
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
@@ -350,6 +359,53 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
       return cuda_fail(err, "moe_plan: cudaFuncSetAttribute");
     }
   }
+  {
+    // ring token buffer: `slots` slots of `cap` 128-row tiles; minibatches of
+    // at least `mbt` tiles (the two-wave floor over the compute SMs)
+    p->movers = c.mover_ctas > 0 ? c.mover_ctas : 8;
+    p->slots = c.ring_slots > 0 ? c.ring_slots : 4;
+    if (p->movers >= p->num_sms - 1 || p->slots < 2) {
+      cudaFree(p->ws);
+      delete p;
+      return fail(MOE_ERR_INVALID_ARG, "moe_plan: need 2 <= ring_slots and mover_ctas < SM count - 1");
+    }
+    int64_t mb_rows = c.minibatch_rows;
+    if (mb_rows <= 0) moe_minibatch_floor(p->num_sms - p->movers, BM, 128, c.F, 2, &mb_rows);
+    p->mbt = (int)std::max<int64_t>(1, (mb_rows + BM - 1) / BM);
+    p->cap = 2 * p->mbt;
+    p->nm_max = (int)(p->Rpm / BM);
+    const size_t slot_rows = (size_t)p->cap * BM;
+    size_t m = 0;
+    const size_t o_rx = m; m += align256(p->slots * slot_rows * c.d * 2);
+    const size_t o_rh = m; m += align256(p->slots * slot_rows * c.F * 2);
+    const size_t o_ct = m; m += align256((1 + 3 * (size_t)p->nm_max) * 4);
+    const size_t o_mb = m; m += align256(((size_t)p->nm_max + 1) * 4);
+    const size_t o_ph = m; m += align256((2 * (size_t)p->nm_max + 1) * 4);
+    const size_t o_nm = m; m += 256;
+    err = cudaMalloc(&p->ring_ws, m);
+    if (err != cudaSuccess) {
+      cudaFree(p->ws);
+      delete p;
+      return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of ring buffer failed: ") + cudaGetErrorString(err));
+    }
+    char* rb = static_cast<char*>(p->ring_ws);
+    p->ring_x = rb + o_rx;
+    p->ring_h = rb + o_rh;
+    p->counters = reinterpret_cast<int*>(rb + o_ct);
+    p->mb_start = reinterpret_cast<int32_t*>(rb + o_mb);
+    p->phase_start = reinterpret_cast<int32_t*>(rb + o_ph);
+    p->n_mb = reinterpret_cast<int32_t*>(rb + o_nm);
+    const uint64_t ring_rows = p->slots * slot_rows;
+    ok = map_kmajor(&p->m_ring_x, p->ring_x, c.d, ring_rows) && map_kmajor(&p->m_ring_h, p->ring_h, c.F, ring_rows) &&
+         map_store(&p->m_ring_h_st, p->ring_h, c.F, ring_rows);
+    err = prepare_fwd_megakernel();
+    if (!ok || err != cudaSuccess) {
+      cudaFree(p->ring_ws);
+      cudaFree(p->ws);
+      delete p;
+      return fail(MOE_ERR_CUDA, "moe_plan: ring buffer tensor maps / megakernel attribute");
+    }
+  }
   if (c.prec == MOE_MXFP8) {
     const size_t wbytes = (size_t)c.E * c.F * c.d;  // E4M3 bytes of one weight tensor
     size_t m = 0;
@@ -399,6 +455,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   }
   for (auto e : p->spare_events) cudaEventDestroy(e);
   if (p->mx_ws) cudaFree(p->mx_ws);
+  if (p->ring_ws) cudaFree(p->ring_ws);
   cudaError_t err = cudaFree(p->ws);
   delete p;
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
@@ -484,6 +541,53 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     b.sfB0 = p->Wds;
     err = timed_launch(p, "gemm_mx_down", st, [&] { return launch_gemm_mx(kDown, b, p->num_sms, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 down GEMM launch");
+    const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
+    err = timed_launch(p, "combine", st,
+                       [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
+    return MOE_OK;
+  }
+  if (!ident && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS)) {
+    // one persistent launch: movers fill ring slots, compute CTAs run the
+    // [a|b]+SwiGLU and down tiles minibatch by minibatch
+    const int counters_len = 1 + 3 * p->nm_max;
+    err = timed_launch(p, "plan_minibatches", st, [&] {
+      return launch_plan_minibatches(rp.mtile_off, c.E, p->mbt, p->cap, c.F / 128, c.d / BN, counters_len,
+                                     p->counters, p->mb_start, p->phase_start, p->n_mb, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: minibatch plan launch");
+    MegaArgs m;
+    memset(&m, 0, sizeof(m));
+    m.mapXr = p->m_ring_x;
+    m.mapWg = p->m_Wg_k;
+    m.mapWu = p->m_Wu_k;
+    m.mapWd = p->m_Wd_k;
+    m.mapHr = p->m_ring_h;
+    m.mapHrSt = p->m_ring_h_st;
+    m.mapABSt = m_ab_st;
+    m.mapYsSt = p->m_Ys_st;
+    m.X = reinterpret_cast<const uint4*>(X);
+    m.ring_x = reinterpret_cast<uint4*>(p->ring_x);
+    m.perm_src = rp.perm_src;
+    m.mtile_off = rp.mtile_off;
+    m.mb_start = p->mb_start;
+    m.phase_start = p->phase_start;
+    m.n_mb = p->n_mb;
+    m.claim = p->counters;
+    m.gathered = p->counters + 1;
+    m.mb_done = p->counters + 1 + p->nm_max;
+    m.g1_done = p->counters + 1 + 2 * p->nm_max;
+    m.status = p->status;
+    m.timeout_ns = (uint64_t)c.wait_timeout_ns;
+    m.E = c.E;
+    m.d = c.d;
+    m.F = c.F;
+    m.k = c.k;
+    m.movers = p->movers;
+    m.slots = p->slots;
+    m.slot_rows = p->cap * BM;
+    err = timed_launch(p, "fwd_megakernel", st, [&] { return launch_fwd_megakernel(m, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: megakernel launch");
     const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
     err = timed_launch(p, "combine", st,
                        [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });

@@ -54,6 +54,14 @@ struct MxArgs;
 cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st);  // kind 0 up, 1 down
 cudaError_t prepare_gemm_mx(int kind);
 
+// Ring-buffer forward megakernel (megakernel.cu)
+struct MegaArgs;
+cudaError_t launch_plan_minibatches(const int32_t* mtile_off, int E, int mbt, int cap, int nt1, int nt2,
+                                    int counters_len, int* counters, int32_t* mb_start, int32_t* phase_start,
+                                    int32_t* n_mb, cudaStream_t st);
+cudaError_t launch_fwd_megakernel(const MegaArgs& a, int grid, cudaStream_t st);
+cudaError_t prepare_fwd_megakernel();
+
 // Record the detail string moe_last_error() returns on this thread.
 void set_error_detail(const char* msg);
 

@@ -1,0 +1,430 @@
+// megakernel.cu -- the forward expert pipeline as one persistent, device-driven
+// kernel over a fixed ring token buffer.
+//
+// Mixture-of-Kittens pages (kucoin page "Cursor's MoK réalise une
+// amélioration des performances de 2,37x sur NVIDIA GB300 NVL72", section 02;
+// fluidifia page "Cursor ouvre MoK, un mégakernel qui accélère l'entraînement
+// MoE", section "Comment MoK tente de gratter des millisecondes partout";
+// laura-martel.com blog, section "Ce qu'il fait réellement"):
+//  * the SMs are split into data movers and compute; GPU-local counters hand
+//    work over in both directions;
+//  * tokens are processed in tunable minibatches of at least two full waves
+//    of the expert-grouped GEMM;
+//  * a fixed ring of slots (the "macrobatch" buffer) is filled by dispatch and
+//    reused as soon as a minibatch's results have gone back, so the combine
+//    side of minibatch i overlaps the dispatch of minibatch i+1, with no CPU
+//    in the loop and no allocation inside the layer.
+//
+// Here (one GPU): mover CTAs pull the routed token rows of minibatch i into
+// ring slot i % S (the local form of pull dispatch).  Compute CTAs claim tiles
+// from one global order -- G1(0), G1(1), G2(0), G1(2), G2(1), ... -- where
+// G1(i) are the [a|b] = x [Wg;Wu]^T + SwiGLU tiles of minibatch i (h goes back
+// into the slot, a|b to the saved context) and G2(i) the y = h Wd^T tiles (y to
+// its sorted row: the push-combine residue).  Counters:
+//   gathered[i] : mover CTAs done with minibatch i      (movers  -> G1 tiles)
+//   g1_done[m]  : G1 warps done with 128-row tile m      (G1      -> G2 tiles)
+//   mb_done[i]  : G1 + G2 warps done with minibatch i    (compute -> movers)
+// Every tile only waits on work claimed before it (or on movers that wait on
+// such work), and the launch is cooperative (all CTAs resident), so progress
+// is guaranteed; every wait is also bounded in time (status word + abort).
+// Each tile still reduces its K range in one fixed order: results are
+// bitwise identical to the separate-kernel path.
+//
+// Minibatches are cut on expert boundaries (see plan_minibatches_kernel), so an
+// expert's weights are streamed once unless it alone exceeds a slot.
+#include "gemm.cuh"
+#include "kernels.h"
+#include "megakernel.cuh"
+
+namespace moe {
+
+constexpr int kQueue = 4;          // tiles in flight between producer and consumers
+constexpr int kMegaThreads = 192;  // warp 0 producer, warp 1 MMA, warps 2..5 epilogue
+constexpr int kMegaStaging = 3 * kStageChunk;  // per epilogue warp
+constexpr int kMegaSmem = kStages * kStageBytes + 4 * kMegaStaging + 1024 + 512;
+
+struct Item {
+  int kind;   // 0 = G1, 1 = G2, -1 = stop
+  int mb, gt, nt, e, ring_row0;
+};
+
+// ----------------------------------------------------------------------------
+// Plan: zero the counters, cut minibatches on expert boundaries (>= mbt tiles
+// when possible, <= cap tiles always; an expert larger than cap is split into
+// cap-sized pieces), and lay out the claim order's phase boundaries.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_minibatches_kernel(const int32_t* __restrict__ mtile_off, int E,
+                                                                  int mbt, int cap, int nt1, int nt2,
+                                                                  int counters_len, int* counters,
+                                                                  int32_t* mb_start, int32_t* phase_start,
+                                                                  int32_t* n_mb) {
+  for (int i = threadIdx.x; i < counters_len; i += blockDim.x) counters[i] = 0;
+  if (threadIdx.x != 0) return;
+  int nb = 0, cur = 0, g = 0;
+  mb_start[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    int t = mtile_off[e + 1] - mtile_off[e];
+    while (t > 0) {
+      if (cur + t <= cap) {
+        cur += t;
+        g += t;
+        t = 0;
+        if (cur >= mbt) {
+          mb_start[++nb] = g;
+          cur = 0;
+        }
+      } else if (cur > 0) {
+        mb_start[++nb] = g;
+        cur = 0;
+      } else {
+        g += cap;
+        t -= cap;
+        mb_start[++nb] = g;
+      }
+    }
+  }
+  if (cur > 0) mb_start[++nb] = g;
+  *n_mb = nb;
+  // phases: G1(0), [G1(i), G2(i-1)] for i = 1..nb-1, G2(nb-1)
+  int acc = 0, p = 0;
+  phase_start[p++] = 0;
+  for (int i = 0; i <= nb; ++i) {
+    if (i < nb) {  // G1(i)
+      acc += (mb_start[i + 1] - mb_start[i]) * nt1;
+      phase_start[p++] = acc;
+    }
+    if (i >= 1) {  // G2(i-1)
+      acc += (mb_start[i] - mb_start[i - 1]) * nt2;
+      phase_start[p++] = acc;
+    }
+  }
+}
+
+__device__ __forceinline__ int find_last_le(const int32_t* a, int n, int v) {  // last i in [0,n) with a[i] <= v
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= v) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Item decode_claim(const MegaArgs& g, int nmb, int c) {
+  Item it;
+  const int p = find_last_le(g.phase_start, 2 * nmb, c);
+  const int local = c - g.phase_start[p];
+  if (p == 0) { it.kind = 0; it.mb = 0; }
+  else if (p == 2 * nmb - 1) { it.kind = 1; it.mb = nmb - 1; }
+  else if (p & 1) { it.kind = 0; it.mb = (p + 1) >> 1; }
+  else { it.kind = 1; it.mb = (p >> 1) - 1; }
+  const int m0 = g.mb_start[it.mb];
+  const int mts = g.mb_start[it.mb + 1] - m0;
+  it.nt = local / mts;
+  const int mt = local - it.nt * mts;
+  it.gt = m0 + mt;
+  it.e = find_last_le(g.mtile_off, g.E + 1, it.gt);
+  while (it.e < g.E && g.mtile_off[it.e + 1] <= it.gt) ++it.e;  // skip empty experts
+  it.ring_row0 = (it.mb % g.slots) * g.slot_rows + mt * BM;
+  return it;
+}
+
+// ----------------------------------------------------------------------------
+// Mover CTA: pull minibatch rows into their ring slot (warp per row).
+// ----------------------------------------------------------------------------
+__device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int nvec = g.d / 8;
+  const int nt1 = g.F / 128, nt2 = g.d / BN;
+  WaitCtl wc{g.status, abort_flag, g.timeout_ns};
+  for (int mb = 0; mb < nmb; ++mb) {
+    if (threadIdx.x == 0 && mb >= g.slots) {
+      const int prev = mb - g.slots;
+      const int target = 4 * (g.mb_start[prev + 1] - g.mb_start[prev]) * (nt1 + nt2);
+      wait_counter_geq(g.mb_done + prev, target, wc);
+    }
+    __syncthreads();
+    if (*abort_flag) return;
+    const int row_base = g.mb_start[mb] * BM;
+    const int nrows = (g.mb_start[mb + 1] - g.mb_start[mb]) * BM;
+    const size_t slot_base = (size_t)(mb % g.slots) * g.slot_rows;
+    for (int i = blockIdx.x * nwarps + warp; i < nrows; i += g.movers * nwarps) {
+      const int src = g.perm_src[row_base + i];
+      uint4* dst = g.ring_x + (slot_base + i) * nvec;
+      if (src < 0) {
+        for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      } else {
+        const uint4* s = g.X + (size_t)(src / g.k) * nvec;
+        for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(s + v);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      fence_proxy_async_global();
+      red_release_gpu_add(g.gathered + mb, 1);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_constant__ MegaArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  uint8_t* staging_base = smem + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging_base + 4 * kMegaStaging);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* qfull = tempty + 2;
+  uint64_t* qempty = qfull + kQueue;
+  Item* queue = reinterpret_cast<Item*>(qempty + kQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(queue + kQueue);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nmb = *g.n_mb;
+  if (threadIdx.x == 0) *abort_flag = 0;
+  __syncthreads();
+  if ((int)blockIdx.x < g.movers) {
+    mover_loop(g, nmb, abort_flag);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    for (int q = 0; q < kQueue; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], 5);  // MMA thread + 4 epilogue warps
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  WaitCtl wc{g.status, abort_flag, g.timeout_ns};
+  const int nt1 = g.F / 128;
+  const int total = g.phase_start[2 * nmb];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------- claimer + producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t s = 0, ph = 0, qi = 0, qph = 0, issued_mask = 0, last_par = 0;
+      bool ok = true;
+      while (ok) {
+        const int c = atomicAdd(g.claim, 1);
+        Item it;
+        if (c >= total) {
+          it.kind = -1;
+        } else {
+          it = decode_claim(g, nmb, c);
+          ok = it.kind == 0 ? wait_counter_geq(g.gathered + it.mb, g.movers, wc)
+                            : wait_counter_geq(g.g1_done + it.gt, 4 * nt1, wc);
+          fence_proxy_async_global();
+          if (!ok) it.kind = -1;
+        }
+        if (!mbar_wait(&qempty[qi], qph ^ 1, wc)) break;
+        queue[qi] = it;
+        mbar_arrive(&qfull[qi]);
+        if (++qi == kQueue) { qi = 0; qph ^= 1; }
+        if (it.kind < 0) break;
+        const int nkb = it.kind == 0 ? g.d / BK : g.F / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          uint8_t* sa = stage_base + s * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          const int k0 = kb * BK;
+          if (it.kind == 0) {
+            tma_load_2d(sa, &g.mapXr, k0, it.ring_row0, &full[s], pol_a);
+            tma_load_2d(sb, &g.mapWg, k0, it.e * g.F + it.nt * 128, &full[s], pol_w);
+            tma_load_2d(sb + kBBytes / 2, &g.mapWu, k0, it.e * g.F + it.nt * 128, &full[s], pol_w);
+          } else {
+            tma_load_2d(sa, &g.mapHr, k0, it.ring_row0, &full[s], pol_a);
+            tma_load_2d(sb, &g.mapWd, k0, it.e * g.d + it.nt * BN, &full[s], pol_w);
+          }
+          issued_mask |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+      if (!ok) {
+        for (int st = 0; st < kStages; ++st) {
+          if (!(issued_mask & (1u << st))) continue;
+          const uint32_t par = (last_par >> st) & 1u;
+          for (uint64_t t0 = globaltimer_ns(); !mbar_try_wait(&full[st], par);)
+            if (globaltimer_ns() - t0 > 50000000ull) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, 0, 0);
+      uint32_t s = 0, ph = 0, acc = 0, aph = 0, qi = 0, qph = 0;
+      for (;;) {
+        if (!mbar_wait(&qfull[qi], qph, wc)) break;
+        const Item it = queue[qi];
+        mbar_arrive(&qempty[qi]);
+        if (++qi == kQueue) { qi = 0; qph ^= 1; }
+        if (it.kind < 0) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        const int nkb = it.kind == 0 ? g.d / BK : g.F / BK;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stage_base + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d_tmem, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------- epilogue
+    const int q = warp & 3;
+    uint8_t* stg = staging_base + (warp - 2) * kMegaStaging;
+    uint32_t acc = 0, aph = 0, qi = 0, qph = 0;
+    int chunk_ctr = 0;
+    for (;;) {
+      if (!mbar_wait(&qfull[qi], qph, wc)) break;
+      const Item it = queue[qi];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty[qi]);
+      if (++qi == kQueue) { qi = 0; qph ^= 1; }
+      if (it.kind < 0) break;
+      if (!mbar_wait(&tfull[acc], aph, wc)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN;
+      const int srow = it.gt * BM + 32 * q;        // sorted padded row of this warp's slab
+      const int rrow = it.ring_row0 + 32 * q;      // ring row of this warp's slab
+      if (it.kind == 0) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tbase + c * 32, ra);
+          tmem_ld32(tbase + 128 + c * 32, rb);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          float a[32], b[32], h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            a[i] = __uint_as_float(ra[i]);
+            b[i] = __uint_as_float(rb[i]);
+            h[i] = a[i] * sigmoidf_(a[i]) * b[i];
+          }
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          stage_row(stg, lane, a);
+          stage_row(stg + kStageChunk, lane, b);
+          stage_row(stg + 2 * kStageChunk, lane, h);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int col = it.nt * 128 + c * 32;
+            tma_store_2d(&g.mapABSt, stg, col, srow);
+            tma_store_2d(&g.mapABSt, stg + kStageChunk, g.F + col, srow);
+            tma_store_2d(&g.mapHrSt, stg + 2 * kStageChunk, col, rrow);
+            bulk_commit();
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t rv[32];
+          tmem_ld32(tbase + c * 32, rv);
+          tmem_ld_wait();
+          if (c == 7) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rv[i]);
+          uint8_t* buf = stg + (chunk_ctr & 1) * kStageChunk;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row(buf, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&g.mapYsSt, buf, it.nt * BN + c * 32, srow);
+            bulk_commit();
+          }
+          ++chunk_ctr;
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+      // results visible before the hand-off counters move
+      if (lane == 0) {
+        bulk_wait<0>();
+        fence_proxy_async_global();
+        if (it.kind == 0) red_release_gpu_add(g.g1_done + it.gt, 1);
+        red_release_gpu_add(g.mb_done + it.mb, 1);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ============================================================================ launchers
+cudaError_t launch_plan_minibatches(const int32_t* mtile_off, int E, int mbt, int cap, int nt1, int nt2,
+                                    int counters_len, int* counters, int32_t* mb_start, int32_t* phase_start,
+                                    int32_t* n_mb, cudaStream_t st) {
+  plan_minibatches_kernel<<<1, 1024, 0, st>>>(mtile_off, E, mbt, cap, nt1, nt2, counters_len, counters, mb_start,
+                                               phase_start, n_mb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_megakernel(const MegaArgs& a, int grid, cudaStream_t st) {
+  void* args[] = {const_cast<MegaArgs*>(&a)};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fwd_megakernel), dim3(grid), dim3(kMegaThreads),
+                                     args, kMegaSmem, st);
+}
+
+cudaError_t prepare_fwd_megakernel() {
+  return cudaFuncSetAttribute(fwd_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaSmem);
+}
+
+size_t mega_args_size() { return sizeof(MegaArgs); }
+
+}  // namespace moe

@@ -77,6 +77,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// ---------------------------------------------------------------- GPU-scope counters
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders generic-proxy accesses with async-proxy (TMA) accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until *p >= target (acquire).  Gives up, recording a timeout,
+// after `timeout_ns`; also gives up as soon as any CTA has recorded an error
+// in the status word or this CTA raised its abort flag.
+__device__ __forceinline__ bool wait_counter_geq(const int* p, int target, const WaitCtl& w) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  uint64_t deadline = 0;
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 31u) == 0) {
+      if (*w.abort) return false;
+      if (w.status && *reinterpret_cast<volatile int32_t*>(w.status) != 0) {
+        *w.abort = 1;
+        return false;
+      }
+      const uint64_t now = globaltimer_ns();
+      if (deadline == 0) deadline = now + w.timeout_ns;
+      else if (now > deadline) {
+        raise_abort(w, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -141,6 +141,36 @@ def test_bitwise_deterministic_over_10_runs():
                     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("mb_rows,slots,movers", [(0, 0, 0), (128, 2, 1), (256, 3, 5), (1024, 2, 2)])
+def test_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers):
+    """The ring-buffer megakernel (movers, minibatches, GPU-local counters) must
+    give exactly the separate-kernel results: same tiles, same K order.  Small
+    minibatches and few slots force many minibatches and ring wrap-around."""
+    T, d, F, E, k = 700, 512, 512, 24, 4
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=31, alpha=1.1)
+    ring = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, minibatch_rows=mb_rows, ring_slots=slots,
+                               mover_ctas=movers))
+    sep = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS)
+    Ya, sa = ring.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    Yb, sb = sep.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    ga = ring.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], sa)
+    gb = sep.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], sb)
+    torch.cuda.synchronize()
+    assert ring.device_status() == 0 and sep.device_status() == 0
+    assert torch.equal(Ya, Yb)
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        assert torch.equal(ga[key], gb[key]), key
+    Yr, _ = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    assert rel_err(Ya, Yr) <= BF16_TOL
+
+
+def test_ring_config_is_validated():
+    with pytest.raises(moe.MoEError):
+        moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, ring_slots=1))
+    with pytest.raises(moe.MoEError):
+        moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, mover_ctas=100000))
+
+
 def test_zero_tokens_is_noop_and_zero_weight_grads():
     d, F, E, k = 256, 256, 4, 2
     plan = _plan(16, d, F, E, k)
