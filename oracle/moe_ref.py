@@ -164,9 +164,10 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
     arrays -- storage only, for full-size layers on a sub-batch of tokens.
 
     MXFP8 emulation (ctx["mx"]): dY along d and Wd along d for u = Wd^T dY;
-    dA, dB along F and Wg, Wu along F for dX; for the weight gradients each
-    operand is quantised along the tokens of its expert (sorted order, padded
-    to a multiple of 32 with zeros): dY and w*h for dWd, dA/dB and x for dWg/dWu.
+    dA, dB along F and Wg, Wu along F for dX.  The weight gradients take the
+    unquantised operands (dY, w*h, dA/dB, x): MXFP8 covers the GEMMs that stream
+    weights; the weight-gradient GEMMs, whose cost is writing dW, stay in the
+    higher precision.
     """
     dY = np.asarray(dY, dtype=np.float64)
     X = np.asarray(X, dtype=np.float64)
@@ -203,10 +204,10 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
         dx = _q(da, 1, mx) @ _q(wg, 0, mx) + _q(db, 1, mx) @ _q(wu, 0, mx)
         np.add.at(dX, tok, dx)
         # weight gradients: K = the expert's tokens in sorted order
-        dWd[e] = _q(dY[tok], 0, mx).T @ _q(wr * h, 0, mx)
-        xs = _q(X[tok], 0, mx)
-        dWg[e] = _q(da, 0, mx).T @ xs
-        dWu[e] = _q(db, 0, mx).T @ xs
+        dWd[e] = dY[tok].T @ (wr * h)
+        xs = X[tok]
+        dWg[e] = da.T @ xs
+        dWu[e] = db.T @ xs
     dg = dg.reshape(T, k)
     s = np.sum(w * dg, axis=1, keepdims=True)
     dsel = w * (dg - s)
@@ -287,9 +288,8 @@ def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False):
     sa = sigmoid(a)
     da = dh * b * sa * (1.0 + a * (1.0 - sa))
     db = dh * silu(a)
-    dWd = _q(dY, 0, mx).T @ _q(wr * h, 0, mx)
-    xs = _q(X, 0, mx)
-    return _q(da, 0, mx).T @ xs, _q(db, 0, mx).T @ xs, dWd
+    dWd = dY.T @ (wr * h)
+    return da.T @ X, db.T @ X, dWd
 
 
 # ----------------------------------------------------------------------------

@@ -145,9 +145,12 @@ def test_mx_exact_inputs_only_intermediates_add_error():
     assert 0 < rel < 2 ** -4
     g0 = moe_ref.backward(dY, X, L, Wg, Wu, Wd, c0)
     g1 = moe_ref.backward(dY, X, L, Wg, Wu, Wd, c1)
-    for key in ("dX", "dWg", "dWu", "dWd"):
-        r = np.abs(g1[key] - g0[key]).max() / np.abs(g0[key]).max()
-        assert 0 < r < 2 ** -3, (key, r)
+    # dX differs only through dA/dB re-quantised along F
+    r = np.abs(g1["dX"] - g0["dX"]).max() / np.abs(g0["dX"]).max()
+    assert 0 < r < 2 ** -3, r
+    # weight gradients take unquantised operands, which are exact here: identical
+    for key in ("dWg", "dWu", "dWd"):
+        assert np.array_equal(g1[key], g0[key]), key
     # dg uses u (exact operands) and the unquantised h: identical
     assert np.array_equal(g0["dg"], g1["dg"])
 
