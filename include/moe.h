@@ -69,7 +69,7 @@ typedef struct {
   int32_t F;              /* expert FFN width; multiple of 256 */
   int32_t E;              /* experts, k <= E <= 1024 */
   int32_t k;              /* experts per token, 1 <= k <= 32 */
-  int32_t prec;           /* moe_precision_t; MOE_MXFP8: forward only (see moe_quantize_weights) */
+  int32_t prec;           /* moe_precision_t (MOE_MXFP8 needs moe_quantize_weights) */
   int32_t minibatch_rows; /* rows per ring slot; 0 = two-wave floor (moe_minibatch_floor) */
   int32_t ring_slots;     /* ring buffer slots; 0 = default */
   int32_t mover_ctas;     /* CTAs that gather (data movers); 0 = default */
@@ -84,8 +84,9 @@ typedef struct moe_plan_s* moe_plan_t;
  * workspace for T <= T_max, and returns it in *out (caller frees with
  * moe_plan_destroy).  Supported: d % 256 == 0, F % 256 == 0, 1 <= k <= 32,
  * k <= E <= 1024, 1 <= T_max <= 2^20, prec MOE_BF16 or MOE_MXFP8 (an MXFP8
- * plan also holds E4M3 copies of the weights; its moe_backward returns
- * MOE_ERR_UNSUPPORTED).  Otherwise
+ * plan also holds E4M3 copies of the weights in both orientations: MXFP8
+ * forward GEMMs and MXFP8 dgrad GEMMs; its weight gradients are computed from
+ * the bf16 operands, since writing dW in bf16 bounds those GEMMs).  Otherwise
  * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG; allocation failure MOE_ERR_OOM. */
 moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out);
 
@@ -121,11 +122,13 @@ moe_status_t moe_backward(moe_plan_t plan, int64_t T, const void* dY, const void
                           moe_stream_t stream);
 
 /* MXFP8 plans only: quantise the bf16 expert weights into the plan's E4M3
- * copies (once per optimiser step, outside the layer's timing).  Wg, Wu are
- * quantised along d and Wd along F, each in blocks of 32 with one E8M0 scale
- * (the layout of moe_mx_quantize).  Must precede moe_forward on an MXFP8
- * plan (moe_forward then reads the plan's copies; the bf16 pointers it is
- * given are not read).  Enqueued on `stream`.  MXFP8 activation quantisation
+ * copies (once per optimiser step, outside the layer's timing).  Forward
+ * orientation: Wg, Wu along d, Wd along F; backward orientation (transposed
+ * copies for the dgrad GEMMs): Wd[e]^T along d, Wg[e]^T and Wu[e]^T along F;
+ * blocks of 32 with one E8M0 scale (the layout of moe_mx_quantize).  Must
+ * precede moe_forward / moe_backward on an MXFP8 plan (their weight-streaming
+ * GEMMs then read the plan's copies).  Enqueued on `stream`.  MXFP8 activation
+ * quantisation
  * is fused into the dispatch / GEMM / SwiGLU datapaths (kucoin page "Cursor's
  * MoK réalise une amélioration des performances de 2,37x sur NVIDIA GB300
  * NVL72", section 02); the format itself is OCP Microscaling v1.0 MXFP8. */

@@ -170,8 +170,12 @@ struct moe_plan_s {
   void* mx_ws = nullptr;
   uint8_t *Wgq = nullptr, *Wuq = nullptr, *Wdq = nullptr, *Wgs = nullptr, *Wus = nullptr, *Wds = nullptr;
   uint8_t *Xq = nullptr, *Xs = nullptr, *Hq = nullptr, *Hs = nullptr;
+  // backward orientation (quantised along the dgrad GEMMs' K) and E4M3 dA|dB
+  uint8_t *WdTq = nullptr, *WgTq = nullptr, *WuTq = nullptr, *WdTs = nullptr, *WgTs = nullptr, *WuTs = nullptr;
+  uint8_t *dABq = nullptr, *dABs = nullptr;
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
+  CUtensorMap m_WdTq, m_WgTq, m_WuTq, m_dABq_k, m_dABq_st;
   // ring-buffer forward megakernel (BF16): ring slots of X and h rows, GPU-local
   // hand-off counters, minibatch table
   void* ring_ws = nullptr;
@@ -315,7 +319,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   const size_t o_dyg = o;   o += align256((size_t)p->Rpm * c.d * 2);
   const size_t o_dab = o;   o += align256((size_t)p->Rpm * 2 * c.F * 2);
   const size_t o_wh = o;    o += align256((size_t)p->Rpm * c.F * 2);
-  const size_t o_dgp = o;   o += align256((size_t)p->Rpm * (c.F / BN) * 4);
+  const size_t o_dgp = o;   o += align256((size_t)p->Rpm * (c.F / 128) * 4);  // <u, h> partials
   err = cudaMalloc(&p->ws, o);
   if (err != cudaSuccess) {
     delete p;
@@ -352,7 +356,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   }
   for (int kind = 0; kind < 6; ++kind) {
     err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
-    if (err == cudaSuccess && kind < 2 && c.prec == MOE_MXFP8) err = prepare_gemm_mx(kind);
+    if (err == cudaSuccess && kind < 4 && c.prec == MOE_MXFP8) err = prepare_gemm_mx(kind);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
       delete p;
@@ -419,6 +423,14 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_xs = m;  m += align256((size_t)R * c.d / 32);
     const size_t o_hq = m;  m += align256((size_t)R * c.F);
     const size_t o_hs = m;  m += align256((size_t)R * c.F / 32);
+    const size_t o_wdt = m; m += align256(wbytes);
+    const size_t o_wgt = m; m += align256(wbytes);
+    const size_t o_wut = m; m += align256(wbytes);
+    const size_t o_wdts = m; m += align256(wbytes / 32);
+    const size_t o_wgts = m; m += align256(wbytes / 32);
+    const size_t o_wuts = m; m += align256(wbytes / 32);
+    const size_t o_dabq = m; m += align256((size_t)R * 2 * c.F);
+    const size_t o_dabs = m; m += align256((size_t)R * 2 * c.F / 32);
     err = cudaMalloc(&p->mx_ws, m);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -430,10 +442,16 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->Wgq = mb + o_wgq; p->Wuq = mb + o_wuq; p->Wdq = mb + o_wdq;
     p->Wgs = mb + o_wgs; p->Wus = mb + o_wus; p->Wds = mb + o_wds;
     p->Xq = mb + o_xq; p->Xs = mb + o_xs; p->Hq = mb + o_hq; p->Hs = mb + o_hs;
+    p->WdTq = mb + o_wdt; p->WgTq = mb + o_wgt; p->WuTq = mb + o_wut;
+    p->WdTs = mb + o_wdts; p->WgTs = mb + o_wgts; p->WuTs = mb + o_wuts;
+    p->dABq = mb + o_dabq; p->dABs = mb + o_dabs;
     const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
     ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, c.d, EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, c.d, EF) &&
          map_fp8_kmajor(&p->m_Wdq, p->Wdq, c.F, Ed, BN) && map_fp8_kmajor(&p->m_Xq, p->Xq, c.d, R) &&
-         map_fp8_kmajor(&p->m_Hq_k, p->Hq, c.F, R) && map_fp8_store(&p->m_Hq_st, p->Hq, c.F, R);
+         map_fp8_kmajor(&p->m_Hq_k, p->Hq, c.F, R) && map_fp8_store(&p->m_Hq_st, p->Hq, c.F, R) &&
+         map_fp8_kmajor(&p->m_WdTq, p->WdTq, c.d, EF, BN) && map_fp8_kmajor(&p->m_WgTq, p->WgTq, c.F, Ed, BN) &&
+         map_fp8_kmajor(&p->m_WuTq, p->WuTq, c.F, Ed, BN) &&
+         map_fp8_kmajor(&p->m_dABq_k, p->dABq, 2 * c.F, R) && map_fp8_store(&p->m_dABq_st, p->dABq, 2 * c.F, R);
     if (!ok) {
       cudaFree(p->mx_ws);
       cudaFree(p->ws);
@@ -630,8 +648,8 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   const moe_config_t& c = p->cfg;
   if (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)
     return fail(MOE_ERR_UNSUPPORTED, "moe_backward: identity-expert debug mode has no backward");
-  if (c.prec == MOE_MXFP8)
-    return fail(MOE_ERR_UNSUPPORTED, "moe_backward: the MXFP8 backward is not built; use a MOE_BF16 plan");
+  if (c.prec == MOE_MXFP8 && !p->weights_quantized)
+    return fail(MOE_ERR_INVALID_ARG, "moe_backward: MXFP8 plan needs moe_quantize_weights first");
   if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_backward: T outside [0, T_max]");
   if (!dWg || !dWu || !dWd || !Wg || !Wu || !Wd)
     return fail(MOE_ERR_INVALID_ARG, "moe_backward: null weight or weight-gradient pointer");
@@ -677,7 +695,51 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     return launch_gather(dY, X, rp.perm_src, rp.totals, c.k, c.d, p->dYg, p->Xg, p->num_sms * 8, st);
   });
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: gather launch");
-  {
+  const bool mx = c.prec == MOE_MXFP8;
+  if (mx) {
+    // MXFP8 dgrad: dY quantised along d as it is gathered; u GEMM against
+    // Wd^T (E4M3 along d) with dA|dB re-quantised along F in its epilogue;
+    // dx GEMM against [Wg^T; Wu^T] (E4M3 along F).  The weight gradients
+    // below use the bf16 operands.
+    err = timed_launch(p, "gather_quant_dy", st, [&] {
+      return launch_gather_quant(dY, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dY gather launch");
+    MxArgs u;
+    memset(&u, 0, sizeof(u));
+    u.poff = rp.poff;
+    u.mtile_off = rp.mtile_off;
+    u.status = p->status;
+    u.timeout_ns = (uint64_t)c.wait_timeout_ns;
+    u.E = c.E;
+    u.d = c.d;
+    u.F = c.F;
+    MxArgs x = u;
+    u.mapA = p->m_Xq;
+    u.mapB0 = p->m_WdTq;
+    u.mapO0 = p->m_dAB_st;
+    u.mapO1 = p->m_dABq_st;
+    u.mapO2 = p->m_wH_st;
+    u.sfA = p->Xs;
+    u.sfB0 = p->WdTs;
+    u.sfO = p->dABs;
+    u.ab = ab;
+    u.perm_src = rp.perm_src;
+    u.wts = rp.w;
+    u.dgp = p->dgp;
+    err = timed_launch(p, "gemm_mx_bwd_u_swiglu", st, [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: MXFP8 u GEMM launch");
+    x.mapA = p->m_dABq_k;
+    x.mapB0 = p->m_WgTq;
+    x.mapB1 = p->m_WuTq;
+    x.mapO0 = p->m_Ys_st;
+    x.sfA = p->dABs;
+    x.sfB0 = p->WgTs;
+    x.sfB1 = p->WuTs;
+    err = timed_launch(p, "gemm_mx_bwd_dx", st, [&] { return launch_gemm_mx(kBwdX, x, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: MXFP8 dx GEMM launch");
+  }
+  if (!mx) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dYg_k;
     a.mapB0 = p->m_Wd_mn;
@@ -690,7 +752,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     err = timed_launch(p, "gemm_bwd_u_swiglu", st, [&] { return launch_gemm_bwd(kBwdU, a, p->num_sms, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: u GEMM launch");
   }
-  {
+  if (!mx) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dAB_k;
     a.mapB0 = p->m_Wg_mn;
@@ -705,7 +767,9 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx reduce launch");
   const int rgrid = (int)std::min<int64_t>((T + 7) / 8, (int64_t)p->num_sms * 8);
   err = timed_launch(p, "router_grad", st, [&] {
-    return launch_router_grad(p->dgp, rp.dest, rp.idx, rp.w, Ti, c.k, c.E, c.F / BN, dg, dlogits, rgrid, st);
+    // <u, h> partials: one per 256 columns (bf16 u GEMM) or per 128 (MXFP8 u GEMM)
+    return launch_router_grad(p->dgp, rp.dest, rp.idx, rp.w, Ti, c.k, c.E, mx ? c.F / 128 : c.F / BN, dg, dlogits,
+                              rgrid, st);
   });
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: router gradient launch");
   {
@@ -781,6 +845,10 @@ moe_status_t moe_quantize_weights(moe_plan_t p, const void* Wg, const void* Wu, 
     cudaError_t e = launch_quant_rows(Wg, EF, c.d, p->Wgq, p->Wgs, grid, st);
     if (e == cudaSuccess) e = launch_quant_rows(Wu, EF, c.d, p->Wuq, p->Wus, grid, st);
     if (e == cudaSuccess) e = launch_quant_rows(Wd, Ed, c.F, p->Wdq, p->Wds, grid, st);
+    // backward orientation: Wd[e]^T [F, d] along d; Wg[e]^T, Wu[e]^T [d, F] along F
+    if (e == cudaSuccess) e = launch_quant_transpose(Wd, c.E, c.d, c.F, p->WdTq, p->WdTs, grid, st);
+    if (e == cudaSuccess) e = launch_quant_transpose(Wg, c.E, c.F, c.d, p->WgTq, p->WgTs, grid, st);
+    if (e == cudaSuccess) e = launch_quant_transpose(Wu, c.E, c.F, c.d, p->WuTq, p->WuTs, grid, st);
     return e;
   });
   if (err != cudaSuccess) return cuda_fail(err, "moe_quantize_weights: launch");

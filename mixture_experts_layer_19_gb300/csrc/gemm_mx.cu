@@ -16,8 +16,20 @@ static cudaError_t prepare_mx_one() {
 }
 
 cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st) {
-  return kind == kUp ? launch_mx_one<kUp>(a, grid, st) : launch_mx_one<kDown>(a, grid, st);
+  switch (kind) {
+    case kUp: return launch_mx_one<kUp>(a, grid, st);
+    case kDown: return launch_mx_one<kDown>(a, grid, st);
+    case kBwdU: return launch_mx_one<kBwdU>(a, grid, st);
+    default: return launch_mx_one<kBwdX>(a, grid, st);
+  }
 }
-cudaError_t prepare_gemm_mx(int kind) { return kind == kUp ? prepare_mx_one<kUp>() : prepare_mx_one<kDown>(); }
+cudaError_t prepare_gemm_mx(int kind) {
+  switch (kind) {
+    case kUp: return prepare_mx_one<kUp>();
+    case kDown: return prepare_mx_one<kDown>();
+    case kBwdU: return prepare_mx_one<kBwdU>();
+    default: return prepare_mx_one<kBwdX>();
+  }
+}
 
 }  // namespace moe

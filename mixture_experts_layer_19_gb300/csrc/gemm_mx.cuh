@@ -24,13 +24,19 @@ namespace moe {
 
 constexpr int kMxBK = 128;  // bytes (= E4M3 values) of K per stage
 
+// Kinds: kUp, kDown (forward); kBwdU  u = dYq . WdTq^T with the SwiGLU-backward
+// epilogue (dA, dB, w h in bf16 for the weight gradients, dA|dB re-quantised
+// along F for the dx GEMM, <u, h> partials); kBwdX  dx = dABq . [WgTq;WuTq]^T.
+// WdTq [E*F, d], WgTq / WuTq [E*d, F] are the weights' backward orientation,
+// quantised along their K (the dgrad GEMMs' K), so every operand is K-major.
 template <int KIND>
 struct MxTraits {
-  static constexpr int stages = (KIND == kUp) ? 3 : 4;
+  static constexpr int stages = (KIND == kUp || KIND == kBwdU) ? 3 : 4;
   static constexpr int epi_warps = 8;
   static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int sf_stage = 1536;  // A atom + two B atoms
-  static constexpr int staging_per_warp = (KIND == kUp) ? (2 * 2048 + 1024) : 2048;
+  static constexpr int staging_per_warp =
+      (KIND == kUp) ? (2 * 2048 + 1024) : (KIND == kBwdU) ? (3 * 2048 + 2 * 1024) : 2048;
   static constexpr int staging_off = (stages * (kStageBytes + sf_stage) + 1023) / 1024 * 1024;
   static constexpr int smem_bytes = staging_off + epi_warps * staging_per_warp + 1024 + 256;
 };
@@ -40,11 +46,16 @@ struct MxArgs {
   CUtensorMap mapB0;  // E4M3 weights (Wg / Wd)
   CUtensorMap mapB1;  // E4M3 weights (Wu) for kUp
   CUtensorMap mapO0;  // bf16 stores (a|b for kUp, Ys for kDown)
-  CUtensorMap mapO1;  // kUp: E4M3 h stores
+  CUtensorMap mapO1;  // E4M3 stores (kUp: h; kBwdU: dA|dB)
+  CUtensorMap mapO2;  // kBwdU: bf16 w h stores
   const uint8_t* sfA;   // scale atoms of A (rows = sorted padded rows)
   const uint8_t* sfB0;  // scale atoms of B0
   const uint8_t* sfB1;  // scale atoms of B1
-  uint8_t* sfO;         // kUp: scale atoms of h
+  uint8_t* sfO;         // scale atoms of the E4M3 output (kUp: h, K = F; kBwdU: dA|dB, K = 2F)
+  const __nv_bfloat16* ab;   // kBwdU: saved a|b [rows, 2F]
+  const int32_t* perm_src;   // kBwdU
+  const float* wts;          // kBwdU
+  float* dgp;                // kBwdU: [rows, F/128] partial <u, h> per 128 columns
   const int32_t* poff;
   const int32_t* mtile_off;
   int32_t* status;
@@ -65,14 +76,27 @@ __device__ __forceinline__ void mx_load_stage(const MxArgs& g, const Tile& t, in
     bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + kb) * 512, 512, bar);
     bulk_load_1d(ssf + 512, g.sfB0 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
     bulk_load_1d(ssf + 1024, g.sfB1 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
-  } else {  // kDown
-    const int kg = g.F / kMxBK;
+  } else if (KIND == kDown || KIND == kBwdU) {
+    // kDown: A = Hq (K = F), B = Wdq rows e*d + n;  kBwdU: A = dYq (K = d), B = WdTq rows e*F + n
+    const int K = (KIND == kDown) ? g.F : g.d;
+    const int kg = K / kMxBK;
     tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
-    const int brow = t.e * g.d + t.nt * BN;
+    const int brow = (KIND == kDown ? t.e * g.d : t.e * g.F) + t.nt * BN;
     tma_load_2d(sb, &g.mapB0, k0, brow, bar, pol_w);
     bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + kb) * 512, 512, bar);
     bulk_load_1d(ssf + 512, g.sfB0 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
     bulk_load_1d(ssf + 1024, g.sfB0 + ((size_t)((brow >> 7) + 1) * kg + kb) * 512, 512, bar);
+  } else {  // kBwdX: A = dABq (K = 2F); B = WgTq for k < F, WuTq for k >= F (rows e*d + n, K = F)
+    const int kga = (2 * g.F) / kMxBK, kgb = g.F / kMxBK;
+    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
+    const bool up = k0 >= g.F;
+    const int kw = up ? k0 - g.F : k0;
+    const int brow = t.e * g.d + t.nt * BN;
+    tma_load_2d(sb, up ? &g.mapB1 : &g.mapB0, kw, brow, bar, pol_w);
+    const uint8_t* sfb = up ? g.sfB1 : g.sfB0;
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kga + kb) * 512, 512, bar);
+    bulk_load_1d(ssf + 512, sfb + ((size_t)(brow >> 7) * kgb + kw / kMxBK) * 512, 512, bar);
+    bulk_load_1d(ssf + 1024, sfb + ((size_t)((brow >> 7) + 1) * kgb + kw / kMxBK) * 512, 512, bar);
   }
 }
 
@@ -115,7 +139,7 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&g.mapA);
     tma_prefetch_desc(&g.mapB0);
-    if (KIND == kUp) tma_prefetch_desc(&g.mapB1);
+    if (KIND == kUp || KIND == kBwdX) tma_prefetch_desc(&g.mapB1);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -127,7 +151,7 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
   const uint32_t tmem_base = *tmem_slot;
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
   const int ntiles = total_tiles<KIND>(g);
-  const int nkb = (KIND == kUp ? g.d : g.F) / kMxBK;
+  const int nkb = (KIND == kUp || KIND == kBwdU ? g.d : KIND == kDown ? g.F : 2 * g.F) / kMxBK;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -200,6 +224,76 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16);
       const int rowq = t.row0 + 32 * q;
+      if (KIND == kBwdU) {
+        // u chunk by chunk (the accumulator is released after the last one):
+        // dh = w u, da = dh b s(a)(1 + a(1 - s(a))), db = dh silu(a); outputs
+        // dA|dB and w h in bf16 (weight gradients), dA|dB in E4M3 along F (dx
+        // GEMM) and the row's <u, h> over this warp's 128 columns.
+        const int r = rowq + lane;
+        const int src = __ldg(g.perm_src + r);
+        const float wr = src >= 0 ? __ldg(g.wts + src) : 0.0f;
+        const __nv_bfloat16* abrow = g.ab + (size_t)r * (2 * g.F);
+        float dgacc = 0.0f;
+        uint32_t sfa = 0, sfb = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ru[32];
+          tmem_ld32(tb + half * 128 + c * 32, ru);
+          const int col = t.nt * BN + half * 128 + c * 32;
+          float a[32], b[32];
+          load_bf16x32(abrow + col, a);
+          load_bf16x32(abrow + g.F + col, b);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+          }
+          float da[32], db[32], wh[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float u = __uint_as_float(ru[i]);
+            const float sa = sigmoidf_(a[i]);
+            const float sl = a[i] * sa;
+            const float hh = sl * b[i];
+            dgacc = fmaf(u, hh, dgacc);
+            const float dh = wr * u;
+            da[i] = dh * b[i] * sa * (1.0f + a[i] * (1.0f - sa));
+            db[i] = dh * sl;
+            wh[i] = wr * hh;
+          }
+          const int Xa = mx_block_exponent(amax32(da));
+          const int Xb = mx_block_exponent(amax32(db));
+          uint32_t qa[8], qb[8];
+          mx_encode32(da, Xa, qa);
+          mx_encode32(db, Xb, qb);
+          sfa |= (uint32_t)(Xa + 127) << (8 * c);
+          sfb |= (uint32_t)(Xb + 127) << (8 * c);
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          stage_row(stg, lane, da);
+          stage_row(stg + kStageChunk, lane, db);
+          stage_row(stg + 2 * kStageChunk, lane, wh);
+          stage_row_fp8(stg + 3 * kStageChunk, lane, qa);
+          stage_row_fp8(stg + 3 * kStageChunk + 1024, lane, qb);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&g.mapO0, stg, col, rowq);
+            tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
+            tma_store_2d(&g.mapO2, stg + 2 * kStageChunk, col, rowq);
+            tma_store_2d(&g.mapO1, stg + 3 * kStageChunk, col, rowq);
+            tma_store_2d(&g.mapO1, stg + 3 * kStageChunk + 1024, g.F + col, rowq);
+            bulk_commit();
+          }
+        }
+        aph ^= 1;
+        const int kba = (t.nt * BN + half * 128) / 32;  // first of this warp's 4 blocks (K = 2F)
+        *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, kba, (2 * g.F) / 32)) = sfa;
+        *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, g.F / 32 + kba, (2 * g.F) / 32)) = sfb;
+        g.dgp[(size_t)r * (g.F / 128) + t.nt * 2 + half] = dgacc;
+        continue;
+      }
       uint32_t acc[4][32];
       if (KIND == kUp) {  // a cols [64 half, +64), b cols 128 + [64 half, +64)
         tmem_ld32(tb + half * 64, acc[0]);

@@ -50,6 +50,8 @@ cudaError_t prepare_gemm_bwd(int kind);
 cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st);
 cudaError_t launch_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d, void* q,
                                 void* sf, int grid, cudaStream_t st);
+cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
+                                   cudaStream_t st);
 struct MxArgs;
 cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st);  // kind 0 up, 1 down
 cudaError_t prepare_gemm_mx(int kind);

@@ -78,6 +78,41 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16* 
   }
 }
 
+// src [E][A][B] bf16 -> q [E][B][A] E4M3 quantised along A (the backward
+// orientation of a weight: the K of the dgrad GEMMs), scale atoms over rows
+// E*B with K = A.  One CTA transposes a 128 (A) x 32 (B) tile through shared
+// memory; thread i then owns output row b0 + i/4, block i%4.
+__global__ void __launch_bounds__(128) quant_transpose_kernel(const __nv_bfloat16* __restrict__ src, int E, int A,
+                                                              int B, uint8_t* __restrict__ q,
+                                                              uint8_t* __restrict__ sf) {
+  __shared__ float tile[128][33];
+  const int na = A / 128, nb = B / 32;
+  const int64_t ntiles = (int64_t)E * na * nb;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int e = (int)(t / (na * nb));
+    const int rem = (int)(t - (int64_t)e * na * nb);
+    const int a0 = (rem / nb) * 128, b0 = (rem % nb) * 32;
+    float v[32];
+    load_bf16x32_f(src + ((int64_t)e * A + a0 + threadIdx.x) * B + b0, v);
+#pragma unroll
+    for (int m = 0; m < 32; ++m) tile[threadIdx.x][m] = v[m];
+    __syncthreads();
+    const int bl = threadIdx.x >> 2, j = threadIdx.x & 3;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) v[m] = tile[32 * j + m][bl];
+    const int64_t orow = (int64_t)e * B + b0 + bl;
+    quant_block_store(v, q + orow * A + a0 + 32 * j, sf + sf_atom_offset(orow, a0 / 32 + j, A / 32));
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
+                                   cudaStream_t st) {
+  quant_transpose_kernel<<<grid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), E, A, B,
+                                               reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st) {
   quant_rows_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), rows, K,
                                           reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));

@@ -80,7 +80,26 @@ def test_mxfp8_forward_parity(case):
     assert err <= MX_TOL, (err, rel_err(Y, Yb))
 
 
-def test_mxfp8_forward_deterministic_and_backward_refused():
+@pytest.mark.parametrize("case", [(128, 256, 512, 8, 2, 0.0), (512, 1024, 512, 32, 4, 1.1), (300, 512, 768, 16, 3, 1.5)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_mxfp8_backward_parity(case):
+    """MXFP8 dgrad GEMMs (dY along d with Wd^T along d; dA/dB along F with
+    Wg^T/Wu^T along F), bf16 weight gradients, against the oracle's emulation."""
+    T, d, F, E, k, alpha = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=22, alpha=alpha)
+    plan = _mx_plan(T, d, F, E, k)
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k, mx=True)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    errs = {key: rel_err(out[key], gr[key]) for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")}
+    assert all(v <= MX_TOL for v in errs.values()), errs
+
+
+def test_mxfp8_bitwise_deterministic():
     T, d, F, E, k = 256, 512, 512, 16, 4
     g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=5, alpha=1.1)
     plan = _mx_plan(T, d, F, E, k)
@@ -88,13 +107,13 @@ def test_mxfp8_forward_deterministic_and_backward_refused():
     ref = None
     for _ in range(5):
         Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+        out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+        cur = [Y.clone()] + [out[n].clone() for n in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")]
         if ref is None:
-            ref = Y.clone()
+            ref = cur
         else:
-            assert torch.equal(ref, Y)
-    with pytest.raises(moe.MoEError) as ei:
-        plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
-    assert ei.value.status == 2
+            for a, b in zip(ref, cur):
+                assert torch.equal(a, b)
 
 
 def test_mxfp8_forward_needs_quantized_weights():
