@@ -310,6 +310,10 @@ def bench_gpu(args):
         del plan, inp, grads, saved, Y
         torch.cuda.empty_cache()
         out["mxfp8_forward"] = [bench_mx_forward(args, dev, ws, peaks, alpha) for alpha in (0.0, ALPHA)]
+        grid = [(Tm, a) for Tm in (2048, 8192, 32768) for a in (0.0, 1.1, 1.5)] if args.sweep else [(8192, ALPHA)]
+        out["mxfp8_fwd_bwd"] = [bench_mx_fwd_bwd(args, dev, ws, peaks, Tm, a) for Tm, a in grid]
+        if args.sweep:
+            out["minibatch_sweep"] = bench_minibatch_sweep(args, dev, ws)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -372,6 +376,95 @@ def bench_mx_forward(args, dev, ws, peaks, alpha):
     del plan, inp, saved, Y
     torch.cuda.empty_cache()
     return res
+
+
+def _alloc_grads(T, d, F, E, k, dev):
+    return {
+        "dX": torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+        "dWg": torch.empty((E, F, d), dtype=torch.bfloat16, device=dev),
+        "dWu": torch.empty((E, F, d), dtype=torch.bfloat16, device=dev),
+        "dWd": torch.empty((E, d, F), dtype=torch.bfloat16, device=dev),
+        "dg": torch.empty((T, k), dtype=torch.float32, device=dev),
+        "dlogits": torch.empty((T, E), dtype=torch.float32, device=dev),
+    }
+
+
+def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha):
+    """MXFP8 forward + backward at T tokens: E4M3 forward and dgrad GEMMs,
+    bf16 weight gradients.  Layer roofline: max(12RdF / fp8 peak + 6RdF / bf16
+    peak, (E4M3 weights fwd + bwd orientation + bf16 dW) / HBM)."""
+    from mixture_experts_layer_19_gb300 import moe
+    d, F, E, k = SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
+    inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, device=dev.index,
+                               debug_flags=moe.MOE_DEBUG_TIMING))
+    stream = torch.cuda.current_stream(dev)
+    plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    grads = _alloc_grads(T, d, F, E, k, dev)
+
+    def step():
+        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        plan.backward(inp.dY, inp.X, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    plan.kernel_times()
+    barrier(ws)
+    steps = max(3, args.steps // 2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status set in the MXFP8 fwd+bwd")
+    el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+    kt = plan.kernel_times()
+    R = T * k
+    fp8_peak, bf16_peak = 2.0 * peaks["bf16_tflops_sustained"], peaks["bf16_tflops_sustained"]
+    t_tc = (12.0 * R * d * F / fp8_peak + 6.0 * R * d * F / bf16_peak) / 1e12 * 1e3
+    t_hbm = (2 * 3.0 * E * F * d * (1 + 1 / 32) + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    ms = el / steps
+    res = {"workload": f"moe_layer_fwd_bwd_mxfp8_T{T}_zipf{alpha:g}", "T": T, "zipf_alpha": alpha,
+           "value": round(ws * T * steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
+                              "frac": round(max(t_tc, t_hbm) / ms, 4)},
+           "kernels": {n: round(v[0] / steps, 4) for n, v in sorted(kt.items(), key=lambda x: -x[1][0])}}
+    del plan, inp, saved, Y, grads
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_minibatch_sweep(args, dev, ws, T=8192, alpha=ALPHA):
+    """BF16 ring-megakernel forward time versus minibatch size (rows per ring
+    slot fill); 0 = the two-wave floor."""
+    from mixture_experts_layer_19_gb300 import moe
+    d, F, E, k = SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
+    inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for mb in (256, 512, 1024, 2048, 0, 4096, 8192):
+        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, minibatch_rows=mb, device=dev.index))
+        saved = plan.new_saved(T)
+        Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup):
+            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        torch.cuda.synchronize(dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        out.append({"minibatch_rows": mb if mb else "two-wave floor", "fwd_ms": round(ev0.elapsed_time(ev1) / args.steps, 4)})
+        del plan, saved, Y
+    del inp
+    torch.cuda.empty_cache()
+    return {"workload": f"bf16 ring-megakernel forward, T={T}, zipf {alpha:g}", "points": out}
 
 
 def bench_e2e(args, plan, inp, Y, saved, grads, stream, dev, ws):
@@ -474,7 +567,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
-    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward measurement")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurements")
+    ap.add_argument("--sweep", action="store_true",
+                    help="MXFP8 fwd+bwd over T in {2048, 8192, 32768} x zipf {0, 1.1, 1.5} and a minibatch sweep")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
