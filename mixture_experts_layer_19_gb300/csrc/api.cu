@@ -173,6 +173,9 @@ struct moe_plan_s {
   // backward orientation (quantised along the dgrad GEMMs' K) and E4M3 dA|dB
   uint8_t *WdTq = nullptr, *WgTq = nullptr, *WuTq = nullptr, *WdTs = nullptr, *WgTs = nullptr, *WuTs = nullptr;
   uint8_t *dABq = nullptr, *dABs = nullptr;
+  // MXFP8 ring slots: E4M3 X and h rows with their scale atoms
+  uint8_t *ring_xq = nullptr, *ring_xs = nullptr, *ring_hq = nullptr, *ring_hs = nullptr;
+  CUtensorMap m_ring_xq, m_ring_hq, m_ring_hq_st;
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
   CUtensorMap m_WdTq, m_WgTq, m_WuTq, m_dABq_k, m_dABq_st;
@@ -431,6 +434,11 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_wuts = m; m += align256(wbytes / 32);
     const size_t o_dabq = m; m += align256((size_t)R * 2 * c.F);
     const size_t o_dabs = m; m += align256((size_t)R * 2 * c.F / 32);
+    const size_t ring_rows = (size_t)p->slots * p->cap * BM;
+    const size_t o_rxq = m; m += align256(ring_rows * c.d);
+    const size_t o_rxs = m; m += align256(ring_rows * c.d / 32);
+    const size_t o_rhq = m; m += align256(ring_rows * c.F);
+    const size_t o_rhs = m; m += align256(ring_rows * c.F / 32);
     err = cudaMalloc(&p->mx_ws, m);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -445,13 +453,17 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->WdTq = mb + o_wdt; p->WgTq = mb + o_wgt; p->WuTq = mb + o_wut;
     p->WdTs = mb + o_wdts; p->WgTs = mb + o_wgts; p->WuTs = mb + o_wuts;
     p->dABq = mb + o_dabq; p->dABs = mb + o_dabs;
+    p->ring_xq = mb + o_rxq; p->ring_xs = mb + o_rxs; p->ring_hq = mb + o_rhq; p->ring_hs = mb + o_rhs;
     const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
     ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, c.d, EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, c.d, EF) &&
          map_fp8_kmajor(&p->m_Wdq, p->Wdq, c.F, Ed, BN) && map_fp8_kmajor(&p->m_Xq, p->Xq, c.d, R) &&
          map_fp8_kmajor(&p->m_Hq_k, p->Hq, c.F, R) && map_fp8_store(&p->m_Hq_st, p->Hq, c.F, R) &&
          map_fp8_kmajor(&p->m_WdTq, p->WdTq, c.d, EF, BN) && map_fp8_kmajor(&p->m_WgTq, p->WgTq, c.F, Ed, BN) &&
          map_fp8_kmajor(&p->m_WuTq, p->WuTq, c.F, Ed, BN) &&
-         map_fp8_kmajor(&p->m_dABq_k, p->dABq, 2 * c.F, R) && map_fp8_store(&p->m_dABq_st, p->dABq, 2 * c.F, R);
+         map_fp8_kmajor(&p->m_dABq_k, p->dABq, 2 * c.F, R) && map_fp8_store(&p->m_dABq_st, p->dABq, 2 * c.F, R) &&
+         map_fp8_kmajor(&p->m_ring_xq, p->ring_xq, c.d, ring_rows) &&
+         map_fp8_kmajor(&p->m_ring_hq, p->ring_hq, c.F, ring_rows) &&
+         map_fp8_store(&p->m_ring_hq_st, p->ring_hq, c.F, ring_rows) && prepare_fwd_megakernel_mx() == cudaSuccess;
     if (!ok) {
       cudaFree(p->mx_ws);
       cudaFree(p->ws);
@@ -524,6 +536,59 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     err = timed_launch(p, "layout_permute", st,
                        [&] { return launch_permute(Ti, c.E, c.k, p->chunk_base, rp, st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: routing launch");
+  if (mx && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS)) {
+    // MXFP8 ring megakernel: movers gather + quantise into the slots, compute
+    // CTAs run the block-scaled [a|b]+SwiGLU (h re-quantised into the slot)
+    // and down tiles minibatch by minibatch
+    const int counters_len = 1 + 3 * p->nm_max;
+    err = timed_launch(p, "plan_minibatches", st, [&] {
+      return launch_plan_minibatches(rp.mtile_off, c.E, p->mbt, p->cap, c.F / 128, c.d / BN, counters_len,
+                                     p->counters, p->mb_start, p->phase_start, p->n_mb, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: minibatch plan launch");
+    MegaMxArgs m;
+    memset(&m, 0, sizeof(m));
+    m.mapXr = p->m_ring_xq;
+    m.mapWg = p->m_Wgq;
+    m.mapWu = p->m_Wuq;
+    m.mapWd = p->m_Wdq;
+    m.mapHr = p->m_ring_hq;
+    m.mapHrSt = p->m_ring_hq_st;
+    m.mapABSt = m_ab_st;
+    m.mapYsSt = p->m_Ys_st;
+    m.X = reinterpret_cast<const __nv_bfloat16*>(X);
+    m.ring_xq = p->ring_xq;
+    m.ring_xs = p->ring_xs;
+    m.ring_hs = p->ring_hs;
+    m.wgs = p->Wgs;
+    m.wus = p->Wus;
+    m.wds = p->Wds;
+    m.perm_src = rp.perm_src;
+    m.mtile_off = rp.mtile_off;
+    m.mb_start = p->mb_start;
+    m.phase_start = p->phase_start;
+    m.n_mb = p->n_mb;
+    m.claim = p->counters;
+    m.gathered = p->counters + 1;
+    m.mb_done = p->counters + 1 + p->nm_max;
+    m.g1_done = p->counters + 1 + 2 * p->nm_max;
+    m.status = p->status;
+    m.timeout_ns = (uint64_t)c.wait_timeout_ns;
+    m.E = c.E;
+    m.d = c.d;
+    m.F = c.F;
+    m.k = c.k;
+    m.movers = p->movers;
+    m.slots = p->slots;
+    m.slot_rows = p->cap * BM;
+    err = timed_launch(p, "fwd_megakernel_mx", st, [&] { return launch_fwd_megakernel_mx(m, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 megakernel launch");
+    const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
+    err = timed_launch(p, "combine", st,
+                       [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
+    return MOE_OK;
+  }
   if (mx) {
     // MXFP8: gather + quantise X along d, block-scaled [a|b] GEMM with SwiGLU and
     // h re-quantised along F in its epilogue, block-scaled down GEMM.

@@ -63,6 +63,9 @@ cudaError_t launch_plan_minibatches(const int32_t* mtile_off, int E, int mbt, in
                                     int32_t* n_mb, cudaStream_t st);
 cudaError_t launch_fwd_megakernel(const MegaArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_fwd_megakernel();
+struct MegaMxArgs;
+cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, cudaStream_t st);
+cudaError_t prepare_fwd_megakernel_mx();
 
 // Record the detail string moe_last_error() returns on this thread.
 void set_error_detail(const char* msg);

@@ -43,11 +43,6 @@ constexpr int kMegaThreads = 192;  // warp 0 producer, warp 1 MMA, warps 2..5 ep
 constexpr int kMegaStaging = 3 * kStageChunk;  // per epilogue warp
 constexpr int kMegaSmem = kStages * kStageBytes + 4 * kMegaStaging + 1024 + 512;
 
-struct Item {
-  int kind;   // 0 = G1, 1 = G2, -1 = stop
-  int mb, gt, nt, e, ring_row0;
-};
-
 // ----------------------------------------------------------------------------
 // Plan: zero the counters, cut minibatches on expert boundaries (>= mbt tiles
 // when possible, <= cap tiles always; an expert larger than cap is split into
@@ -98,34 +93,6 @@ __global__ void __launch_bounds__(1024) plan_minibatches_kernel(const int32_t* _
       phase_start[p++] = acc;
     }
   }
-}
-
-__device__ __forceinline__ int find_last_le(const int32_t* a, int n, int v) {  // last i in [0,n) with a[i] <= v
-  int lo = 0, hi = n;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (a[mid] <= v) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ Item decode_claim(const MegaArgs& g, int nmb, int c) {
-  Item it;
-  const int p = find_last_le(g.phase_start, 2 * nmb, c);
-  const int local = c - g.phase_start[p];
-  if (p == 0) { it.kind = 0; it.mb = 0; }
-  else if (p == 2 * nmb - 1) { it.kind = 1; it.mb = nmb - 1; }
-  else if (p & 1) { it.kind = 0; it.mb = (p + 1) >> 1; }
-  else { it.kind = 1; it.mb = (p >> 1) - 1; }
-  const int m0 = g.mb_start[it.mb];
-  const int mts = g.mb_start[it.mb + 1] - m0;
-  it.nt = local / mts;
-  const int mt = local - it.nt * mts;
-  it.gt = m0 + mt;
-  it.e = find_last_le(g.mtile_off, g.E + 1, it.gt);
-  while (it.e < g.E && g.mtile_off[it.e + 1] <= it.gt) ++it.e;  // skip empty experts
-  it.ring_row0 = (it.mb % g.slots) * g.slot_rows + mt * BM;
-  return it;
 }
 
 // ----------------------------------------------------------------------------

@@ -2,6 +2,7 @@
 // (megakernel.cu), shared with the host code that fills it (api.cu).
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace moe {
@@ -21,6 +22,80 @@ struct MegaArgs {
   const int32_t* mtile_off;   // [E+1]
   const int32_t* mb_start;    // [n_mb+1] first 128-row tile of each minibatch
   const int32_t* phase_start; // [2 n_mb + 1] first claim index of each phase
+  const int32_t* n_mb;
+  int* claim;
+  int* gathered;
+  int* g1_done;
+  int* mb_done;
+  int32_t* status;
+  uint64_t timeout_ns;
+  int E, d, F, k, movers, slots, slot_rows;
+};
+
+// One claimed unit of work of a ring megakernel.
+struct Item {
+  int kind;   // 0 = G1 ([a|b] + SwiGLU tile), 1 = G2 (down tile), -1 = stop
+  int mb, gt, nt, e, ring_row0;
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ int find_last_le(const int32_t* a, int n, int v) {  // last i in [0,n) with a[i] <= v
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= v) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Claim index -> work item.  Claim order: phases G1(0), G1(1), G2(0), G1(2),
+// G2(1), ..., G2(n-1) (phase_start holds their first claim indices); inside a
+// phase the N tile is the slow index and the minibatch's 128-row tile the
+// fast one.  A is any argument block with phase_start, mb_start, mtile_off,
+// E, slots, slot_rows.
+template <class A>
+__device__ __forceinline__ Item decode_claim(const A& g, int nmb, int c) {
+  Item it;
+  const int p = find_last_le(g.phase_start, 2 * nmb, c);
+  const int local = c - g.phase_start[p];
+  if (p == 0) { it.kind = 0; it.mb = 0; }
+  else if (p == 2 * nmb - 1) { it.kind = 1; it.mb = nmb - 1; }
+  else if (p & 1) { it.kind = 0; it.mb = (p + 1) >> 1; }
+  else { it.kind = 1; it.mb = (p >> 1) - 1; }
+  const int m0 = g.mb_start[it.mb];
+  const int mts = g.mb_start[it.mb + 1] - m0;
+  it.nt = local / mts;
+  const int mt = local - it.nt * mts;
+  it.gt = m0 + mt;
+  it.e = find_last_le(g.mtile_off, g.E + 1, it.gt);
+  while (it.e < g.E && g.mtile_off[it.e + 1] <= it.gt) ++it.e;  // skip empty experts
+  it.ring_row0 = (it.mb % g.slots) * g.slot_rows + mt * 128;
+  return it;
+}
+#endif
+
+// Argument block of the MXFP8 ring megakernel (megakernel_mx.cu): the ring
+// holds E4M3 X and h rows with their scale atoms (rows = ring rows).
+struct MegaMxArgs {
+  CUtensorMap mapXr;    // ring Xq, K-major {d bytes, ring rows}, box 128 x 128
+  CUtensorMap mapWg;    // Wgq {d, E*F}, box 128 x 128
+  CUtensorMap mapWu;
+  CUtensorMap mapWd;    // Wdq {F, E*d}, box 128 x 256
+  CUtensorMap mapHr;    // ring Hq loads {F, ring rows}, box 128 x 128
+  CUtensorMap mapHrSt;  // ring Hq stores, box 32 x 32 bytes
+  CUtensorMap mapABSt;  // saved a|b bf16 stores
+  CUtensorMap mapYsSt;  // sorted y rows bf16 stores
+  const __nv_bfloat16* X;
+  uint8_t* ring_xq;     // [ring rows, d] E4M3
+  uint8_t* ring_xs;     // scale atoms of ring_xq (K = d)
+  uint8_t* ring_hs;     // scale atoms of the ring Hq rows (K = F)
+  const uint8_t* wgs;
+  const uint8_t* wus;
+  const uint8_t* wds;
+  const int32_t* perm_src;
+  const int32_t* mtile_off;
+  const int32_t* mb_start;
+  const int32_t* phase_start;
   const int32_t* n_mb;
   int* claim;
   int* gathered;

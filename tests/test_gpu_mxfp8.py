@@ -99,6 +99,32 @@ def test_mxfp8_backward_parity(case):
     assert all(v <= MX_TOL for v in errs.values()), errs
 
 
+@pytest.mark.parametrize("mb_rows,slots,movers", [(0, 0, 0), (128, 2, 1), (512, 3, 4)])
+def test_mxfp8_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers):
+    """The MXFP8 ring megakernel (movers quantise while they gather; h is
+    re-quantised into the ring slot) must equal the separate-kernel MXFP8
+    schedule bit for bit, forward and backward."""
+    T, d, F, E, k = 700, 512, 512, 24, 4
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=41, alpha=1.1)
+    ring = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, minibatch_rows=mb_rows,
+                               ring_slots=slots, mover_ctas=movers))
+    sep = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8,
+                              debug_flags=moe.MOE_DEBUG_SEPARATE_KERNELS))
+    for p in (ring, sep):
+        p.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Ya, sa = ring.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    Yb, sb = sep.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    ga = ring.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], sa)
+    gb = sep.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], sb)
+    torch.cuda.synchronize()
+    assert ring.device_status() == 0 and sep.device_status() == 0
+    assert torch.equal(Ya, Yb)
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        assert torch.equal(ga[key], gb[key]), key
+    Yr, _ = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k, mx=True)
+    assert rel_err(Ya, Yr) <= MX_TOL
+
+
 def test_mxfp8_bitwise_deterministic():
     T, d, F, E, k = 256, 512, 512, 16, 4
     g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=5, alpha=1.1)
