@@ -328,30 +328,40 @@ def bench_mx_forward(args, dev, ws, peaks, alpha):
     from mixture_experts_layer_19_gb300 import moe
     T, d, F, E, k = MX_SHAPE["T"], SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
-    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, device=dev.index,
-                               debug_flags=moe.MOE_DEBUG_TIMING))
     stream = torch.cuda.current_stream(dev)
-    plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
-    wq = plan.kernel_times()
-    saved = plan.new_saved(T)
-    Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-    for _ in range(args.warmup):
-        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
-    torch.cuda.synchronize(dev)
-    plan.kernel_times()
-    barrier(ws)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    if plan.device_status() != 0:
-        raise RuntimeError("device status set in the MXFP8 forward")
-    el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
-    kt = plan.kernel_times()
+
+    def run(flags, steps):
+        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, device=dev.index,
+                                   debug_flags=moe.MOE_DEBUG_TIMING | flags))
+        plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
+        wq = plan.kernel_times()
+        saved = plan.new_saved(T)
+        Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup):
+            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        torch.cuda.synchronize(dev)
+        plan.kernel_times()
+        barrier(ws)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if plan.device_status() != 0:
+            raise RuntimeError("device status set in the MXFP8 forward")
+        el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+        kt = plan.kernel_times()
+        del plan, saved, Y
+        return el, kt, wq
+
+    # default MXFP8 schedule (separate kernels) and the ring megakernel beside it
+    el, kt, wq = run(0, args.steps)
+    el_ring, ktr, _ = run(moe.MOE_DEBUG_RING_MEGAKERNEL, max(3, args.steps // 2))
     R = T * k
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # nominal fp8/bf16 dense ratio x measured bf16
+    mk_ms = ktr["fwd_megakernel_mx"][0] / ktr["fwd_megakernel_mx"][1]
+    mk_tf = 6.0 * R * d * F / (mk_ms / 1e3) / 1e12
     up_ms = kt["gemm_mx_up_swiglu"][0] / kt["gemm_mx_up_swiglu"][1]
     dn_ms = kt["gemm_mx_down"][0] / kt["gemm_mx_down"][1]
     up_tf = 4.0 * R * d * F / (up_ms / 1e3) / 1e12
@@ -368,12 +378,15 @@ def bench_mx_forward(args, dev, ws, peaks, alpha):
                      "traffic": None,
                      "peak_source": peaks["source"] + " bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"},
         "down_gemm": {"achieved": round(dn_tf, 1), "unit": "TFLOP/s", "frac": round(dn_tf / fp8_peak, 4)},
+        "ring_megakernel": {"ms_per_step": round(el_ring / max(3, args.steps // 2), 4),
+                            "megakernel_ms": round(mk_ms, 4), "achieved": round(mk_tf, 1), "unit": "TFLOP/s",
+                            "frac": round(mk_tf / fp8_peak, 4), "flops": "6*R*d*F per launch"},
         "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
                            "frac": round(max(t_tc, t_hbm) / ms, 4)},
         "kernels": {n: {"ms_per_step": round(v[0] / args.steps, 4), "launches": v[1]} for n, v in kt.items()},
         "weight_quant_ms": round(wq.get("quant_weights", (0.0, 0))[0], 3),
     }
-    del plan, inp, saved, Y
+    del inp
     torch.cuda.empty_cache()
     return res
 

@@ -60,8 +60,12 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision_t;
 /* debug_flags bits */
 #define MOE_DEBUG_IDENTITY_EXPERTS 0x1u /* experts return their input (y = x); GEMMs skipped */
 #define MOE_DEBUG_TIMING 0x2u           /* bracket each kernel with CUDA events (moe_kernel_times) */
-#define MOE_DEBUG_SEPARATE_KERNELS 0x4u /* BF16 forward as separate gather / GEMM launches over full
-                                           sorted buffers instead of the ring-buffer megakernel */
+/* Forward schedule.  BF16 plans run the ring-buffer megakernel unless
+ * MOE_DEBUG_SEPARATE_KERNELS is set; MXFP8 plans run separate kernels (on
+ * GB300 they are faster at the measured shapes) unless MOE_DEBUG_RING_MEGAKERNEL
+ * is set.  Both schedules give bitwise identical results. */
+#define MOE_DEBUG_SEPARATE_KERNELS 0x4u /* gather / GEMM launches over full sorted buffers */
+#define MOE_DEBUG_RING_MEGAKERNEL 0x8u  /* MXFP8: use the ring-buffer megakernel */
 
 typedef struct {
   int64_t T_max;          /* largest token count a call may pass */

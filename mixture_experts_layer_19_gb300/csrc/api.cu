@@ -175,6 +175,7 @@ struct moe_plan_s {
   uint8_t *dABq = nullptr, *dABs = nullptr;
   // MXFP8 ring slots: E4M3 X and h rows with their scale atoms
   uint8_t *ring_xq = nullptr, *ring_xs = nullptr, *ring_hq = nullptr, *ring_hs = nullptr;
+  uint8_t *Xtq = nullptr, *Xts = nullptr;  // tokens quantised once per token (ring path)
   CUtensorMap m_ring_xq, m_ring_hq, m_ring_hq_st;
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
@@ -439,6 +440,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_rxs = m; m += align256(ring_rows * c.d / 32);
     const size_t o_rhq = m; m += align256(ring_rows * c.F);
     const size_t o_rhs = m; m += align256(ring_rows * c.F / 32);
+    const size_t t_pad = ((size_t)c.T_max + BM - 1) / BM * BM;
+    const size_t o_xtq = m; m += align256(t_pad * c.d);
+    const size_t o_xts = m; m += align256(t_pad * c.d / 32);
     err = cudaMalloc(&p->mx_ws, m);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -454,6 +458,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->WdTs = mb + o_wdts; p->WgTs = mb + o_wgts; p->WuTs = mb + o_wuts;
     p->dABq = mb + o_dabq; p->dABs = mb + o_dabs;
     p->ring_xq = mb + o_rxq; p->ring_xs = mb + o_rxs; p->ring_hq = mb + o_rhq; p->ring_hs = mb + o_rhs;
+    p->Xtq = mb + o_xtq; p->Xts = mb + o_xts;
     const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
     ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, c.d, EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, c.d, EF) &&
          map_fp8_kmajor(&p->m_Wdq, p->Wdq, c.F, Ed, BN) && map_fp8_kmajor(&p->m_Xq, p->Xq, c.d, R) &&
@@ -536,7 +541,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     err = timed_launch(p, "layout_permute", st,
                        [&] { return launch_permute(Ti, c.E, c.k, p->chunk_base, rp, st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: routing launch");
-  if (mx && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS)) {
+  if (mx && (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS)) {
     // MXFP8 ring megakernel: movers gather + quantise into the slots, compute
     // CTAs run the block-scaled [a|b]+SwiGLU (h re-quantised into the slot)
     // and down tiles minibatch by minibatch
@@ -546,6 +551,10 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
                                      p->counters, p->mb_start, p->phase_start, p->n_mb, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: minibatch plan launch");
+    err = timed_launch(p, "quant_tokens", st, [&] {
+      return launch_quant_rows(X, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: token quantisation launch");
     MegaMxArgs m;
     memset(&m, 0, sizeof(m));
     m.mapXr = p->m_ring_xq;
@@ -556,7 +565,8 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     m.mapHrSt = p->m_ring_hq_st;
     m.mapABSt = m_ab_st;
     m.mapYsSt = p->m_Ys_st;
-    m.X = reinterpret_cast<const __nv_bfloat16*>(X);
+    m.xq = p->Xtq;
+    m.xs = p->Xts;
     m.ring_xq = p->ring_xq;
     m.ring_xs = p->ring_xs;
     m.ring_hs = p->ring_hs;

@@ -85,7 +85,8 @@ struct MegaMxArgs {
   CUtensorMap mapHrSt;  // ring Hq stores, box 32 x 32 bytes
   CUtensorMap mapABSt;  // saved a|b bf16 stores
   CUtensorMap mapYsSt;  // sorted y rows bf16 stores
-  const __nv_bfloat16* X;
+  const uint8_t* xq;    // [T, d] E4M3 tokens, quantised once per token along d
+  const uint8_t* xs;    // their scale atoms (rows = tokens, K = d)
   uint8_t* ring_xq;     // [ring rows, d] E4M3
   uint8_t* ring_xs;     // scale atoms of ring_xq (K = d)
   uint8_t* ring_hs;     // scale atoms of the ring Hq rows (K = F)

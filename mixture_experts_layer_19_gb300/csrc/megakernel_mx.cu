@@ -3,10 +3,12 @@
 // counters as the bf16 megakernel (megakernel.cu), with the MXFP8 datapath of
 // gemm_mx.cuh.
 //
-// Mover CTAs pull each routed token row into its ring slot and quantise it
-// along d on the way (E4M3 + E8M0 scale atoms): MXFP8 activation quantisation
-// fused into the dispatch datapath (kucoin page "Cursor's MoK réalise une
-// amélioration des performances de 2,37x sur NVIDIA GB300 NVL72", section 02).
+// The tokens are quantised along d once per token (all SMs, just before this
+// kernel); mover CTAs then pull each routed row's E4M3 bytes and scale words
+// into its ring slot -- MXFP8 activation quantisation in the dispatch datapath
+// (kucoin page "Cursor's MoK réalise une amélioration des performances de
+// 2,37x sur NVIDIA GB300 NVL72", section 02), done k times less often than a
+// per-row quantisation and leaving the movers plain copies.
 // G1 tiles run the block-scaled [a|b] GEMM, SwiGLU, and re-quantise h along F
 // straight into the slot; G2 tiles run the block-scaled down GEMM from the
 // slot.  Eight epilogue warps per compute CTA each bump the hand-off counters
@@ -42,28 +44,27 @@ __device__ void mx_mover_loop(const MegaMxArgs& g, int nmb, int* abort_flag) {
     const int row_base = g.mb_start[mb] * BM;
     const int nrows = (g.mb_start[mb + 1] - g.mb_start[mb]) * BM;
     const int slot_base = (mb % g.slots) * g.slot_rows;
+    // copy the token's E4M3 row (16-byte vectors) and its scale words (4
+    // consecutive blocks share one 32-bit word of an atom) into the ring row
+    const int nvec = g.d / 16, nwords = kblocks / 4;
     for (int i = blockIdx.x * nwarps + warp; i < nrows; i += g.movers * nwarps) {
       const int src = g.perm_src[row_base + i];
       const int rr = slot_base + i;   // ring row
-      uint8_t* qrow = g.ring_xq + (size_t)rr * g.d;
-      for (int kb = lane; kb < kblocks; kb += 32) {
-        uint8_t* dq = qrow + kb * 32;
-        uint8_t* sfp = g.ring_xs + sf_atom_offset(rr, kb, kblocks);
-        if (src < 0) {
-          reinterpret_cast<uint4*>(dq)[0] = make_uint4(0, 0, 0, 0);
-          reinterpret_cast<uint4*>(dq)[1] = make_uint4(0, 0, 0, 0);
-          *sfp = 0;
-          continue;
-        }
-        float v[32];
-        load_bf16x32(g.X + (size_t)(src / g.k) * g.d + kb * 32, v);
-        const int X = mx_block_exponent(amax32(v));
-        uint32_t o[8];
-        mx_encode32(v, X, o);
-        reinterpret_cast<uint4*>(dq)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        reinterpret_cast<uint4*>(dq)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        *sfp = (uint8_t)(X + 127);
+      uint4* qdst = reinterpret_cast<uint4*>(g.ring_xq + (size_t)rr * g.d);
+      const size_t rw = (size_t)(rr & 31) * 16 + (size_t)((rr >> 5) & 3) * 4;
+      if (src < 0) {
+        for (int v = lane; v < nvec; v += 32) qdst[v] = make_uint4(0, 0, 0, 0);
+        for (int j = lane; j < nwords; j += 32)
+          *reinterpret_cast<uint32_t*>(g.ring_xs + ((size_t)(rr >> 7) * nwords + j) * 512 + rw) = 0u;
+        continue;
       }
+      const int t = src / g.k;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(g.xq + (size_t)t * g.d);
+      for (int v = lane; v < nvec; v += 32) qdst[v] = __ldg(qsrc + v);
+      const size_t tw = (size_t)(t & 31) * 16 + (size_t)((t >> 5) & 3) * 4;
+      for (int j = lane; j < nwords; j += 32)
+        *reinterpret_cast<uint32_t*>(g.ring_xs + ((size_t)(rr >> 7) * nwords + j) * 512 + rw) =
+            __ldg(reinterpret_cast<const uint32_t*>(g.xs + ((size_t)(t >> 7) * nwords + j) * 512 + tw));
     }
     __syncthreads();
     if (threadIdx.x == 0) {

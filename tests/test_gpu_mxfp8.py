@@ -107,7 +107,7 @@ def test_mxfp8_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, 
     T, d, F, E, k = 700, 512, 512, 24, 4
     g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=41, alpha=1.1)
     ring = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, minibatch_rows=mb_rows,
-                               ring_slots=slots, mover_ctas=movers))
+                               ring_slots=slots, mover_ctas=movers, debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL))
     sep = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8,
                               debug_flags=moe.MOE_DEBUG_SEPARATE_KERNELS))
     for p in (ring, sep):
