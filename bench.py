@@ -123,34 +123,91 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- roofline bookkeeping
-def algorithmic_bytes(shape, R: int):
-    """Compulsory HBM bytes per launch of each kernel (bf16 = 2 B): the weights
-    it must stream once plus the rows it must read and write (R routed rows,
-    padding excluded)."""
-    d, F, E = shape["d"], shape["F"], shape["E"]
-    W = E * F * d * 2          # one weight tensor
+def algorithmic_bytes(shape, R: int, e_act: int):
+    """Compulsory HBM bytes per launch of each kernel (bf16 = 2 B).
+
+    Weight reads count only the ``e_act`` experts that received at least one
+    routed row: an expert with no rows need not be read.  Weight-gradient
+    writes count all E experts, since an idle expert's dW is still written
+    (zeros).  Activation terms count R routed rows, padding excluded; a token
+    row that is gathered k times is counted once where the gather is served
+    by L2 (the ring megakernel reads X once per token from HBM)."""
+    T, d, F, E = shape["T"], shape["d"], shape["F"], shape["E"]
+    Wa = e_act * F * d * 2     # one weight tensor, active experts only
+    Wall = E * F * d * 2       # one weight-gradient tensor, all experts
     return {
-        "gemm_up_swiglu": 2 * W + R * d * 2 + R * 3 * F * 2,
-        "gemm_down": W + R * F * 2 + R * d * 2,
-        "gemm_bwd_u_swiglu": W + R * d * 2 + R * 2 * F * 2 + R * 3 * F * 2,
-        "gemm_bwd_dx": 2 * W + R * 2 * F * 2 + R * d * 2,
-        "gemm_wgrad_down": W + R * d * 2 + R * F * 2,
-        "gemm_wgrad_gate_up": 2 * W + R * 2 * F * 2 + R * d * 2,
+        "fwd_megakernel": 3 * Wa + T * d * 2 + R * 2 * F * 2 + R * d * 2,
+        "gemm_up_swiglu": 2 * Wa + R * d * 2 + R * 3 * F * 2,
+        "gemm_down": Wa + R * F * 2 + R * d * 2,
+        "gemm_bwd_u_swiglu": Wa + R * d * 2 + R * 2 * F * 2 + R * 3 * F * 2,
+        "gemm_bwd_dx": 2 * Wa + R * 2 * F * 2 + R * d * 2,
+        "gemm_wgrad_down": Wall + R * d * 2 + R * F * 2,
+        "gemm_wgrad_gate_up": 2 * Wall + R * 2 * F * 2 + R * d * 2,
     }
 
 
-def layer_roofline(shape, peaks):
-    """Roofline time of one fwd+bwd: max(FLOPs / bf16 peak, compulsory bytes / HBM peak)."""
+def layer_roofline(shape, peaks, e_act: int):
+    """Roofline time of one fwd+bwd: max(FLOPs / bf16 peak, compulsory bytes / HBM peak).
+
+    Compulsory bytes: the active experts' weights read in the forward and again
+    in the backward, every expert's weight gradient written once, and the
+    layer's own inputs and outputs."""
     T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
     R = T * k
     flops = 18.0 * R * d * F
-    W = 3.0 * E * F * d * 2
+    Wa = 3.0 * e_act * F * d * 2
+    Wall = 3.0 * E * F * d * 2
     act = T * d * 2 * 4 + T * E * 4 * 2   # X, dY in; Y, dX out; logits in, dlogits out
-    byts = 2 * W + W + act                # weights read fwd + bwd, weight grads written
+    byts = 2 * Wa + Wall + act
     t_tc = flops / (peaks["bf16_tflops_sustained"] * 1e12)
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
     return {"flops": flops, "bytes": byts, "t_ms": max(t_tc, t_hbm) * 1e3,
             "bound": "hbm" if t_hbm >= t_tc else "tensor"}
+
+
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, mean
+# over the launches) from one single-pass ncu launch-list capture of this
+# bench's default workload.  The figures hold only for the kernel sources they
+# were taken on: their digest is kept beside them, and any change to a kernel
+# source makes measured_traffic() report null until a new capture is taken.
+NCU_TRAFFIC = {
+    "workload": WORKLOAD,
+    "csrc_sha256": "a49b012f7aa10f6e1f34f2d3245803f203e1b4f267afdb2ad070f2995767fc7d",
+    "bytes": {
+        "fwd_megakernel": 18770420275,
+        "gemm_wgrad_gate_up": 16191103232,
+        "gemm_bwd_dx": 10723478579,
+        "gemm_wgrad_down": 8502097459,
+        "gemm_bwd_u_swiglu": 6878221568,
+    },
+}
+
+
+def csrc_digest() -> str:
+    """sha256 over the CUDA/C++ sources of the extension (names and contents)."""
+    import hashlib
+    src = os.path.join(ROOT, "mixture_experts_layer_19_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(name.encode())
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    t = NCU_TRAFFIC
+    if workload != t["workload"] or kernel not in t["bytes"] or csrc_digest() != t["csrc_sha256"]:
+        return None
+    return t["bytes"][kernel]
+
+
+def active_experts(plan, saved, T):
+    """Number of experts that received at least one routed row, read from the
+    plan's own routing of the last forward."""
+    counts = plan.routing(saved, T)["counts"]
+    return int((counts > 0).sum().item())
 
 
 def load_peaks():
@@ -244,6 +301,8 @@ def bench_gpu(args):
     if plan.device_status() != 0:
         raise RuntimeError("device status set during warm-up")
     plan.kernel_times()  # discard warm-up records
+    e_act = active_experts(plan, saved, T)
+    plan.kernel_times()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -270,20 +329,26 @@ def bench_gpu(args):
     # ---- roofline of the dominant kernel (largest share of device time)
     peaks = load_peaks()
     R = T * k
-    ab = algorithmic_bytes(shape, R)
+    ab = algorithmic_bytes(shape, R, e_act)
     gemm_names = [n for n in ktimes if n in ab]
     dom = max(gemm_names, key=lambda n: ktimes[n][0])
     dom_ms = ktimes[dom][0] / ktimes[dom][1]
     achieved = ab[dom] / (dom_ms / 1e3) / 1e9
+    workload = WORKLOAD if not (args.experts or args.tokens) else f"profile_T{T}_E{E}"
+    traffic = measured_traffic(dom, workload)
     roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
             "peak_source": peaks["source"] + " hbm_gbs (STREAM copy)",
             "algorithmic_bytes": ab[dom], "avg_launch_ms": round(dom_ms, 4)}
+    per_kernel = {n: {"achieved_gbs": round(ab[n] / (ktimes[n][0] / ktimes[n][1] / 1e3) / 1e9, 1),
+                      "frac": round(ab[n] / (ktimes[n][0] / ktimes[n][1] / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                      "algorithmic_bytes": ab[n], "traffic": measured_traffic(n, workload)}
+                  for n in gemm_names}
     total_dev = sum(v[0] for v in ktimes.values())
     kernels = {n: {"ms_per_step": round(v[0] / args.steps, 4), "launches": v[1],
                    "share": round(v[0] / total_dev, 4)} for n, v in sorted(ktimes.items(), key=lambda x: -x[1][0])}
     launches = int(sum(v[1] for v in ktimes.values()))
-    lr = layer_roofline(shape, peaks)
+    lr = layer_roofline(shape, peaks, e_act)
 
     # ---- end-to-end through the public API with host buffers
     e2e = None if args.no_e2e else bench_e2e(args, plan, inp, Y, saved, grads, stream, dev, ws)
@@ -292,13 +357,15 @@ def bench_gpu(args):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if not (args.experts or args.tokens) else f"profile_T{T}_E{E}", "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
-                   "seed": SEED, "tokens_per_gpu": T, "parallelism": f"replicas{ws}",
+        "config": {"workload": workload, "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
+                   "seed": SEED, "tokens_per_gpu": T, "experts_active": e_act, "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass, 129 MB L2)"},
         "roofline": roof,
+        "kernel_rooflines": per_kernel,
         "layer_roofline": {"bound": lr["bound"], "t_ms": round(lr["t_ms"], 4),
                            "frac": round(lr["t_ms"] / ms_per_step, 4),
-                           "note": "max(18*R*d*F / sustained bf16 peak, weights read twice + dW written + I/O / HBM peak)"},
+                           "note": "max(18*R*d*F / sustained bf16 peak, active experts' weights read twice "
+                                   "+ all dW written + I/O / HBM peak)"},
         "kernels": kernels,
         "gpu_launches": launches,
         "clocks": clk,
@@ -352,12 +419,13 @@ def bench_mx_forward(args, dev, ws, peaks, alpha):
             raise RuntimeError("device status set in the MXFP8 forward")
         el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
         kt = plan.kernel_times()
+        e_act = active_experts(plan, saved, T)
         del plan, saved, Y
-        return el, kt, wq
+        return el, kt, wq, e_act
 
     # default MXFP8 schedule (separate kernels) and the ring megakernel beside it
-    el, kt, wq = run(0, args.steps)
-    el_ring, ktr, _ = run(moe.MOE_DEBUG_RING_MEGAKERNEL, max(3, args.steps // 2))
+    el, kt, wq, e_act = run(0, args.steps)
+    el_ring, ktr, _, _ = run(moe.MOE_DEBUG_RING_MEGAKERNEL, max(3, args.steps // 2))
     R = T * k
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # nominal fp8/bf16 dense ratio x measured bf16
     mk_ms = ktr["fwd_megakernel_mx"][0] / ktr["fwd_megakernel_mx"][1]
@@ -368,9 +436,9 @@ def bench_mx_forward(args, dev, ws, peaks, alpha):
     dn_tf = 2.0 * R * d * F / (dn_ms / 1e3) / 1e12
     ms = el / args.steps
     t_tc = 6.0 * R * d * F / (fp8_peak * 1e12) * 1e3
-    t_hbm = (3.0 * E * F * d * (1 + 1 / 32) + T * d * 2 * 2 + T * E * 4) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_hbm = (3.0 * e_act * F * d * (1 + 1 / 32) + T * d * 2 * 2 + T * E * 4) / (peaks["hbm_gbs"] * 1e9) * 1e3
     res = {
-        "workload": f"moe_layer_fwd_mxfp8_T{T}_d{d}_F{F}_E{E}_top{k}_zipf{alpha:g}",
+        "workload": f"moe_layer_fwd_mxfp8_T{T}_d{d}_F{F}_E{E}_top{k}_zipf{alpha:g}", "experts_active": e_act,
         "value": round(ws * T * args.steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
         "dtype": "e4m3+e8m0 (fp32 accumulate, bf16 out)",
         "roofline": {"kernel": "gemm_mx_up_swiglu", "bound": "tensor", "achieved": round(up_tf, 1),
@@ -437,12 +505,15 @@ def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha):
         raise RuntimeError("device status set in the MXFP8 fwd+bwd")
     el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
     kt = plan.kernel_times()
+    e_act = active_experts(plan, saved, T)
     R = T * k
     fp8_peak, bf16_peak = 2.0 * peaks["bf16_tflops_sustained"], peaks["bf16_tflops_sustained"]
     t_tc = (12.0 * R * d * F / fp8_peak + 6.0 * R * d * F / bf16_peak) / 1e12 * 1e3
-    t_hbm = (2 * 3.0 * E * F * d * (1 + 1 / 32) + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    # E4M3 weights of the active experts in both orientations, bf16 dW of every expert
+    t_hbm = (2 * 3.0 * e_act * F * d * (1 + 1 / 32) + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
     ms = el / steps
     res = {"workload": f"moe_layer_fwd_bwd_mxfp8_T{T}_zipf{alpha:g}", "T": T, "zipf_alpha": alpha,
+           "experts_active": e_act,
            "value": round(ws * T * steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
                               "frac": round(max(t_tc, t_hbm) / ms, 4)},

@@ -264,8 +264,14 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
-      const uint64_t pol_w = policy_evict_first();   // weights: streamed once
-      const uint64_t pol_a = policy_evict_last();    // activations: re-read by N tiles
+      // L2 policies, chosen by measurement at d=7168, F=2048, E=256, top-8.
+      // Grouped GEMMs: a weight tile is read by every M tile of its expert,
+      // by CTAs that drift apart in time; evict_last keeps it for the late
+      // ones (evict_first cost ~1 GB of DRAM re-reads and ~0.1 ms per launch).
+      // Weight-gradient GEMMs: the B source is streamed once per output tile
+      // (evict_first); the A rows are re-read by every tile of the expert.
+      const uint64_t pol_w = KindTraits<KIND>::grouped ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
       uint32_t s = 0, ph = 0;
       uint32_t issued_mask = 0, last_par = 0;
       bool ok = true;

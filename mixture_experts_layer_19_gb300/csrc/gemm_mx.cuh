@@ -155,7 +155,9 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // weight tiles are re-read by every M tile of their expert: evict_last,
+      // as in the bf16 grouped GEMMs
+      const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_a = policy_evict_last();
       uint32_t s = 0, ph = 0, issued_mask = 0, last_par = 0;
       bool ok = true;
