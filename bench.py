@@ -278,7 +278,8 @@ def bench_gpu(args):
         shape["T"] = args.tokens
     T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED + rank, alpha=ALPHA, device=dev)
-    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, device=local, debug_flags=moe.MOE_DEBUG_TIMING))
+    flags = moe.MOE_DEBUG_TIMING | (moe.MOE_DEBUG_SINGLE_CTA if args.single_cta else 0)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, device=local, debug_flags=flags))
     saved = plan.new_saved(T)
     Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     grads = {
@@ -652,6 +653,8 @@ def main(argv=None):
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurements")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="bf16 GEMMs one CTA per tile (no 2-CTA operand sharing), for comparison")
     ap.add_argument("--sweep", action="store_true",
                     help="MXFP8 fwd+bwd over T in {2048, 8192, 32768} x zipf {0, 1.1, 1.5} and a minibatch sweep")
     args = ap.parse_args(argv)

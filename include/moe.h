@@ -66,6 +66,11 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision_t;
  * is set.  Both schedules give bitwise identical results. */
 #define MOE_DEBUG_SEPARATE_KERNELS 0x4u /* gather / GEMM launches over full sorted buffers */
 #define MOE_DEBUG_RING_MEGAKERNEL 0x8u  /* MXFP8: use the ring-buffer megakernel */
+/* The separate bf16 GEMMs run as 2-CTA clusters whose two CTAs share one
+ * operand tile per pipeline stage (TMA multicast), halving its L2 reads; with
+ * this flag every GEMM runs one CTA per tile instead.  Results are bitwise
+ * identical either way. */
+#define MOE_DEBUG_SINGLE_CTA 0x10u
 
 typedef struct {
   int64_t T_max;          /* largest token count a call may pass */

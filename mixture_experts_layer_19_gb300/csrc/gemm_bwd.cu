@@ -11,31 +11,28 @@
 
 namespace moe {
 
-template <int KIND>
-static cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t st) {
-  gemm_kernel<KIND><<<grid, KindTraits<KIND>::threads, KindTraits<KIND>::smem_bytes, st>>>(a);
-  return cudaGetLastError();
-}
-template <int KIND>
-static cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              KindTraits<KIND>::smem_bytes);
-}
-
-cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, cudaStream_t st) {
+cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st) {
   switch (kind) {
-    case kBwdU: return launch_one<kBwdU>(a, grid, st);
-    case kBwdX: return launch_one<kBwdX>(a, grid, st);
-    case kWgradD: return launch_one<kWgradD>(a, grid, st);
-    default: return launch_one<kWgradGU>(a, grid, st);
+    case kBwdU: return gemm_launch<kBwdU>(a, grid, pair, st);
+    case kBwdX: return gemm_launch<kBwdX>(a, grid, pair, st);
+    case kWgradD: return gemm_launch<kWgradD>(a, grid, pair, st);
+    default: return gemm_launch<kWgradGU>(a, grid, pair, st);
   }
 }
 cudaError_t prepare_gemm_bwd(int kind) {
   switch (kind) {
-    case kBwdU: return prepare_one<kBwdU>();
-    case kBwdX: return prepare_one<kBwdX>();
-    case kWgradD: return prepare_one<kWgradD>();
-    default: return prepare_one<kWgradGU>();
+    case kBwdU: return gemm_prepare<kBwdU>();
+    case kBwdX: return gemm_prepare<kBwdX>();
+    case kWgradD: return gemm_prepare<kWgradD>();
+    default: return gemm_prepare<kWgradGU>();
+  }
+}
+int gemm_pair_grid_bwd(int kind) {
+  switch (kind) {
+    case kBwdU: return gemm_pair_grid<kBwdU>();
+    case kBwdX: return gemm_pair_grid<kBwdX>();
+    case kWgradD: return gemm_pair_grid<kWgradD>();
+    default: return gemm_pair_grid<kWgradGU>();
   }
 }
 

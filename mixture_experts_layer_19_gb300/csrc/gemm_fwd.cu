@@ -8,20 +8,10 @@
 
 namespace moe {
 
-template <int KIND>
-static cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t st) {
-  gemm_kernel<KIND><<<grid, KindTraits<KIND>::threads, KindTraits<KIND>::smem_bytes, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st) {
+  return kind == kUp ? gemm_launch<kUp>(a, grid, pair, st) : gemm_launch<kDown>(a, grid, pair, st);
 }
-template <int KIND>
-static cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              KindTraits<KIND>::smem_bytes);
-}
-
-cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, cudaStream_t st) {
-  return kind == kUp ? launch_one<kUp>(a, grid, st) : launch_one<kDown>(a, grid, st);
-}
-cudaError_t prepare_gemm_fwd(int kind) { return kind == kUp ? prepare_one<kUp>() : prepare_one<kDown>(); }
+cudaError_t prepare_gemm_fwd(int kind) { return kind == kUp ? gemm_prepare<kUp>() : gemm_prepare<kDown>(); }
+int gemm_pair_grid_fwd(int kind) { return kind == kUp ? gemm_pair_grid<kUp>() : gemm_pair_grid<kDown>(); }
 
 }  // namespace moe

@@ -164,6 +164,36 @@ def test_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers
     assert rel_err(Ya, Yr) <= BF16_TOL
 
 
+@pytest.mark.parametrize("case", [(700, 512, 512, 24, 4, 1.1), (300, 768, 768, 16, 3, 1.5), (64, 256, 512, 8, 2, 0.0)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_paired_gemms_match_single_cta_bitwise(case):
+    """2-CTA clusters that share one operand tile per stage (B over two M tiles
+    of an expert, or A over two N tiles of an odd last M tile; the weight
+    gradients pair M tiles) compute every tile exactly as one CTA does.
+    d=768 / F=768 give odd N-tile counts, where those GEMMs stay single-CTA."""
+    T, d, F, E, k, alpha = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=43, alpha=alpha)
+    pair = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS)
+    one = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS | moe.MOE_DEBUG_SINGLE_CTA)
+    ring = _plan(T, d, F, E, k)
+    outs = []
+    for p in (pair, one, ring):
+        Y, s = p.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+        gr = p.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], s)
+        outs.append((Y, gr))
+    torch.cuda.synchronize()
+    assert all(p.device_status() == 0 for p in (pair, one, ring))
+    for Y, gr in outs[1:]:
+        assert torch.equal(outs[0][0], Y)
+        for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+            assert torch.equal(outs[0][1][key], gr[key]), key
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    gref = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    assert rel_err(outs[0][0], Yr) <= BF16_TOL
+    for key in ("dX", "dWg", "dWu", "dWd"):
+        assert rel_err(outs[0][1][key], gref[key]) <= BF16_TOL, key
+
+
 def test_ring_config_is_validated():
     with pytest.raises(moe.MoEError):
         moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, ring_slots=1))
