@@ -136,7 +136,9 @@ def algorithmic_bytes(shape, R: int, e_act: int):
     Wa = e_act * F * d * 2     # one weight tensor, active experts only
     Wall = E * F * d * 2       # one weight-gradient tensor, all experts
     return {
-        "fwd_megakernel": 3 * Wa + T * d * 2 + R * 2 * F * 2 + R * d * 2,
+        # one-launch forward: also reads the logits and writes Y (routing and
+        # combine run inside it)
+        "fwd_megakernel": 3 * Wa + T * d * 2 + R * 2 * F * 2 + R * d * 2 + T * shape["E"] * 4 + T * d * 2,
         "gemm_up_swiglu": 2 * Wa + R * d * 2 + R * 3 * F * 2,
         "gemm_down": Wa + R * F * 2 + R * d * 2,
         "gemm_bwd_u_swiglu": Wa + R * d * 2 + R * 2 * F * 2 + R * 3 * F * 2,
@@ -374,6 +376,8 @@ def bench_gpu(args):
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, k, args.cpu_tokens)
+    if not args.no_ring:
+        out["ring_megakernel_forward"] = bench_ring_forward(args, plan, inp, Y, saved, stream, dev, ws)
     if not args.no_mx:
         del plan, inp, grads, saved, Y
         torch.cuda.empty_cache()
@@ -386,6 +390,44 @@ def bench_gpu(args):
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def bench_ring_forward(args, plan_sep, inp, Y, saved, stream, dev, ws):
+    """Forward-only time of the three bf16 forward schedules on the headline
+    workload: separate kernels (the default), the ring megakernel as one
+    launch (routing and combine inside), and the ring megakernel between
+    separate routing / combine launches.  All are bitwise identical."""
+    from mixture_experts_layer_19_gb300 import moe
+    c = plan_sep.cfg
+    res = {}
+    schedules = (("separate", plan_sep), ("ring_one_launch", None), ("ring_multi_launch", None))
+    flag_of = {"ring_one_launch": moe.MOE_DEBUG_RING_MEGAKERNEL,
+               "ring_multi_launch": moe.MOE_DEBUG_RING_MEGAKERNEL | moe.MOE_DEBUG_MULTI_LAUNCH}
+    for name, plan in schedules:
+        own = plan is None
+        if own:
+            plan = moe.Plan(moe.Config(T_max=c.T_max, d=c.d, F=c.F, E=c.E, k=c.k, device=dev.index,
+                                       debug_flags=flag_of[name] | moe.MOE_DEBUG_TIMING))
+        for _ in range(args.warmup):
+            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        torch.cuda.synchronize(dev)
+        plan.kernel_times()
+        steps = max(3, args.steps // 2)
+        barrier(ws)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if plan.device_status() != 0:
+            raise RuntimeError(f"device status set in the {name} forward")
+        kt = plan.kernel_times()
+        res[name] = {"fwd_ms": round(max_over_ranks(ev0.elapsed_time(ev1), ws, dev) / steps, 4),
+                     "kernels": {n: round(v[0] / steps, 4) for n, v in kt.items()}}
+        if own:
+            del plan
+    return res
 
 
 def bench_mx_forward(args, dev, ws, peaks, alpha):
@@ -537,7 +579,8 @@ def bench_minibatch_sweep(args, dev, ws, T=8192, alpha=ALPHA):
     stream = torch.cuda.current_stream(dev)
     out = []
     for mb in (256, 512, 1024, 2048, 0, 4096, 8192):
-        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, minibatch_rows=mb, device=dev.index))
+        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, minibatch_rows=mb, device=dev.index,
+                                   debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL))
         saved = plan.new_saved(T)
         Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         for _ in range(args.warmup):
@@ -657,6 +700,7 @@ def main(argv=None):
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurements")
+    ap.add_argument("--no-ring", action="store_true", help="skip the ring-megakernel forward line")
     ap.add_argument("--single-cta", action="store_true",
                     help="bf16 GEMMs one CTA per tile (no 2-CTA operand sharing), for comparison")
     ap.add_argument("--sweep", action="store_true",

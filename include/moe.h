@@ -60,17 +60,25 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision_t;
 /* debug_flags bits */
 #define MOE_DEBUG_IDENTITY_EXPERTS 0x1u /* experts return their input (y = x); GEMMs skipped */
 #define MOE_DEBUG_TIMING 0x2u           /* bracket each kernel with CUDA events (moe_kernel_times) */
-/* Forward schedule.  BF16 plans run the ring-buffer megakernel unless
- * MOE_DEBUG_SEPARATE_KERNELS is set; MXFP8 plans run separate kernels (on
- * GB300 they are faster at the measured shapes) unless MOE_DEBUG_RING_MEGAKERNEL
- * is set.  Both schedules give bitwise identical results. */
-#define MOE_DEBUG_SEPARATE_KERNELS 0x4u /* gather / GEMM launches over full sorted buffers */
-#define MOE_DEBUG_RING_MEGAKERNEL 0x8u  /* MXFP8: use the ring-buffer megakernel */
+/* Forward schedule.  By default both precisions run separate kernels
+ * (routing, gather, grouped GEMMs over the full sorted buffers, combine): with
+ * the paired-CTA GEMMs that is the fastest schedule measured on GB300.
+ * MOE_DEBUG_RING_MEGAKERNEL selects the ring-buffer megakernel (movers fill a
+ * fixed ring of minibatch slots, compute CTAs run the [a|b] and down tiles
+ * minibatch by minibatch); for BF16 it is one launch that also routes and
+ * combines, or, with MOE_DEBUG_MULTI_LAUNCH, the megakernel between separate
+ * routing and combine launches.  Every schedule gives bitwise identical
+ * results. */
+#define MOE_DEBUG_SEPARATE_KERNELS 0x4u /* force separate kernels (overrides the ring flag) */
+#define MOE_DEBUG_RING_MEGAKERNEL 0x8u  /* use the ring-buffer megakernel */
 /* The separate bf16 GEMMs run as 2-CTA clusters whose two CTAs share one
  * operand tile per pipeline stage (TMA multicast), halving its L2 reads; with
  * this flag every GEMM runs one CTA per tile instead.  Results are bitwise
  * identical either way. */
 #define MOE_DEBUG_SINGLE_CTA 0x10u
+/* BF16 ring schedule: routing, layout, the minibatch plan and the combine as
+ * separate launches around the ring megakernel instead of inside it. */
+#define MOE_DEBUG_MULTI_LAUNCH 0x20u
 
 typedef struct {
   int64_t T_max;          /* largest token count a call may pass */

@@ -190,6 +190,10 @@ struct moe_plan_s {
   int32_t *mb_start = nullptr, *phase_start = nullptr, *n_mb = nullptr;
   int movers = 0, slots = 0, mbt = 0, cap = 0, nm_max = 0;
   CUtensorMap m_ring_x, m_ring_h, m_ring_h_st;
+  // one-launch forward: per-(token, 256-column block) arrival counts of the
+  // in-kernel combine; grid-barrier arrivals and CTA exits (zero between launches)
+  int* tok_cnt = nullptr;
+  unsigned long long* gbar = nullptr;
   // timing (MOE_DEBUG_TIMING)
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
@@ -250,6 +254,42 @@ bool use_pair(const moe_plan_s* p, int kind) {
   return nt % 2 == 0;
 }
 int gemm_grid(const moe_plan_s* p, int kind) { return use_pair(p, kind) ? p->pair_grid[kind] : p->num_sms; }
+
+// Ring-pipeline fields of the BF16 forward megakernel's argument block.
+MegaArgs mega_args(moe_plan_s* p, const RoutingPtrs& rp, const void* X, const CUtensorMap& m_ab_st) {
+  const moe_config_t& c = p->cfg;
+  MegaArgs m;
+  memset(&m, 0, sizeof(m));
+  m.mapXr = p->m_ring_x;
+  m.mapWg = p->m_Wg_k;
+  m.mapWu = p->m_Wu_k;
+  m.mapWd = p->m_Wd_k;
+  m.mapHr = p->m_ring_h;
+  m.mapHrSt = p->m_ring_h_st;
+  m.mapABSt = m_ab_st;
+  m.mapYsSt = p->m_Ys_st;
+  m.X = reinterpret_cast<const uint4*>(X);
+  m.ring_x = reinterpret_cast<uint4*>(p->ring_x);
+  m.perm_src = rp.perm_src;
+  m.mtile_off = rp.mtile_off;
+  m.mb_start = p->mb_start;
+  m.phase_start = p->phase_start;
+  m.n_mb = p->n_mb;
+  m.claim = p->counters;
+  m.gathered = p->counters + 1;
+  m.mb_done = p->counters + 1 + p->nm_max;
+  m.g1_done = p->counters + 1 + 2 * p->nm_max;
+  m.status = p->status;
+  m.timeout_ns = (uint64_t)c.wait_timeout_ns;
+  m.E = c.E;
+  m.d = c.d;
+  m.F = c.F;
+  m.k = c.k;
+  m.movers = p->movers;
+  m.slots = p->slots;
+  m.slot_rows = p->cap * BM;
+  return m;
+}
 
 GemmArgs base_args(moe_plan_s* p, const RoutingPtrs& rp) {
   GemmArgs a;
@@ -408,6 +448,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_mb = m; m += align256(((size_t)p->nm_max + 1) * 4);
     const size_t o_ph = m; m += align256((2 * (size_t)p->nm_max + 1) * 4);
     const size_t o_nm = m; m += 256;
+    const size_t o_gb = m; m += 256;
+    const size_t o_tc = m; m += align256((size_t)c.T_max * (c.d / BN) * 4);
     err = cudaMalloc(&p->ring_ws, m);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -421,6 +463,15 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->mb_start = reinterpret_cast<int32_t*>(rb + o_mb);
     p->phase_start = reinterpret_cast<int32_t*>(rb + o_ph);
     p->n_mb = reinterpret_cast<int32_t*>(rb + o_nm);
+    p->gbar = reinterpret_cast<unsigned long long*>(rb + o_gb);
+    p->tok_cnt = reinterpret_cast<int*>(rb + o_tc);
+    err = cudaMemset(p->gbar, 0, 2 * sizeof(unsigned long long));
+    if (err != cudaSuccess) {
+      cudaFree(p->ring_ws);
+      cudaFree(p->ws);
+      delete p;
+      return cuda_fail(err, "moe_plan: cudaMemset of the grid-barrier counter");
+    }
     const uint64_t ring_rows = p->slots * slot_rows;
     ok = map_kmajor(&p->m_ring_x, p->ring_x, c.d, ring_rows) && map_kmajor(&p->m_ring_h, p->ring_h, c.F, ring_rows) &&
          map_store(&p->m_ring_h_st, p->ring_h, c.F, ring_rows);
@@ -550,6 +601,28 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   if (!ident && !map_store(&m_ab_st, static_cast<char*>(saved) + L.ab, 2 * c.F, L.rows))
     return fail(MOE_ERR_CUDA, "moe_forward: saved tensor map");
 
+  // BF16 ring schedule, one launch: routing, layout, ring pipeline and
+  // combine in one cooperative persistent kernel
+  const bool ring = (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS);
+  if (!mx && !ident && ring && !(c.debug_flags & MOE_DEBUG_MULTI_LAUNCH)) {
+    MegaArgs m = mega_args(p, rp, X, m_ab_st);
+    m.logits = logits;
+    m.rp = rp;
+    m.chunk_hist = p->chunk_hist;
+    m.chunk_base = p->chunk_base;
+    m.counters = p->counters;
+    m.counters_len = 1 + 3 * p->nm_max;
+    m.Ys = reinterpret_cast<const uint4*>(p->Ys);
+    m.Y = reinterpret_cast<uint4*>(Y);
+    m.tok_cnt = p->tok_cnt;
+    m.gbar = p->gbar;
+    m.T = Ti;
+    m.mbt = p->mbt;
+    m.cap = p->cap;
+    err = timed_launch(p, "fwd_megakernel", st, [&] { return launch_fwd_megakernel(m, p->num_sms, true, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: one-launch megakernel launch");
+    return MOE_OK;
+  }
   err = timed_launch(p, "router_topk_hist", st,
                      [&] { return launch_router(logits, Ti, c.E, c.k, p->chunk_hist, rp, st); });
   if (err == cudaSuccess)
@@ -559,7 +632,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     err = timed_launch(p, "layout_permute", st,
                        [&] { return launch_permute(Ti, c.E, c.k, p->chunk_base, rp, st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: routing launch");
-  if (mx && (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS)) {
+  if (mx && ring) {
     // MXFP8 ring megakernel: movers gather + quantise into the slots, compute
     // CTAs run the block-scaled [a|b]+SwiGLU (h re-quantised into the slot)
     // and down tiles minibatch by minibatch
@@ -658,7 +731,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
     return MOE_OK;
   }
-  if (!ident && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS)) {
+  if (!ident && ring) {
     // one persistent launch: movers fill ring slots, compute CTAs run the
     // [a|b]+SwiGLU and down tiles minibatch by minibatch
     const int counters_len = 1 + 3 * p->nm_max;
@@ -667,37 +740,8 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
                                      p->counters, p->mb_start, p->phase_start, p->n_mb, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: minibatch plan launch");
-    MegaArgs m;
-    memset(&m, 0, sizeof(m));
-    m.mapXr = p->m_ring_x;
-    m.mapWg = p->m_Wg_k;
-    m.mapWu = p->m_Wu_k;
-    m.mapWd = p->m_Wd_k;
-    m.mapHr = p->m_ring_h;
-    m.mapHrSt = p->m_ring_h_st;
-    m.mapABSt = m_ab_st;
-    m.mapYsSt = p->m_Ys_st;
-    m.X = reinterpret_cast<const uint4*>(X);
-    m.ring_x = reinterpret_cast<uint4*>(p->ring_x);
-    m.perm_src = rp.perm_src;
-    m.mtile_off = rp.mtile_off;
-    m.mb_start = p->mb_start;
-    m.phase_start = p->phase_start;
-    m.n_mb = p->n_mb;
-    m.claim = p->counters;
-    m.gathered = p->counters + 1;
-    m.mb_done = p->counters + 1 + p->nm_max;
-    m.g1_done = p->counters + 1 + 2 * p->nm_max;
-    m.status = p->status;
-    m.timeout_ns = (uint64_t)c.wait_timeout_ns;
-    m.E = c.E;
-    m.d = c.d;
-    m.F = c.F;
-    m.k = c.k;
-    m.movers = p->movers;
-    m.slots = p->slots;
-    m.slot_rows = p->cap * BM;
-    err = timed_launch(p, "fwd_megakernel", st, [&] { return launch_fwd_megakernel(m, p->num_sms, st); });
+    const MegaArgs m = mega_args(p, rp, X, m_ab_st);
+    err = timed_launch(p, "fwd_megakernel", st, [&] { return launch_fwd_megakernel(m, p->num_sms, false, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: megakernel launch");
     const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
     err = timed_launch(p, "combine", st,

@@ -66,7 +66,7 @@ struct MegaArgs;
 cudaError_t launch_plan_minibatches(const int32_t* mtile_off, int E, int mbt, int cap, int nt1, int nt2,
                                     int counters_len, int* counters, int32_t* mb_start, int32_t* phase_start,
                                     int32_t* n_mb, cudaStream_t st);
-cudaError_t launch_fwd_megakernel(const MegaArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_fwd_megakernel(const MegaArgs& a, int grid, bool fused, cudaStream_t st);  // fused: one-launch forward
 cudaError_t prepare_fwd_megakernel();
 struct MegaMxArgs;
 cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, cudaStream_t st);

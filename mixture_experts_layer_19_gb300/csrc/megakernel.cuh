@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace moe {
 
 struct MegaArgs {
@@ -20,9 +22,9 @@ struct MegaArgs {
   uint4* ring_x;        // [slots * slot_rows, d] bf16
   const int32_t* perm_src;
   const int32_t* mtile_off;   // [E+1]
-  const int32_t* mb_start;    // [n_mb+1] first 128-row tile of each minibatch
-  const int32_t* phase_start; // [2 n_mb + 1] first claim index of each phase
-  const int32_t* n_mb;
+  int32_t* mb_start;          // [n_mb+1] first 128-row tile of each minibatch
+  int32_t* phase_start;       // [2 n_mb + 1] first claim index of each phase
+  int32_t* n_mb;              // (written by the plan step, or in-kernel by the one-launch forward)
   int* claim;
   int* gathered;
   int* g1_done;
@@ -30,6 +32,19 @@ struct MegaArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int E, d, F, k, movers, slots, slot_rows;
+  // One-launch forward (fwd_megakernel<true>): routing, minibatch planning
+  // and the combine run inside the kernel.
+  const float* logits;        // [T, E] router logits
+  RoutingPtrs rp;             // routing state, written into the saved context
+  int32_t* chunk_hist;        // [ceil(T/64), E] per-chunk expert counts
+  int32_t* chunk_base;        // [ceil(T/64), E] per-chunk running sums
+  int* counters;              // claim, gathered, g1_done, mb_done (zeroed in the kernel)
+  int counters_len;
+  const uint4* Ys;            // sorted y rows (what mapYsSt stores), read back by the combine
+  uint4* Y;                   // [T, d] bf16 layer output
+  int* tok_cnt;               // [T * d/256] y blocks stored per (token, 256-column block)
+  unsigned long long* gbar;   // [2] grid-barrier arrivals, CTA exits (both zero between launches)
+  int T, mbt, cap;
 };
 
 // One claimed unit of work of a ring megakernel.

@@ -126,6 +126,41 @@ __device__ __forceinline__ bool wait_counter_geq(const int* p, int target, const
   }
 }
 
+// 64-bit variant for counters that grow across launches.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_counter64_geq(const unsigned long long* p, unsigned long long target,
+                                                   const WaitCtl& w) {
+  if (ld_acquire_gpu_u64(p) >= target) return true;
+  uint64_t deadline = 0;
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(100);
+    if (ld_acquire_gpu_u64(p) >= target) return true;
+    if ((it & 31u) == 0) {
+      if (*w.abort) return false;
+      if (w.status && *reinterpret_cast<volatile int32_t*>(w.status) != 0) {
+        *w.abort = 1;
+        return false;
+      }
+      const uint64_t now = globaltimer_ns();
+      if (deadline == 0) deadline = now + w.timeout_ns;
+      else if (now > deadline) {
+        raise_abort(w, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+// Integer add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -18,17 +18,15 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "routing.cuh"
 
 namespace moe {
 
-constexpr int kRouteChunk = 64;   // tokens per router block / permutation chunk
 constexpr int kRouteThreads = 256;
 
 // -----------------------------------------------------------------------------
-// S1: one warp per token.  Lane l holds logits l, l+32, ...; k rounds of a
-// warp arg-max (larger logit wins, lower id on ties) pick the experts in
-// descending order; weights are the softmax over the k picked logits, taken
-// relative to the first (largest) one.  The block also histograms its chunk.
+// S1: one warp per token (route_token, routing.cuh); the block also
+// histograms its chunk of kRouteChunk tokens.
 // -----------------------------------------------------------------------------
 __global__ void __launch_bounds__(kRouteThreads) router_kernel(const float* __restrict__ logits, int T, int E,
                                                                  int k, int32_t* __restrict__ idx,
@@ -38,59 +36,10 @@ __global__ void __launch_bounds__(kRouteThreads) router_kernel(const float* __re
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const int nper = (E + 31) >> 5;
   for (int tt = warp; tt < kRouteChunk; tt += kRouteThreads / 32) {
     const int t = blockIdx.x * kRouteChunk + tt;
     if (t >= T) break;
-    const float* row = logits + (size_t)t * E;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (i < nper && e < E) ? __ldg(row + e) : -INFINITY;
-    }
-    uint32_t taken = 0;
-    int my_id = 0;
-    float my_val = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      float best = -INFINITY;
-      int bid = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = lane + 32 * i;
-        if (i < nper && e < E && !((taken >> i) & 1u)) {
-          if (v[i] > best || (v[i] == best && e < bid)) {
-            best = v[i];
-            bid = e;
-          }
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bid, off);
-        if (ob > best || (ob == best && oi < bid)) {
-          best = ob;
-          bid = oi;
-        }
-      }
-      if (bid == 0x7fffffff) bid = 0;  // only reachable with NaN logits (outside the contract)
-      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-      if (lane == j) {
-        my_id = bid;
-        my_val = best;
-      }
-    }
-    const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
-    const float z = lane < k ? expf(my_val - vmax) : 0.0f;
-    float sum = z;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane < k) {
-      idx[(size_t)t * k + lane] = my_id;
-      w[(size_t)t * k + lane] = z / sum;
-      atomicAdd(&hist[my_id], 1);
-    }
+    route_token(logits, t, E, k, lane, idx, w, hist);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
@@ -168,29 +117,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
 __global__ void __launch_bounds__(32) permute_kernel(const int32_t* __restrict__ chunk_base, int T, int E, int k,
                                                      RoutingPtrs rp) {
   extern __shared__ int cursor[];
-  const int lane = threadIdx.x;
-  const int c = blockIdx.x;
-  for (int e = lane; e < E; e += 32) cursor[e] = rp.poff[e] + chunk_base[(size_t)c * E + e];
-  __syncwarp();
-  const int p0 = c * kRouteChunk * k;
-  const int p1 = min(T, (c + 1) * kRouteChunk) * k;
-  for (int base = p0; base < p1; base += 32) {
-    const int p = base + lane;
-    const bool valid = p < p1;
-    const int e = valid ? rp.idx[p] : -1;
-    const unsigned grp = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(grp & ((1u << lane) - 1u));
-    int slot = 0;
-    if (valid) slot = cursor[e];
-    __syncwarp();
-    if (valid && rank == 0) cursor[e] = slot + __popc(grp);
-    __syncwarp();
-    if (valid) {
-      const int dst = slot + rank;
-      rp.dest[p] = dst;
-      rp.perm_src[dst] = p;
-    }
-  }
+  permute_chunk(chunk_base, T, E, k, blockIdx.x, rp, cursor, threadIdx.x);
 }
 
 // -----------------------------------------------------------------------------
@@ -236,35 +163,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
                                                       const float* __restrict__ w, int T, int k, int d,
                                                       uint4* __restrict__ Y) {
   const int nvec = d / 8;
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-      float acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const int r = __ldg(dest + (size_t)t * k + j);
-        const float wj = w ? __ldg(w + (size_t)t * k + j) : 1.0f;
-        const uint4 v = __ldg(S + (size_t)r * nvec + i);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]));
-          acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
-          acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
-        }
-      }
-      uint4 o;
-      __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
-      __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4], acc[5]);
-      __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6], acc[7]);
-      o.x = *reinterpret_cast<uint32_t*>(&b0);
-      o.y = *reinterpret_cast<uint32_t*>(&b1);
-      o.z = *reinterpret_cast<uint32_t*>(&b2);
-      o.w = *reinterpret_cast<uint32_t*>(&b3);
-      Y[(size_t)t * nvec + i] = o;
-    }
-  }
+  for (int t = blockIdx.x; t < T; t += gridDim.x)
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x)
+      Y[(size_t)t * nvec + i] = combine_vec<true>(S, dest, w, t, k, nvec, i);
 }
 
 // -----------------------------------------------------------------------------

@@ -122,11 +122,12 @@ def test_k_equals_E():
         assert rel_err(out[key], gr[key]) <= BF16_TOL, key
 
 
-def test_bitwise_deterministic_over_10_runs():
+@pytest.mark.parametrize("flags", [0, moe.MOE_DEBUG_RING_MEGAKERNEL], ids=["separate", "ring_one_launch"])
+def test_bitwise_deterministic_over_10_runs(flags):
     T, d, F, E, k = 512, 512, 512, 16, 4
     for alpha in (0.0, 1.1, 1.5):
         g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=12, alpha=alpha)
-        plan = _plan(T, d, F, E, k)
+        plan = _plan(T, d, F, E, k, flags=flags)
         ref = None
         for _ in range(10):
             Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
@@ -149,7 +150,7 @@ def test_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers
     T, d, F, E, k = 700, 512, 512, 24, 4
     g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=31, alpha=1.1)
     ring = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, minibatch_rows=mb_rows, ring_slots=slots,
-                               mover_ctas=movers))
+                               mover_ctas=movers, debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL))
     sep = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS)
     Ya, sa = ring.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
     Yb, sb = sep.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
@@ -173,9 +174,9 @@ def test_paired_gemms_match_single_cta_bitwise(case):
     d=768 / F=768 give odd N-tile counts, where those GEMMs stay single-CTA."""
     T, d, F, E, k, alpha = case
     g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=43, alpha=alpha)
-    pair = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS)
-    one = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS | moe.MOE_DEBUG_SINGLE_CTA)
-    ring = _plan(T, d, F, E, k)
+    pair = _plan(T, d, F, E, k)
+    one = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SINGLE_CTA)
+    ring = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_RING_MEGAKERNEL)
     outs = []
     for p in (pair, one, ring):
         Y, s = p.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
@@ -192,6 +193,60 @@ def test_paired_gemms_match_single_cta_bitwise(case):
     assert rel_err(outs[0][0], Yr) <= BF16_TOL
     for key in ("dX", "dWg", "dWu", "dWd"):
         assert rel_err(outs[0][1][key], gref[key]) <= BF16_TOL, key
+
+
+@pytest.mark.parametrize("case", [(700, 512, 512, 24, 4, 1.1), (1000, 256, 256, 64, 8, 1.5), (33, 256, 512, 8, 2, 0.0)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_one_launch_forward_matches_multi_launch_and_separate_bitwise(case):
+    """The BF16 ring schedule's one-launch forward routes, lays out, plans
+    minibatches and combines inside the persistent kernel (the combine is done
+    by the last of a token's k down tiles to arrive).  Routing, saved context
+    and Y must equal the multi-launch ring schedule and the separate kernels."""
+    T, d, F, E, k, alpha = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=47, alpha=alpha)
+    ring = moe.MOE_DEBUG_RING_MEGAKERNEL
+    plans = [_plan(T, d, F, E, k, flags=ring), _plan(T, d, F, E, k, flags=ring | moe.MOE_DEBUG_MULTI_LAUNCH),
+             _plan(T, d, F, E, k)]
+    outs = []
+    for p in plans:
+        Y, s = p.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+        outs.append((Y, s, p.routing(s, T)))
+    torch.cuda.synchronize()
+    assert all(p.device_status() == 0 for p in plans)
+    for Y, s, r in outs[1:]:
+        assert torch.equal(outs[0][0], Y)
+        for key in ("idx", "w", "counts", "offsets", "perm_src", "dest"):
+            assert torch.equal(outs[0][2][key], r[key]), key
+    idx_ref, _ = moe_ref.route(h["logits"], k)
+    assert np.array_equal(outs[0][2]["idx"].cpu().numpy(), idx_ref)
+    Yr, _ = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    assert rel_err(outs[0][0], Yr) <= BF16_TOL
+
+
+@pytest.mark.parametrize("flags", [0, moe.MOE_DEBUG_RING_MEGAKERNEL], ids=["separate", "ring_one_launch"])
+def test_forward_replays_from_a_cuda_graph(flags):
+    """A captured forward can be replayed: the enqueued work needs no host
+    state, and the one-launch forward's grid barriers reset themselves at the
+    end of every launch."""
+    T, d, F, E, k = 300, 256, 512, 16, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=48, alpha=1.1)
+    plan = _plan(T, d, F, E, k, flags=flags)
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+    stream.synchronize()
+    ref = Y.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+    for _ in range(3):
+        Y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert torch.equal(Y, ref)
 
 
 def test_ring_config_is_validated():
