@@ -14,6 +14,9 @@ Recipe (one ``torch.Generator`` seeded with ``seed``; draws in this order):
 * ``Wg``, ``Wu`` [E, F, d]  N(0, std=1/sqrt(d)), bf16, drawn expert by expert.
 * ``Wd``     [E, d, F]  N(0, std=1/sqrt(F)), bf16, drawn expert by expert.
 * ``dY``     [T, d]    N(0, 1), bf16 (the upstream gradient).
+* ``Wr``     [E, d]    N(0, std=1/sqrt(d)), bf16, the router weight, drawn
+  last and only when asked for (``router=True``), so the draws above do not
+  depend on it.
 
 The layer shape used by the pages' benchmark models is hidden 7168 and expert
 width 2048 (Mixture-of-Kittens coverage, kucoin page, section 02); the weights
@@ -49,6 +52,7 @@ class LayerInputs:
     Wu: Optional[torch.Tensor]
     Wd: Optional[torch.Tensor]
     dY: torch.Tensor
+    Wr: Optional[torch.Tensor] = None
 
 
 def zipf_bias(E: int, alpha: float, gen: torch.Generator, device) -> torch.Tensor:
@@ -60,7 +64,7 @@ def zipf_bias(E: int, alpha: float, gen: torch.Generator, device) -> torch.Tenso
 
 
 def make_inputs(shape: LayerShape, seed: int = 0, alpha: float = 0.0,
-                device="cpu", weights: bool = True) -> LayerInputs:
+                device="cpu", weights: bool = True, router: bool = False) -> LayerInputs:
     """Draw the layer inputs on ``device`` following the recipe above."""
     T, d, F, E = shape.T, shape.d, shape.F, shape.E
     gen = torch.Generator(device=device)
@@ -78,7 +82,10 @@ def make_inputs(shape: LayerShape, seed: int = 0, alpha: float = 0.0,
             for e in range(E):
                 W[e].copy_(torch.randn(W.shape[1:], generator=gen, device=device) * s)
     dY = torch.randn((T, d), generator=gen, device=device).to(torch.bfloat16)
-    return LayerInputs(X=X, logits=logits.contiguous(), Wg=Wg, Wu=Wu, Wd=Wd, dY=dY)
+    Wr = None
+    if router:
+        Wr = (torch.randn((E, d), generator=gen, device=device) / math.sqrt(d)).to(torch.bfloat16)
+    return LayerInputs(X=X, logits=logits.contiguous(), Wg=Wg, Wu=Wu, Wd=Wd, dY=dY, Wr=Wr)
 
 
 def to_f64(t: torch.Tensor):

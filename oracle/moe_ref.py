@@ -54,6 +54,28 @@ def silu(a):
 
 
 # ----------------------------------------------------------------------------
+# 0. Router GEMM, the step before the layer: logits = X Wr^T.
+# ----------------------------------------------------------------------------
+def router_logits(X, Wr):
+    """logits[t, e] = sum_i X[t, i] Wr[e, i], in fp64.
+
+    The pages say the router re-decides each token's experts at every step
+    (kucoin page, section 01) but print no router.  The plain reading: one
+    linear map from the token to one logit per expert, weight Wr [E, d] in
+    the [out, in] convention, no bias.
+    """
+    return np.asarray(X, dtype=np.float64) @ np.asarray(Wr, dtype=np.float64).T
+
+
+def router_backward(X, Wr, dlogits):
+    """Gradients of <dlogits, X Wr^T>: dX = dlogits Wr, dWr = dlogits^T X (fp64)."""
+    X = np.asarray(X, dtype=np.float64)
+    Wr = np.asarray(Wr, dtype=np.float64)
+    G = np.asarray(dlogits, dtype=np.float64)
+    return {"dX": G @ Wr, "dWr": G.T @ X}
+
+
+# ----------------------------------------------------------------------------
 # 1. Router: top-k experts per token and their gate weights.
 # ----------------------------------------------------------------------------
 def route(logits, k):
