@@ -172,6 +172,31 @@ moe_status_t moe_get_routing(moe_plan_t plan, int64_t T, const void* saved, int3
                              float* w, int32_t* counts, int32_t* offsets, int32_t* perm_src,
                              int32_t* dest, moe_stream_t stream);
 
+/* Router GEMM, the step before the layer: logits = X Wr^T (kucoin page,
+ * section 01: the router re-decides each token's experts at every step; the
+ * pages print no router, and the plain reading is a linear map without bias).
+ *   X      [T, d]  bf16 device, row-major (the same tokens moe_forward takes)
+ *   Wr     [E, d]  bf16 device, row-major ([out, in] convention)
+ *   logits [T, E]  fp32 device, written (the input moe_forward takes)
+ * fp32 accumulation on the tensor cores.  Needs E % 8 == 0
+ * (MOE_ERR_UNSUPPORTED otherwise); T <= T_max; all pointers 16-byte aligned
+ * (MOE_ERR_INVALID_ARG otherwise, nothing enqueued).  T = 0 is a no-op.
+ * Enqueued on `stream`. */
+moe_status_t moe_router_forward(moe_plan_t plan, int64_t T, const void* X, const void* Wr, float* logits,
+                                moe_stream_t stream);
+
+/* Router GEMM backward.  Given dlogits [T, E] fp32 (moe_backward's dlogits):
+ *   dX  [T, d]  bf16 device, read and written: dX += dlogits Wr (fp32 sum,
+ *               one bf16 rounding), so passing moe_backward's dX gives the
+ *               token gradient through both the experts and the router;
+ *   dWr [E, d]  bf16 device, written: dWr = dlogits^T X, reduced over the T
+ *               tokens in one fixed order (bitwise deterministic).
+ * dlogits is rounded to bf16 for the tensor cores (into plan workspace).
+ * Same shape, alignment and error rules as moe_router_forward; with T = 0,
+ * dWr is zeroed and the other pointers are not used. */
+moe_status_t moe_router_backward(moe_plan_t plan, int64_t T, const void* X, const void* Wr,
+                                 const float* dlogits, void* dX, void* dWr, moe_stream_t stream);
+
 /* Synchronise `stream`, read the plan's device status word into *status
  * (a moe_status_t value; MOE_OK if no device error), and clear it. */
 moe_status_t moe_device_status(moe_plan_t plan, moe_stream_t stream, int32_t* status);

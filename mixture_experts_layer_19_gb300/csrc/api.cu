@@ -9,7 +9,9 @@
 //   reduce -> router gradient -> dWd GEMM -> dWg/dWu GEMM.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
+#include <initializer_list>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -26,9 +28,14 @@ using namespace moe;
 namespace {
 
 thread_local std::string g_last_error;
+thread_local std::string g_encode_detail;  // last tensor-map encoding failure, appended by fail()
 
 moe_status_t fail(moe_status_t s, const std::string& msg) {
   g_last_error = msg;
+  if (!g_encode_detail.empty()) {
+    g_last_error += " [" + g_encode_detail + "]";
+    g_encode_detail.clear();
+  }
   return s;
 }
 moe_status_t cuda_fail(cudaError_t e, const char* what) {
@@ -65,6 +72,12 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   CUresult r = enc(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                    const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled error %d: base %p, %llu x %llu, box %u x %u", (int)r, base,
+             (unsigned long long)outer, (unsigned long long)inner, box_out, box_in);
+    g_encode_detail = buf;
+  }
   return r == CUDA_SUCCESS;
 }
 // E4M3 operand loads: 128-byte K slices, 128 (or 256) rows, 128-byte swizzle.
@@ -127,12 +140,16 @@ RoutingPtrs routing_ptrs(const SavedLayout& L, void* saved) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Makes the plan's device current for the call, and always binds its primary
+// context to the calling thread: the tensor-map encoder is a driver call and
+// fails on a thread (such as autograd's backward worker) that has not yet
+// made a runtime call.
 struct DeviceGuard {
   int old = -1;
   bool ok = true;
   explicit DeviceGuard(int dev) {
     if (cudaGetDevice(&old) != cudaSuccess) old = -1;
-    if (old != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    ok = cudaSetDevice(dev) == cudaSuccess;
   }
   ~DeviceGuard() {
     int cur = -1;
@@ -194,6 +211,8 @@ struct moe_plan_s {
   // in-kernel combine; grid-barrier arrivals and CTA exits (zero between launches)
   int* tok_cnt = nullptr;
   unsigned long long* gbar = nullptr;
+  // router GEMM backward: dlogits in bf16 [T_max, E]
+  void* dlg_bf16 = nullptr;
   // timing (MOE_DEBUG_TIMING)
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
@@ -514,6 +533,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_xts = m; m += align256(t_pad * c.d / 32);
     err = cudaMalloc(&p->mx_ws, m);
     if (err != cudaSuccess) {
+      if (p->ring_ws) cudaFree(p->ring_ws);
       cudaFree(p->ws);
       delete p;
       return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of MXFP8 workspace failed: ") +
@@ -540,10 +560,22 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
          map_fp8_store(&p->m_ring_hq_st, p->ring_hq, c.F, ring_rows) && prepare_fwd_megakernel_mx() == cudaSuccess;
     if (!ok) {
       cudaFree(p->mx_ws);
+      if (p->ring_ws) cudaFree(p->ring_ws);
       cudaFree(p->ws);
       delete p;
       return fail(MOE_ERR_CUDA, "moe_plan: MXFP8 tensor map encoding failed");
     }
+  }
+  // router GEMM backward: dlogits rounded to bf16 for the tensor cores
+  err = cudaMalloc(&p->dlg_bf16, (size_t)std::max<int64_t>(1, c.T_max) * c.E * 2);
+  if (err == cudaSuccess) err = prepare_gemm_router();
+  if (err != cudaSuccess) {
+    if (p->dlg_bf16) cudaFree(p->dlg_bf16);
+    if (p->mx_ws) cudaFree(p->mx_ws);
+    if (p->ring_ws) cudaFree(p->ring_ws);
+    cudaFree(p->ws);
+    delete p;
+    return cuda_fail(err, "moe_plan: router workspace / GEMM attribute");
   }
   *out = p;
   return MOE_OK;
@@ -560,6 +592,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   for (auto e : p->spare_events) cudaEventDestroy(e);
   if (p->mx_ws) cudaFree(p->mx_ws);
   if (p->ring_ws) cudaFree(p->ring_ws);
+  if (p->dlg_bf16) cudaFree(p->dlg_bf16);
   cudaError_t err = cudaFree(p->ws);
   delete p;
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
@@ -963,6 +996,86 @@ moe_status_t moe_get_routing(moe_plan_t p, int64_t T, const void* saved, int32_t
     err = launch_unpad_routing(rp, (int)R, perm_src, dest, st);
     if (err != cudaSuccess) return cuda_fail(err, "moe_get_routing: unpad launch");
   }
+  return MOE_OK;
+}
+
+namespace {
+// Shape rules first; the pointers are checked only when T > 0 (a T = 0
+// call may pass empty tensors), except those listed in `always`.
+moe_status_t router_check(moe_plan_t p, int64_t T, const char* who, std::initializer_list<const void*> ptrs,
+                          std::initializer_list<const void*> always = {}) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, std::string(who) + ": null plan");
+  const moe_config_t& c = p->cfg;
+  if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, std::string(who) + ": T outside [0, T_max]");
+  if (c.E % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, std::string(who) + ": the router GEMM needs E % 8 == 0");
+  for (const void* q : always)
+    if (!q || !aligned16(q)) return fail(MOE_ERR_INVALID_ARG, std::string(who) + ": null or misaligned pointer");
+  if (T > 0)
+    for (const void* q : ptrs)
+      if (!q || !aligned16(q)) return fail(MOE_ERR_INVALID_ARG, std::string(who) + ": null or misaligned pointer");
+  return MOE_OK;
+}
+GemmArgs router_args(moe_plan_s* p, int64_t T) {
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.status = p->status;
+  a.timeout_ns = (uint64_t)p->cfg.wait_timeout_ns;
+  a.E = p->cfg.E;
+  a.d = p->cfg.d;
+  a.F = p->cfg.F;
+  a.T = (int)T;
+  return a;
+}
+int router_grid(const moe_plan_s* p, int64_t tiles) { return (int)std::min<int64_t>(tiles, p->num_sms); }
+}  // namespace
+
+moe_status_t moe_router_forward(moe_plan_t p, int64_t T, const void* X, const void* Wr, float* logits,
+                                moe_stream_t stream) {
+  if (moe_status_t s = router_check(p, T, "moe_router_forward", {X, Wr, logits})) return s;
+  if (T == 0) return MOE_OK;
+  const moe_config_t& c = p->cfg;
+  DeviceGuard guard(c.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  GemmArgs a = router_args(p, T);
+  if (!map_kmajor(&a.mapA, X, c.d, T) || !map_kmajor(&a.mapB0, Wr, c.d, c.E, BN))
+    return fail(MOE_ERR_CUDA, "moe_router_forward: tensor maps");
+  a.out_f32 = logits;
+  const int64_t tiles = ((T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
+  cudaError_t err = timed_launch(p, "gemm_router", st,
+                                 [&] { return launch_gemm_router(kRouter, a, router_grid(p, tiles), st); });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_router_forward: launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_router_backward(moe_plan_t p, int64_t T, const void* X, const void* Wr, const float* dlogits,
+                                 void* dX, void* dWr, moe_stream_t stream) {
+  if (moe_status_t s = router_check(p, T, "moe_router_backward", {X, Wr, dlogits, dX}, {dWr})) return s;
+  const moe_config_t& c = p->cfg;
+  DeviceGuard guard(c.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {  // no tokens: dWr = 0, dX untouched
+    cudaError_t err = cudaMemsetAsync(dWr, 0, (size_t)c.E * c.d * 2, st);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_router_backward: zero dWr");
+  }
+  cudaError_t err = timed_launch(p, "router_dlogits_bf16", st, [&] {
+    return launch_to_bf16(dlogits, p->dlg_bf16, T * c.E, p->num_sms * 4, st);
+  });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_router_backward: dlogits conversion launch");
+  GemmArgs x = router_args(p, T);
+  GemmArgs w = router_args(p, T);
+  if (!map_kmajor(&x.mapA, p->dlg_bf16, c.E, T) || !map_mnmajor(&x.mapB0, Wr, c.d, c.E) ||
+      !map_mnmajor(&w.mapA, p->dlg_bf16, c.E, T) || !map_mnmajor(&w.mapB0, X, c.d, T) ||
+      !map_store(&w.mapO0, dWr, c.d, c.E))
+    return fail(MOE_ERR_CUDA, "moe_router_backward: tensor maps");
+  x.io_bf16 = static_cast<__nv_bfloat16*>(dX);
+  const int64_t tx = ((T + BM - 1) / BM) * (c.d / BN);
+  err = timed_launch(p, "gemm_router_dx", st,
+                     [&] { return launch_gemm_router(kRouterDX, x, router_grid(p, tx), st); });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_router_backward: dX launch");
+  const int64_t tw = ((c.E + BM - 1) / BM) * (c.d / BN);
+  err = timed_launch(p, "gemm_router_dw", st,
+                     [&] { return launch_gemm_router(kRouterDW, w, router_grid(p, tw), st); });
+  if (err != cudaSuccess) return cuda_fail(err, "moe_router_backward: dWr launch");
   return MOE_OK;
 }
 

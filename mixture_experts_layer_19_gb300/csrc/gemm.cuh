@@ -23,6 +23,10 @@
 //   kBwdX   dXs   = dAB . [Wg;Wu]       A K-major, B MN-major
 //   kWgradD dWd   = dYg^T . (w h)       A MN-major, B MN-major (K = expert's rows)
 //   kWgradGU [dWg;dWu] = dAB^T . Xg     A MN-major, B MN-major (K = expert's rows)
+// and the dense router GEMM in front of the layer (tiles over T or E, no experts):
+//   kRouter   logits = X . Wr^T         A K-major, B K-major   (fp32 output)
+//   kRouterDX dX    += dlogits . Wr     A K-major, B MN-major  (adds into bf16 dX)
+//   kRouterDW dWr    = dlogits^T . X    A MN-major, B MN-major (K = T tokens)
 #pragma once
 #include "ptx.cuh"
 
@@ -38,13 +42,15 @@ constexpr int kBBytes = BN * BK * 2;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
 constexpr int kStageChunk = 32 * 32 * 2;         // one epilogue staging tile: 32 rows x 32 bf16
 
-enum GemmKind { kUp = 0, kDown = 1, kBwdU = 2, kBwdX = 3, kWgradD = 4, kWgradGU = 5 };
+enum GemmKind { kUp = 0, kDown = 1, kBwdU = 2, kBwdX = 3, kWgradD = 4, kWgradGU = 5,
+                kRouter = 6, kRouterDX = 7, kRouterDW = 8 };
 
 template <int KIND>
 struct KindTraits {
-  static constexpr bool a_mn = (KIND == kWgradD || KIND == kWgradGU);
-  static constexpr bool b_mn = (KIND != kUp && KIND != kDown);
+  static constexpr bool a_mn = (KIND == kWgradD || KIND == kWgradGU || KIND == kRouterDW);
+  static constexpr bool b_mn = (KIND != kUp && KIND != kDown && KIND != kRouter);
   static constexpr bool grouped = (KIND <= kBwdX);          // tiles follow expert segments
+  static constexpr bool dense = (KIND >= kRouter);          // plain M x N tiles (router GEMM)
   static constexpr int n_out = (KIND == kUp || KIND == kBwdU) ? 3 : 1;
   static constexpr int n_buf = (n_out == 3) ? 1 : 2;
   // single-output epilogues are store-bound (weight gradients write 64 KB per
@@ -71,9 +77,12 @@ struct GemmArgs {
   const int32_t* perm_src;   // kBwdU: flat pair of each sorted row (-1 = padding)
   const float* wts;          // kBwdU: gate weights [T*k]
   float* dgp;                // kBwdU: [R, F/256] partial <u, h> per N tile
+  float* out_f32;            // kRouter: logits [T, E]
+  __nv_bfloat16* io_bf16;    // kRouterDX: dX [T, d], read and written
   int32_t* status;
   uint64_t timeout_ns;
   int E, d, F;
+  int T;                     // dense kinds: tokens
 };
 
 struct Tile {
@@ -105,8 +114,25 @@ __device__ __forceinline__ int k_blocks_grouped(const G& g) {
   return (2 * g.F) / BK;  // kBwdX
 }
 
+// Dense (router) kinds: M = T (kRouter, kRouterDX) or E (kRouterDW); N = E
+// (kRouter) or d; K = d (kRouter), E (kRouterDX) or T (kRouterDW).  Ragged
+// edges read as zeros (TMA out-of-bounds fill) and are not stored.
+template <int KIND, class G>
+__device__ __forceinline__ int dense_mt(const G& g) {
+  return ((KIND == kRouterDW ? g.E : g.T) + BM - 1) / BM;
+}
+template <int KIND, class G>
+__device__ __forceinline__ int dense_nt(const G& g) {
+  return KIND == kRouter ? (g.E + BN - 1) / BN : g.d / BN;
+}
+template <int KIND, class G>
+__device__ __forceinline__ int dense_nkb(const G& g) {
+  return ((KIND == kRouter ? g.d : KIND == kRouterDX ? g.E : g.T) + BK - 1) / BK;
+}
+
 template <int KIND, class G>
 __device__ __forceinline__ int total_tiles(const G& g) {
+  if constexpr (KindTraits<KIND>::dense) return dense_mt<KIND>(g) * dense_nt<KIND>(g);
   if (KindTraits<KIND>::grouped) return g.mtile_off[g.E] * n_tiles_n<KIND>(g);
   return g.E * n_tiles_m_wgrad<KIND>(g) * n_tiles_n<KIND>(g);
 }
@@ -114,6 +140,17 @@ __device__ __forceinline__ int total_tiles(const G& g) {
 template <int KIND, class G>
 __device__ __forceinline__ Tile decode_tile(const G& g, int tile) {
   Tile t;
+  if constexpr (KindTraits<KIND>::dense) {  // (n, m) with m fastest
+    const int MT = dense_mt<KIND>(g);
+    t.e = 0;
+    t.nt = tile / MT;
+    t.mt = tile - t.nt * MT;
+    t.row0 = t.mt * BM;
+    t.nkb = dense_nkb<KIND>(g);
+    t.kbase = 0;
+    t.share = 0;
+    return t;
+  }
   const int NT = n_tiles_n<KIND>(g);
   if (KindTraits<KIND>::grouped) {
     // expert e owns tiles [mtile_off[e]*NT, mtile_off[e+1]*NT), ordered (n, m) with m fastest
@@ -173,6 +210,18 @@ __device__ __forceinline__ void load_stage(const GemmArgs& g, const Tile& t, int
     const int krow = t.e * g.F + (up ? k0 - g.F : k0);
 #pragma unroll
     for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, mb, t.nt * BN + j * 64, krow, bar, pol_w);
+  } else if (KIND == kRouter) {
+    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);         // X rows
+    tma_load_2d(sb, &g.mapB0, k0, t.nt * BN, bar, pol_w);     // Wr rows
+  } else if (KIND == kRouterDX) {
+    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);         // dlogits rows (bf16), K = E
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &g.mapB0, t.nt * BN + j * 64, k0, bar, pol_w);  // Wr
+  } else if (KIND == kRouterDW) {                              // K = tokens
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * 8192, &g.mapA, t.row0 + j * 64, k0, bar, pol_a);     // dlogits
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &g.mapB0, t.nt * BN + j * 64, k0, bar, pol_a);  // X
   } else {  // wgrad: both operands MN-major, K = sorted rows of expert e
     const int kr = t.kbase + k0;
 #pragma unroll
@@ -565,8 +614,48 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
           }
         }
         g.dgp[(size_t)r * (g.F / BN) + t.nt] = dgacc;
+      } else if (KIND == kRouter || KIND == kRouterDX) {
+        // one token row per lane: logits stored as fp32, or dX += tile (fp32
+        // add, one bf16 rounding); rows past T and columns past E are skipped
+        constexpr int kChunks = 8 / (TR::epi_warps / 4);
+        const int c0 = ((warp - 2) >> 2) * kChunks;
+        const int row = rowq + lane;
+#pragma unroll 1
+        for (int c = c0; c < c0 + kChunks; ++c) {
+          uint32_t rv[32];
+          tmem_ld32(tbase + c * 32, rv);
+          tmem_ld_wait();
+          if (c == c0 + kChunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          const int col0 = t.nt * BN + c * 32;
+          if (row < g.T) {
+            if (KIND == kRouter) {
+              float4* dst = reinterpret_cast<float4*>(g.out_f32 + (size_t)row * g.E + col0);
+              const int nv = min(32, g.E - col0) / 4;  // E % 8 == 0: whole 16-byte vectors
+              for (int v = 0; v < nv; ++v)
+                dst[v] = make_float4(__uint_as_float(rv[4 * v]), __uint_as_float(rv[4 * v + 1]),
+                                     __uint_as_float(rv[4 * v + 2]), __uint_as_float(rv[4 * v + 3]));
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(g.io_bf16 + (size_t)row * g.d + col0);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 o = dst[v];
+                uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+                  w[i] = pack_bf16(f.x + __uint_as_float(rv[8 * v + 2 * i]), f.y + __uint_as_float(rv[8 * v + 2 * i + 1]));
+                }
+                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+        }
       } else {
-        // plain bf16 store of the 128 x 256 tile: kDown, kBwdX, kWgradD, kWgradGU
+        // plain bf16 store of the 128 x 256 tile: kDown, kBwdX, kWgradD, kWgradGU, kRouterDW
         const CUtensorMap* om = &g.mapO0;
         int orow = rowq;
         if (KIND == kWgradD) {
@@ -603,7 +692,8 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(om, buf, t.nt * BN + c * 32, orow);
+            // kRouterDW: a 32-row slab wholly past the last expert is not stored
+            if (KIND != kRouterDW || orow < g.E) tma_store_2d(om, buf, t.nt * BN + c * 32, orow);
             bulk_commit();
           }
           ++chunk_ctr;

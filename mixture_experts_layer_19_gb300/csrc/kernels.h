@@ -50,6 +50,10 @@ int gemm_pair_grid_fwd(int kind);
 cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st);
 cudaError_t prepare_gemm_bwd(int kind);
 int gemm_pair_grid_bwd(int kind);
+// Router GEMM (gemm_router.cu): kind 6 logits, 7 dX += dlogits Wr, 8 dWr.
+cudaError_t launch_gemm_router(int kind, const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t prepare_gemm_router();
+cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, int grid, cudaStream_t st);
 
 // MXFP8 (mx_quant.cu, gemm_mx.cu)
 cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st);

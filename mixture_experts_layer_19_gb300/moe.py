@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "moe_backward",
             "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
             "moe_status_string", "moe_last_error", "moe_route_noalloc", "moe_quantize_weights",
-            "moe_mx_quantize")
+            "moe_mx_quantize", "moe_router_forward", "moe_router_backward")
 
 
 class moe_config_t(ctypes.Structure):
@@ -65,6 +65,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_route_noalloc": [I64, I32, I32, FP, VP, VP, VP, VP, VP, VP, P],
         "moe_quantize_weights": [P, VP, VP, VP, P],
         "moe_mx_quantize": [VP, I64, I64, VP, VP, P],
+        "moe_router_forward": [P, I64, VP, VP, FP, P],
+        "moe_router_backward": [P, I64, VP, VP, FP, VP, VP, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -238,6 +240,23 @@ class Plan:
         _check(lib().moe_device_status(self.handle, _stream(stream), ctypes.byref(st)), "moe_device_status")
         return st.value
 
+    def router_forward(self, X, Wr, logits=None, stream=None):
+        """logits = X Wr^T (fp32) on the tensor cores."""
+        T = X.shape[0]
+        if logits is None:
+            logits = torch.empty((T, self.cfg.E), dtype=torch.float32, device=self.device)
+        _check(lib().moe_router_forward(self.handle, T, _ptr(X), _ptr(Wr), _ptr(logits), _stream(stream)),
+               "moe_router_forward")
+        return logits
+
+    def router_backward(self, X, Wr, dlogits, dX, dWr=None, stream=None):
+        """dX += dlogits Wr (in place); returns dWr = dlogits^T X."""
+        if dWr is None:
+            dWr = torch.empty((self.cfg.E, self.cfg.d), dtype=torch.bfloat16, device=self.device)
+        _check(lib().moe_router_backward(self.handle, X.shape[0], _ptr(X), _ptr(Wr), _ptr(dlogits), _ptr(dX),
+                                         _ptr(dWr), _stream(stream)), "moe_router_backward")
+        return dWr
+
     def kernel_times(self):
         cap = 64
         names = (ctypes.c_char_p * cap)()
@@ -263,6 +282,27 @@ class _MoEFunction(torch.autograd.Function):
         return None, g["dX"], g["dlogits"], g["dWg"], g["dWu"], g["dWd"]
 
 
+class _RoutedMoEFunction(torch.autograd.Function):
+    """Router GEMM + MoE layer: logits = X Wr^T, then the layer; the backward
+    adds the router's share of dX to the experts' share."""
+
+    @staticmethod
+    def forward(ctx, plan: Plan, X, Wr, Wg, Wu, Wd):
+        X = X.contiguous()
+        logits = plan.router_forward(X, Wr)
+        Y, saved = plan.forward(X, logits, Wg, Wu, Wd)
+        ctx.plan = plan
+        ctx.save_for_backward(X, Wr, Wg, Wu, Wd, saved)
+        return Y
+
+    @staticmethod
+    def backward(ctx, dY):
+        X, Wr, Wg, Wu, Wd, saved = ctx.saved_tensors
+        g = ctx.plan.backward(dY.contiguous(), X, Wg, Wu, Wd, saved, want_dlogits=True)
+        dWr = ctx.plan.router_backward(X, Wr, g["dlogits"], g["dX"])
+        return None, g["dX"], dWr, g["dWg"], g["dWu"], g["dWd"]
+
+
 class MoELayer(torch.nn.Module):
     """Fused MoE layer over bf16 expert weights; router logits are an input."""
 
@@ -277,3 +317,14 @@ class MoELayer(torch.nn.Module):
 
     def forward(self, X, logits):
         return _MoEFunction.apply(self.plan, X, logits, self.Wg, self.Wu, self.Wd)
+
+
+class RoutedMoELayer(MoELayer):
+    """Fused MoE layer with its router: logits = X Wr^T (bf16 Wr [E, d])."""
+
+    def __init__(self, d: int, F: int, E: int, k: int, T_max: int, device=0, debug_flags: int = 0):
+        super().__init__(d, F, E, k, T_max, device=device, debug_flags=debug_flags)
+        self.Wr = torch.nn.Parameter(torch.empty((E, d), dtype=torch.bfloat16, device=self.Wg.device))
+
+    def forward(self, X):
+        return _RoutedMoEFunction.apply(self.plan, X, self.Wr, self.Wg, self.Wu, self.Wd)
