@@ -174,13 +174,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # source makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "a49b012f7aa10f6e1f34f2d3245803f203e1b4f267afdb2ad070f2995767fc7d",
+    "csrc_sha256": "c51bf9c8ad5231b9758324b3d7b19f7a9e873a70fd6156030ba931de4b7623d8",
     "bytes": {
-        "fwd_megakernel": 18770420275,
-        "gemm_wgrad_gate_up": 16191103232,
-        "gemm_bwd_dx": 10723478579,
-        "gemm_wgrad_down": 8502097459,
-        "gemm_bwd_u_swiglu": 6878221568,
+        "gemm_up_swiglu": 11897036236,
+        "gemm_down": 5729063833,
+        "gemm_bwd_u_swiglu": 6939509248,
+        "gemm_bwd_dx": 11179104256,
+        "gemm_wgrad_down": 8524878899,
+        "gemm_wgrad_gate_up": 16124098099,
     },
 }
 
@@ -378,6 +379,7 @@ def bench_gpu(args):
         out["cpu_baseline"] = cpu_baseline(inp, k, args.cpu_tokens)
     if not args.no_ring:
         out["ring_megakernel_forward"] = bench_ring_forward(args, plan, inp, Y, saved, stream, dev, ws)
+    out["router_gemm"] = bench_router(args, plan, inp, stream, dev, ws, peaks)
     if not args.no_mx:
         del plan, inp, grads, saved, Y
         torch.cuda.empty_cache()
@@ -390,6 +392,41 @@ def bench_gpu(args):
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def bench_router(args, plan, inp, stream, dev, ws, peaks):
+    """Router GEMM in front of the layer (logits = X Wr^T) and its backward
+    (dX += dlogits Wr, dWr = dlogits^T X) on the headline shape."""
+    c = plan.cfg
+    T = inp.X.shape[0]
+    gen = torch.Generator(device=dev).manual_seed(SEED + 1)
+    Wr = (torch.randn((c.E, c.d), generator=gen, device=dev) / math.sqrt(c.d)).to(torch.bfloat16)
+    dlog = torch.randn((T, c.E), generator=gen, device=dev)
+    dX = torch.zeros((T, c.d), dtype=torch.bfloat16, device=dev)
+    dWr = torch.empty((c.E, c.d), dtype=torch.bfloat16, device=dev)
+    logits = torch.empty((T, c.E), dtype=torch.float32, device=dev)
+    steps = max(3, args.steps // 2)
+    res = {}
+    for name, fn in (("forward", lambda: plan.router_forward(inp.X, Wr, logits, stream=stream)),
+                     ("backward", lambda: plan.router_backward(inp.X, Wr, dlog, dX, dWr, stream=stream))):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev) / steps
+        flops = (2 if name == "forward" else 4) * T * c.E * c.d
+        res[name] = {"ms": round(ms, 4), "tflops": round(flops / (ms / 1e3) / 1e12, 1)}
+    plan.kernel_times()
+    if plan.device_status() != 0:
+        raise RuntimeError("device status set in the router GEMM")
+    res["shape"] = {"T": T, "E": c.E, "d": c.d}
+    return res
 
 
 def bench_ring_forward(args, plan_sep, inp, Y, saved, stream, dev, ws):
