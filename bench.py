@@ -380,6 +380,8 @@ def bench_gpu(args):
     if not args.no_ring:
         out["ring_megakernel_forward"] = bench_ring_forward(args, plan, inp, Y, saved, stream, dev, ws)
     out["router_gemm"] = bench_router(args, plan, inp, stream, dev, ws, peaks)
+    if not args.no_ep:
+        out["virtual_rank_ep"] = bench_ep(args, plan, inp, Y, saved, grads, stream, dev, ws)
     if not args.no_mx:
         del plan, inp, grads, saved, Y
         torch.cuda.empty_cache()
@@ -392,6 +394,42 @@ def bench_gpu(args):
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def bench_ep(args, plan_one, inp, Y, saved, grads, stream, dev, ws, ranks=8):
+    """The same fwd+bwd step as expert parallelism over `ranks` virtual ranks
+    on the one GPU (pull dispatch / push combine and their reverses as
+    flag-signalled cooperative launches); bitwise equal to the headline path."""
+    from mixture_experts_layer_19_gb300 import moe
+    c = plan_one.cfg
+    plan = moe.Plan(moe.Config(T_max=c.T_max, d=c.d, F=c.F, E=c.E, k=c.k, device=dev.index, ep_ranks=ranks,
+                               debug_flags=moe.MOE_DEBUG_TIMING))
+
+    def step():
+        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        plan.backward(inp.dY, inp.X, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    plan.kernel_times()
+    steps = max(3, args.steps // 2)
+    barrier(ws)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status set in the virtual-rank EP step")
+    kt = plan.kernel_times()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev) / steps
+    res = {"ranks": ranks, "ms_per_step": round(ms, 4),
+           "value": round(ws * inp.X.shape[0] / (ms / 1e3), 1), "unit": "tokens/s",
+           "exchange_ms": {n: round(v[0] / steps, 4) for n, v in kt.items() if n.startswith("ep_")}}
+    del plan
+    return res
 
 
 def bench_router(args, plan, inp, stream, dev, ws, peaks):
@@ -738,6 +776,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurements")
     ap.add_argument("--no-ring", action="store_true", help="skip the ring-megakernel forward line")
+    ap.add_argument("--no-ep", action="store_true", help="skip the virtual-rank expert-parallel line")
     ap.add_argument("--single-cta", action="store_true",
                     help="bf16 GEMMs one CTA per tile (no 2-CTA operand sharing), for comparison")
     ap.add_argument("--sweep", action="store_true",

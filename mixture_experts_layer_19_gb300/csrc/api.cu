@@ -213,6 +213,12 @@ struct moe_plan_s {
   unsigned long long* gbar = nullptr;
   // router GEMM backward: dlogits in bf16 [T_max, E]
   void* dlg_bf16 = nullptr;
+  // virtual-rank expert parallelism (ep_ranks >= 2): home slots of the pushed
+  // rows [T_max * k, d] bf16, of the pushed <u, h> partials, and the flags
+  void* ep_ws = nullptr;
+  void* ep_slot = nullptr;
+  float* ep_dgslot = nullptr;
+  int* ep_ctr = nullptr;
   // timing (MOE_DEBUG_TIMING)
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
@@ -273,6 +279,32 @@ bool use_pair(const moe_plan_s* p, int kind) {
   return nt % 2 == 0;
 }
 int gemm_grid(const moe_plan_s* p, int kind) { return use_pair(p, kind) ? p->pair_grid[kind] : p->num_sms; }
+
+// Virtual-rank expert parallelism: the argument block shared by its three
+// exchanges (R ranks of G CTAs each).
+EpArgs ep_args(moe_plan_s* p, const RoutingPtrs& rp, int64_t T) {
+  const moe_config_t& c = p->cfg;
+  EpArgs a;
+  memset(&a, 0, sizeof(a));
+  a.R = c.ep_ranks;
+  a.G = std::max(1, p->num_sms / c.ep_ranks);
+  a.T = (int)T;
+  a.d = c.d;
+  a.F = c.F;
+  a.E = c.E;
+  a.k = c.k;
+  a.ntu = c.F / BN;
+  a.nch = route_chunks((int)T);
+  a.rp = rp;
+  a.chunk_hist = p->chunk_hist;
+  a.chunk_base = p->chunk_base;
+  a.slot = static_cast<uint4*>(p->ep_slot);
+  a.dgslot = p->ep_dgslot;
+  a.ctr = p->ep_ctr;
+  a.status = p->status;
+  a.timeout_ns = (uint64_t)c.wait_timeout_ns;
+  return a;
+}
 
 // Ring-pipeline fields of the BF16 forward megakernel's argument block.
 MegaArgs mega_args(moe_plan_s* p, const RoutingPtrs& rp, const void* X, const CUtensorMap& m_ab_st) {
@@ -367,6 +399,11 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: prec must be MOE_BF16 or MOE_MXFP8");
   if ((int64_t)c.E * c.F * c.d >= (int64_t)1 << 40)
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: weight tensor too large");
+  if (c.ep_ranks < 0 || c.ep_ranks > 64)
+    return fail(MOE_ERR_INVALID_ARG, "moe_plan: ep_ranks must be in [0, 64]");
+  if (c.ep_ranks >= 2 && (c.E % c.ep_ranks != 0 || c.prec != MOE_BF16 || (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: virtual-rank expert parallelism needs a BF16 plan, ep_ranks dividing "
+                                     "E, and real experts");
   if (!encode_fn()) return fail(MOE_ERR_CUDA, "moe_plan: cuTensorMapEncodeTiled unavailable");
 
   DeviceGuard guard(c.device);
@@ -569,7 +606,21 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   // router GEMM backward: dlogits rounded to bf16 for the tensor cores
   err = cudaMalloc(&p->dlg_bf16, (size_t)std::max<int64_t>(1, c.T_max) * c.E * 2);
   if (err == cudaSuccess) err = prepare_gemm_router();
+  if (err == cudaSuccess && c.ep_ranks >= 2) {
+    const size_t pairs = (size_t)c.T_max * c.k;
+    const size_t o_slot = 0, o_dgs = align256(pairs * c.d * 2), o_ctr = o_dgs + align256(pairs * (c.F / BN) * 4);
+    err = cudaMalloc(&p->ep_ws, o_ctr + 4096);
+    if (err == cudaSuccess) {
+      char* eb = static_cast<char*>(p->ep_ws);
+      p->ep_slot = eb + o_slot;
+      p->ep_dgslot = reinterpret_cast<float*>(eb + o_dgs);
+      p->ep_ctr = reinterpret_cast<int*>(eb + o_ctr);
+      err = cudaMemset(p->ep_ctr, 0, 4096);
+    }
+    if (err == cudaSuccess) err = prepare_ep();
+  }
   if (err != cudaSuccess) {
+    if (p->ep_ws) cudaFree(p->ep_ws);
     if (p->dlg_bf16) cudaFree(p->dlg_bf16);
     if (p->mx_ws) cudaFree(p->mx_ws);
     if (p->ring_ws) cudaFree(p->ring_ws);
@@ -593,6 +644,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   if (p->mx_ws) cudaFree(p->mx_ws);
   if (p->ring_ws) cudaFree(p->ring_ws);
   if (p->dlg_bf16) cudaFree(p->dlg_bf16);
+  if (p->ep_ws) cudaFree(p->ep_ws);
   cudaError_t err = cudaFree(p->ws);
   delete p;
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
@@ -636,6 +688,42 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
 
   // BF16 ring schedule, one launch: routing, layout, ring pipeline and
   // combine in one cooperative persistent kernel
+  if (c.ep_ranks >= 2) {
+    // expert parallelism over virtual ranks: routing + pull dispatch (one
+    // cooperative launch), the grouped GEMMs over the ranks' regions, then
+    // push combine with the home-side weighted sum
+    EpArgs ea = ep_args(p, rp, T);
+    ea.logits = logits;
+    ea.X = reinterpret_cast<const uint4*>(X);
+    ea.Xg = static_cast<uint4*>(p->Xg);
+    err = timed_launch(p, "ep_pull_dispatch", st, [&] { return launch_ep_dispatch(ea, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP dispatch launch");
+    GemmArgs a = base_args(p, rp);
+    a.mapA = p->m_Xg_k;
+    a.mapAh = p->m_Xg_kh;
+    a.mapB0 = p->m_Wg_k;
+    a.mapB1 = p->m_Wu_k;
+    a.mapO0 = m_ab_st;
+    a.mapO1 = p->m_H_st;
+    err = timed_launch(p, "gemm_up_swiglu", st,
+                       [&] { return launch_gemm_fwd(kUp, a, gemm_grid(p, kUp), use_pair(p, kUp), st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: up GEMM launch");
+    GemmArgs b = base_args(p, rp);
+    b.mapA = p->m_H_k;
+    b.mapAh = p->m_H_kh;
+    b.mapB0 = p->m_Wd_k;
+    b.mapB0h = p->m_Wd_kh;
+    b.mapO0 = p->m_Ys_st;
+    err = timed_launch(p, "gemm_down", st,
+                       [&] { return launch_gemm_fwd(kDown, b, gemm_grid(p, kDown), use_pair(p, kDown), st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: down GEMM launch");
+    ea.Ys = static_cast<const uint4*>(p->Ys);
+    ea.out = static_cast<uint4*>(Y);
+    ea.w_out = rp.w;
+    err = timed_launch(p, "ep_push_combine", st, [&] { return launch_ep_push(ea, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP combine launch");
+    return MOE_OK;
+  }
   const bool ring = (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS);
   if (!mx && !ident && ring && !(c.debug_flags & MOE_DEBUG_MULTI_LAUNCH)) {
     MegaArgs m = mega_args(p, rp, X, m_ab_st);
@@ -866,9 +954,19 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   }
   const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(saved) + L.ab);
 
-  err = timed_launch(p, "gather_bwd", st, [&] {
-    return launch_gather(dY, X, rp.perm_src, rp.totals, c.k, c.d, p->dYg, p->Xg, p->num_sms * 8, st);
-  });
+  const bool ep = c.ep_ranks >= 2;
+  if (ep) {  // pull reverse-combine: each expert rank pulls the dY and X rows of its pairs
+    EpArgs ea = ep_args(p, rp, T);
+    ea.X = reinterpret_cast<const uint4*>(X);
+    ea.dY = reinterpret_cast<const uint4*>(dY);
+    ea.Xg = static_cast<uint4*>(p->Xg);
+    ea.dYg = static_cast<uint4*>(p->dYg);
+    err = timed_launch(p, "ep_pull_reverse_combine", st, [&] { return launch_ep_pull(ea, st); });
+  } else {
+    err = timed_launch(p, "gather_bwd", st, [&] {
+      return launch_gather(dY, X, rp.perm_src, rp.totals, c.k, c.d, p->dYg, p->Xg, p->num_sms * 8, st);
+    });
+  }
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: gather launch");
   const bool mx = c.prec == MOE_MXFP8;
   if (mx) {
@@ -940,17 +1038,31 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
                        [&] { return launch_gemm_bwd(kBwdX, a, gemm_grid(p, kBwdX), use_pair(p, kBwdX), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx GEMM launch");
   }
-  const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
-  err = timed_launch(p, "reduce_dx", st,
-                     [&] { return launch_combine(p->Ys, rp.dest, nullptr, Ti, c.k, c.d, dX, cgrid, st); });
-  if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx reduce launch");
-  const int rgrid = (int)std::min<int64_t>((T + 7) / 8, (int64_t)p->num_sms * 8);
-  err = timed_launch(p, "router_grad", st, [&] {
-    // <u, h> partials: one per 256 columns (bf16 u GEMM) or per 128 (MXFP8 u GEMM)
-    return launch_router_grad(p->dgp, rp.dest, rp.idx, rp.w, Ti, c.k, c.E, mx ? c.F / 128 : c.F / BN, dg, dlogits,
-                              rgrid, st);
-  });
-  if (err != cudaSuccess) return cuda_fail(err, "moe_backward: router gradient launch");
+  if (ep) {
+    // push reverse-dispatch: each expert rank pushes the dx rows and <u, h>
+    // partials of its pairs to their tokens' homes, which sum dX and form
+    // the router gradient
+    EpArgs ea = ep_args(p, rp, T);
+    ea.Ys = static_cast<const uint4*>(p->Ys);
+    ea.out = static_cast<uint4*>(dX);
+    ea.dgp = p->dgp;
+    ea.dg = dg;
+    ea.dlogits = dlogits;
+    err = timed_launch(p, "ep_push_reverse_dispatch", st, [&] { return launch_ep_push(ea, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: EP reverse-dispatch launch");
+  } else {
+    const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
+    err = timed_launch(p, "reduce_dx", st,
+                       [&] { return launch_combine(p->Ys, rp.dest, nullptr, Ti, c.k, c.d, dX, cgrid, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx reduce launch");
+    const int rgrid = (int)std::min<int64_t>((T + 7) / 8, (int64_t)p->num_sms * 8);
+    err = timed_launch(p, "router_grad", st, [&] {
+      // <u, h> partials: one per 256 columns (bf16 u GEMM) or per 128 (MXFP8 u GEMM)
+      return launch_router_grad(p->dgp, rp.dest, rp.idx, rp.w, Ti, c.k, c.E, mx ? c.F / 128 : c.F / BN, dg, dlogits,
+                                rgrid, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: router gradient launch");
+  }
   {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dYg_mn;

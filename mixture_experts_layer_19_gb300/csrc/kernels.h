@@ -50,6 +50,37 @@ int gemm_pair_grid_fwd(int kind);
 cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st);
 cudaError_t prepare_gemm_bwd(int kind);
 int gemm_pair_grid_bwd(int kind);
+// Expert parallelism over R virtual ranks on one GPU (ep.cu).  Cooperative
+// launches of R * G CTAs; ctr holds 3R + 1 flags, zero between launches.
+struct EpArgs {
+  int R, G;                 // virtual ranks, CTAs per rank
+  int T, d, F, E, k, ntu;   // shapes; ntu = <u, h> partials per pair
+  int nch;                  // 64-token chunks
+  RoutingPtrs rp;           // routing state (saved context)
+  const float* logits;      // dispatch: router logits [T, E]
+  int32_t* chunk_hist;      // dispatch: per-chunk expert counts
+  int32_t* chunk_base;
+  const uint4* X;           // token rows (dispatch / backward pull)
+  const uint4* dY;          // backward pull: upstream gradient rows
+  uint4* Xg;                // sorted rows pulled by the expert ranks
+  uint4* dYg;
+  const uint4* Ys;          // push: sorted result rows (y, or dx per pair)
+  uint4* slot;              // push: home slots [T * k, d] bf16
+  const float* dgp;         // push (backward): [sorted rows, ntu] partials, or null
+  float* dgslot;            // push (backward): home copies [T * k, ntu]
+  uint4* out;               // home output [T, d] bf16 (Y or dX)
+  const float* w_out;       // combine weights (forward) or null (dX: plain sum)
+  float* dg;                // backward: [T, k]
+  float* dlogits;           // backward: [T, E] or null
+  int* ctr;
+  int32_t* status;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_ep_dispatch(const EpArgs& a, cudaStream_t st);
+cudaError_t launch_ep_pull(const EpArgs& a, cudaStream_t st);
+cudaError_t launch_ep_push(const EpArgs& a, cudaStream_t st);
+cudaError_t prepare_ep();
+
 // Router GEMM (gemm_router.cu): kind 6 logits, 7 dX += dlogits Wr, 8 dWr.
 cudaError_t launch_gemm_router(int kind, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_gemm_router();

@@ -41,7 +41,7 @@ class moe_config_t(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("prec", ctypes.c_int32),
                 ("minibatch_rows", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
                 ("mover_ctas", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_int64),
-                ("debug_flags", ctypes.c_uint32), ("device", ctypes.c_int32)]
+                ("debug_flags", ctypes.c_uint32), ("device", ctypes.c_int32), ("ep_ranks", ctypes.c_int32)]
 
 
 def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
@@ -149,11 +149,12 @@ class Config:
     wait_timeout_ns: int = 0
     debug_flags: int = 0
     device: int = 0
+    ep_ranks: int = 0
 
     def to_c(self) -> moe_config_t:
         return moe_config_t(self.T_max, self.d, self.F, self.E, self.k, self.prec, self.minibatch_rows,
                             self.ring_slots, self.mover_ctas, self.wait_timeout_ns, self.debug_flags,
-                            self.device)
+                            self.device, self.ep_ranks)
 
 
 class Plan:

@@ -1,0 +1,57 @@
+"""Expert parallelism over virtual ranks on one GPU (pull dispatch, push
+combine, pull reverse-combine, push reverse-dispatch with flag signalling).
+
+Rank r owns a contiguous slice of the tokens and of the experts; each rank
+lays out and pulls its own experts' rows, so the sorted layout, every GEMM
+tile and every reduction order equal the single-GPU path.  The whole layer --
+routing, Y, dX, dW, dg, dlogits -- must therefore match it bit for bit, for
+several rank counts, ragged token counts (ranks without tokens), and repeated
+calls (the flags reset themselves)."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_19_gb300 import moe
+from oracle import moe_ref
+from tests.util import BF16_TOL, cpu_and_gpu_inputs, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(plan, g, T):
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    r = plan.routing(saved, T)
+    return Y, out, r
+
+
+@pytest.mark.parametrize("case", [(700, 512, 512, 24, 4, 1.1, 2), (700, 512, 512, 24, 4, 1.1, 8),
+                                  (1000, 256, 256, 64, 8, 1.5, 4), (33, 256, 512, 8, 2, 0.0, 4)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g_R%d" % c)
+def test_virtual_rank_ep_matches_single_gpu_bitwise(case):
+    T, d, F, E, k, alpha, R = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=51, alpha=alpha)
+    ep = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, ep_ranks=R))
+    one = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k))
+    runs = [_run(ep, g, T) for _ in range(3)]
+    Yb, outb, rb = _run(one, g, T)
+    torch.cuda.synchronize()
+    assert ep.device_status() == 0 and one.device_status() == 0
+    for Y, out, r in runs:
+        assert torch.equal(Y, Yb)
+        for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+            assert torch.equal(out[key], outb[key]), key
+        for key in ("idx", "w", "counts", "offsets", "perm_src", "dest"):
+            assert torch.equal(r[key], rb[key]), key
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    assert rel_err(runs[0][0], Yr) <= BF16_TOL
+    assert np.array_equal(runs[0][2]["idx"].cpu().numpy(), moe_ref.route(h["logits"], k)[0])
+
+
+def test_virtual_rank_ep_config_is_validated():
+    with pytest.raises(moe.MoEError) as ei:
+        moe.Plan(moe.Config(T_max=64, d=256, F=256, E=12, k=2, ep_ranks=5))   # 5 does not divide 12
+    assert ei.value.status == 2
+    with pytest.raises(moe.MoEError) as ei:
+        moe.Plan(moe.Config(T_max=64, d=256, F=256, E=8, k=2, ep_ranks=2, prec=moe.MOE_MXFP8))
+    assert ei.value.status == 2
