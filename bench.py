@@ -169,12 +169,12 @@ def layer_roofline(shape, peaks, e_act: int):
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, mean
 # over the launches) from one single-pass ncu launch-list capture of this
-# bench's default workload.  The figures hold only for the kernel sources they
-# were taken on: their digest is kept beside them, and any change to a kernel
-# source makes measured_traffic() report null until a new capture is taken.
+# bench's default workload.  The figures hold only for the GEMM sources they
+# were taken on: their digest is kept beside them, and any change to those
+# sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "c51bf9c8ad5231b9758324b3d7b19f7a9e873a70fd6156030ba931de4b7623d8",
+    "csrc_sha256": "0c42726475cd3076f0b094b6b9f8ff646e13dcd0bde46e9fef9ede74308681ad",
     "bytes": {
         "gemm_up_swiglu": 11897036236,
         "gemm_down": 5729063833,
@@ -186,16 +186,19 @@ NCU_TRAFFIC = {
 }
 
 
+# The files that define the GEMM kernels the traffic figures belong to.
+GEMM_SOURCES = ("gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "gemm_bwd.cu")
+
+
 def csrc_digest() -> str:
-    """sha256 over the CUDA/C++ sources of the extension (names and contents)."""
+    """sha256 over the sources of the GEMM kernels (names and contents)."""
     import hashlib
     src = os.path.join(ROOT, "mixture_experts_layer_19_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(name.encode())
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(f.read())
+    for name in GEMM_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 

@@ -287,7 +287,7 @@ EpArgs ep_args(moe_plan_s* p, const RoutingPtrs& rp, int64_t T) {
   EpArgs a;
   memset(&a, 0, sizeof(a));
   a.R = c.ep_ranks;
-  a.G = std::max(1, p->num_sms / c.ep_ranks);
+  a.G = std::max(1, 2 * p->num_sms / c.ep_ranks);  // two CTAs per SM (all co-resident)
   a.T = (int)T;
   a.d = c.d;
   a.F = c.F;

@@ -72,10 +72,19 @@ __device__ __forceinline__ void ep_exit(const EpArgs& a) {
   }
 }
 
-// copy one row of d bf16 (or zeros) with a warp, 16-byte vectors
+// copy one row of d bf16 (or zeros) with a warp, 16-byte vectors, four
+// loads in flight per lane
 __device__ __forceinline__ void warp_copy_row(uint4* dst, const uint4* src, int nvec, int lane) {
   if (src) {
-    for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+    for (int v = lane; v < nvec; v += 128) {
+      uint4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < nvec) t[u] = src[v + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < nvec) dst[v + 32 * u] = t[u];
+    }
   } else {
     for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
   }
