@@ -165,6 +165,15 @@ moe_status_t moe_quantize_weights(moe_plan_t plan, const void* Wg, const void* W
  * and saturate at +-448.  The same kernel quantises the weights. */
 moe_status_t moe_mx_quantize(const void* src, int64_t rows, int64_t K, void* q, void* sf, moe_stream_t stream);
 
+/* Quantise the transposes of E bf16 row-major [A, B] device matrices
+ * (src [E, A, B]) to MXFP8 along A: q [E, B, A] E4M3 bytes, so row e*B + b
+ * holds src[e, :, b]; sf the scale atoms of those E*B rows with K = A
+ * (the layout of moe_mx_quantize).  A % 128 == 0 and B % 64 == 0
+ * (MOE_ERR_INVALID_ARG otherwise).  The same kernel makes the transposed
+ * weight copies of moe_quantize_weights.  Enqueued on `stream`. */
+moe_status_t moe_mx_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, void* q, void* sf,
+                                        moe_stream_t stream);
+
 /* Copy the routing a forward stored in `saved` into caller device buffers
  * (any pointer may be NULL to skip it):
  *   idx [T, k] int32, w [T, k] fp32, counts [E] int32, offsets [E+1] int32

@@ -1205,6 +1205,22 @@ moe_status_t moe_mx_quantize(const void* src, int64_t rows, int64_t K, void* q, 
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_mx_quantize: launch");
 }
 
+moe_status_t moe_mx_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, void* q, void* sf,
+                                        moe_stream_t stream) {
+  if (E < 0 || A <= 0 || B <= 0 || A % 128 != 0 || B % 64 != 0 || E * A * B >= ((int64_t)1 << 40) ||
+      A > (1 << 30) || B > (1 << 30))
+    return fail(MOE_ERR_INVALID_ARG, "moe_mx_quantize_transposed: need A % 128 == 0, B % 64 == 0, E >= 0");
+  if (E == 0) return MOE_OK;
+  if (!src || !q || !sf || !aligned16(src) || !aligned16(q) || !aligned16(sf))
+    return fail(MOE_ERR_INVALID_ARG, "moe_mx_quantize_transposed: null or misaligned pointer");
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t err = launch_quant_transpose(src, (int)E, (int)A, (int)B, q, sf, std::max(1, sms) * 8,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_mx_quantize_transposed: launch");
+}
+
 moe_status_t moe_quantize_weights(moe_plan_t p, const void* Wg, const void* Wu, const void* Wd, moe_stream_t stream) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: null plan");
   const moe_config_t& c = p->cfg;

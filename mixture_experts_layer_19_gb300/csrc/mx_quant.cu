@@ -80,27 +80,39 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16* 
 
 // src [E][A][B] bf16 -> q [E][B][A] E4M3 quantised along A (the backward
 // orientation of a weight: the K of the dgrad GEMMs), scale atoms over rows
-// E*B with K = A.  One CTA transposes a 128 (A) x 32 (B) tile through shared
-// memory; thread i then owns output row b0 + i/4, block i%4.
-__global__ void __launch_bounds__(128) quant_transpose_kernel(const __nv_bfloat16* __restrict__ src, int E, int A,
+// E*B with K = A.  One CTA transposes a 128 (A) x 64 (B) tile through shared
+// memory; thread i then owns output row b0 + i/4, block i%4 (four threads
+// write one 128-byte output row).
+__global__ void __launch_bounds__(256) quant_transpose_kernel(const __nv_bfloat16* __restrict__ src, int E, int A,
                                                               int B, uint8_t* __restrict__ q,
                                                               uint8_t* __restrict__ sf) {
-  __shared__ float tile[128][33];
-  const int na = A / 128, nb = B / 32;
+  // tile of 128 A-rows x 64 B-columns.  Loads: 8 threads per row, 16 bytes
+  // each, so every row is read as one 128-byte line.  Row r is stored with
+  // its columns shifted by 8 * (r / 32) (row stride 88 bf16), which makes the
+  // column reads of one 32-row quantisation block bank-conflict-free.
+  constexpr int kStride = 88;
+  __shared__ __align__(16) __nv_bfloat16 tile[128 * kStride];
+  const int na = A / 128, nb = B / 64;
   const int64_t ntiles = (int64_t)E * na * nb;
+  const int tid = threadIdx.x;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int e = (int)(t / (na * nb));
     const int rem = (int)(t - (int64_t)e * na * nb);
-    const int a0 = (rem / nb) * 128, b0 = (rem % nb) * 32;
-    float v[32];
-    load_bf16x32_f(src + ((int64_t)e * A + a0 + threadIdx.x) * B + b0, v);
+    const int a0 = (rem / nb) * 128, b0 = (rem % nb) * 64;
+    const int piece = tid & 7;
 #pragma unroll
-    for (int m = 0; m < 32; ++m) tile[threadIdx.x][m] = v[m];
+    for (int pass = 0; pass < 4; ++pass) {
+      const int r = pass * 32 + (tid >> 3);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + ((int64_t)e * A + a0 + r) * B + b0) + piece);
+      *reinterpret_cast<uint4*>(tile + r * kStride + 8 * (r >> 5) + piece * 8) = v;
+    }
     __syncthreads();
-    const int bl = threadIdx.x >> 2, j = threadIdx.x & 3;
+    // one thread per (output row b, 32-element block j along A)
+    const int b = tid >> 2, j = tid & 3;
+    float v[32];
 #pragma unroll
-    for (int m = 0; m < 32; ++m) v[m] = tile[32 * j + m][bl];
-    const int64_t orow = (int64_t)e * B + b0 + bl;
+    for (int m = 0; m < 32; ++m) v[m] = __bfloat162float(tile[(32 * j + m) * kStride + 8 * j + b]);
+    const int64_t orow = (int64_t)e * B + b0 + b;
     quant_block_store(v, q + orow * A + a0 + 32 * j, sf + sf_atom_offset(orow, a0 / 32 + j, A / 32));
     __syncthreads();
   }
@@ -108,7 +120,7 @@ __global__ void __launch_bounds__(128) quant_transpose_kernel(const __nv_bfloat1
 
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
                                    cudaStream_t st) {
-  quant_transpose_kernel<<<grid, 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), E, A, B,
+  quant_transpose_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), E, A, B,
                                                reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }

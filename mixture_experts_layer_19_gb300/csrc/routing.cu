@@ -144,12 +144,24 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ X
         if (g1) g1[i] = z;
       }
     } else {
+      // four 16-byte loads in flight per lane and source
       const size_t t = (size_t)(src / k);
       const uint4* x0 = X0 + t * nvec;
       const uint4* x1 = X1 ? X1 + t * nvec : nullptr;
-      for (int i = lane; i < nvec; i += 32) {
-        g0[i] = __ldg(x0 + i);
-        if (g1) g1[i] = __ldg(x1 + i);
+      for (int i = lane; i < nvec; i += 128) {
+        uint4 a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i + 32 * u < nvec) {
+            a[u] = __ldg(x0 + i + 32 * u);
+            if (g1) b[u] = __ldg(x1 + i + 32 * u);
+          }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i + 32 * u < nvec) {
+            g0[i + 32 * u] = a[u];
+            if (g1) g1[i + 32 * u] = b[u];
+          }
       }
     }
   }

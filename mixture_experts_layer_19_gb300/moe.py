@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "moe_backward",
             "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
             "moe_status_string", "moe_last_error", "moe_route_noalloc", "moe_quantize_weights",
-            "moe_mx_quantize", "moe_router_forward", "moe_router_backward")
+            "moe_mx_quantize", "moe_router_forward", "moe_router_backward", "moe_mx_quantize_transposed")
 
 
 class moe_config_t(ctypes.Structure):
@@ -65,6 +65,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_route_noalloc": [I64, I32, I32, FP, VP, VP, VP, VP, VP, VP, P],
         "moe_quantize_weights": [P, VP, VP, VP, P],
         "moe_mx_quantize": [VP, I64, I64, VP, VP, P],
+        "moe_mx_quantize_transposed": [VP, I64, I64, I64, VP, VP, P],
         "moe_router_forward": [P, I64, VP, VP, FP, P],
         "moe_router_backward": [P, I64, VP, VP, FP, VP, VP, P],
     }
@@ -123,6 +124,17 @@ def mx_quantize(src: torch.Tensor, stream=None):
     q = torch.empty((rows, K), dtype=torch.uint8, device=src.device)
     sf = torch.empty(((rows + 127) // 128) * (K // 128) * 512, dtype=torch.uint8, device=src.device)
     _check(lib().moe_mx_quantize(_ptr(src), rows, K, _ptr(q), _ptr(sf), _stream(stream)), "moe_mx_quantize")
+    return q, sf
+
+
+def mx_quantize_transposed(src: torch.Tensor, stream=None):
+    """MXFP8 of the transposes of a bf16 [E, A, B] CUDA tensor along A: (E4M3 bytes
+    [E, B, A] uint8, scale atoms of the E*B rows with K = A)."""
+    E, A, B = src.shape
+    q = torch.empty((E, B, A), dtype=torch.uint8, device=src.device)
+    sf = torch.empty(((E * B + 127) // 128) * (A // 128) * 512, dtype=torch.uint8, device=src.device)
+    _check(lib().moe_mx_quantize_transposed(_ptr(src), E, A, B, _ptr(q), _ptr(sf), _stream(stream)),
+           "moe_mx_quantize_transposed")
     return q, sf
 
 

@@ -149,3 +149,16 @@ def test_mxfp8_forward_needs_quantized_weights():
     with pytest.raises(moe.MoEError) as ei:
         plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("E,A,B", [(2, 128, 64), (3, 256, 192), (1, 7168 // 4, 128)])
+def test_mx_quantize_transposed_bit_exact(E, A, B):
+    """The transposed weight quantiser (the dgrad GEMMs' copies) against the
+    oracle's codec applied to each transposed matrix, byte for byte."""
+    src = torch.stack([_special_matrix(A, B, seed=E * 100 + i + A) for i in range(E)])
+    q, sf = moe.mx_quantize_transposed(src.cuda())
+    torch.cuda.synchronize()
+    T = src.to(torch.float64).transpose(1, 2).reshape(E * B, A).numpy()
+    codes, scales = mxfp8.mx_quantize(T, axis=1)
+    assert np.array_equal(q.cpu().numpy().reshape(E * B, A), codes)
+    assert np.array_equal(sf.cpu().numpy()[_atom_offsets(E * B, A)], scales)
