@@ -366,6 +366,7 @@ def bench_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload, "T": T, "d": d, "F": F, "E": E, "k": k, "zipf_alpha": ALPHA,
                    "seed": SEED, "tokens_per_gpu": T, "experts_active": e_act, "parallelism": f"replicas{ws}",
+                   "launch": plan.info(),
                    "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass, 129 MB L2)"},
         "roofline": roof,
         "kernel_rooflines": per_kernel,

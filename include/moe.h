@@ -220,6 +220,13 @@ moe_status_t moe_device_status(moe_plan_t plan, moe_stream_t stream, int32_t* st
 moe_status_t moe_kernel_times(moe_plan_t plan, const char** names, double* total_ms,
                               int64_t* launches, int32_t cap, int32_t* n);
 
+/* Launch geometry the plan chose on this device: num_sms, and for each of
+ * the six expert GEMM kinds (up, down, bwd u, bwd dx, wgrad down, wgrad
+ * gate/up) the grid of its 2-CTA-cluster variant (pair_grid[6]; twice the
+ * co-resident clusters, 0 if none), which depends on how the chip's enabled
+ * SMs fall into clusters.  Host-only; any pointer may be NULL. */
+moe_status_t moe_plan_info(moe_plan_t plan, int32_t* num_sms, int32_t* pair_grid);
+
 /* Two-wave minibatch floor: the smallest row count m for which a grouped
  * GEMM of output width n_out cut into tile_m x tile_n tiles gives `waves`
  * full waves on `num_sms` SMs: m = ceil(waves * num_sms * tile_m * tile_n / n_out).

@@ -650,6 +650,14 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
 }
 
+moe_status_t moe_plan_info(moe_plan_t p, int32_t* num_sms, int32_t* pair_grid) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_plan_info: null plan");
+  if (num_sms) *num_sms = p->num_sms;
+  if (pair_grid)
+    for (int i = 0; i < 6; ++i) pair_grid[i] = p->pair_grid[i];
+  return MOE_OK;
+}
+
 moe_status_t moe_saved_bytes(moe_plan_t p, int64_t T, size_t* bytes) {
   if (!p || !bytes) return fail(MOE_ERR_INVALID_ARG, "moe_saved_bytes: null argument");
   if (T < 0 || T > p->cfg.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_saved_bytes: T outside [0, T_max]");

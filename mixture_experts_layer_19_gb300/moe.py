@@ -33,7 +33,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "moe_backward",
             "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
             "moe_status_string", "moe_last_error", "moe_route_noalloc", "moe_quantize_weights",
-            "moe_mx_quantize", "moe_router_forward", "moe_router_backward", "moe_mx_quantize_transposed")
+            "moe_mx_quantize", "moe_router_forward", "moe_router_backward", "moe_mx_quantize_transposed",
+            "moe_plan_info")
 
 
 class moe_config_t(ctypes.Structure):
@@ -66,6 +67,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_quantize_weights": [P, VP, VP, VP, P],
         "moe_mx_quantize": [VP, I64, I64, VP, VP, P],
         "moe_mx_quantize_transposed": [VP, I64, I64, I64, VP, VP, P],
+        "moe_plan_info": [P, ctypes.POINTER(I32), ctypes.POINTER(I32)],
         "moe_router_forward": [P, I64, VP, VP, FP, P],
         "moe_router_backward": [P, I64, VP, VP, FP, VP, VP, P],
     }
@@ -252,6 +254,13 @@ class Plan:
         st = ctypes.c_int32()
         _check(lib().moe_device_status(self.handle, _stream(stream), ctypes.byref(st)), "moe_device_status")
         return st.value
+
+    def info(self):
+        """Launch geometry: {"num_sms": n, "pair_grid": [6 grids of the paired GEMM kinds]}."""
+        n = ctypes.c_int32()
+        grids = (ctypes.c_int32 * 6)()
+        _check(lib().moe_plan_info(self.handle, ctypes.byref(n), grids), "moe_plan_info")
+        return {"num_sms": n.value, "pair_grid": list(grids)}
 
     def router_forward(self, X, Wr, logits=None, stream=None):
         """logits = X Wr^T (fp32) on the tensor cores."""
