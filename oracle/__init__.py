@@ -7,9 +7,10 @@ never imports the library (they share only the seeded input recipe in
 ``mixture_experts_layer_19_gb300.workload``).
 
 Modules:
-  moe_ref -- routing, layout, SwiGLU experts, combine, backward (BF16 and
-             MXFP8 quantisation points).
+  moe_ref -- routing, layout, SwiGLU experts, combine, backward (BF16,
+             MXFP8 and NVFP4 quantisation points), router GEMM.
   mxfp8   -- OCP MX v1.0 E8M0 block scale + OCP FP8 E4M3 element codec.
+  nvfp4   -- E2M1 elements, E4M3 scale per 16 elements, fp32 tensor scale.
 
 Parity pins for every function live in ``tests/test_oracle_*.py``; no oracle
 function is unpinned.

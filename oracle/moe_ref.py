@@ -38,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import mxfp8
+from . import mxfp8, nvfp4
 
 
 def _expert(W, e):
@@ -123,8 +123,33 @@ def layout(idx, E):
 # ----------------------------------------------------------------------------
 # 3. Experts and 4. combine (forward).
 # ----------------------------------------------------------------------------
-def _q(v, axis, on):
-    return mxfp8.mx_fake_quant(v, axis) if on else v
+def _fmt(mx):
+    """Quantisation recipe named by a call's ``mx`` argument: None (BF16
+    arithmetic), "mxfp8" (True or "mxfp8") or "nvfp4"."""
+    if mx is None or mx is False:
+        return None
+    if mx is True or mx == "mxfp8":
+        return "mxfp8"
+    if mx == "nvfp4":
+        return "nvfp4"
+    raise ValueError("mx must be False, True, 'mxfp8' or 'nvfp4'")
+
+
+def _q(v, axis, fmt, g=1.0):
+    """Dequantised image of v along axis in the recipe ``fmt`` (v itself for None).
+    g is the NVFP4 tensor scale (weights); activations take 1."""
+    if fmt == "mxfp8":
+        return mxfp8.mx_fake_quant(v, axis)
+    if fmt == "nvfp4":
+        return nvfp4.nv_fake_quant(v, axis, g)
+    return v
+
+
+def _wscales(fmt, Wg, Wu, Wd, wscales):
+    """NVFP4 tensor scales (g_gu, g_d) of the weights; (1, 1) for other recipes."""
+    if fmt != "nvfp4":
+        return 1.0, 1.0
+    return wscales if wscales is not None else nvfp4.weight_scales(Wg, Wu, Wd)
 
 
 def _segment_rows(lay, e):
@@ -132,11 +157,14 @@ def _segment_rows(lay, e):
     return lay["perm_src"][o[e]:o[e + 1]]
 
 
-def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False):
+def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False, wscales=None):
     """Layer forward.  Returns (Y [T, d] float64, ctx dict for :func:`backward`).
 
-    mx=True emulates the MXFP8 quantisation points: X, Wg, Wu along d;
-    h along F; Wd along F (each GEMM operand along that GEMM's K).
+    mx=True (or "mxfp8") emulates the MXFP8 quantisation points: X, Wg, Wu
+    along d; h along F; Wd along F (each GEMM operand along that GEMM's K).
+    mx="nvfp4" emulates NVFP4 at the same points, the weights with their
+    tensor scales (g_gu for Wg and Wu, g_d for Wd: ``wscales``, computed from
+    the weights when None), the activations with tensor scale 1.
     identity=True replaces every expert by y = x (plumbing check).
     """
     X = np.asarray(X, dtype=np.float64)
@@ -145,7 +173,9 @@ def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False):
     idx, w = route(logits, k)
     lay = layout(idx, E)
     R = T * k
-    Xq = _q(X, 1, mx)
+    fmt = _fmt(mx)
+    g_gu, g_d = (1.0, 1.0) if identity else _wscales(fmt, Wg, Wu, Wd, wscales)
+    Xq = _q(X, 1, fmt)
     a_all = b_all = h_all = None
     if not identity:
         F = _expert(Wg, 0).shape[0]
@@ -162,16 +192,17 @@ def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False):
             y_all[rows] = X[rows // k]
             continue
         wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
-        a = x @ _q(wg, 1, mx).T
-        b = x @ _q(wu, 1, mx).T
+        a = x @ _q(wg, 1, fmt, g_gu).T
+        b = x @ _q(wu, 1, fmt, g_gu).T
         h = silu(a) * b
-        y = _q(h, 1, mx) @ _q(wd, 1, mx).T
+        y = _q(h, 1, fmt) @ _q(wd, 1, fmt, g_d).T
         a_all[rows], b_all[rows], h_all[rows], y_all[rows] = a, b, h, y
     Y = np.zeros((T, d))
     for j in range(k):
         Y += w[:, j:j + 1] * y_all[np.arange(T) * k + j]
     ctx = {"idx": idx, "w": w, "layout": lay, "a": a_all, "b": b_all, "h": h_all,
-           "y": y_all, "k": k, "mx": mx}
+           "y": y_all, "k": k, "mx": fmt,
+           "wscales": (g_gu, g_d)}
     return Y, ctx
 
 
@@ -185,8 +216,9 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
     experts that received tokens (others are zero) instead of dense [E, ...]
     arrays -- storage only, for full-size layers on a sub-batch of tokens.
 
-    MXFP8 emulation (ctx["mx"]): dY along d and Wd along d for u = Wd^T dY;
-    dA, dB along F and Wg, Wu along F for dX.  The weight gradients take the
+    MXFP8 / NVFP4 emulation (ctx["mx"]): dY along d and Wd along d for
+    u = Wd^T dY; dA, dB along F and Wg, Wu along F for dX (NVFP4: the weights
+    with the forward's tensor scales, activations with scale 1).  The weight gradients take the
     unquantised operands (dY, w*h, dA/dB, x): MXFP8 covers the GEMMs that stream
     weights; the weight-gradient GEMMs, whose cost is writing dW, stay in the
     higher precision.
@@ -194,6 +226,7 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
     dY = np.asarray(dY, dtype=np.float64)
     X = np.asarray(X, dtype=np.float64)
     k, mx = ctx["k"], ctx["mx"]
+    g_gu, g_d = ctx.get("wscales", (1.0, 1.0))
     idx, w, lay = ctx["idx"], ctx["w"], ctx["layout"]
     T, d = X.shape
     E = np.asarray(logits).shape[1]
@@ -217,13 +250,13 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
         wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
         a, b, h = ctx["a"][rows], ctx["b"][rows], ctx["h"][rows]
         wr = wflat[rows][:, None]
-        u = dYq[tok] @ _q(wd, 0, mx)                 # [m, F] = (Wd^T dY)^T, K = d
+        u = dYq[tok] @ _q(wd, 0, mx, g_d)            # [m, F] = (Wd^T dY)^T, K = d
         dg[rows] = np.sum(u * h, axis=1)            # <dY, y> = <Wd^T dY, h>
         dh = wr * u
         sa = sigmoid(a)
         da = dh * b * sa * (1.0 + a * (1.0 - sa))
         db = dh * silu(a)
-        dx = _q(da, 1, mx) @ _q(wg, 0, mx) + _q(db, 1, mx) @ _q(wu, 0, mx)
+        dx = _q(da, 1, mx) @ _q(wg, 0, mx, g_gu) + _q(db, 1, mx) @ _q(wu, 0, mx, g_gu)
         np.add.at(dX, tok, dx)
         # weight gradients: K = the expert's tokens in sorted order
         dWd[e] = dY[tok].T @ (wr * h)
@@ -242,18 +275,22 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
 # Sampled forms for full-size layers: the same arithmetic restricted to a
 # subset of tokens (per-token outputs) or of experts (per-expert dW).
 # ----------------------------------------------------------------------------
-def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False):
+def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False, wscales=None):
     """Y, dX, dg, dlogits for the listed tokens only (BF16 arithmetic unless mx).
 
     Routing and every per-token quantity depend on that token alone, so this
     equals the corresponding rows of :func:`forward` / :func:`backward`.
+    NVFP4 takes the whole weights' tensor scales ``wscales`` (computed from
+    the weights when None).
     """
+    fmt = _fmt(mx)
+    g_gu, g_d = _wscales(fmt, Wg, Wu, Wd, wscales)
     tokens = np.asarray(tokens, dtype=np.int64)
     logits = np.asarray(logits, dtype=np.float64)
     idx, w = route(logits[tokens], k)
     X = np.asarray(X, dtype=np.float64)[tokens]
     dY = np.asarray(dY, dtype=np.float64)[tokens]
-    Xq, dYq = _q(X, 1, mx), _q(dY, 1, mx)
+    Xq, dYq = _q(X, 1, fmt), _q(dY, 1, fmt)
     n, d = X.shape
     E = logits.shape[1]
     Y = np.zeros((n, d))
@@ -263,32 +300,30 @@ def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False):
         wg, wu, wd = _expert(Wg, e), _expert(Wu, e), _expert(Wd, e)
         for i, j in zip(*np.nonzero(idx == e)):
             x = Xq[i]
-            a = _q(wg, 1, mx) @ x
-            b = _q(wu, 1, mx) @ x
+            a = _q(wg, 1, fmt, g_gu) @ x
+            b = _q(wu, 1, fmt, g_gu) @ x
             h = silu(a) * b
-            if mx:  # h is quantised along F as one row
-                hq = _q(h[None, :], 1, True)[0]
-            else:
-                hq = h
-            y = _q(wd, 1, mx) @ hq
+            hq = _q(h[None, :], 1, fmt)[0]       # h is quantised along F as one row
+            y = _q(wd, 1, fmt, g_d) @ hq
             Y[i] += w[i, j] * y
-            u = _q(wd, 0, mx).T @ dYq[i]
+            u = _q(wd, 0, fmt, g_d).T @ dYq[i]
             dg[i, j] = u @ h
             dh = w[i, j] * u
             sa = sigmoid(a)
             da = dh * b * sa * (1.0 + a * (1.0 - sa))
             db = dh * silu(a)
-            if mx:
-                da, db = _q(da[None], 1, True)[0], _q(db[None], 1, True)[0]
-            dX[i] += _q(wg, 0, mx).T @ da + _q(wu, 0, mx).T @ db
+            da, db = _q(da[None], 1, fmt)[0], _q(db[None], 1, fmt)[0]
+            dX[i] += _q(wg, 0, fmt, g_gu).T @ da + _q(wu, 0, fmt, g_gu).T @ db
     s = np.sum(w * dg, axis=1, keepdims=True)
     dlogits = np.zeros((n, E))
     np.put_along_axis(dlogits, idx, w * (dg - s), axis=1)
     return {"Y": Y, "dX": dX, "dg": dg, "dlogits": dlogits, "idx": idx, "w": w}
 
 
-def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False):
+def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False, wscales=None):
     """dWg[e], dWu[e], dWd[e] over every token routed to expert e (sorted order)."""
+    fmt = _fmt(mx)
+    g_gu, g_d = _wscales(fmt, Wg, Wu, Wd, wscales)
     idx, w = route(logits, k)
     E = np.asarray(logits).shape[1]
     lay = layout(idx, E)
@@ -301,11 +336,11 @@ def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False):
     X = np.asarray(X, dtype=np.float64)[tok]
     dY = np.asarray(dY, dtype=np.float64)[tok]
     wr = w.reshape(-1)[rows][:, None]
-    Xq, dYq = _q(X, 1, mx), _q(dY, 1, mx)
-    a = Xq @ _q(wg, 1, mx).T
-    b = Xq @ _q(wu, 1, mx).T
+    Xq, dYq = _q(X, 1, fmt), _q(dY, 1, fmt)
+    a = Xq @ _q(wg, 1, fmt, g_gu).T
+    b = Xq @ _q(wu, 1, fmt, g_gu).T
     h = silu(a) * b
-    u = dYq @ _q(wd, 0, mx)
+    u = dYq @ _q(wd, 0, fmt, g_d)
     dh = wr * u
     sa = sigmoid(a)
     da = dh * b * sa * (1.0 + a * (1.0 - sa))
