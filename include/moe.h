@@ -55,7 +55,11 @@ typedef enum {
   MOE_ERR_INTERNAL = 6
 } moe_status_t;
 
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision_t;
+/* MOE_NVFP4: E2M1 elements with one E4M3 scale per 16 elements along each
+ * GEMM's K and an fp32 scale per weight tensor (Wg and Wu share one);
+ * activations quantised with tensor scale 1 (the rules are those of
+ * moe_nv_quantize). */
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_NVFP4 = 2 } moe_precision_t;
 
 /* debug_flags bits */
 #define MOE_DEBUG_IDENTITY_EXPERTS 0x1u /* experts return their input (y = x); GEMMs skipped */
@@ -86,7 +90,7 @@ typedef struct {
   int32_t F;              /* expert FFN width; multiple of 256 */
   int32_t E;              /* experts, k <= E <= 1024 */
   int32_t k;              /* experts per token, 1 <= k <= 32 */
-  int32_t prec;           /* moe_precision_t (MOE_MXFP8 needs moe_quantize_weights) */
+  int32_t prec;           /* moe_precision_t (MOE_MXFP8 / MOE_NVFP4 need moe_quantize_weights) */
   int32_t minibatch_rows; /* rows per ring slot; 0 = two-wave floor (moe_minibatch_floor) */
   int32_t ring_slots;     /* ring buffer slots; 0 = default */
   int32_t mover_ctas;     /* CTAs that gather (data movers); 0 = default */
@@ -103,10 +107,11 @@ typedef struct moe_plan_s* moe_plan_t;
 /* Create a plan: validates `cfg`, binds `cfg->device`, allocates all device
  * workspace for T <= T_max, and returns it in *out (caller frees with
  * moe_plan_destroy).  Supported: d % 256 == 0, F % 256 == 0, 1 <= k <= 32,
- * k <= E <= 1024, 1 <= T_max <= 2^20, prec MOE_BF16 or MOE_MXFP8 (an MXFP8
- * plan also holds E4M3 copies of the weights in both orientations: MXFP8
- * forward GEMMs and MXFP8 dgrad GEMMs; its weight gradients are computed from
- * the bf16 operands, since writing dW in bf16 bounds those GEMMs).  Otherwise
+ * k <= E <= 1024, 1 <= T_max <= 2^20, prec MOE_BF16, MOE_MXFP8 or MOE_NVFP4
+ * (a block-scaled plan also holds quantised copies of the weights in both
+ * orientations: block-scaled forward GEMMs and dgrad GEMMs; its weight
+ * gradients are computed from the bf16 operands, since writing dW in bf16
+ * bounds those GEMMs; NVFP4 plans run the separate-kernel schedule).  Otherwise
  * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG; allocation failure MOE_ERR_OOM. */
 moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out);
 
@@ -141,8 +146,9 @@ moe_status_t moe_backward(moe_plan_t plan, int64_t T, const void* dY, const void
                           void* dX, void* dWg, void* dWu, void* dWd, float* dg, float* dlogits,
                           moe_stream_t stream);
 
-/* MXFP8 plans only: quantise the bf16 expert weights into the plan's E4M3
- * copies (once per optimiser step, outside the layer's timing).  Forward
+/* MXFP8 and NVFP4 plans: quantise the bf16 expert weights into the plan's
+ * E4M3 (MXFP8) or E2M1 (NVFP4: after computing the tensor scales, Wg and Wu
+ * sharing one) copies (once per optimiser step, outside the layer's timing).  Forward
  * orientation: Wg, Wu along d, Wd along F; backward orientation (transposed
  * copies for the dgrad GEMMs): Wd[e]^T along d, Wg[e]^T and Wu[e]^T along F;
  * blocks of 32 with one E8M0 scale (the layout of moe_mx_quantize).  Must
@@ -173,6 +179,46 @@ moe_status_t moe_mx_quantize(const void* src, int64_t rows, int64_t K, void* q, 
  * weight copies of moe_quantize_weights.  Enqueued on `stream`. */
 moe_status_t moe_mx_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, void* q, void* sf,
                                         moe_stream_t stream);
+
+/* NVFP4 tensor scale of one or two bf16 device tensors (x1 may be NULL with
+ * n1 = 0): *g = fl32(amax / 2688) over all n0 + n1 elements (2688 = largest
+ * E2M1 times largest E4M3), or 1 when every element is zero.  g is a device
+ * float, written on `stream`.  Both tensors 16-byte aligned, finite values
+ * (MOE_ERR_INVALID_ARG otherwise).  NVIDIA's NVFP4: a second-level fp32
+ * scale per tensor; the pages name NVFP4 kernels only (fluidifia page
+ * "Cursor ouvre MoK, un mégakernel qui accélère l'entraînement MoE", section
+ * "Quand la communication devient le vrai problème"). */
+moe_status_t moe_nv_tensor_scale(const void* x0, int64_t n0, const void* x1, int64_t n1, float* g,
+                                 moe_stream_t stream);
+
+/* Quantise a bf16 row-major [rows, K] device matrix to NVFP4 along K
+ * (K % 64 == 0) with the tensor scale *g (device float; NULL = 1):
+ *   rc = fl32(1 / fl32(6 g));  per 16-element block s = E4M3(fl32(amax * rc))
+ *   (round to nearest even, saturating at 448);  element code =
+ *   E2M1(fl32(v * fl32(1 / fl32(s g)))) (nearest even, saturating at +-6, sign
+ *   kept); a block whose scale is 0 gets zero codes.
+ *   q  [rows, K / 2] bytes: element 2i in the low nibble of byte i;
+ *   sf the E4M3 scale bytes in 512-byte atoms: rows [128 i, 128 i + 128) and
+ *      blocks [4 j, 4 j + 4) form atom i * (K / 64) + j; row r / block b sits
+ *      at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + b % 4 of its atom;
+ *      ceil(rows / 128) * (K / 64) * 512 bytes.
+ * All pointers 16-byte aligned (MOE_ERR_INVALID_ARG otherwise).  Enqueued on
+ * `stream`.  The same kernel quantises an NVFP4 plan's weights. */
+moe_status_t moe_nv_quantize(const void* src, int64_t rows, int64_t K, const float* g, void* q, void* sf,
+                             moe_stream_t stream);
+
+/* NVFP4 quantisation of the transposes of E bf16 row-major [A, B] device
+ * matrices (src [E, A, B]) along A, tensor scale *g (NULL = 1): q [E, B, A / 2]
+ * bytes (row e*B + b holds src[e, :, b]), sf the scale atoms of those E*B rows
+ * with K = A (the layout of moe_nv_quantize).  A % 128 == 0, B % 64 == 0
+ * (MOE_ERR_INVALID_ARG otherwise).  Enqueued on `stream`. */
+moe_status_t moe_nv_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, const float* g,
+                                        void* q, void* sf, moe_stream_t stream);
+
+/* NVFP4 plans: copy the two fp32 tensor scales moe_quantize_weights computed
+ * ([0] Wg and Wu together, [1] Wd) into out (2 device floats), on `stream`.
+ * MOE_ERR_INVALID_ARG for a null argument or a plan that is not MOE_NVFP4. */
+moe_status_t moe_nv_weight_scales(moe_plan_t plan, float* out, moe_stream_t stream);
 
 /* Copy the routing a forward stored in `saved` into caller device buffers
  * (any pointer may be NULL to skip it):

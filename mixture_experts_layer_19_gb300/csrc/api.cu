@@ -84,9 +84,10 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 bool map_fp8_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows = BM) {
   return encode_2d(m, b, inner, outer, 128, rows, CU_TENSOR_MAP_SWIZZLE_128B, 1);
 }
-// E4M3 stores of 32 rows x 32 bytes, no swizzle.
-bool map_fp8_store(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
-  return encode_2d(m, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE, 1);
+// Quantised stores of 32 rows x box_in bytes (32 E4M3 or 32 packed E2M1
+// values: 32 or 16 bytes), no swizzle.
+bool map_fp8_store(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t box_in = 32) {
+  return encode_2d(m, b, inner, outer, box_in, 32, CU_TENSOR_MAP_SWIZZLE_NONE, 1);
 }
 // The three shapes the GEMMs use.
 bool map_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows = BM) {
@@ -199,6 +200,10 @@ struct moe_plan_s {
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
   CUtensorMap m_WdTq, m_WgTq, m_WuTq, m_dABq_k, m_dABq_st;
+  // NVFP4 (prec == MOE_NVFP4) reuses the block-scaled buffers above with
+  // packed E2M1 values and a scale per 16; its fp32 tensor scales: [0] Wg and
+  // Wu together, [1] Wd
+  float* nv_scale = nullptr;
   // ring-buffer forward megakernel (BF16): ring slots of X and h rows, GPU-local
   // hand-off counters, minibatch table
   void* ring_ws = nullptr;
@@ -395,8 +400,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: need 1 <= k <= 32 and k <= E <= 1024");
   if (c.d <= 0 || c.F <= 0 || c.d % BN || c.F % BN)
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: d and F must be positive multiples of 256");
-  if (c.prec != MOE_BF16 && c.prec != MOE_MXFP8)
-    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: prec must be MOE_BF16 or MOE_MXFP8");
+  if (c.prec != MOE_BF16 && c.prec != MOE_MXFP8 && c.prec != MOE_NVFP4)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: prec must be MOE_BF16, MOE_MXFP8 or MOE_NVFP4");
   if ((int64_t)c.E * c.F * c.d >= (int64_t)1 << 40)
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: weight tensor too large");
   if (c.ep_ranks < 0 || c.ep_ranks > 64)
@@ -473,7 +478,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   }
   for (int kind = 0; kind < 6; ++kind) {
     err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
-    if (err == cudaSuccess && kind < 4 && c.prec == MOE_MXFP8) err = prepare_gemm_mx(kind);
+    if (err == cudaSuccess && kind < 4 && c.prec != MOE_BF16) err = prepare_gemm_mx(kind, c.prec == MOE_NVFP4);
     if (err == cudaSuccess) p->pair_grid[kind] = kind < 2 ? gemm_pair_grid_fwd(kind) : gemm_pair_grid_bwd(kind);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -539,41 +544,49 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
       return fail(MOE_ERR_CUDA, "moe_plan: ring buffer tensor maps / megakernel attribute");
     }
   }
-  if (c.prec == MOE_MXFP8) {
-    const size_t wbytes = (size_t)c.E * c.F * c.d;  // E4M3 bytes of one weight tensor
+  if (c.prec == MOE_MXFP8 || c.prec == MOE_NVFP4) {
+    // quantised weights (both orientations), activations and their scale
+    // atoms: MXFP8 one byte per value and a scale per 32 values, NVFP4 half a
+    // byte per value and a scale per 16 (plus the two tensor scales)
+    const bool nv = c.prec == MOE_NVFP4;
+    const size_t nw = (size_t)c.E * c.F * c.d;  // values of one weight tensor
+    auto qb = [nv](size_t v) { return nv ? v / 2 : v; };
+    auto sb = [nv](size_t v) { return nv ? v / 16 : v / 32; };
     size_t m = 0;
-    const size_t o_wgq = m; m += align256(wbytes);
-    const size_t o_wuq = m; m += align256(wbytes);
-    const size_t o_wdq = m; m += align256(wbytes);
-    const size_t o_wgs = m; m += align256(wbytes / 32);
-    const size_t o_wus = m; m += align256(wbytes / 32);
-    const size_t o_wds = m; m += align256(wbytes / 32);
-    const size_t o_xq = m;  m += align256((size_t)R * c.d);
-    const size_t o_xs = m;  m += align256((size_t)R * c.d / 32);
-    const size_t o_hq = m;  m += align256((size_t)R * c.F);
-    const size_t o_hs = m;  m += align256((size_t)R * c.F / 32);
-    const size_t o_wdt = m; m += align256(wbytes);
-    const size_t o_wgt = m; m += align256(wbytes);
-    const size_t o_wut = m; m += align256(wbytes);
-    const size_t o_wdts = m; m += align256(wbytes / 32);
-    const size_t o_wgts = m; m += align256(wbytes / 32);
-    const size_t o_wuts = m; m += align256(wbytes / 32);
-    const size_t o_dabq = m; m += align256((size_t)R * 2 * c.F);
-    const size_t o_dabs = m; m += align256((size_t)R * 2 * c.F / 32);
-    const size_t ring_rows = (size_t)p->slots * p->cap * BM;
+    const size_t o_wgq = m; m += align256(qb(nw));
+    const size_t o_wuq = m; m += align256(qb(nw));
+    const size_t o_wdq = m; m += align256(qb(nw));
+    const size_t o_wgs = m; m += align256(sb(nw));
+    const size_t o_wus = m; m += align256(sb(nw));
+    const size_t o_wds = m; m += align256(sb(nw));
+    const size_t o_xq = m;  m += align256(qb((size_t)R * c.d));
+    const size_t o_xs = m;  m += align256(sb((size_t)R * c.d));
+    const size_t o_hq = m;  m += align256(qb((size_t)R * c.F));
+    const size_t o_hs = m;  m += align256(sb((size_t)R * c.F));
+    const size_t o_wdt = m; m += align256(qb(nw));
+    const size_t o_wgt = m; m += align256(qb(nw));
+    const size_t o_wut = m; m += align256(qb(nw));
+    const size_t o_wdts = m; m += align256(sb(nw));
+    const size_t o_wgts = m; m += align256(sb(nw));
+    const size_t o_wuts = m; m += align256(sb(nw));
+    const size_t o_dabq = m; m += align256(qb((size_t)R * 2 * c.F));
+    const size_t o_dabs = m; m += align256(sb((size_t)R * 2 * c.F));
+    // MXFP8 ring slots (an NVFP4 plan runs the separate-kernel schedule only)
+    const size_t ring_rows = nv ? 0 : (size_t)p->slots * p->cap * BM;
     const size_t o_rxq = m; m += align256(ring_rows * c.d);
     const size_t o_rxs = m; m += align256(ring_rows * c.d / 32);
     const size_t o_rhq = m; m += align256(ring_rows * c.F);
     const size_t o_rhs = m; m += align256(ring_rows * c.F / 32);
-    const size_t t_pad = ((size_t)c.T_max + BM - 1) / BM * BM;
+    const size_t t_pad = nv ? 0 : ((size_t)c.T_max + BM - 1) / BM * BM;
     const size_t o_xtq = m; m += align256(t_pad * c.d);
     const size_t o_xts = m; m += align256(t_pad * c.d / 32);
+    const size_t o_nvs = m; m += 256;
     err = cudaMalloc(&p->mx_ws, m);
     if (err != cudaSuccess) {
       if (p->ring_ws) cudaFree(p->ring_ws);
       cudaFree(p->ws);
       delete p;
-      return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of MXFP8 workspace failed: ") +
+      return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of the block-scaled workspace failed: ") +
                                    cudaGetErrorString(err));
     }
     uint8_t* mb = static_cast<uint8_t*>(p->mx_ws);
@@ -585,22 +598,27 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->dABq = mb + o_dabq; p->dABs = mb + o_dabs;
     p->ring_xq = mb + o_rxq; p->ring_xs = mb + o_rxs; p->ring_hq = mb + o_rhq; p->ring_hs = mb + o_rhs;
     p->Xtq = mb + o_xtq; p->Xts = mb + o_xts;
+    p->nv_scale = reinterpret_cast<float*>(mb + o_nvs);
     const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
-    ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, c.d, EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, c.d, EF) &&
-         map_fp8_kmajor(&p->m_Wdq, p->Wdq, c.F, Ed, BN) && map_fp8_kmajor(&p->m_Xq, p->Xq, c.d, R) &&
-         map_fp8_kmajor(&p->m_Hq_k, p->Hq, c.F, R) && map_fp8_store(&p->m_Hq_st, p->Hq, c.F, R) &&
-         map_fp8_kmajor(&p->m_WdTq, p->WdTq, c.d, EF, BN) && map_fp8_kmajor(&p->m_WgTq, p->WgTq, c.F, Ed, BN) &&
-         map_fp8_kmajor(&p->m_WuTq, p->WuTq, c.F, Ed, BN) &&
-         map_fp8_kmajor(&p->m_dABq_k, p->dABq, 2 * c.F, R) && map_fp8_store(&p->m_dABq_st, p->dABq, 2 * c.F, R) &&
-         map_fp8_kmajor(&p->m_ring_xq, p->ring_xq, c.d, ring_rows) &&
-         map_fp8_kmajor(&p->m_ring_hq, p->ring_hq, c.F, ring_rows) &&
-         map_fp8_store(&p->m_ring_hq_st, p->ring_hq, c.F, ring_rows) && prepare_fwd_megakernel_mx() == cudaSuccess;
+    const uint32_t qbox = nv ? 16 : 32;  // bytes of 32 quantised values
+    ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, qb(c.d), EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, qb(c.d), EF) &&
+         map_fp8_kmajor(&p->m_Wdq, p->Wdq, qb(c.F), Ed, BN) && map_fp8_kmajor(&p->m_Xq, p->Xq, qb(c.d), R) &&
+         map_fp8_kmajor(&p->m_Hq_k, p->Hq, qb(c.F), R) && map_fp8_store(&p->m_Hq_st, p->Hq, qb(c.F), R, qbox) &&
+         map_fp8_kmajor(&p->m_WdTq, p->WdTq, qb(c.d), EF, BN) &&
+         map_fp8_kmajor(&p->m_WgTq, p->WgTq, qb(c.F), Ed, BN) &&
+         map_fp8_kmajor(&p->m_WuTq, p->WuTq, qb(c.F), Ed, BN) &&
+         map_fp8_kmajor(&p->m_dABq_k, p->dABq, qb(2 * c.F), R) &&
+         map_fp8_store(&p->m_dABq_st, p->dABq, qb(2 * c.F), R, qbox);
+    if (ok && !nv)
+      ok = map_fp8_kmajor(&p->m_ring_xq, p->ring_xq, c.d, ring_rows) &&
+           map_fp8_kmajor(&p->m_ring_hq, p->ring_hq, c.F, ring_rows) &&
+           map_fp8_store(&p->m_ring_hq_st, p->ring_hq, c.F, ring_rows) && prepare_fwd_megakernel_mx() == cudaSuccess;
     if (!ok) {
       cudaFree(p->mx_ws);
       if (p->ring_ws) cudaFree(p->ring_ws);
       cudaFree(p->ws);
       delete p;
-      return fail(MOE_ERR_CUDA, "moe_plan: MXFP8 tensor map encoding failed");
+      return fail(MOE_ERR_CUDA, "moe_plan: block-scaled tensor map encoding failed");
     }
   }
   // router GEMM backward: dlogits rounded to bf16 for the tensor cores
@@ -686,9 +704,10 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   const int Ti = (int)T;
   cudaError_t err;
 
-  const bool mx = c.prec == MOE_MXFP8 && !ident;
+  const bool mx = (c.prec == MOE_MXFP8 || c.prec == MOE_NVFP4) && !ident;  // block-scaled GEMMs
+  const bool nv = c.prec == MOE_NVFP4;
   if (mx && !p->weights_quantized)
-    return fail(MOE_ERR_INVALID_ARG, "moe_forward: MXFP8 plan needs moe_quantize_weights before the forward");
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward: block-scaled plan needs moe_quantize_weights before the forward");
   if (!ident && !ensure_weight_maps(p, Wg, Wu, Wd)) return fail(MOE_ERR_CUDA, "moe_forward: weight tensor maps");
   CUtensorMap m_ab_st;
   if (!ident && !map_store(&m_ab_st, static_cast<char*>(saved) + L.ab, 2 * c.F, L.rows))
@@ -761,7 +780,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     err = timed_launch(p, "layout_permute", st,
                        [&] { return launch_permute(Ti, c.E, c.k, p->chunk_base, rp, st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: routing launch");
-  if (mx && ring) {
+  if (mx && ring && !nv) {
     // MXFP8 ring megakernel: movers gather + quantise into the slots, compute
     // CTAs run the block-scaled [a|b]+SwiGLU (h re-quantised into the slot)
     // and down tiles minibatch by minibatch
@@ -820,10 +839,11 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     return MOE_OK;
   }
   if (mx) {
-    // MXFP8: gather + quantise X along d, block-scaled [a|b] GEMM with SwiGLU and
-    // h re-quantised along F in its epilogue, block-scaled down GEMM.
+    // MXFP8 / NVFP4: gather + quantise X along d, block-scaled [a|b] GEMM with
+    // SwiGLU and h re-quantised along F in its epilogue, block-scaled down GEMM.
     err = timed_launch(p, "gather_quant", st, [&] {
-      return launch_gather_quant(X, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+      return nv ? launch_nv_gather_quant(X, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st)
+                : launch_gather_quant(X, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
     MxArgs a;
@@ -845,15 +865,19 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     a.sfB0 = p->Wgs;
     a.sfB1 = p->Wus;
     a.sfO = p->Hs;
-    err = timed_launch(p, "gemm_mx_up_swiglu", st, [&] { return launch_gemm_mx(kUp, a, p->num_sms, st); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 up GEMM launch");
+    a.tsB = nv ? p->nv_scale : nullptr;
+    err = timed_launch(p, nv ? "gemm_nv_up_swiglu" : "gemm_mx_up_swiglu", st,
+                       [&] { return launch_gemm_mx(kUp, a, p->num_sms, st, nv); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled up GEMM launch");
     b.mapA = p->m_Hq_k;
     b.mapB0 = p->m_Wdq;
     b.mapO0 = p->m_Ys_st;
     b.sfA = p->Hs;
     b.sfB0 = p->Wds;
-    err = timed_launch(p, "gemm_mx_down", st, [&] { return launch_gemm_mx(kDown, b, p->num_sms, st); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 down GEMM launch");
+    b.tsB = nv ? p->nv_scale + 1 : nullptr;
+    err = timed_launch(p, nv ? "gemm_nv_down" : "gemm_mx_down", st,
+                       [&] { return launch_gemm_mx(kDown, b, p->num_sms, st, nv); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled down GEMM launch");
     const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
     err = timed_launch(p, "combine", st,
                        [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
@@ -919,8 +943,8 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   const moe_config_t& c = p->cfg;
   if (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)
     return fail(MOE_ERR_UNSUPPORTED, "moe_backward: identity-expert debug mode has no backward");
-  if (c.prec == MOE_MXFP8 && !p->weights_quantized)
-    return fail(MOE_ERR_INVALID_ARG, "moe_backward: MXFP8 plan needs moe_quantize_weights first");
+  if (c.prec != MOE_BF16 && !p->weights_quantized)
+    return fail(MOE_ERR_INVALID_ARG, "moe_backward: block-scaled plan needs moe_quantize_weights first");
   if (T < 0 || T > c.T_max) return fail(MOE_ERR_INVALID_ARG, "moe_backward: T outside [0, T_max]");
   if (!dWg || !dWu || !dWd || !Wg || !Wu || !Wd)
     return fail(MOE_ERR_INVALID_ARG, "moe_backward: null weight or weight-gradient pointer");
@@ -976,14 +1000,16 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     });
   }
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: gather launch");
-  const bool mx = c.prec == MOE_MXFP8;
+  const bool mx = c.prec != MOE_BF16;  // block-scaled dgrad GEMMs
+  const bool nv = c.prec == MOE_NVFP4;
   if (mx) {
-    // MXFP8 dgrad: dY quantised along d as it is gathered; u GEMM against
-    // Wd^T (E4M3 along d) with dA|dB re-quantised along F in its epilogue;
-    // dx GEMM against [Wg^T; Wu^T] (E4M3 along F).  The weight gradients
-    // below use the bf16 operands.
+    // MXFP8 / NVFP4 dgrad: dY quantised along d as it is gathered; u GEMM
+    // against Wd^T (quantised along d) with dA|dB re-quantised along F in its
+    // epilogue; dx GEMM against [Wg^T; Wu^T] (quantised along F).  The weight
+    // gradients below use the bf16 operands.
     err = timed_launch(p, "gather_quant_dy", st, [&] {
-      return launch_gather_quant(dY, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+      return nv ? launch_nv_gather_quant(dY, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st)
+                : launch_gather_quant(dY, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dY gather launch");
     MxArgs u;
@@ -1008,8 +1034,10 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     u.perm_src = rp.perm_src;
     u.wts = rp.w;
     u.dgp = p->dgp;
-    err = timed_launch(p, "gemm_mx_bwd_u_swiglu", st, [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: MXFP8 u GEMM launch");
+    u.tsB = nv ? p->nv_scale + 1 : nullptr;
+    err = timed_launch(p, nv ? "gemm_nv_bwd_u_swiglu" : "gemm_mx_bwd_u_swiglu", st,
+                       [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st, nv); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled u GEMM launch");
     x.mapA = p->m_dABq_k;
     x.mapB0 = p->m_WgTq;
     x.mapB1 = p->m_WuTq;
@@ -1017,8 +1045,10 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     x.sfA = p->dABs;
     x.sfB0 = p->WgTs;
     x.sfB1 = p->WuTs;
-    err = timed_launch(p, "gemm_mx_bwd_dx", st, [&] { return launch_gemm_mx(kBwdX, x, p->num_sms, st); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: MXFP8 dx GEMM launch");
+    x.tsB = nv ? p->nv_scale : nullptr;
+    err = timed_launch(p, nv ? "gemm_nv_bwd_dx" : "gemm_mx_bwd_dx", st,
+                       [&] { return launch_gemm_mx(kBwdX, x, p->num_sms, st, nv); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled dx GEMM launch");
   }
   if (!mx) {
     GemmArgs a = base_args(p, rp);
@@ -1065,7 +1095,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx reduce launch");
     const int rgrid = (int)std::min<int64_t>((T + 7) / 8, (int64_t)p->num_sms * 8);
     err = timed_launch(p, "router_grad", st, [&] {
-      // <u, h> partials: one per 256 columns (bf16 u GEMM) or per 128 (MXFP8 u GEMM)
+      // <u, h> partials: one per 256 columns (bf16 u GEMM) or per 128 (block-scaled u GEMM)
       return launch_router_grad(p->dgp, rp.dest, rp.idx, rp.w, Ti, c.k, c.E, mx ? c.F / 128 : c.F / BN, dg, dlogits,
                                 rgrid, st);
     });
@@ -1229,29 +1259,102 @@ moe_status_t moe_mx_quantize_transposed(const void* src, int64_t E, int64_t A, i
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_mx_quantize_transposed: launch");
 }
 
+static int current_sms() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return std::max(1, sms);
+}
+
+moe_status_t moe_nv_tensor_scale(const void* x0, int64_t n0, const void* x1, int64_t n1, float* g,
+                                 moe_stream_t stream) {
+  if (n0 < 0 || n1 < 0 || !g || (n0 > 0 && !x0) || (n1 > 0 && !x1) || (x0 && !aligned16(x0)) ||
+      (x1 && !aligned16(x1)) || (reinterpret_cast<uintptr_t>(g) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "moe_nv_tensor_scale: null or misaligned pointer, or negative size");
+  cudaError_t err = launch_nv_tensor_scale(n0 > 0 ? x0 : nullptr, n0, n1 > 0 ? x1 : nullptr, n1, g,
+                                           current_sms() * 8, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_nv_tensor_scale: launch");
+}
+
+moe_status_t moe_nv_quantize(const void* src, int64_t rows, int64_t K, const float* g, void* q, void* sf,
+                             moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 64 != 0 || K > (1 << 30) || rows * K >= ((int64_t)1 << 40))
+    return fail(MOE_ERR_INVALID_ARG, "moe_nv_quantize: need K a positive multiple of 64 and rows >= 0");
+  if (rows == 0) return MOE_OK;
+  if (!src || !q || !sf || !aligned16(src) || !aligned16(q) || !aligned16(sf) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "moe_nv_quantize: null or misaligned pointer");
+  cudaError_t err = launch_nv_quant_rows(src, rows, (int)K, g, q, sf, current_sms() * 8,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_nv_quantize: launch");
+}
+
+moe_status_t moe_nv_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, const float* g,
+                                        void* q, void* sf, moe_stream_t stream) {
+  if (E < 0 || A <= 0 || B <= 0 || A % 128 != 0 || B % 64 != 0 || E * A * B >= ((int64_t)1 << 40) ||
+      A > (1 << 30) || B > (1 << 30))
+    return fail(MOE_ERR_INVALID_ARG, "moe_nv_quantize_transposed: need A % 128 == 0, B % 64 == 0, E >= 0");
+  if (E == 0) return MOE_OK;
+  if (!src || !q || !sf || !aligned16(src) || !aligned16(q) || !aligned16(sf) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "moe_nv_quantize_transposed: null or misaligned pointer");
+  cudaError_t err = launch_nv_quant_transpose(src, (int)E, (int)A, (int)B, g, q, sf, current_sms() * 8,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_nv_quantize_transposed: launch");
+}
+
 moe_status_t moe_quantize_weights(moe_plan_t p, const void* Wg, const void* Wu, const void* Wd, moe_stream_t stream) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: null plan");
   const moe_config_t& c = p->cfg;
-  if (c.prec != MOE_MXFP8) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: plan is not MOE_MXFP8");
+  if (c.prec != MOE_MXFP8 && c.prec != MOE_NVFP4)
+    return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: plan is not MOE_MXFP8 or MOE_NVFP4");
   if (!Wg || !Wu || !Wd || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))
     return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights: null or misaligned weight pointer");
   DeviceGuard guard(c.device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t EF = (int64_t)c.E * c.F, Ed = (int64_t)c.E * c.d;
   const int grid = p->num_sms * 8;
-  cudaError_t err = timed_launch(p, "quant_weights", st, [&] {
-    cudaError_t e = launch_quant_rows(Wg, EF, c.d, p->Wgq, p->Wgs, grid, st);
-    if (e == cudaSuccess) e = launch_quant_rows(Wu, EF, c.d, p->Wuq, p->Wus, grid, st);
-    if (e == cudaSuccess) e = launch_quant_rows(Wd, Ed, c.F, p->Wdq, p->Wds, grid, st);
-    // backward orientation: Wd[e]^T [F, d] along d; Wg[e]^T, Wu[e]^T [d, F] along F
-    if (e == cudaSuccess) e = launch_quant_transpose(Wd, c.E, c.d, c.F, p->WdTq, p->WdTs, grid, st);
-    if (e == cudaSuccess) e = launch_quant_transpose(Wg, c.E, c.F, c.d, p->WgTq, p->WgTs, grid, st);
-    if (e == cudaSuccess) e = launch_quant_transpose(Wu, c.E, c.F, c.d, p->WuTq, p->WuTs, grid, st);
-    return e;
-  });
+  cudaError_t err;
+  if (c.prec == MOE_NVFP4) {
+    // tensor scales first: [0] over Wg and Wu together (the dx GEMM contracts
+    // over both), [1] over Wd; every copy of a weight uses its tensor's scale
+    const float* g_gu = p->nv_scale;
+    const float* g_d = p->nv_scale + 1;
+    err = timed_launch(p, "quant_weights", st, [&] {
+      cudaError_t e = launch_nv_tensor_scale(Wg, EF * c.d, Wu, EF * c.d, p->nv_scale, grid, st);
+      if (e == cudaSuccess) e = launch_nv_tensor_scale(Wd, Ed * c.F, nullptr, 0, p->nv_scale + 1, grid, st);
+      if (e == cudaSuccess) e = launch_nv_quant_rows(Wg, EF, c.d, g_gu, p->Wgq, p->Wgs, grid, st);
+      if (e == cudaSuccess) e = launch_nv_quant_rows(Wu, EF, c.d, g_gu, p->Wuq, p->Wus, grid, st);
+      if (e == cudaSuccess) e = launch_nv_quant_rows(Wd, Ed, c.F, g_d, p->Wdq, p->Wds, grid, st);
+      if (e == cudaSuccess) e = launch_nv_quant_transpose(Wd, c.E, c.d, c.F, g_d, p->WdTq, p->WdTs, grid, st);
+      if (e == cudaSuccess) e = launch_nv_quant_transpose(Wg, c.E, c.F, c.d, g_gu, p->WgTq, p->WgTs, grid, st);
+      if (e == cudaSuccess) e = launch_nv_quant_transpose(Wu, c.E, c.F, c.d, g_gu, p->WuTq, p->WuTs, grid, st);
+      return e;
+    });
+  } else {
+    err = timed_launch(p, "quant_weights", st, [&] {
+      cudaError_t e = launch_quant_rows(Wg, EF, c.d, p->Wgq, p->Wgs, grid, st);
+      if (e == cudaSuccess) e = launch_quant_rows(Wu, EF, c.d, p->Wuq, p->Wus, grid, st);
+      if (e == cudaSuccess) e = launch_quant_rows(Wd, Ed, c.F, p->Wdq, p->Wds, grid, st);
+      // backward orientation: Wd[e]^T [F, d] along d; Wg[e]^T, Wu[e]^T [d, F] along F
+      if (e == cudaSuccess) e = launch_quant_transpose(Wd, c.E, c.d, c.F, p->WdTq, p->WdTs, grid, st);
+      if (e == cudaSuccess) e = launch_quant_transpose(Wg, c.E, c.F, c.d, p->WgTq, p->WgTs, grid, st);
+      if (e == cudaSuccess) e = launch_quant_transpose(Wu, c.E, c.F, c.d, p->WuTq, p->WuTs, grid, st);
+      return e;
+    });
+  }
   if (err != cudaSuccess) return cuda_fail(err, "moe_quantize_weights: launch");
   p->weights_quantized = true;
   return MOE_OK;
+}
+
+moe_status_t moe_nv_weight_scales(moe_plan_t p, float* out, moe_stream_t stream) {
+  if (!p || !out) return fail(MOE_ERR_INVALID_ARG, "moe_nv_weight_scales: null argument");
+  if (p->cfg.prec != MOE_NVFP4) return fail(MOE_ERR_INVALID_ARG, "moe_nv_weight_scales: plan is not MOE_NVFP4");
+  DeviceGuard guard(p->cfg.device);
+  cudaError_t err = cudaMemcpyAsync(out, p->nv_scale, 2 * sizeof(float), cudaMemcpyDeviceToDevice,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_nv_weight_scales: copy");
 }
 
 moe_status_t moe_device_status(moe_plan_t p, moe_stream_t stream, int32_t* status) {

@@ -16,42 +16,58 @@
 // 256-column fp32 accumulator plus a 16-column scale slot per stage, so the
 // eight epilogue warps first drain the whole accumulator into registers
 // (128 columns each), release it, and only then do the math and the stores.
+// NVFP4 variant (NV = true): the same pipeline over packed E2M1 operands
+// (128 bytes = 256 values of K per stage) with one E4M3 scale per 16 values:
+// a 512-byte scale atom then covers one MMA's K = 64, so a stage brings four
+// atoms per 128 rows, copies each into its own four TMEM columns, and issues
+// four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=256,
+// K=64).  The weights' fp32 tensor scale multiplies the accumulator in the
+// epilogue; h and dA|dB are re-quantised to NVFP4 (tensor scale 1).
 #pragma once
 #include "gemm.cuh"
 #include "mx.cuh"
+#include "nv.cuh"
 
 namespace moe {
 
-constexpr int kMxBK = 128;  // bytes (= E4M3 values) of K per stage
+constexpr int kMxBK = 128;  // bytes of K per stage (128 E4M3 or 256 E2M1 values)
 
 // Kinds: kUp, kDown (forward); kBwdU  u = dYq . WdTq^T with the SwiGLU-backward
 // epilogue (dA, dB, w h in bf16 for the weight gradients, dA|dB re-quantised
 // along F for the dx GEMM, <u, h> partials); kBwdX  dx = dABq . [WgTq;WuTq]^T.
 // WdTq [E*F, d], WgTq / WuTq [E*d, F] are the weights' backward orientation,
 // quantised along their K (the dgrad GEMMs' K), so every operand is K-major.
-template <int KIND>
+template <int KIND, bool NV = false>
 struct MxTraits {
-  static constexpr int stages = (KIND == kUp || KIND == kBwdU) ? 3 : 4;
+  static constexpr int stages = NV ? 3 : (KIND == kUp || KIND == kBwdU) ? 3 : 4;
   static constexpr int epi_warps = 8;
   static constexpr int threads = 64 + 32 * epi_warps;
-  static constexpr int sf_stage = 1536;  // A atom + two B atoms
+  static constexpr int kelems = NV ? 256 : 128;         // K values per stage
+  static constexpr int atom_k = NV ? 64 : 128;          // K values per scale atom
+  static constexpr int sf_rows = NV ? 2048 : 512;       // scale bytes per 128 rows per stage
+  static constexpr int sf_stage = 3 * sf_rows;          // A atoms + two B row blocks
+  static constexpr int sf_cols = NV ? 48 : 16;          // TMEM columns of one stage's scales
+  static constexpr int qout = NV ? 512 : 1024;          // one 32 x 32 quantised staging tile
   static constexpr int staging_per_warp =
-      (KIND == kUp) ? (2 * 2048 + 1024) : (KIND == kBwdU) ? (3 * 2048 + 2 * 1024) : 2048;
+      (KIND == kUp) ? (2 * 2048 + qout) : (KIND == kBwdU) ? (3 * 2048 + 2 * qout) : 2048;
   static constexpr int staging_off = (stages * (kStageBytes + sf_stage) + 1023) / 1024 * 1024;
   static constexpr int smem_bytes = staging_off + epi_warps * staging_per_warp + 1024 + 256;
+  static_assert(smem_bytes <= 232448, "shared memory per CTA");
+  static_assert(BN + stages * sf_cols <= 512, "TMEM columns");
 };
 
 struct MxArgs {
-  CUtensorMap mapA;   // E4M3 activations [rows, K]
-  CUtensorMap mapB0;  // E4M3 weights (Wg / Wd)
-  CUtensorMap mapB1;  // E4M3 weights (Wu) for kUp
+  CUtensorMap mapA;   // quantised activations [rows, K bytes]
+  CUtensorMap mapB0;  // quantised weights (Wg / Wd)
+  CUtensorMap mapB1;  // quantised weights (Wu) for kUp
   CUtensorMap mapO0;  // bf16 stores (a|b for kUp, Ys for kDown)
-  CUtensorMap mapO1;  // E4M3 stores (kUp: h; kBwdU: dA|dB)
+  CUtensorMap mapO1;  // quantised stores (kUp: h; kBwdU: dA|dB)
   CUtensorMap mapO2;  // kBwdU: bf16 w h stores
   const uint8_t* sfA;   // scale atoms of A (rows = sorted padded rows)
   const uint8_t* sfB0;  // scale atoms of B0
   const uint8_t* sfB1;  // scale atoms of B1
-  uint8_t* sfO;         // scale atoms of the E4M3 output (kUp: h, K = F; kBwdU: dA|dB, K = 2F)
+  uint8_t* sfO;         // scale atoms of the quantised output (kUp: h, K = F; kBwdU: dA|dB, K = 2F)
+  const float* tsB;     // NVFP4: device fp32 tensor scale of the B operand (weights)
   const __nv_bfloat16* ab;   // kBwdU: saved a|b [rows, 2F]
   const int32_t* perm_src;   // kBwdU
   const float* wts;          // kBwdU
@@ -63,40 +79,48 @@ struct MxArgs {
   int E, d, F;
 };
 
-template <int KIND>
+// One stage: the A and B tiles (TMA; x coordinates in bytes) and their scale
+// atoms (1-D bulk copies).  Atoms of consecutive K groups are adjacent, so the
+// four NVFP4 atoms of a stage are one 2 KB copy per 128-row block.
+template <int KIND, bool NV>
 __device__ __forceinline__ void mx_load_stage(const MxArgs& g, const Tile& t, int kb, uint8_t* sa, uint8_t* sb,
                                               uint8_t* ssf, uint64_t* bar, uint64_t pol_w, uint64_t pol_a) {
-  const int k0 = kb * kMxBK;
+  using TR = MxTraits<KIND, NV>;
+  constexpr uint32_t SFB = TR::sf_rows;
+  const int x0 = kb * kMxBK;          // byte coordinate along K
+  const int ke = kb * TR::kelems;     // value coordinate along K
   if (KIND == kUp) {
-    const int kg = g.d / kMxBK;  // scale atoms per 128-row block
-    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
+    const int kg = g.d / TR::atom_k;  // scale atoms per 128-row block
+    tma_load_2d(sa, &g.mapA, x0, t.row0, bar, pol_a);
     const int brow = t.e * g.F + t.nt * 128;
-    tma_load_2d(sb, &g.mapB0, k0, brow, bar, pol_w);
-    tma_load_2d(sb + kBBytes / 2, &g.mapB1, k0, brow, bar, pol_w);
-    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + kb) * 512, 512, bar);
-    bulk_load_1d(ssf + 512, g.sfB0 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
-    bulk_load_1d(ssf + 1024, g.sfB1 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
+    tma_load_2d(sb, &g.mapB0, x0, brow, bar, pol_w);
+    tma_load_2d(sb + kBBytes / 2, &g.mapB1, x0, brow, bar, pol_w);
+    const int ka = ke / TR::atom_k;
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + ka) * 512, SFB, bar);
+    bulk_load_1d(ssf + SFB, g.sfB0 + ((size_t)(brow >> 7) * kg + ka) * 512, SFB, bar);
+    bulk_load_1d(ssf + 2 * SFB, g.sfB1 + ((size_t)(brow >> 7) * kg + ka) * 512, SFB, bar);
   } else if (KIND == kDown || KIND == kBwdU) {
     // kDown: A = Hq (K = F), B = Wdq rows e*d + n;  kBwdU: A = dYq (K = d), B = WdTq rows e*F + n
     const int K = (KIND == kDown) ? g.F : g.d;
-    const int kg = K / kMxBK;
-    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
+    const int kg = K / TR::atom_k;
+    const int ka = ke / TR::atom_k;
+    tma_load_2d(sa, &g.mapA, x0, t.row0, bar, pol_a);
     const int brow = (KIND == kDown ? t.e * g.d : t.e * g.F) + t.nt * BN;
-    tma_load_2d(sb, &g.mapB0, k0, brow, bar, pol_w);
-    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + kb) * 512, 512, bar);
-    bulk_load_1d(ssf + 512, g.sfB0 + ((size_t)(brow >> 7) * kg + kb) * 512, 512, bar);
-    bulk_load_1d(ssf + 1024, g.sfB0 + ((size_t)((brow >> 7) + 1) * kg + kb) * 512, 512, bar);
+    tma_load_2d(sb, &g.mapB0, x0, brow, bar, pol_w);
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + ka) * 512, SFB, bar);
+    bulk_load_1d(ssf + SFB, g.sfB0 + ((size_t)(brow >> 7) * kg + ka) * 512, SFB, bar);
+    bulk_load_1d(ssf + 2 * SFB, g.sfB0 + ((size_t)((brow >> 7) + 1) * kg + ka) * 512, SFB, bar);
   } else {  // kBwdX: A = dABq (K = 2F); B = WgTq for k < F, WuTq for k >= F (rows e*d + n, K = F)
-    const int kga = (2 * g.F) / kMxBK, kgb = g.F / kMxBK;
-    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
-    const bool up = k0 >= g.F;
-    const int kw = up ? k0 - g.F : k0;
+    const int kga = (2 * g.F) / TR::atom_k, kgb = g.F / TR::atom_k;
+    tma_load_2d(sa, &g.mapA, x0, t.row0, bar, pol_a);
+    const bool up = ke >= g.F;
+    const int kw = up ? ke - g.F : ke;           // value coordinate inside Wg^T / Wu^T
     const int brow = t.e * g.d + t.nt * BN;
-    tma_load_2d(sb, up ? &g.mapB1 : &g.mapB0, kw, brow, bar, pol_w);
+    tma_load_2d(sb, up ? &g.mapB1 : &g.mapB0, NV ? kw / 2 : kw, brow, bar, pol_w);
     const uint8_t* sfb = up ? g.sfB1 : g.sfB0;
-    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kga + kb) * 512, 512, bar);
-    bulk_load_1d(ssf + 512, sfb + ((size_t)(brow >> 7) * kgb + kw / kMxBK) * 512, 512, bar);
-    bulk_load_1d(ssf + 1024, sfb + ((size_t)((brow >> 7) + 1) * kgb + kw / kMxBK) * 512, 512, bar);
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kga + ke / TR::atom_k) * 512, SFB, bar);
+    bulk_load_1d(ssf + SFB, sfb + ((size_t)(brow >> 7) * kgb + kw / TR::atom_k) * 512, SFB, bar);
+    bulk_load_1d(ssf + 2 * SFB, sfb + ((size_t)((brow >> 7) + 1) * kgb + kw / TR::atom_k) * 512, SFB, bar);
   }
 }
 
@@ -107,9 +131,14 @@ __device__ __forceinline__ void stage_row_fp8(uint8_t* buf, int lane, const uint
   p[1] = make_uint4(q[4], q[5], q[6], q[7]);
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(const __grid_constant__ MxArgs g) {
-  using TR = MxTraits<KIND>;
+// 32 values -> 16 packed E2M1 bytes of one row into an unswizzled 32x16-byte staging tile.
+__device__ __forceinline__ void stage_row_fp4(uint8_t* buf, int lane, const uint4& q) {
+  *reinterpret_cast<uint4*>(buf + lane * 16) = q;
+}
+
+template <int KIND, bool NV = false>
+__global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel(const __grid_constant__ MxArgs g) {
+  using TR = MxTraits<KIND, NV>;
   constexpr int S = TR::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -151,7 +180,7 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
   const uint32_t tmem_base = *tmem_slot;
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
   const int ntiles = total_tiles<KIND>(g);
-  const int nkb = (KIND == kUp || KIND == kBwdU ? g.d : KIND == kDown ? g.F : 2 * g.F) / kMxBK;
+  const int nkb = (KIND == kUp || KIND == kBwdU ? g.d : KIND == kDown ? g.F : 2 * g.F) / TR::kelems;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -167,7 +196,7 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
           if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kStageBytes + TR::sf_stage);
           uint8_t* sa = stage_base + s * kStageBytes;
-          mx_load_stage<KIND>(g, t, kb, sa, sa + kABytes, sf_base + s * TR::sf_stage, &full[s], pol_w, pol_a);
+          mx_load_stage<KIND, NV>(g, t, kb, sa, sa + kABytes, sf_base + s * TR::sf_stage, &full[s], pol_w, pol_a);
           issued_mask |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
           if (++s == S) { s = 0; ph ^= 1; }
@@ -195,16 +224,35 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
           const uint32_t sa = smem_u32(stage_base + s * kStageBytes);
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = smem_u32(sf_base + s * TR::sf_stage);
-          const uint32_t sfa_t = tmem_base + BN + s * 16;  // 4 columns
-          const uint32_t sfb_t = sfa_t + 8;                // 8 columns
-          tmem_cp_32x128_x4(sfa_t, sdesc_plain(ssf));
-          tmem_cp_32x128_x4(sfb_t, sdesc_plain(ssf + 512));
-          tmem_cp_32x128_x4(sfb_t + 4, sdesc_plain(ssf + 1024));
+          const uint32_t sfa_t = tmem_base + BN + s * TR::sf_cols;
+          if constexpr (NV) {
+            // atom kk of each 128-row block -> its own 4 TMEM columns: A at
+            // sfa_t + 4 kk, B rows 0-127 at sfb_t + 8 kk, rows 128-255 at +4
+            const uint32_t sfb_t = sfa_t + 16;
 #pragma unroll
-          for (int kk = 0; kk < kMxBK / 32; ++kk) {
-            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_mxf8(tmem_base, ad, bd, idesc_mxf8(BM, BN, 0, 0, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              tmem_cp_32x128_x4(sfa_t + 4 * kk, sdesc_plain(ssf + 512 * kk));
+              tmem_cp_32x128_x4(sfb_t + 8 * kk, sdesc_plain(ssf + TR::sf_rows + 512 * kk));
+              tmem_cp_32x128_x4(sfb_t + 8 * kk + 4, sdesc_plain(ssf + 2 * TR::sf_rows + 512 * kk));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+              umma_nvf4(tmem_base, ad, bd, idesc_nvf4(BM, BN), sfa_t + 4 * kk, sfb_t + 8 * kk,
+                        (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+            const uint32_t sfb_t = sfa_t + 8;  // 8 columns
+            tmem_cp_32x128_x4(sfa_t, sdesc_plain(ssf));
+            tmem_cp_32x128_x4(sfb_t, sdesc_plain(ssf + 512));
+            tmem_cp_32x128_x4(sfb_t + 4, sdesc_plain(ssf + 1024));
+#pragma unroll
+            for (int kk = 0; kk < kMxBK / 32; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+              umma_mxf8(tmem_base, ad, bd, idesc_mxf8(BM, BN, 0, 0, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(&empty[s]);
           if (++s == S) { s = 0; ph ^= 1; }
@@ -219,6 +267,8 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
     const int q = warp & 3;            // TMEM lane quadrant
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
     uint8_t* stg = staging_base + (warp - 2) * TR::staging_per_warp;
+    const float gs = NV ? __ldg(g.tsB) : 1.0f;   // weights' tensor scale (NVFP4)
+    const float rc1 = nv_rc(1.0f);               // activations: tensor scale 1
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const Tile t = decode_tile<KIND>(g, tile);
@@ -229,14 +279,14 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
       if (KIND == kBwdU) {
         // u chunk by chunk (the accumulator is released after the last one):
         // dh = w u, da = dh b s(a)(1 + a(1 - s(a))), db = dh silu(a); outputs
-        // dA|dB and w h in bf16 (weight gradients), dA|dB in E4M3 along F (dx
-        // GEMM) and the row's <u, h> over this warp's 128 columns.
+        // dA|dB and w h in bf16 (weight gradients), dA|dB quantised along F
+        // for the dx GEMM, and the row's <u, h> over this warp's 128 columns.
         const int r = rowq + lane;
         const int src = __ldg(g.perm_src + r);
         const float wr = src >= 0 ? __ldg(g.wts + src) : 0.0f;
         const __nv_bfloat16* abrow = g.ab + (size_t)r * (2 * g.F);
         float dgacc = 0.0f;
-        uint32_t sfa = 0, sfb = 0;
+        uint32_t sfa[2] = {0u, 0u}, sfb[2] = {0u, 0u};
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ru[32];
@@ -254,7 +304,7 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
           float da[32], db[32], wh[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float u = __uint_as_float(ru[i]);
+            const float u = NV ? __uint_as_float(ru[i]) * gs : __uint_as_float(ru[i]);
             const float sa = sigmoidf_(a[i]);
             const float sl = a[i] * sa;
             const float hh = sl * b[i];
@@ -264,35 +314,55 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
             db[i] = dh * sl;
             wh[i] = wr * hh;
           }
-          const int Xa = mx_block_exponent(amax32(da));
-          const int Xb = mx_block_exponent(amax32(db));
-          uint32_t qa[8], qb[8];
-          mx_encode32(da, Xa, qa);
-          mx_encode32(db, Xb, qb);
-          sfa |= (uint32_t)(Xa + 127) << (8 * c);
-          sfb |= (uint32_t)(Xb + 127) << (8 * c);
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           stage_row(stg, lane, da);
           stage_row(stg + kStageChunk, lane, db);
           stage_row(stg + 2 * kStageChunk, lane, wh);
-          stage_row_fp8(stg + 3 * kStageChunk, lane, qa);
-          stage_row_fp8(stg + 3 * kStageChunk + 1024, lane, qb);
+          if constexpr (NV) {
+            uint4 qa, qb;
+            sfa[c >> 1] |= nv_encode32(da, rc1, 1.0f, qa) << (16 * (c & 1));
+            sfb[c >> 1] |= nv_encode32(db, rc1, 1.0f, qb) << (16 * (c & 1));
+            stage_row_fp4(stg + 3 * kStageChunk, lane, qa);
+            stage_row_fp4(stg + 3 * kStageChunk + TR::qout, lane, qb);
+          } else {
+            const int Xa = mx_block_exponent(amax32(da));
+            const int Xb = mx_block_exponent(amax32(db));
+            uint32_t qa[8], qb[8];
+            mx_encode32(da, Xa, qa);
+            mx_encode32(db, Xb, qb);
+            sfa[0] |= (uint32_t)(Xa + 127) << (8 * c);
+            sfb[0] |= (uint32_t)(Xb + 127) << (8 * c);
+            stage_row_fp8(stg + 3 * kStageChunk, lane, qa);
+            stage_row_fp8(stg + 3 * kStageChunk + TR::qout, lane, qb);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
+            constexpr int qd = NV ? 2 : 1;   // values per quantised byte
             tma_store_2d(&g.mapO0, stg, col, rowq);
             tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
             tma_store_2d(&g.mapO2, stg + 2 * kStageChunk, col, rowq);
-            tma_store_2d(&g.mapO1, stg + 3 * kStageChunk, col, rowq);
-            tma_store_2d(&g.mapO1, stg + 3 * kStageChunk + 1024, g.F + col, rowq);
+            tma_store_2d(&g.mapO1, stg + 3 * kStageChunk, col / qd, rowq);
+            tma_store_2d(&g.mapO1, stg + 3 * kStageChunk + TR::qout, (g.F + col) / qd, rowq);
             bulk_commit();
           }
         }
         aph ^= 1;
-        const int kba = (t.nt * BN + half * 128) / 32;  // first of this warp's 4 blocks (K = 2F)
-        *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, kba, (2 * g.F) / 32)) = sfa;
-        *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, g.F / 32 + kba, (2 * g.F) / 32)) = sfb;
+        if constexpr (NV) {
+          // 8 blocks of 16 per operand: two scale words, in consecutive atoms
+          const int kba = (t.nt * BN + half * 128) / 16;
+          const int nb = (2 * g.F) / 16;
+#pragma unroll
+          for (int w2 = 0; w2 < 2; ++w2) {
+            *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, kba + 4 * w2, nb)) = sfa[w2];
+            *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, g.F / 16 + kba + 4 * w2, nb)) = sfb[w2];
+          }
+        } else {
+          const int kba = (t.nt * BN + half * 128) / 32;  // first of this warp's 4 blocks (K = 2F)
+          *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, kba, (2 * g.F) / 32)) = sfa[0];
+          *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, g.F / 32 + kba, (2 * g.F) / 32)) = sfb[0];
+        }
         g.dgp[(size_t)r * (g.F / 128) + t.nt * 2 + half] = dgacc;
         continue;
       }
@@ -318,39 +388,50 @@ __global__ void __launch_bounds__(MxTraits<KIND>::threads, 1) gemm_mx_kernel(con
           float a[32], b[32], h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            a[i] = __uint_as_float(acc[c2][i]);
-            b[i] = __uint_as_float(acc[2 + c2][i]);
+            a[i] = NV ? __uint_as_float(acc[c2][i]) * gs : __uint_as_float(acc[c2][i]);
+            b[i] = NV ? __uint_as_float(acc[2 + c2][i]) * gs : __uint_as_float(acc[2 + c2][i]);
             h[i] = a[i] * sigmoidf_(a[i]) * b[i];
           }
-          const int X = mx_block_exponent(amax32(h));
-          uint32_t hq[8];
-          mx_encode32(h, X, hq);
-          sfw |= (uint32_t)(X + 127) << (8 * c2);
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           stage_row(stg, lane, a);
           stage_row(stg + kStageChunk, lane, b);
-          stage_row_fp8(stg + 2 * kStageChunk, lane, hq);
+          if constexpr (NV) {
+            uint4 hq;
+            sfw |= nv_encode32(h, rc1, 1.0f, hq) << (16 * c2);
+            stage_row_fp4(stg + 2 * kStageChunk, lane, hq);
+          } else {
+            const int X = mx_block_exponent(amax32(h));
+            uint32_t hq[8];
+            mx_encode32(h, X, hq);
+            sfw |= (uint32_t)(X + 127) << (8 * c2);
+            stage_row_fp8(stg + 2 * kStageChunk, lane, hq);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             const int col = t.nt * 128 + half * 64 + c2 * 32;
             tma_store_2d(&g.mapO0, stg, col, rowq);
             tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
-            tma_store_2d(&g.mapO1, stg + 2 * kStageChunk, col, rowq);
+            tma_store_2d(&g.mapO1, stg + 2 * kStageChunk, NV ? col / 2 : col, rowq);
             bulk_commit();
           }
         }
-        // two consecutive scale bytes of this row (blocks 4 nt + 2 half, +1)
         const int r = rowq + lane;
-        const int kb = t.nt * 4 + half * 2;
-        *reinterpret_cast<uint16_t*>(g.sfO + sf_atom_offset(r, kb, g.F / 32)) = (uint16_t)sfw;
+        if constexpr (NV) {
+          // four scale bytes of this row (blocks 8 nt + 4 half .. +3): one word
+          *reinterpret_cast<uint32_t*>(g.sfO + sf_atom_offset(r, t.nt * 8 + half * 4, g.F / 16)) = sfw;
+        } else {
+          // two consecutive scale bytes of this row (blocks 4 nt + 2 half, +1)
+          const int kb = t.nt * 4 + half * 2;
+          *reinterpret_cast<uint16_t*>(g.sfO + sf_atom_offset(r, kb, g.F / 32)) = (uint16_t)sfw;
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[c][i]);
+          for (int i = 0; i < 32; ++i) v[i] = NV ? __uint_as_float(acc[c][i]) * gs : __uint_as_float(acc[c][i]);
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           stage_row(stg, lane, v);

@@ -93,8 +93,20 @@ cudaError_t launch_gather_quant(const void* X, const int32_t* perm_src, const in
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
                                    cudaStream_t st);
 struct MxArgs;
-cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st);  // kind 0 up, 1 down
-cudaError_t prepare_gemm_mx(int kind);
+// kind 0 up, 1 down, 2 bwd-u, 3 bwd-x; nv: the NVFP4 variant (E2M1 operands,
+// E4M3 scales per 16, tensor scales in MxArgs::tsB)
+cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st, bool nv = false);
+cudaError_t prepare_gemm_mx(int kind, bool nv = false);
+
+// NVFP4 (nv_quant.cu): g = amax(a, b) / 2688 written to the device float *g
+cudaError_t launch_nv_tensor_scale(const void* a, int64_t na, const void* b, int64_t nb, float* g, int grid,
+                                   cudaStream_t st);
+cudaError_t launch_nv_quant_rows(const void* src, int64_t rows, int K, const float* g, void* q, void* sf, int grid,
+                                 cudaStream_t st);
+cudaError_t launch_nv_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d,
+                                   void* q, void* sf, int grid, cudaStream_t st);
+cudaError_t launch_nv_quant_transpose(const void* src, int E, int A, int B, const float* g, void* q, void* sf,
+                                      int grid, cudaStream_t st);
 
 // Ring-buffer forward megakernel (megakernel.cu)
 struct MegaArgs;

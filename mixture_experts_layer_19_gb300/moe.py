@@ -19,6 +19,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so"
 MOE_OK = 0
 MOE_BF16 = 0
 MOE_MXFP8 = 1
+MOE_NVFP4 = 2
 MOE_DEBUG_IDENTITY_EXPERTS = 0x1
 MOE_DEBUG_TIMING = 0x2
 MOE_DEBUG_SEPARATE_KERNELS = 0x4
@@ -34,7 +35,8 @@ EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "m
             "moe_get_routing", "moe_device_status", "moe_kernel_times", "moe_minibatch_floor",
             "moe_status_string", "moe_last_error", "moe_route_noalloc", "moe_quantize_weights",
             "moe_mx_quantize", "moe_router_forward", "moe_router_backward", "moe_mx_quantize_transposed",
-            "moe_plan_info")
+            "moe_plan_info", "moe_nv_tensor_scale", "moe_nv_quantize", "moe_nv_quantize_transposed",
+            "moe_nv_weight_scales")
 
 
 class moe_config_t(ctypes.Structure):
@@ -70,6 +72,10 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_plan_info": [P, ctypes.POINTER(I32), ctypes.POINTER(I32)],
         "moe_router_forward": [P, I64, VP, VP, FP, P],
         "moe_router_backward": [P, I64, VP, VP, FP, VP, VP, P],
+        "moe_nv_tensor_scale": [VP, I64, VP, I64, FP, P],
+        "moe_nv_quantize": [VP, I64, I64, FP, VP, VP, P],
+        "moe_nv_quantize_transposed": [VP, I64, I64, I64, FP, VP, VP, P],
+        "moe_nv_weight_scales": [P, FP, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -137,6 +143,39 @@ def mx_quantize_transposed(src: torch.Tensor, stream=None):
     sf = torch.empty(((E * B + 127) // 128) * (A // 128) * 512, dtype=torch.uint8, device=src.device)
     _check(lib().moe_mx_quantize_transposed(_ptr(src), E, A, B, _ptr(q), _ptr(sf), _stream(stream)),
            "moe_mx_quantize_transposed")
+    return q, sf
+
+
+def nv_tensor_scale(x0: torch.Tensor, x1: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """NVFP4 tensor scale amax / 2688 over one or two bf16 CUDA tensors, as a
+    one-element fp32 CUDA tensor (1 for all-zero input)."""
+    g = torch.empty((1,), dtype=torch.float32, device=x0.device)
+    n1 = x1.numel() if x1 is not None else 0
+    _check(lib().moe_nv_tensor_scale(_ptr(x0), x0.numel(), _ptr(x1), n1, _ptr(g), _stream(stream)),
+           "moe_nv_tensor_scale")
+    return g
+
+
+def nv_quantize(src: torch.Tensor, g: Optional[torch.Tensor] = None, stream=None):
+    """NVFP4 of a bf16 [rows, K] CUDA tensor along K with tensor scale g (a
+    one-element fp32 CUDA tensor, None = 1): (packed E2M1 bytes [rows, K/2]
+    uint8, E4M3 scale atoms uint8 [ceil(rows/128) * K/64 * 512])."""
+    rows, K = src.shape
+    q = torch.empty((rows, K // 2), dtype=torch.uint8, device=src.device)
+    sf = torch.empty(((rows + 127) // 128) * (K // 64) * 512, dtype=torch.uint8, device=src.device)
+    _check(lib().moe_nv_quantize(_ptr(src), rows, K, _ptr(g), _ptr(q), _ptr(sf), _stream(stream)),
+           "moe_nv_quantize")
+    return q, sf
+
+
+def nv_quantize_transposed(src: torch.Tensor, g: Optional[torch.Tensor] = None, stream=None):
+    """NVFP4 of the transposes of a bf16 [E, A, B] CUDA tensor along A: (packed
+    bytes [E, B, A/2] uint8, scale atoms of the E*B rows with K = A)."""
+    E, A, B = src.shape
+    q = torch.empty((E, B, A // 2), dtype=torch.uint8, device=src.device)
+    sf = torch.empty(((E * B + 127) // 128) * (A // 64) * 512, dtype=torch.uint8, device=src.device)
+    _check(lib().moe_nv_quantize_transposed(_ptr(src), E, A, B, _ptr(g), _ptr(q), _ptr(sf), _stream(stream)),
+           "moe_nv_quantize_transposed")
     return q, sf
 
 
@@ -246,9 +285,15 @@ class Plan:
         return out
 
     def quantize_weights(self, Wg, Wu, Wd, stream=None):
-        """MXFP8 plans: fill the plan's E4M3 weight copies (once per weight update)."""
+        """MXFP8 / NVFP4 plans: fill the plan's quantised weight copies (once per weight update)."""
         _check(lib().moe_quantize_weights(self.handle, _ptr(Wg), _ptr(Wu), _ptr(Wd), _stream(stream)),
                "moe_quantize_weights")
+
+    def nv_weight_scales(self, stream=None) -> torch.Tensor:
+        """NVFP4 plans: the weights' tensor scales [g(Wg, Wu), g(Wd)] as a 2-element fp32 CUDA tensor."""
+        out = torch.empty((2,), dtype=torch.float32, device=self.device)
+        _check(lib().moe_nv_weight_scales(self.handle, _ptr(out), _stream(stream)), "moe_nv_weight_scales")
+        return out
 
     def device_status(self, stream=None) -> int:
         st = ctypes.c_int32()

@@ -206,6 +206,26 @@ def forward(X, logits, Wg, Wu, Wd, k, mx=False, identity=False, wscales=None):
     return Y, ctx
 
 
+def bf16_round(v):
+    """Round to bfloat16 (8 significand bits), nearest even, through fp32:
+    fp64 -> fp32 -> bf16, as the device rounds its fp32 values.  Finite input."""
+    x = np.asarray(v, dtype=np.float32)
+    b = x.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def stored_context(ctx):
+    """The saved context as the layer stores it for the backward: the gate and
+    up pre-activations a|b in bf16, h recomputed from them.  The backward's
+    inputs are what the forward saved; the block-scaled backward decides the
+    codes of dA|dB from these stored values."""
+    out = dict(ctx)
+    out["a"], out["b"] = bf16_round(ctx["a"]), bf16_round(ctx["b"])
+    out["h"] = silu(out["a"]) * out["b"]
+    return out
+
+
 # ----------------------------------------------------------------------------
 # 5. Backward (reverse combine, expert backward, reverse dispatch, dW, router).
 # ----------------------------------------------------------------------------
@@ -275,13 +295,14 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
 # Sampled forms for full-size layers: the same arithmetic restricted to a
 # subset of tokens (per-token outputs) or of experts (per-expert dW).
 # ----------------------------------------------------------------------------
-def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False, wscales=None):
+def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False, wscales=None, stored=False):
     """Y, dX, dg, dlogits for the listed tokens only (BF16 arithmetic unless mx).
 
     Routing and every per-token quantity depend on that token alone, so this
-    equals the corresponding rows of :func:`forward` / :func:`backward`.
-    NVFP4 takes the whole weights' tensor scales ``wscales`` (computed from
-    the weights when None).
+    equals the corresponding rows of :func:`forward` / :func:`backward`
+    (stored=True: of :func:`backward` on :func:`stored_context`, i.e. the
+    backward reads a|b rounded to bf16).  NVFP4 takes the whole weights'
+    tensor scales ``wscales`` (computed from the weights when None).
     """
     fmt = _fmt(mx)
     g_gu, g_d = _wscales(fmt, Wg, Wu, Wd, wscales)
@@ -306,6 +327,9 @@ def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False, wsca
             hq = _q(h[None, :], 1, fmt)[0]       # h is quantised along F as one row
             y = _q(wd, 1, fmt, g_d) @ hq
             Y[i] += w[i, j] * y
+            if stored:
+                a, b = bf16_round(a), bf16_round(b)
+                h = silu(a) * b
             u = _q(wd, 0, fmt, g_d).T @ dYq[i]
             dg[i, j] = u @ h
             dh = w[i, j] * u

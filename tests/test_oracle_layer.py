@@ -170,3 +170,29 @@ def test_sampled_forms_equal_full_forms():
             assert np.allclose(dwg, g["dWg"][e], rtol=1e-12, atol=1e-12)
             assert np.allclose(dwu, g["dWu"][e], rtol=1e-12, atol=1e-12)
             assert np.allclose(dwd, g["dWd"][e], rtol=1e-12, atol=1e-12)
+
+
+def test_bf16_round_matches_torch_and_ties():
+    import torch
+    rng = np.random.default_rng(4)
+    v = np.concatenate([rng.standard_normal(20000) * np.exp2(rng.integers(-60, 60, 20000)),
+                        [0.0, -0.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 65504.0]])
+    want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(moe_ref.bf16_round(v), want)
+    # ties go to the even significand: 1 + 2^-8 -> 1, 1 + 3 * 2^-8 -> 1 + 2^-6
+    assert moe_ref.bf16_round(1.0 + 2.0 ** -8) == 1.0
+    assert moe_ref.bf16_round(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+
+
+def test_stored_context_sampled_form_matches_full_form():
+    T, d, F, E, k = 24, 64, 64, 5, 2
+    X, L, Wg, Wu, Wd, dY = _inputs(T, d, F, E, k, seed=8, alpha=0.5)
+    for mx in (False, "mxfp8", "nvfp4"):
+        Y, ctx = moe_ref.forward(X, L, Wg, Wu, Wd, k, mx=mx)
+        st = moe_ref.stored_context(ctx)
+        assert np.array_equal(st["a"], moe_ref.bf16_round(ctx["a"])) and not np.array_equal(st["a"], ctx["a"])
+        g = moe_ref.backward(dY, X, L, Wg, Wu, Wd, st)
+        toks = np.array([1, 9, 23])
+        s = moe_ref.forward_backward_tokens(X, L, Wg, Wu, Wd, dY, k, toks, mx=mx, stored=True)
+        for key, full in (("Y", Y), ("dX", g["dX"]), ("dg", g["dg"]), ("dlogits", g["dlogits"])):
+            assert np.allclose(s[key], full[toks], rtol=1e-12, atol=1e-12), (mx, key)
