@@ -174,14 +174,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "0c42726475cd3076f0b094b6b9f8ff646e13dcd0bde46e9fef9ede74308681ad",
+    "csrc_sha256": "4ea95fbf9d5bc311f8f8441e864fe38705ba175ed2fb79961eeff8188b811204",
     "bytes": {
-        "gemm_up_swiglu": 11897036236,
-        "gemm_down": 5729063833,
-        "gemm_bwd_u_swiglu": 6939509248,
-        "gemm_bwd_dx": 11179104256,
-        "gemm_wgrad_down": 8524878899,
-        "gemm_wgrad_gate_up": 16124098099,
+        "gemm_up_swiglu": 11881291622,
+        "gemm_down": 5720642150,
+        "gemm_bwd_u_swiglu": 6929362790,
+        "gemm_bwd_dx": 11184908595,
+        "gemm_wgrad_down": 8713543834,
+        "gemm_wgrad_gate_up": 16361207142,
     },
 }
 
@@ -390,10 +390,19 @@ def bench_gpu(args):
         del plan, inp, grads, saved, Y
         torch.cuda.empty_cache()
         out["mxfp8_forward"] = [bench_mx_forward(args, dev, ws, peaks, alpha) for alpha in (0.0, ALPHA)]
-        grid = [(Tm, a) for Tm in (2048, 8192, 32768) for a in (0.0, 1.1, 1.5)] if args.sweep else [(8192, ALPHA)]
+        grid = [(Tm, a) for Tm in (2048, 8192, 32768) for a in (0.0, 1.1, 1.5)] if args.sweep else \
+            [(args.tokens or 8192, ALPHA)]
         out["mxfp8_fwd_bwd"] = [bench_mx_fwd_bwd(args, dev, ws, peaks, Tm, a) for Tm, a in grid]
         if args.sweep:
             out["minibatch_sweep"] = bench_minibatch_sweep(args, dev, ws)
+    if not args.no_nv:
+        from mixture_experts_layer_19_gb300 import moe
+        if args.no_mx:
+            del plan, inp, grads, saved, Y
+            torch.cuda.empty_cache()
+        out["nvfp4_forward"] = [bench_mx_forward(args, dev, ws, peaks, ALPHA, prec=moe.MOE_NVFP4)]
+        out["nvfp4_fwd_bwd"] = [bench_mx_fwd_bwd(args, dev, ws, peaks, Tn, ALPHA, prec=moe.MOE_NVFP4)
+                                for Tn in ((args.tokens,) if args.tokens else (4096, 8192))]
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -509,18 +518,32 @@ def bench_ring_forward(args, plan_sep, inp, Y, saved, stream, dev, ws):
     return res
 
 
-def bench_mx_forward(args, dev, ws, peaks, alpha):
-    """MXFP8 forward of the layer at T=16384 (uniform or Zipf routing): E4M3
-    gather, block-scaled [a|b] GEMM + SwiGLU + h re-quantisation, block-scaled
-    down GEMM, combine.  Weight quantisation (once per optimiser step) is timed
-    on its own and is not part of the step."""
+def _block_format(prec):
+    """(name, kernel-name tag, tensor-peak multiple of bf16, bytes per weight value incl. scales, dtype)."""
     from mixture_experts_layer_19_gb300 import moe
-    T, d, F, E, k = MX_SHAPE["T"], SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
+    if prec == moe.MOE_NVFP4:
+        return ("nvfp4", "nv", 6.0, 0.5 + 1 / 16,
+                "e2m1 + e4m3 scale per 16 + fp32 tensor scale (fp32 accumulate, bf16 out)")
+    return "mxfp8", "mx", 2.0, 1 + 1 / 32, "e4m3+e8m0 (fp32 accumulate, bf16 out)"
+
+
+def bench_mx_forward(args, dev, ws, peaks, alpha, prec=None):
+    """Block-scaled forward of the layer at T=16384 (uniform or Zipf routing):
+    quantising gather, block-scaled [a|b] GEMM + SwiGLU + h re-quantisation,
+    block-scaled down GEMM, combine; MXFP8 (with the ring megakernel beside
+    the default schedule) or NVFP4.  Weight quantisation (once per optimiser
+    step) is timed on its own and is not part of the step."""
+    from mixture_experts_layer_19_gb300 import moe
+    prec = moe.MOE_MXFP8 if prec is None else prec
+    fname, tag, mult, wbytes, dtype = _block_format(prec)
+    # --tokens / --experts shrink the layer for profiler captures only
+    T, d, F, k = args.tokens or MX_SHAPE["T"], SHAPE["d"], SHAPE["F"], SHAPE["k"]
+    E = args.experts or SHAPE["E"]
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def run(flags, steps):
-        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, device=dev.index,
+        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, device=dev.index,
                                    debug_flags=moe.MOE_DEBUG_TIMING | flags))
         # the first call also pays for loading the kernels; time the second
         plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
@@ -542,44 +565,46 @@ def bench_mx_forward(args, dev, ws, peaks, alpha):
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         if plan.device_status() != 0:
-            raise RuntimeError("device status set in the MXFP8 forward")
+            raise RuntimeError(f"device status set in the {fname} forward")
         el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
         kt = plan.kernel_times()
         e_act = active_experts(plan, saved, T)
         del plan, saved, Y
         return el, kt, wq, e_act
 
-    # default MXFP8 schedule (separate kernels) and the ring megakernel beside it
+    # default schedule (separate kernels); for MXFP8 the ring megakernel beside it
     el, kt, wq, e_act = run(0, args.steps)
-    el_ring, ktr, _, _ = run(moe.MOE_DEBUG_RING_MEGAKERNEL, max(3, args.steps // 2))
     R = T * k
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # nominal fp8/bf16 dense ratio x measured bf16
-    mk_ms = ktr["fwd_megakernel_mx"][0] / ktr["fwd_megakernel_mx"][1]
-    mk_tf = 6.0 * R * d * F / (mk_ms / 1e3) / 1e12
-    up_ms = kt["gemm_mx_up_swiglu"][0] / kt["gemm_mx_up_swiglu"][1]
-    dn_ms = kt["gemm_mx_down"][0] / kt["gemm_mx_down"][1]
+    tpeak = mult * peaks["bf16_tflops_sustained"]      # nominal fp8 (x2) / fp4 (x6) : bf16 dense ratio
+    up_ms = kt[f"gemm_{tag}_up_swiglu"][0] / kt[f"gemm_{tag}_up_swiglu"][1]
+    dn_ms = kt[f"gemm_{tag}_down"][0] / kt[f"gemm_{tag}_down"][1]
     up_tf = 4.0 * R * d * F / (up_ms / 1e3) / 1e12
     dn_tf = 2.0 * R * d * F / (dn_ms / 1e3) / 1e12
     ms = el / args.steps
-    t_tc = 6.0 * R * d * F / (fp8_peak * 1e12) * 1e3
-    t_hbm = (3.0 * e_act * F * d * (1 + 1 / 32) + T * d * 2 * 2 + T * E * 4) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_tc = 6.0 * R * d * F / (tpeak * 1e12) * 1e3
+    t_hbm = (3.0 * e_act * F * d * wbytes + T * d * 2 * 2 + T * E * 4) / (peaks["hbm_gbs"] * 1e9) * 1e3
     res = {
-        "workload": f"moe_layer_fwd_mxfp8_T{T}_d{d}_F{F}_E{E}_top{k}_zipf{alpha:g}", "experts_active": e_act,
+        "workload": f"moe_layer_fwd_{fname}_T{T}_d{d}_F{F}_E{E}_top{k}_zipf{alpha:g}", "experts_active": e_act,
         "value": round(ws * T * args.steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
-        "dtype": "e4m3+e8m0 (fp32 accumulate, bf16 out)",
-        "roofline": {"kernel": "gemm_mx_up_swiglu", "bound": "tensor", "achieved": round(up_tf, 1),
-                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(up_tf / fp8_peak, 4),
+        "dtype": dtype,
+        "roofline": {"kernel": f"gemm_{tag}_up_swiglu", "bound": "tensor", "achieved": round(up_tf, 1),
+                     "peak": round(tpeak, 1), "unit": "TFLOP/s", "frac": round(up_tf / tpeak, 4),
                      "traffic": None,
-                     "peak_source": peaks["source"] + " bf16_tflops_sustained x 2 (nominal fp8:bf16 ratio)"},
-        "down_gemm": {"achieved": round(dn_tf, 1), "unit": "TFLOP/s", "frac": round(dn_tf / fp8_peak, 4)},
-        "ring_megakernel": {"ms_per_step": round(el_ring / max(3, args.steps // 2), 4),
-                            "megakernel_ms": round(mk_ms, 4), "achieved": round(mk_tf, 1), "unit": "TFLOP/s",
-                            "frac": round(mk_tf / fp8_peak, 4), "flops": "6*R*d*F per launch"},
+                     "peak_source": peaks["source"] + f" bf16_tflops_sustained x {mult:g} (nominal "
+                                                      f"{'fp4' if tag == 'nv' else 'fp8'}:bf16 ratio)"},
+        "down_gemm": {"achieved": round(dn_tf, 1), "unit": "TFLOP/s", "frac": round(dn_tf / tpeak, 4)},
         "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
                            "frac": round(max(t_tc, t_hbm) / ms, 4)},
         "kernels": {n: {"ms_per_step": round(v[0] / args.steps, 4), "launches": v[1]} for n, v in kt.items()},
         "weight_quant_ms": round(wq.get("quant_weights", (0.0, 0))[0], 3),
     }
+    if prec == moe.MOE_MXFP8:
+        el_ring, ktr, _, _ = run(moe.MOE_DEBUG_RING_MEGAKERNEL, max(3, args.steps // 2))
+        mk_ms = ktr["fwd_megakernel_mx"][0] / ktr["fwd_megakernel_mx"][1]
+        mk_tf = 6.0 * R * d * F / (mk_ms / 1e3) / 1e12
+        res["ring_megakernel"] = {"ms_per_step": round(el_ring / max(3, args.steps // 2), 4),
+                                  "megakernel_ms": round(mk_ms, 4), "achieved": round(mk_tf, 1), "unit": "TFLOP/s",
+                                  "frac": round(mk_tf / tpeak, 4), "flops": "6*R*d*F per launch"}
     del inp
     torch.cuda.empty_cache()
     return res
@@ -596,14 +621,18 @@ def _alloc_grads(T, d, F, E, k, dev):
     }
 
 
-def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha):
-    """MXFP8 forward + backward at T tokens: E4M3 forward and dgrad GEMMs,
-    bf16 weight gradients.  Layer roofline: max(12RdF / fp8 peak + 6RdF / bf16
-    peak, (E4M3 weights fwd + bwd orientation + bf16 dW) / HBM)."""
+def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha, prec=None):
+    """Block-scaled (MXFP8 or NVFP4) forward + backward at T tokens: quantised
+    forward and dgrad GEMMs, bf16 weight gradients.  Layer roofline:
+    max(12RdF / fp8 or fp4 peak + 6RdF / bf16 peak, (quantised weights fwd +
+    bwd orientation + bf16 dW) / HBM)."""
     from mixture_experts_layer_19_gb300 import moe
-    d, F, E, k = SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
+    prec = moe.MOE_MXFP8 if prec is None else prec
+    fname, _, mult, wbytes, _ = _block_format(prec)
+    d, F, k = SHAPE["d"], SHAPE["F"], SHAPE["k"]
+    E = args.experts or SHAPE["E"]
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
-    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, device=dev.index,
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, device=dev.index,
                                debug_flags=moe.MOE_DEBUG_TIMING))
     stream = torch.cuda.current_stream(dev)
     plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
@@ -628,17 +657,17 @@ def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha):
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     if plan.device_status() != 0:
-        raise RuntimeError("device status set in the MXFP8 fwd+bwd")
+        raise RuntimeError(f"device status set in the {fname} fwd+bwd")
     el = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
     kt = plan.kernel_times()
     e_act = active_experts(plan, saved, T)
     R = T * k
-    fp8_peak, bf16_peak = 2.0 * peaks["bf16_tflops_sustained"], peaks["bf16_tflops_sustained"]
-    t_tc = (12.0 * R * d * F / fp8_peak + 6.0 * R * d * F / bf16_peak) / 1e12 * 1e3
-    # E4M3 weights of the active experts in both orientations, bf16 dW of every expert
-    t_hbm = (2 * 3.0 * e_act * F * d * (1 + 1 / 32) + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    tpeak, bf16_peak = mult * peaks["bf16_tflops_sustained"], peaks["bf16_tflops_sustained"]
+    t_tc = (12.0 * R * d * F / tpeak + 6.0 * R * d * F / bf16_peak) / 1e12 * 1e3
+    # quantised weights of the active experts in both orientations, bf16 dW of every expert
+    t_hbm = (2 * 3.0 * e_act * F * d * wbytes + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
     ms = el / steps
-    res = {"workload": f"moe_layer_fwd_bwd_mxfp8_T{T}_zipf{alpha:g}", "T": T, "zipf_alpha": alpha,
+    res = {"workload": f"moe_layer_fwd_bwd_{fname}_T{T}_zipf{alpha:g}", "T": T, "zipf_alpha": alpha,
            "experts_active": e_act,
            "value": round(ws * T * steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
@@ -779,6 +808,7 @@ def main(argv=None):
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures on a smaller layer)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurements")
+    ap.add_argument("--no-nv", action="store_true", help="skip the NVFP4 measurements")
     ap.add_argument("--no-ring", action="store_true", help="skip the ring-megakernel forward line")
     ap.add_argument("--no-ep", action="store_true", help="skip the virtual-rank expert-parallel line")
     ap.add_argument("--single-cta", action="store_true",
