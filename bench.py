@@ -174,7 +174,7 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "4ea95fbf9d5bc311f8f8441e864fe38705ba175ed2fb79961eeff8188b811204",
+    "csrc_sha256": "c61b200a06e2133612eb62ee24a025956bf3c51db23f556ee4ef6b3708ee595e",
     "bytes": {
         "gemm_up_swiglu": 11881291622,
         "gemm_down": 5720642150,
@@ -190,15 +190,39 @@ NCU_TRAFFIC = {
 GEMM_SOURCES = ("gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "gemm_bwd.cu")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank lines (string literals kept):
+    a comment cannot change a kernel, so it does not change the digest."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                       # string literal, escapes kept
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def csrc_digest() -> str:
-    """sha256 over the sources of the GEMM kernels (names and contents)."""
+    """sha256 over the code (comments stripped) of the GEMM kernels' sources."""
     import hashlib
     src = os.path.join(ROOT, "mixture_experts_layer_19_gb300", "csrc")
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
         h.update(name.encode())
-        with open(os.path.join(src, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(src, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

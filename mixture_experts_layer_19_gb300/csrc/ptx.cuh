@@ -1,6 +1,8 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers with bounded
 // waits, TMA (cp.async.bulk.tensor) loads/stores, and tcgen05 (TMEM alloc,
-// UMMA issue/commit, TMEM loads).  No multicast forms are used anywhere.
+// UMMA issue/commit, TMEM loads).  The multicast forms (TMA loads and UMMA
+// commits to both CTAs of a 2-CTA cluster) serve the paired bf16 GEMMs; they
+// only address this GPU's own memory.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
