@@ -284,3 +284,36 @@ def test_argument_errors_are_synchronous():
     with pytest.raises(moe.MoEError):
         plan.forward(Xmis, g["logits"], g["Wg"], g["Wu"], g["Wd"])
     assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_BF16, moe.MOE_NVFP4], ids=["bf16", "nvfp4"])
+def test_maximum_experts_and_top_k(prec):
+    """The largest supported routing: E = 1024 experts and k = 32 slots per
+    token (most experts get one or two rows, each padded to a 128-row tile),
+    plus the ring and one-launch schedules on the BF16 plan."""
+    T, d, F, E, k = 64, 256, 256, 1024, 32
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=13, alpha=1.1)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec))
+    if prec != moe.MOE_BF16:
+        plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    _check_routing(plan, saved, T, k, E, h["logits"])
+    fmt = "nvfp4" if prec == moe.MOE_NVFP4 else False
+    tol = 4e-2 if fmt else BF16_TOL
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k, mx=fmt)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"],
+                          moe_ref.stored_context(ctx) if fmt else ctx)
+    errs = {"Y": rel_err(Y, Yr)}
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        errs[key] = rel_err(out[key], gr[key])
+    assert all(v <= tol for v in errs.values()), errs
+    if prec == moe.MOE_BF16:
+        for flags in (moe.MOE_DEBUG_RING_MEGAKERNEL, moe.MOE_DEBUG_RING_MEGAKERNEL | moe.MOE_DEBUG_MULTI_LAUNCH):
+            other = _plan(T, d, F, E, k, flags)
+            Y2, _ = other.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+            torch.cuda.synchronize()
+            assert other.device_status() == 0
+            assert torch.equal(Y2, Y), flags
