@@ -83,6 +83,11 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_NVFP4 = 2 } moe_precision_t;
 /* BF16 ring schedule: routing, layout, the minibatch plan and the combine as
  * separate launches around the ring megakernel instead of inside it. */
 #define MOE_DEBUG_MULTI_LAUNCH 0x20u
+/* Block-scaled plans (MXFP8, NVFP4): the plan keeps the fp32 values its fused
+ * epilogues quantise -- h in the forward's up GEMM, dA|dB in the backward's
+ * u GEMM -- for moe_debug_quant_dump.  The forward then runs the separate
+ * kernels (the ring megakernel keeps no copy). */
+#define MOE_DEBUG_DUMP_QUANT 0x40u
 
 typedef struct {
   int64_t T_max;          /* largest token count a call may pass */
@@ -214,6 +219,24 @@ moe_status_t moe_nv_quantize(const void* src, int64_t rows, int64_t K, const flo
  * (MOE_ERR_INVALID_ARG otherwise).  Enqueued on `stream`. */
 moe_status_t moe_nv_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, const float* g,
                                         void* q, void* sf, moe_stream_t stream);
+
+/* Block-scaled plans created with MOE_DEBUG_DUMP_QUANT: copy, from the last
+ * forward (which = 0: h) or backward (which = 1: dA|dB), the fp32 values the
+ * fused epilogue quantised and the bytes it wrote, over the plan's full
+ * padded row capacity P (the sorted rows of the routing, each expert's
+ * segment padded to 128 rows; rows past the last segment are not written):
+ *   vals [P, C] fp32 with C = F (h) or 2F (dA|dB);
+ *   q    [P, C] E4M3 bytes (MXFP8) or [P, C / 2] packed E2M1 (NVFP4);
+ *   sf   scale atoms of the P rows with K = C (moe_mx_quantize /
+ *        moe_nv_quantize layout).
+ * P = moe_plan_padded_rows.  Any pointer may be NULL to skip it.  Synchronous
+ * argument errors (MOE_ERR_INVALID_ARG) for a plan without the flag, a BF16
+ * plan or another `which`.  Enqueued on `stream`. */
+moe_status_t moe_debug_quant_dump(moe_plan_t plan, int32_t which, float* vals, void* q, void* sf,
+                                  moe_stream_t stream);
+
+/* Padded sorted-row capacity P of a plan (for T = T_max). */
+moe_status_t moe_plan_padded_rows(moe_plan_t plan, int64_t* rows);
 
 /* NVFP4 plans: copy the two fp32 tensor scales moe_quantize_weights computed
  * ([0] Wg and Wu together, [1] Wd) into out (2 device floats), on `stream`.

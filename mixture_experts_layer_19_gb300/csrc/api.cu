@@ -204,6 +204,8 @@ struct moe_plan_s {
   // packed E2M1 values and a scale per 16; its fp32 tensor scales: [0] Wg and
   // Wu together, [1] Wd
   float* nv_scale = nullptr;
+  // MOE_DEBUG_DUMP_QUANT: fp32 values the fused epilogues quantise (h, dA|dB)
+  float *dbg_h = nullptr, *dbg_dab = nullptr;
   // ring-buffer forward megakernel (BF16): ring slots of X and h rows, GPU-local
   // hand-off counters, minibatch table
   void* ring_ws = nullptr;
@@ -581,6 +583,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_xtq = m; m += align256(t_pad * c.d);
     const size_t o_xts = m; m += align256(t_pad * c.d / 32);
     const size_t o_nvs = m; m += 256;
+    const bool dump = (c.debug_flags & MOE_DEBUG_DUMP_QUANT) != 0;
+    const size_t o_dbh = m; m += dump ? align256((size_t)R * c.F * 4) : 0;
+    const size_t o_dbd = m; m += dump ? align256((size_t)R * 2 * c.F * 4) : 0;
     err = cudaMalloc(&p->mx_ws, m);
     if (err != cudaSuccess) {
       if (p->ring_ws) cudaFree(p->ring_ws);
@@ -599,6 +604,10 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->ring_xq = mb + o_rxq; p->ring_xs = mb + o_rxs; p->ring_hq = mb + o_rhq; p->ring_hs = mb + o_rhs;
     p->Xtq = mb + o_xtq; p->Xts = mb + o_xts;
     p->nv_scale = reinterpret_cast<float*>(mb + o_nvs);
+    if (dump) {
+      p->dbg_h = reinterpret_cast<float*>(mb + o_dbh);
+      p->dbg_dab = reinterpret_cast<float*>(mb + o_dbd);
+    }
     const uint64_t EF = (uint64_t)c.E * c.F, Ed = (uint64_t)c.E * c.d;
     const uint32_t qbox = nv ? 16 : 32;  // bytes of 32 quantised values
     ok = map_fp8_kmajor(&p->m_Wgq, p->Wgq, qb(c.d), EF) && map_fp8_kmajor(&p->m_Wuq, p->Wuq, qb(c.d), EF) &&
@@ -751,7 +760,8 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP combine launch");
     return MOE_OK;
   }
-  const bool ring = (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS);
+  const bool ring = (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) && !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS) &&
+                    !(mx && (c.debug_flags & MOE_DEBUG_DUMP_QUANT));
   if (!mx && !ident && ring && !(c.debug_flags & MOE_DEBUG_MULTI_LAUNCH)) {
     MegaArgs m = mega_args(p, rp, X, m_ab_st);
     m.logits = logits;
@@ -866,6 +876,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     a.sfB1 = p->Wus;
     a.sfO = p->Hs;
     a.tsB = nv ? p->nv_scale : nullptr;
+    a.dbg = p->dbg_h;
     err = timed_launch(p, nv ? "gemm_nv_up_swiglu" : "gemm_mx_up_swiglu", st,
                        [&] { return launch_gemm_mx(kUp, a, p->num_sms, st, nv); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled up GEMM launch");
@@ -1035,6 +1046,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     u.wts = rp.w;
     u.dgp = p->dgp;
     u.tsB = nv ? p->nv_scale + 1 : nullptr;
+    u.dbg = p->dbg_dab;
     err = timed_launch(p, nv ? "gemm_nv_bwd_u_swiglu" : "gemm_mx_bwd_u_swiglu", st,
                        [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st, nv); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled u GEMM launch");
@@ -1346,6 +1358,32 @@ moe_status_t moe_quantize_weights(moe_plan_t p, const void* Wg, const void* Wu, 
   if (err != cudaSuccess) return cuda_fail(err, "moe_quantize_weights: launch");
   p->weights_quantized = true;
   return MOE_OK;
+}
+
+moe_status_t moe_plan_padded_rows(moe_plan_t p, int64_t* rows) {
+  if (!p || !rows) return fail(MOE_ERR_INVALID_ARG, "moe_plan_padded_rows: null argument");
+  *rows = p->Rpm;
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_quant_dump(moe_plan_t p, int32_t which, float* vals, void* q, void* sf, moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: null plan");
+  const moe_config_t& c = p->cfg;
+  if (c.prec == MOE_BF16 || !(c.debug_flags & MOE_DEBUG_DUMP_QUANT) || !p->dbg_h)
+    return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: needs a block-scaled plan made with MOE_DEBUG_DUMP_QUANT");
+  if (which != 0 && which != 1) return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: which must be 0 (h) or 1 (dA|dB)");
+  DeviceGuard guard(c.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool nv = c.prec == MOE_NVFP4;
+  const size_t cols = (size_t)(which == 0 ? c.F : 2 * c.F);
+  const size_t n = (size_t)p->Rpm * cols;
+  cudaError_t err = cudaSuccess;
+  if (vals) err = cudaMemcpyAsync(vals, which == 0 ? p->dbg_h : p->dbg_dab, n * 4, cudaMemcpyDeviceToDevice, st);
+  if (q && err == cudaSuccess)
+    err = cudaMemcpyAsync(q, which == 0 ? p->Hq : p->dABq, nv ? n / 2 : n, cudaMemcpyDeviceToDevice, st);
+  if (sf && err == cudaSuccess)
+    err = cudaMemcpyAsync(sf, which == 0 ? p->Hs : p->dABs, nv ? n / 16 : n / 32, cudaMemcpyDeviceToDevice, st);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_debug_quant_dump: copy");
 }
 
 moe_status_t moe_nv_weight_scales(moe_plan_t p, float* out, moe_stream_t stream) {

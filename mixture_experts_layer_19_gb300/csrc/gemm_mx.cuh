@@ -72,6 +72,8 @@ struct MxArgs {
   const int32_t* perm_src;   // kBwdU
   const float* wts;          // kBwdU
   float* dgp;                // kBwdU: [rows, F/128] partial <u, h> per 128 columns
+  float* dbg;                // debug (or null): the fp32 values the epilogue quantises,
+                             //   kUp h [rows, F], kBwdU dA|dB [rows, 2F]
   const int32_t* poff;
   const int32_t* mtile_off;
   int32_t* status;
@@ -314,6 +316,15 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             db[i] = dh * sl;
             wh[i] = wr * hh;
           }
+          if (g.dbg) {
+            float4* pa = reinterpret_cast<float4*>(g.dbg + (size_t)r * (2 * g.F) + col);
+            float4* pb = reinterpret_cast<float4*>(g.dbg + (size_t)r * (2 * g.F) + g.F + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              pa[i] = make_float4(da[4 * i], da[4 * i + 1], da[4 * i + 2], da[4 * i + 3]);
+              pb[i] = make_float4(db[4 * i], db[4 * i + 1], db[4 * i + 2], db[4 * i + 3]);
+            }
+          }
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           stage_row(stg, lane, da);
@@ -391,6 +402,12 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             a[i] = NV ? __uint_as_float(acc[c2][i]) * gs : __uint_as_float(acc[c2][i]);
             b[i] = NV ? __uint_as_float(acc[2 + c2][i]) * gs : __uint_as_float(acc[2 + c2][i]);
             h[i] = a[i] * sigmoidf_(a[i]) * b[i];
+          }
+          if (g.dbg) {
+            float4* ph = reinterpret_cast<float4*>(g.dbg + (size_t)(rowq + lane) * g.F + t.nt * 128 + half * 64 +
+                                                   c2 * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ph[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
           }
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();

@@ -26,6 +26,7 @@ MOE_DEBUG_SEPARATE_KERNELS = 0x4
 MOE_DEBUG_RING_MEGAKERNEL = 0x8
 MOE_DEBUG_SINGLE_CTA = 0x10
 MOE_DEBUG_MULTI_LAUNCH = 0x20
+MOE_DEBUG_DUMP_QUANT = 0x40
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_INTERNAL"}
@@ -36,7 +37,7 @@ EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_saved_bytes", "moe_forward", "m
             "moe_status_string", "moe_last_error", "moe_route_noalloc", "moe_quantize_weights",
             "moe_mx_quantize", "moe_router_forward", "moe_router_backward", "moe_mx_quantize_transposed",
             "moe_plan_info", "moe_nv_tensor_scale", "moe_nv_quantize", "moe_nv_quantize_transposed",
-            "moe_nv_weight_scales")
+            "moe_nv_weight_scales", "moe_debug_quant_dump", "moe_plan_padded_rows")
 
 
 class moe_config_t(ctypes.Structure):
@@ -76,6 +77,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "moe_nv_quantize": [VP, I64, I64, FP, VP, VP, P],
         "moe_nv_quantize_transposed": [VP, I64, I64, I64, FP, VP, VP, P],
         "moe_nv_weight_scales": [P, FP, P],
+        "moe_debug_quant_dump": [P, I32, FP, VP, VP, P],
+        "moe_plan_padded_rows": [P, ctypes.POINTER(I64)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +291,27 @@ class Plan:
         """MXFP8 / NVFP4 plans: fill the plan's quantised weight copies (once per weight update)."""
         _check(lib().moe_quantize_weights(self.handle, _ptr(Wg), _ptr(Wu), _ptr(Wd), _stream(stream)),
                "moe_quantize_weights")
+
+    def padded_rows(self) -> int:
+        """Padded sorted-row capacity of the plan (T = T_max)."""
+        n = ctypes.c_int64()
+        _check(lib().moe_plan_padded_rows(self.handle, ctypes.byref(n)), "moe_plan_padded_rows")
+        return n.value
+
+    def debug_quant_dump(self, which: int, stream=None):
+        """MOE_DEBUG_DUMP_QUANT plans: (fp32 values, quantised bytes, scale atoms)
+        of the fused epilogue quantisation -- which 0: h of the last forward,
+        1: dA|dB of the last backward -- over the padded row capacity."""
+        c = self.cfg
+        P = self.padded_rows()
+        cols = c.F if which == 0 else 2 * c.F
+        nv = c.prec == MOE_NVFP4
+        vals = torch.empty((P, cols), dtype=torch.float32, device=self.device)
+        q = torch.empty((P, cols // 2 if nv else cols), dtype=torch.uint8, device=self.device)
+        sf = torch.empty((P * cols // (16 if nv else 32),), dtype=torch.uint8, device=self.device)
+        _check(lib().moe_debug_quant_dump(self.handle, which, _ptr(vals), _ptr(q), _ptr(sf), _stream(stream)),
+               "moe_debug_quant_dump")
+        return vals, q, sf
 
     def nv_weight_scales(self, stream=None) -> torch.Tensor:
         """NVFP4 plans: the weights' tensor scales [g(Wg, Wu), g(Wd)] as a 2-element fp32 CUDA tensor."""

@@ -1,0 +1,66 @@
+"""The quantisers fused into the block-scaled GEMM epilogues, bit for bit.
+
+With MOE_DEBUG_DUMP_QUANT the plan keeps the fp32 values its epilogues
+quantise -- h in the forward's up GEMM (along F), dA|dB in the backward's u
+GEMM (along 2F) -- next to the bytes they wrote.  Re-quantising the GPU's own
+fp32 values with the oracle's codec (OCP MX for MXFP8; E2M1 with E4M3 scales
+per 16 and tensor scale 1 for NVFP4) must reproduce every element byte and
+every scale byte, padding rows included.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_19_gb300 import moe
+from oracle import mxfp8, nvfp4
+from tests.util import cpu_and_gpu_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _atom_offsets(rows, K, blk):
+    # scale byte of (row r, block b): atom (r // 128) * (K // (4 blk)) + b // 4,
+    # byte (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4 inside the 512-byte atom
+    r = np.arange(rows)[:, None]
+    b = np.arange(K // blk)[None, :]
+    atom = (r // 128) * (K // (4 * blk)) + b // 4
+    return atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("case", [(300, 512, 768, 16, 3, 1.5), (128, 256, 512, 8, 2, 0.0)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_fused_epilogue_quantisation_bit_exact(prec, case):
+    T, d, F, E, k, alpha = case
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=17, alpha=alpha)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, debug_flags=moe.MOE_DEBUG_DUMP_QUANT))
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    counts = plan.routing(saved, T)["counts"].cpu().numpy()
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    rows = int(sum((c + 127) // 128 * 128 for c in counts))   # padded sorted rows in use
+    nv = prec == moe.MOE_NVFP4
+    blk = 16 if nv else 32
+    for which, C in ((0, F), (1, 2 * F)):
+        vals, q, sf = plan.debug_quant_dump(which)
+        torch.cuda.synchronize()
+        v = vals[:rows].cpu().double().numpy()
+        assert np.isfinite(v).all() and np.abs(v).max() > 0
+        if nv:
+            codes, scales = nvfp4.nv_quantize(v, axis=1, g=1.0)
+            got = nvfp4.nv_unpack(q[:rows].cpu().numpy())
+        else:
+            codes, scales = mxfp8.mx_quantize(v, axis=1)
+            got = q[:rows].cpu().numpy()
+        bad = np.argwhere(got != codes)
+        assert bad.size == 0, (which, bad[:5].tolist(), v[tuple(bad[0])] if bad.size else None)
+        assert np.array_equal(sf.cpu().numpy()[_atom_offsets(rows, C, blk)], scales), which
+
+
+def test_dump_needs_the_flag():
+    plan = moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, prec=moe.MOE_NVFP4))
+    with pytest.raises(moe.MoEError) as ei:
+        plan.debug_quant_dump(0)
+    assert ei.value.status == 1
