@@ -174,14 +174,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "c61b200a06e2133612eb62ee24a025956bf3c51db23f556ee4ef6b3708ee595e",
+    "csrc_sha256": "c598148442bfe6df2b403cf83efa3cce4e286297a77ae318aca90ef713f1aec2",
     "bytes": {
-        "gemm_up_swiglu": 11881291622,
-        "gemm_down": 5720642150,
-        "gemm_bwd_u_swiglu": 6929362790,
-        "gemm_bwd_dx": 11184908595,
-        "gemm_wgrad_down": 8713543834,
-        "gemm_wgrad_gate_up": 16361207142,
+        "gemm_up_swiglu": 11898674944,
+        "gemm_down": 5725603123,
+        "gemm_bwd_u_swiglu": 6932607437,
+        "gemm_bwd_dx": 11177339136,
+        "gemm_wgrad_down": 8550838579,
+        "gemm_wgrad_gate_up": 16573376614,
     },
 }
 

@@ -926,6 +926,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     a.mapB1 = p->m_Wu_k;
     a.mapO0 = m_ab_st;
     a.mapO1 = p->m_H_st;
+    a.stall = (c.debug_flags & MOE_DEBUG_STALL_TEST) ? 1 : 0;
     err = timed_launch(p, "gemm_up_swiglu", st,
                        [&] { return launch_gemm_fwd(kUp, a, gemm_grid(p, kUp), use_pair(p, kUp), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: up GEMM launch");

@@ -83,6 +83,8 @@ struct GemmArgs {
   uint64_t timeout_ns;
   int E, d, F;
   int T;                     // dense kinds: tokens
+  int stall;                 // fault-injection test hook: the producer issues nothing, so the
+                             //   consumers' bounded waits expire (MOE_DEBUG_STALL_TEST)
 };
 
 struct Tile {
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
       uint32_t s = 0, ph = 0;
       uint32_t issued_mask = 0, last_par = 0;
       bool ok = true;
-      for (int w = w0; w < nwork && ok; w += wstep) {
+      for (int w = w0; w < nwork && ok && !g.stall; w += wstep) {
         const Tile t = PAIR ? decode_job<KIND>(g, w, rank) : decode_tile<KIND>(g, w);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
       }
-      if (PAIR && ok) {
+      if (PAIR && ok && !g.stall) {
         // the peer's last commits arrive on these barriers: they must land
         // before this CTA may exit
         for (int i = 0; i < kStages; ++i) {

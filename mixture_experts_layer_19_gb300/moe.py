@@ -27,6 +27,8 @@ MOE_DEBUG_RING_MEGAKERNEL = 0x8
 MOE_DEBUG_SINGLE_CTA = 0x10
 MOE_DEBUG_MULTI_LAUNCH = 0x20
 MOE_DEBUG_DUMP_QUANT = 0x40
+MOE_DEBUG_STALL_TEST = 0x80
+MOE_ERR_TIMEOUT = 5
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_INTERNAL"}
