@@ -204,6 +204,12 @@ struct moe_plan_s {
   // packed E2M1 values and a scale per 16; its fp32 tensor scales: [0] Wg and
   // Wu together, [1] Wd
   float* nv_scale = nullptr;
+  // The separate-kernel BF16 forward leaves the sorted X rows in Xg; the
+  // backward of that same forward (same X, saved context and T, no forward
+  // in between) reads them instead of gathering X again.
+  const void* xg_X = nullptr;
+  const void* xg_saved = nullptr;
+  int64_t xg_T = -1;
   // MOE_DEBUG_DUMP_QUANT: fp32 values the fused epilogues quantise (h, dA|dB)
   float *dbg_h = nullptr, *dbg_dab = nullptr;
   // ring-buffer forward megakernel (BF16): ring slots of X and h rows, GPU-local
@@ -712,6 +718,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   const RoutingPtrs rp = routing_ptrs(L, saved);
   const int Ti = (int)T;
   cudaError_t err;
+  p->xg_X = nullptr;  // set again below by the schedule that leaves X's sorted rows in Xg
 
   const bool mx = (c.prec == MOE_MXFP8 || c.prec == MOE_NVFP4) && !ident;  // block-scaled GEMMs
   const bool nv = c.prec == MOE_NVFP4;
@@ -945,6 +952,11 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   err = timed_launch(p, "combine", st,
                      [&] { return launch_combine(ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
+  if (!ident) {
+    p->xg_X = X;
+    p->xg_saved = saved;
+    p->xg_T = T;
+  }
   return MOE_OK;
 }
 
@@ -1007,8 +1019,12 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     ea.dYg = static_cast<uint4*>(p->dYg);
     err = timed_launch(p, "ep_pull_reverse_combine", st, [&] { return launch_ep_pull(ea, st); });
   } else {
+    // X's sorted rows are still in Xg when this is the backward of the plan's
+    // last forward, which ran the separate schedule: gather dY alone then
+    const bool xg_current = p->xg_X == X && p->xg_saved == saved && p->xg_T == T;
     err = timed_launch(p, "gather_bwd", st, [&] {
-      return launch_gather(dY, X, rp.perm_src, rp.totals, c.k, c.d, p->dYg, p->Xg, p->num_sms * 8, st);
+      return launch_gather(dY, xg_current ? nullptr : X, rp.perm_src, rp.totals, c.k, c.d, p->dYg,
+                           xg_current ? nullptr : p->Xg, p->num_sms * 8, st);
     });
   }
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: gather launch");

@@ -317,3 +317,24 @@ def test_maximum_experts_and_top_k(prec):
             torch.cuda.synchronize()
             assert other.device_status() == 0
             assert torch.equal(Y2, Y), flags
+
+
+@pytest.mark.parametrize("flags", [0, moe.MOE_DEBUG_SINGLE_CTA], ids=["paired", "single_cta"])
+def test_backward_reuses_sorted_x_only_for_its_own_forward(flags):
+    """The backward of the plan's last (separate-schedule) forward reads X's
+    sorted rows left by that forward; after another forward on the plan it
+    gathers them again.  Both must give the same gradients bit for bit."""
+    T, d, F, E, k = 300, 512, 512, 16, 4
+    gA, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=41, alpha=1.1)
+    gB, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=42, alpha=0.0)
+    W = (gA["Wg"], gA["Wu"], gA["Wd"])
+    plan = _plan(T, d, F, E, k, flags)
+    _, sA = plan.forward(gA["X"], gA["logits"], *W)
+    reused = plan.backward(gA["dY"], gA["X"], *W, sA)
+    _, sA2 = plan.forward(gA["X"], gA["logits"], *W)
+    plan.forward(gB["X"], gB["logits"], *W)             # another forward: its rows replace A's
+    regathered = plan.backward(gA["dY"], gA["X"], *W, sA2)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+        assert torch.equal(reused[key], regathered[key]), key
