@@ -39,7 +39,12 @@ constexpr int kMxBK = 128;  // bytes of K per stage (128 E4M3 or 256 E2M1 values
 // quantised along their K (the dgrad GEMMs' K), so every operand is K-major.
 template <int KIND, bool NV = false>
 struct MxTraits {
-  static constexpr int stages = NV ? 3 : (KIND == kUp || KIND == kBwdU) ? 3 : 4;
+  // MXFP8 keeps four stages in every kind: its multi-output epilogues (up:
+  // a, b, h; bwd-u: dA, dB, w h) stage their bf16 tiles one after another
+  // through a single buffer (seq), which leaves room for the fourth stage.
+  // NVFP4's 54 KB stages fit three.
+  static constexpr bool seq = !NV;
+  static constexpr int stages = NV ? 3 : 4;
   static constexpr int epi_warps = 8;
   static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int kelems = NV ? 256 : 128;         // K values per stage
@@ -49,7 +54,8 @@ struct MxTraits {
   static constexpr int sf_cols = NV ? 48 : 16;          // TMEM columns of one stage's scales
   static constexpr int qout = NV ? 512 : 1024;          // one 32 x 32 quantised staging tile
   static constexpr int staging_per_warp =
-      (KIND == kUp) ? (2 * 2048 + qout) : (KIND == kBwdU) ? (3 * 2048 + 2 * qout) : 2048;
+      (KIND == kUp) ? ((seq ? 1 : 2) * 2048 + qout)
+      : (KIND == kBwdU) ? (seq ? 2048 + qout : 3 * 2048 + 2 * qout) : 2048;
   static constexpr int staging_off = (stages * (kStageBytes + sf_stage) + 1023) / 1024 * 1024;
   static constexpr int smem_bytes = staging_off + epi_warps * staging_per_warp + 1024 + 256;
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
@@ -325,6 +331,50 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
               pb[i] = make_float4(db[4 * i], db[4 * i + 1], db[4 * i + 2], db[4 * i + 3]);
             }
           }
+          constexpr int qd = NV ? 2 : 1;   // values per quantised byte
+          if constexpr (TR::seq) {
+            // one bf16 and one quantised buffer, reused output by output
+            uint32_t qa[8], qb[8];
+            const int Xa = mx_block_exponent(amax32(da));
+            const int Xb = mx_block_exponent(amax32(db));
+            mx_encode32(da, Xa, qa);
+            mx_encode32(db, Xb, qb);
+            sfa[0] |= (uint32_t)(Xa + 127) << (8 * c);
+            sfb[0] |= (uint32_t)(Xb + 127) << (8 * c);
+            uint8_t* sq = stg + kStageChunk;
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            stage_row(stg, lane, da);
+            stage_row_fp8(sq, lane, qa);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&g.mapO0, stg, col, rowq);
+              tma_store_2d(&g.mapO1, sq, col / qd, rowq);
+              bulk_commit();
+              bulk_wait_read<0>();
+            }
+            __syncwarp();
+            stage_row(stg, lane, db);
+            stage_row_fp8(sq, lane, qb);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&g.mapO0, stg, g.F + col, rowq);
+              tma_store_2d(&g.mapO1, sq, (g.F + col) / qd, rowq);
+              bulk_commit();
+              bulk_wait_read<0>();
+            }
+            __syncwarp();
+            stage_row(stg, lane, wh);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&g.mapO2, stg, col, rowq);
+              bulk_commit();
+            }
+            continue;
+          }
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           stage_row(stg, lane, da);
@@ -350,7 +400,6 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            constexpr int qd = NV ? 2 : 1;   // values per quantised byte
             tma_store_2d(&g.mapO0, stg, col, rowq);
             tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
             tma_store_2d(&g.mapO2, stg + 2 * kStageChunk, col, rowq);
@@ -408,6 +457,35 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
                                                    c2 * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i) ph[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          }
+          if constexpr (TR::seq) {
+            // a, then b with h, through one bf16 buffer and one E4M3 buffer
+            const int X = mx_block_exponent(amax32(h));
+            uint32_t hq[8];
+            mx_encode32(h, X, hq);
+            sfw |= (uint32_t)(X + 127) << (8 * c2);
+            const int col = t.nt * 128 + half * 64 + c2 * 32;
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            stage_row(stg, lane, a);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&g.mapO0, stg, col, rowq);
+              bulk_commit();
+              bulk_wait_read<0>();
+            }
+            __syncwarp();
+            stage_row(stg, lane, b);
+            stage_row_fp8(stg + kStageChunk, lane, hq);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&g.mapO0, stg, g.F + col, rowq);
+              tma_store_2d(&g.mapO1, stg + kStageChunk, col, rowq);
+              bulk_commit();
+            }
+            continue;
           }
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
