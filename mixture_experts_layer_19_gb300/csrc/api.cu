@@ -99,6 +99,10 @@ bool map_mnmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) 
 bool map_store(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
   return encode_2d(m, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
+// bf16 stores of 32 rows x 16 columns, no swizzle (the NVFP4 GEMMs' half-chunk staging).
+bool map_store16(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return encode_2d(m, b, inner, outer, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 
 struct SavedLayout {
   size_t idx, w, dest, counts, offsets, poff, mtile, totals, perm, ab, total;
@@ -200,6 +204,7 @@ struct moe_plan_s {
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
   CUtensorMap m_WdTq, m_WgTq, m_WuTq, m_dABq_k, m_dABq_st;
+  CUtensorMap m_Ys_st16;  // NVFP4: Ys stores in 16-column boxes
   // NVFP4 (prec == MOE_NVFP4) reuses the block-scaled buffers above with
   // packed E2M1 values and a scale per 16; its fp32 tensor scales: [0] Wg and
   // Wu together, [1] Wd
@@ -623,7 +628,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
          map_fp8_kmajor(&p->m_WgTq, p->WgTq, qb(c.F), Ed, BN) &&
          map_fp8_kmajor(&p->m_WuTq, p->WuTq, qb(c.F), Ed, BN) &&
          map_fp8_kmajor(&p->m_dABq_k, p->dABq, qb(2 * c.F), R) &&
-         map_fp8_store(&p->m_dABq_st, p->dABq, qb(2 * c.F), R, qbox);
+         map_fp8_store(&p->m_dABq_st, p->dABq, qb(2 * c.F), R, qbox) &&
+         (!nv || map_store16(&p->m_Ys_st16, p->Ys, c.d, R));
     if (ok && !nv)
       ok = map_fp8_kmajor(&p->m_ring_xq, p->ring_xq, c.d, ring_rows) &&
            map_fp8_kmajor(&p->m_ring_hq, p->ring_hq, c.F, ring_rows) &&
@@ -725,8 +731,10 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   if (mx && !p->weights_quantized)
     return fail(MOE_ERR_INVALID_ARG, "moe_forward: block-scaled plan needs moe_quantize_weights before the forward");
   if (!ident && !ensure_weight_maps(p, Wg, Wu, Wd)) return fail(MOE_ERR_CUDA, "moe_forward: weight tensor maps");
-  CUtensorMap m_ab_st;
+  CUtensorMap m_ab_st, m_ab_st16;
   if (!ident && !map_store(&m_ab_st, static_cast<char*>(saved) + L.ab, 2 * c.F, L.rows))
+    return fail(MOE_ERR_CUDA, "moe_forward: saved tensor map");
+  if (mx && c.prec == MOE_NVFP4 && !map_store16(&m_ab_st16, static_cast<char*>(saved) + L.ab, 2 * c.F, L.rows))
     return fail(MOE_ERR_CUDA, "moe_forward: saved tensor map");
 
   // BF16 ring schedule, one launch: routing, layout, ring pipeline and
@@ -876,7 +884,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     a.mapA = p->m_Xq;
     a.mapB0 = p->m_Wgq;
     a.mapB1 = p->m_Wuq;
-    a.mapO0 = m_ab_st;
+    a.mapO0 = nv ? m_ab_st16 : m_ab_st;
     a.mapO1 = p->m_Hq_st;
     a.sfA = p->Xs;
     a.sfB0 = p->Wgs;
@@ -889,7 +897,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled up GEMM launch");
     b.mapA = p->m_Hq_k;
     b.mapB0 = p->m_Wdq;
-    b.mapO0 = p->m_Ys_st;
+    b.mapO0 = nv ? p->m_Ys_st16 : p->m_Ys_st;
     b.sfA = p->Hs;
     b.sfB0 = p->Wds;
     b.tsB = nv ? p->nv_scale + 1 : nullptr;
@@ -1070,7 +1078,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     x.mapA = p->m_dABq_k;
     x.mapB0 = p->m_WgTq;
     x.mapB1 = p->m_WuTq;
-    x.mapO0 = p->m_Ys_st;
+    x.mapO0 = nv ? p->m_Ys_st16 : p->m_Ys_st;
     x.sfA = p->dABs;
     x.sfB0 = p->WgTs;
     x.sfB1 = p->WuTs;

@@ -43,8 +43,13 @@ struct MxTraits {
   // a, b, h; bwd-u: dA, dB, w h) stage their bf16 tiles one after another
   // through a single buffer (seq), which leaves room for the fourth stage.
   // NVFP4's 54 KB stages fit three.
+  // NVFP4's 54 KB stages fit four in the up, down and dx kinds when their
+  // bf16 outputs go out 16 columns at a time through one 1 KB buffer per
+  // warp (half16); its bwd-u kind releases TMEM only after its stores, so it
+  // keeps three stages and the roomier staging.
   static constexpr bool seq = !NV;
-  static constexpr int stages = NV ? 3 : 4;
+  static constexpr bool half16 = NV && KIND != kBwdU;
+  static constexpr int stages = (NV && KIND == kBwdU) ? 3 : 4;
   static constexpr int epi_warps = 8;
   static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int kelems = NV ? 256 : 128;         // K values per stage
@@ -54,7 +59,8 @@ struct MxTraits {
   static constexpr int sf_cols = NV ? 48 : 16;          // TMEM columns of one stage's scales
   static constexpr int qout = NV ? 512 : 1024;          // one 32 x 32 quantised staging tile
   static constexpr int staging_per_warp =
-      (KIND == kUp) ? ((seq ? 1 : 2) * 2048 + qout)
+      half16 ? 1024
+      : (KIND == kUp) ? ((seq ? 1 : 2) * 2048 + qout)
       : (KIND == kBwdU) ? (seq ? 2048 + qout : 3 * 2048 + 2 * qout) : 2048;
   static constexpr int staging_off = (stages * (kStageBytes + sf_stage) + 1023) / 1024 * 1024;
   static constexpr int smem_bytes = staging_off + epi_warps * staging_per_warp + 1024 + 256;
@@ -66,7 +72,7 @@ struct MxArgs {
   CUtensorMap mapA;   // quantised activations [rows, K bytes]
   CUtensorMap mapB0;  // quantised weights (Wg / Wd)
   CUtensorMap mapB1;  // quantised weights (Wu) for kUp
-  CUtensorMap mapO0;  // bf16 stores (a|b for kUp, Ys for kDown)
+  CUtensorMap mapO0;  // bf16 stores (a|b for kUp, Ys for kDown); NVFP4 up/down/dx: 16-column boxes
   CUtensorMap mapO1;  // quantised stores (kUp: h; kBwdU: dA|dB)
   CUtensorMap mapO2;  // kBwdU: bf16 w h stores
   const uint8_t* sfA;   // scale atoms of A (rows = sorted padded rows)
@@ -137,6 +143,16 @@ __device__ __forceinline__ void stage_row_fp8(uint8_t* buf, int lane, const uint
   uint4* p = reinterpret_cast<uint4*>(buf + lane * 32);
   p[0] = make_uint4(q[0], q[1], q[2], q[3]);
   p[1] = make_uint4(q[4], q[5], q[6], q[7]);
+}
+
+// 16 floats -> 16 bf16 of one row into an unswizzled 32-row x 32-byte staging tile.
+__device__ __forceinline__ void stage_row16(uint8_t* buf, int lane, const float* v) {
+  uint32_t p[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+  uint4* d = reinterpret_cast<uint4*>(buf + lane * 32);
+  d[0] = make_uint4(p[0], p[1], p[2], p[3]);
+  d[1] = make_uint4(p[4], p[5], p[6], p[7]);
 }
 
 // 32 values -> 16 packed E2M1 bytes of one row into an unswizzled 32x16-byte staging tile.
@@ -458,6 +474,29 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
 #pragma unroll
             for (int i = 0; i < 8; ++i) ph[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
           }
+          if constexpr (TR::half16) {
+            // a and b in 16-column halves, then h, through one 1 KB buffer
+            uint4 hq;
+            sfw |= nv_encode32(h, rc1, 1.0f, hq) << (16 * c2);
+            const int col = t.nt * 128 + half * 64 + c2 * 32;
+#pragma unroll
+            for (int part = 0; part < 5; ++part) {
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              if (part < 2) stage_row16(stg, lane, a + 16 * part);
+              else if (part < 4) stage_row16(stg, lane, b + 16 * (part - 2));
+              else stage_row_fp4(stg, lane, hq);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (part < 2) tma_store_2d(&g.mapO0, stg, col + 16 * part, rowq);
+                else if (part < 4) tma_store_2d(&g.mapO0, stg, g.F + col + 16 * (part - 2), rowq);
+                else tma_store_2d(&g.mapO1, stg, col / 2, rowq);
+                bulk_commit();
+              }
+            }
+            continue;
+          }
           if constexpr (TR::seq) {
             // a, then b with h, through one bf16 buffer and one E4M3 buffer
             const int X = mx_block_exponent(amax32(h));
@@ -527,6 +566,21 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = NV ? __uint_as_float(acc[c][i]) * gs : __uint_as_float(acc[c][i]);
+          if constexpr (TR::half16) {
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              stage_row16(stg, lane, v + 16 * part);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&g.mapO0, stg, t.nt * BN + half * 128 + c * 32 + 16 * part, rowq);
+                bulk_commit();
+              }
+            }
+            continue;
+          }
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           stage_row(stg, lane, v);
