@@ -199,7 +199,7 @@ struct moe_plan_s {
   uint8_t *dABq = nullptr, *dABs = nullptr;
   // MXFP8 ring slots: E4M3 X and h rows with their scale atoms
   uint8_t *ring_xq = nullptr, *ring_xs = nullptr, *ring_hq = nullptr, *ring_hs = nullptr;
-  uint8_t *Xtq = nullptr, *Xts = nullptr;  // tokens quantised once per token (ring path)
+  uint8_t *Xtq = nullptr, *Xts = nullptr;  // tokens (X, or dY in the backward) quantised once per token
   CUtensorMap m_ring_xq, m_ring_hq, m_ring_hq_st;
   bool weights_quantized = false;
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
@@ -590,9 +590,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_rxs = m; m += align256(ring_rows * c.d / 32);
     const size_t o_rhq = m; m += align256(ring_rows * c.F);
     const size_t o_rhs = m; m += align256(ring_rows * c.F / 32);
-    const size_t t_pad = nv ? 0 : ((size_t)c.T_max + BM - 1) / BM * BM;
-    const size_t o_xtq = m; m += align256(t_pad * c.d);
-    const size_t o_xts = m; m += align256(t_pad * c.d / 32);
+    const size_t t_pad = ((size_t)c.T_max + BM - 1) / BM * BM;
+    const size_t o_xtq = m; m += align256(qb(t_pad * c.d));
+    const size_t o_xts = m; m += align256(sb(t_pad * c.d));
     const size_t o_nvs = m; m += 256;
     const bool dump = (c.debug_flags & MOE_DEBUG_DUMP_QUANT) != 0;
     const size_t o_dbh = m; m += dump ? align256((size_t)R * c.F * 4) : 0;
@@ -866,10 +866,17 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   if (mx) {
     // MXFP8 / NVFP4: gather + quantise X along d, block-scaled [a|b] GEMM with
     // SwiGLU and h re-quantised along F in its epilogue, block-scaled down GEMM.
-    err = timed_launch(p, "gather_quant", st, [&] {
-      return nv ? launch_nv_gather_quant(X, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st)
-                : launch_gather_quant(X, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+    // each token quantised once, then its bytes and scale words copied into
+    // the sorted rows (the same bytes as quantising every routed row)
+    err = timed_launch(p, "quant_tokens", st, [&] {
+      return nv ? launch_nv_quant_rows(X, T, c.d, nullptr, p->Xtq, p->Xts, p->num_sms * 8, st)
+                : launch_quant_rows(X, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
     });
+    if (err == cudaSuccess)
+      err = timed_launch(p, "gather_quant", st, [&] {
+        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.totals, c.k, nv ? c.d / 2 : c.d,
+                                    nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
+      });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
     MxArgs a;
     memset(&a, 0, sizeof(a));
@@ -1043,10 +1050,15 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     // against Wd^T (quantised along d) with dA|dB re-quantised along F in its
     // epilogue; dx GEMM against [Wg^T; Wu^T] (quantised along F).  The weight
     // gradients below use the bf16 operands.
-    err = timed_launch(p, "gather_quant_dy", st, [&] {
-      return nv ? launch_nv_gather_quant(dY, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st)
-                : launch_gather_quant(dY, rp.perm_src, rp.totals, c.k, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+    err = timed_launch(p, "quant_tokens_dy", st, [&] {
+      return nv ? launch_nv_quant_rows(dY, T, c.d, nullptr, p->Xtq, p->Xts, p->num_sms * 8, st)
+                : launch_quant_rows(dY, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
     });
+    if (err == cudaSuccess)
+      err = timed_launch(p, "gather_quant_dy", st, [&] {
+        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.totals, c.k, nv ? c.d / 2 : c.d,
+                                    nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
+      });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dY gather launch");
     MxArgs u;
     memset(&u, 0, sizeof(u));

@@ -88,10 +88,12 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, int grid, cud
 
 // MXFP8 (mx_quant.cu, gemm_mx.cu)
 cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st);
-cudaError_t launch_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d, void* q,
-                                void* sf, int grid, cudaStream_t st);
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
                                    cudaStream_t st);
+// Sorted rows <- token-quantised rows (E4M3 or packed E2M1 bytes, row_bytes
+// per row, and nblk scale bytes per row in the atom layout).
+cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* totals,
+                                 int k, int row_bytes, int nblk, void* q, void* sf, int grid, cudaStream_t st);
 struct MxArgs;
 // kind 0 up, 1 down, 2 bwd-u, 3 bwd-x; nv: the NVFP4 variant (E2M1 operands,
 // E4M3 scales per 16, tensor scales in MxArgs::tsB)
@@ -103,8 +105,6 @@ cudaError_t launch_nv_tensor_scale(const void* a, int64_t na, const void* b, int
                                    cudaStream_t st);
 cudaError_t launch_nv_quant_rows(const void* src, int64_t rows, int K, const float* g, void* q, void* sf, int grid,
                                  cudaStream_t st);
-cudaError_t launch_nv_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d,
-                                   void* q, void* sf, int grid, cudaStream_t st);
 cudaError_t launch_nv_quant_transpose(const void* src, int E, int A, int B, const float* g, void* q, void* sf,
                                       int grid, cudaStream_t st);
 

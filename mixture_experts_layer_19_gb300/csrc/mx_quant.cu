@@ -3,12 +3,15 @@
 //  * quant_rows_kernel: a bf16 row-major [rows, K] matrix -> E4M3 [rows, K] +
 //    scale atoms, blocks of 32 along K (the expert weights once per optimiser
 //    step, and the public moe_mx_quantize utility).
-//  * gather_quant_kernel: the forward gather with the quantisation fused in
-//    (MXFP8 activation quantisation inside the dispatch datapath: kucoin page
-//    "Cursor's MoK réalise une amélioration des performances de 2,37x sur
-//    NVIDIA GB300 NVL72", section 02): sorted row r <- MXFP8(X[perm_src[r]/k]),
-//    padding rows -> zero bytes and zero scales.
-// One thread per 32-element block: 64 contiguous input bytes, 32 output bytes.
+//    The same kernel quantises the tokens (X, or dY in the backward) once per
+//    token for the dispatch (MXFP8 activation quantisation inside the
+//    dispatch datapath: kucoin page "Cursor's MoK réalise une amélioration des
+//    performances de 2,37x sur NVIDIA GB300 NVL72", section 02).
+//  * gather_rows_q_kernel: sorted row r <- the quantised row of token
+//    perm_src[r] / k, element bytes and scale words; padding rows -> zero
+//    bytes and zero scales (MXFP8 and NVFP4 rows alike).
+// Quantisers: one thread per 32-element block: 64 contiguous input bytes, 32
+// output bytes.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -55,29 +58,6 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
   }
 }
 
-__global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16* __restrict__ X,
-                                                           const int32_t* __restrict__ perm_src,
-                                                           const int32_t* __restrict__ totals, int k, int d,
-                                                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
-  const int kblocks = d >> 5;
-  const int64_t total = (int64_t)totals[0] * kblocks;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / kblocks;
-    const int kb = (int)(i - r * kblocks);
-    const int src = perm_src[r];
-    uint8_t* dq = q + r * d + kb * 32;
-    if (src < 0) {
-      reinterpret_cast<uint4*>(dq)[0] = make_uint4(0, 0, 0, 0);
-      reinterpret_cast<uint4*>(dq)[1] = make_uint4(0, 0, 0, 0);
-      sf[sf_atom_offset(r, kb, kblocks)] = 0;
-      continue;
-    }
-    float v[32];
-    load_bf16x32_f(X + (int64_t)(src / k) * d + kb * 32, v);
-    quant_block_store(v, dq, sf + sf_atom_offset(r, kb, kblocks));
-  }
-}
-
 // src [E][A][B] bf16 -> q [E][B][A] E4M3 quantised along A (the backward
 // orientation of a weight: the K of the dgrad GEMMs), scale atoms over rows
 // E*B with K = A.  One CTA transposes a 128 (A) x 64 (B) tile through shared
@@ -118,6 +98,55 @@ __global__ void __launch_bounds__(256) quant_transpose_kernel(const __nv_bfloat1
   }
 }
 
+// Sorted row r <- the quantised row of token perm_src[r] / k: its
+// row_bytes element bytes and its scale words (4 blocks = 4 bytes per atom
+// word), from the token-quantised copy (one quantisation per token, made by
+// quant_rows_kernel / nv_quant_rows_kernel) into the sorted rows' atoms;
+// padding rows get zero bytes and zero scales.  Same bytes as quantising each
+// routed row.  One warp per row; nblk = scale blocks per row (a multiple of 4).
+__global__ void __launch_bounds__(256) gather_rows_q_kernel(const uint8_t* __restrict__ q_tok,
+                                                            const uint8_t* __restrict__ sf_tok,
+                                                            const int32_t* __restrict__ perm_src,
+                                                            const int32_t* __restrict__ totals, int k, int row_bytes,
+                                                            int nblk, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int rows = totals[0];
+  const int nvec = row_bytes / 16;
+  const int nwords = nblk / 4;
+  const int lane = threadIdx.x & 31;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps_total) {
+    const int src = perm_src[r];
+    uint4* dq = reinterpret_cast<uint4*>(q + (size_t)r * row_bytes);
+    if (src < 0) {
+      for (int i = lane; i < nvec; i += 32) dq[i] = make_uint4(0, 0, 0, 0);
+      for (int w = lane; w < nwords; w += 32) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) = 0u;
+      continue;
+    }
+    const int64_t t = src / k;
+    const uint4* sq = reinterpret_cast<const uint4*>(q_tok + (size_t)t * row_bytes);
+    for (int i = lane; i < nvec; i += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i + 32 * u < nvec) v[u] = __ldg(sq + i + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i + 32 * u < nvec) dq[i + 32 * u] = v[u];
+    }
+    for (int w = lane; w < nwords; w += 32)
+      *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) =
+          __ldg(reinterpret_cast<const uint32_t*>(sf_tok + sf_atom_offset(t, 4 * w, nblk)));
+  }
+}
+
+cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* totals,
+                                 int k, int row_bytes, int nblk, void* q, void* sf, int grid, cudaStream_t st) {
+  gather_rows_q_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(q_tok),
+                                             reinterpret_cast<const uint8_t*>(sf_tok), perm_src, totals, k, row_bytes,
+                                             nblk, reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
                                    cudaStream_t st) {
   quant_transpose_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), E, A, B,
@@ -131,11 +160,5 @@ cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, voi
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d, void* q,
-                                void* sf, int grid, cudaStream_t st) {
-  gather_quant_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), perm_src, totals, k, d,
-                                            reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
-  return cudaGetLastError();
-}
 
 }  // namespace moe

@@ -5,9 +5,8 @@
 //    share one scale), 1 for an all-zero tensor;
 //  * nv_quant_rows_kernel: a bf16 row-major [rows, K] matrix -> packed E2M1
 //    [rows, K / 2] + scale atoms, blocks of 16 along K;
-//  * nv_gather_quant_kernel: the gather with the quantisation fused in
-//    (sorted row r <- NVFP4(X[perm_src[r] / k]), tensor scale 1), padding rows
-//    -> zero bytes and zero scales;
+//    (also the tokens, X or dY, once per token with tensor scale 1, before
+//    gather_rows_q_kernel copies them into the sorted rows);
 //  * nv_quant_transpose_kernel: a weight's backward orientation, quantised
 //    along its other axis.
 // One thread per 32 elements: 64 input bytes, 16 output bytes, 2 scale bytes.
@@ -104,28 +103,6 @@ __global__ void __launch_bounds__(256) nv_quant_rows_kernel(const __nv_bfloat16*
   }
 }
 
-__global__ void __launch_bounds__(256) nv_gather_quant_kernel(const __nv_bfloat16* __restrict__ X,
-                                                              const int32_t* __restrict__ perm_src,
-                                                              const int32_t* __restrict__ totals, int k, int d,
-                                                              uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
-  const float rc = nv_rc(1.0f);
-  const int chunks = d >> 5;
-  const int64_t total = (int64_t)totals[0] * chunks;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / chunks;
-    const int c0 = (int)(i - r * chunks) * 32;
-    const int src = perm_src[r];
-    if (src < 0) {
-      *reinterpret_cast<uint4*>(q + r * (d / 2) + c0 / 2) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint16_t*>(sf + sf_atom_offset(r, c0 / 16, d / 16)) = 0;
-      continue;
-    }
-    float v[32];
-    load32_bf16(X + (int64_t)(src / k) * d + c0, v);
-    nv_store32(v, rc, 1.0f, q + r * (d / 2), sf, r, c0, d / 16);
-  }
-}
-
 // src [E][A][B] bf16 -> q [E][B][A / 2] packed E2M1 quantised along A, scale
 // atoms over rows E * B with K = A.  One CTA transposes a 128 (A) x 64 (B)
 // tile through shared memory (the skewed layout of the MXFP8 transposer:
@@ -180,13 +157,6 @@ cudaError_t launch_nv_quant_rows(const void* src, int64_t rows, int K, const flo
                                  cudaStream_t st) {
   nv_quant_rows_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), rows, K, g,
                                              reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_nv_gather_quant(const void* X, const int32_t* perm_src, const int32_t* totals, int k, int d,
-                                   void* q, void* sf, int grid, cudaStream_t st) {
-  nv_gather_quant_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(X), perm_src, totals, k, d,
-                                               reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }
 
