@@ -184,3 +184,55 @@ def test_nvfp4_needs_quantized_weights_and_validates():
     with pytest.raises(moe.MoEError) as ei:
         moe.nv_quantize(torch.zeros((4, 48), dtype=torch.bfloat16, device="cuda"))   # K % 64 != 0
     assert ei.value.status == 1
+
+
+def _block_scaled_parity(prec, plan, g, h, k, T):
+    """Forward + backward of a block-scaled plan against the oracle's emulation
+    of its quantisation points (backward on the saved context as stored)."""
+    fmt = "nvfp4" if prec == moe.MOE_NVFP4 else "mxfp8"
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    r = plan.routing(saved, T)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert np.array_equal(r["idx"].cpu().numpy(), moe_ref.route(h["logits"], k)[0])
+    ws = _weight_scales(h) if fmt == "nvfp4" else None
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k, mx=fmt, wscales=ws)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], moe_ref.stored_context(ctx))
+    errs = {"Y": rel_err(Y, Yr)}
+    errs.update({key: rel_err(out[key], gr[key]) for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")})
+    assert all(v <= NV_TOL for v in errs.values()), errs
+    return out
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("T", [1, 3, 129])
+def test_block_scaled_ragged_token_counts(prec, T):
+    d, F, E, k = 256, 256, 8, 2
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=100 + T)
+    plan = moe.Plan(moe.Config(T_max=256, d=d, F=F, E=E, k=k, prec=prec))
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    _block_scaled_parity(prec, plan, g, h, k, T)
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
+def test_block_scaled_degenerate_routing_and_zero_tokens(prec):
+    # every token picks experts 5 then 9; the other ten get nothing
+    T, d, F, E, k = 300, 256, 256, 12, 2
+    bias = torch.zeros(E)
+    bias[5], bias[9] = 40.0, 30.0
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=8, logits_fn=lambda L: L + bias[None, :])
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec))
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    out = _block_scaled_parity(prec, plan, g, h, k, T)
+    empty = [e for e in range(E) if e not in (5, 9)]
+    for key in ("dWg", "dWu", "dWd"):
+        assert torch.count_nonzero(out[key][empty]).item() == 0
+    # no tokens: a no-op forward and zero weight gradients
+    X0 = g["X"][:0].contiguous()
+    Y0, s0 = plan.forward(X0, g["logits"][:0].contiguous(), g["Wg"], g["Wu"], g["Wd"])
+    out0 = plan.backward(X0, X0, g["Wg"], g["Wu"], g["Wd"], s0)
+    torch.cuda.synchronize()
+    assert Y0.shape == (0, d)
+    for key in ("dWg", "dWu", "dWd"):
+        assert torch.count_nonzero(out0[key]).item() == 0
