@@ -238,10 +238,11 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
 
     MXFP8 / NVFP4 emulation (ctx["mx"]): dY along d and Wd along d for
     u = Wd^T dY; dA, dB along F and Wg, Wu along F for dX (NVFP4: the weights
-    with the forward's tensor scales, activations with scale 1).  The weight gradients take the
-    unquantised operands (dY, w*h, dA/dB, x): MXFP8 covers the GEMMs that stream
-    weights; the weight-gradient GEMMs, whose cost is writing dW, stay in the
-    higher precision.
+    with the forward's tensor scales, activations with scale 1).  The weight
+    gradients' operands (dY, w*h, dA/dB, x) are quantised along the tokens,
+    i.e. along the expert's rows in sorted order, in blocks from the segment's
+    first row (the last one zero-padded); dA/dB and w*h from the bf16 values
+    the layer keeps of them (their codes are decided from those).
     """
     dY = np.asarray(dY, dtype=np.float64)
     X = np.asarray(X, dtype=np.float64)
@@ -279,10 +280,7 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
         dx = _q(da, 1, mx) @ _q(wg, 0, mx, g_gu) + _q(db, 1, mx) @ _q(wu, 0, mx, g_gu)
         np.add.at(dX, tok, dx)
         # weight gradients: K = the expert's tokens in sorted order
-        dWd[e] = dY[tok].T @ (wr * h)
-        xs = X[tok]
-        dWg[e] = da.T @ xs
-        dWu[e] = db.T @ xs
+        dWd[e], dWg[e], dWu[e] = _weight_grads(dY[tok], X[tok], wr * h, da, db, mx)
     dg = dg.reshape(T, k)
     s = np.sum(w * dg, axis=1, keepdims=True)
     dsel = w * (dg - s)
@@ -295,6 +293,17 @@ def backward(dY, X, logits, Wg, Wu, Wd, ctx, sparse_dw=False):
 # Sampled forms for full-size layers: the same arithmetic restricted to a
 # subset of tokens (per-token outputs) or of experts (per-expert dW).
 # ----------------------------------------------------------------------------
+def _weight_grads(dy, xs, wh, da, db, fmt):
+    """(dWd, dWg, dWu) of one expert from its rows in sorted order (K = the
+    rows).  Block-scaled recipes quantise every operand along the rows: dy and
+    xs as given (bf16 inputs), w h, dA and dB from their bf16 values."""
+    if not fmt:
+        return dy.T @ wh, da.T @ xs, db.T @ xs
+    qt = lambda v: _q(v, 0, fmt)
+    xq = qt(xs)
+    return (qt(dy).T @ qt(bf16_round(wh)), qt(bf16_round(da)).T @ xq, qt(bf16_round(db)).T @ xq)
+
+
 def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False, wscales=None, stored=False):
     """Y, dX, dg, dlogits for the listed tokens only (BF16 arithmetic unless mx).
 
@@ -344,8 +353,9 @@ def forward_backward_tokens(X, logits, Wg, Wu, Wd, dY, k, tokens, mx=False, wsca
     return {"Y": Y, "dX": dX, "dg": dg, "dlogits": dlogits, "idx": idx, "w": w}
 
 
-def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False, wscales=None):
-    """dWg[e], dWu[e], dWd[e] over every token routed to expert e (sorted order)."""
+def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False, wscales=None, stored=False):
+    """dWg[e], dWu[e], dWd[e] over every token routed to expert e (sorted order);
+    stored=True: from a|b as the saved context stores them (bf16)."""
     fmt = _fmt(mx)
     g_gu, g_d = _wscales(fmt, Wg, Wu, Wd, wscales)
     idx, w = route(logits, k)
@@ -363,14 +373,16 @@ def expert_weight_grads(X, logits, Wg, Wu, Wd, dY, k, e, mx=False, wscales=None)
     Xq, dYq = _q(X, 1, fmt), _q(dY, 1, fmt)
     a = Xq @ _q(wg, 1, fmt, g_gu).T
     b = Xq @ _q(wu, 1, fmt, g_gu).T
+    if stored:
+        a, b = bf16_round(a), bf16_round(b)
     h = silu(a) * b
     u = dYq @ _q(wd, 0, fmt, g_d)
     dh = wr * u
     sa = sigmoid(a)
     da = dh * b * sa * (1.0 + a * (1.0 - sa))
     db = dh * silu(a)
-    dWd = dY.T @ (wr * h)
-    return da.T @ X, db.T @ X, dWd
+    dWd, dWg, dWu = _weight_grads(dY, X, wr * h, da, db, fmt)
+    return dWg, dWu, dWd
 
 
 # ----------------------------------------------------------------------------

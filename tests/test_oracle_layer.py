@@ -148,9 +148,28 @@ def test_mx_exact_inputs_only_intermediates_add_error():
     # dX differs only through dA/dB re-quantised along F
     r = np.abs(g1["dX"] - g0["dX"]).max() / np.abs(g0["dX"]).max()
     assert 0 < r < 2 ** -3, r
-    # weight gradients take unquantised operands, which are exact here: identical
-    for key in ("dWg", "dWu", "dWd"):
-        assert np.array_equal(g1[key], g0[key]), key
+    # weight gradients: every operand quantised along the expert's tokens;
+    # dY and X are exact along any axis, so only w*h, dA and dB (quantised from
+    # their bf16 values) change
+    qt = lambda v: mxfp8.mx_fake_quant(v, 0)
+    lay = c0["layout"]
+    for e in range(E):
+        rows = lay["perm_src"][lay["offsets"][e]:lay["offsets"][e + 1]]
+        if rows.size == 0:
+            continue
+        tok = rows // k
+        wr = c0["w"].reshape(-1)[rows][:, None]
+        a, b, h = c0["a"][rows], c0["b"][rows], c0["h"][rows]
+        u = dY[tok] @ Wd[e]
+        sa = moe_ref.sigmoid(a)
+        da = wr * u * b * sa * (1 + a * (1 - sa))
+        db = wr * u * moe_ref.silu(a)
+        assert np.array_equal(qt(dY[tok]), dY[tok]) and np.array_equal(qt(X[tok]), X[tok])
+        assert np.allclose(g1["dWd"][e], dY[tok].T @ qt(moe_ref.bf16_round(wr * h)), rtol=1e-12, atol=1e-12)
+        assert np.allclose(g1["dWg"][e], qt(moe_ref.bf16_round(da)).T @ X[tok], rtol=1e-12, atol=1e-12)
+        assert np.allclose(g1["dWu"][e], qt(moe_ref.bf16_round(db)).T @ X[tok], rtol=1e-12, atol=1e-12)
+    rel_w = np.abs(g1["dWg"] - g0["dWg"]).max() / np.abs(g0["dWg"]).max()
+    assert 0 < rel_w < 2 ** -3, rel_w
     # dg uses u (exact operands) and the unquantised h: identical
     assert np.array_equal(g0["dg"], g1["dg"])
 
@@ -196,3 +215,7 @@ def test_stored_context_sampled_form_matches_full_form():
         s = moe_ref.forward_backward_tokens(X, L, Wg, Wu, Wd, dY, k, toks, mx=mx, stored=True)
         for key, full in (("Y", Y), ("dX", g["dX"]), ("dg", g["dg"]), ("dlogits", g["dlogits"])):
             assert np.allclose(s[key], full[toks], rtol=1e-12, atol=1e-12), (mx, key)
+        e = int(np.argmax(ctx["layout"]["counts"]))
+        dwg, dwu, dwd = moe_ref.expert_weight_grads(X, L, Wg, Wu, Wd, dY, k, e, mx=mx, stored=True)
+        for name, got in (("dWg", dwg), ("dWu", dwu), ("dWd", dwd)):
+            assert np.allclose(got, g[name][e], rtol=1e-12, atol=1e-12), (mx, name)

@@ -207,12 +207,16 @@ def test_nvfp4_exact_inputs_only_intermediates_add_error():
               + nvfp4.nv_fake_quant(db, 1) @ nvfp4.nv_fake_quant(Wu[e], 0, g_gu))
         np.add.at(dX, tok, dx)
         assert np.allclose(g1["dg"].reshape(-1)[rows], np.sum(u * c0["h"][rows], axis=1), rtol=1e-12, atol=1e-12)
-        # weight gradients: unquantised dA, dB (from the quantised-weight u) and x
-        assert np.allclose(g1["dWg"][e], da.T @ X[tok], rtol=1e-12, atol=1e-12)
-        assert np.allclose(g1["dWu"][e], db.T @ X[tok], rtol=1e-12, atol=1e-12)
+        # weight gradients: every operand quantised along the expert's tokens
+        # (tensor scale 1), dA, dB and w*h from their bf16 values
+        qt = lambda v: nvfp4.nv_fake_quant(v, 0)
+        xq = qt(X[tok])
+        assert np.allclose(g1["dWg"][e], qt(moe_ref.bf16_round(da)).T @ xq, rtol=1e-12, atol=1e-12)
+        assert np.allclose(g1["dWu"][e], qt(moe_ref.bf16_round(db)).T @ xq, rtol=1e-12, atol=1e-12)
+        assert np.allclose(g1["dWd"][e], qt(dY[tok]).T @ qt(moe_ref.bf16_round(wr * c0["h"][rows])),
+                           rtol=1e-12, atol=1e-12)
     assert np.abs(g1["dX"] - dX).max() <= 1e-12 * np.abs(dX).max()
-    # dWd = (w dY)^T h takes no quantised operand: identical to the BF16-arithmetic oracle
-    assert np.array_equal(g1["dWd"], g0["dWd"])
+    assert not np.array_equal(g1["dWd"], g0["dWd"])
 
 
 def test_nvfp4_sampled_forms_equal_full_forms():
