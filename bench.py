@@ -646,10 +646,11 @@ def _alloc_grads(T, d, F, E, k, dev):
 
 
 def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha, prec=None):
-    """Block-scaled (MXFP8 or NVFP4) forward + backward at T tokens: quantised
-    forward and dgrad GEMMs, bf16 weight gradients.  Layer roofline:
-    max(12RdF / fp8 or fp4 peak + 6RdF / bf16 peak, (quantised weights fwd +
-    bwd orientation + bf16 dW) / HBM)."""
+    """Block-scaled (MXFP8 or NVFP4) forward + backward at T tokens: every
+    expert GEMM block-scaled (forward, dgrad, and the weight gradients with
+    their operands quantised along the tokens).  Layer roofline:
+    max(18RdF / fp8 or fp4 peak, (quantised weights fwd + bwd orientation +
+    bf16 dW) / HBM)."""
     from mixture_experts_layer_19_gb300 import moe
     prec = moe.MOE_MXFP8 if prec is None else prec
     fname, _, mult, wbytes, _ = _block_format(prec)
@@ -686,8 +687,8 @@ def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha, prec=None):
     kt = plan.kernel_times()
     e_act = active_experts(plan, saved, T)
     R = T * k
-    tpeak, bf16_peak = mult * peaks["bf16_tflops_sustained"], peaks["bf16_tflops_sustained"]
-    t_tc = (12.0 * R * d * F / tpeak + 6.0 * R * d * F / bf16_peak) / 1e12 * 1e3
+    tpeak = mult * peaks["bf16_tflops_sustained"]
+    t_tc = 18.0 * R * d * F / tpeak / 1e12 * 1e3
     # quantised weights of the active experts in both orientations, bf16 dW of every expert
     t_hbm = (2 * 3.0 * e_act * F * d * wbytes + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
     ms = el / steps

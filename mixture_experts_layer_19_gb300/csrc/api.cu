@@ -205,6 +205,12 @@ struct moe_plan_s {
   CUtensorMap m_Wgq, m_Wuq, m_Wdq, m_Xq, m_Hq_k, m_Hq_st;
   CUtensorMap m_WdTq, m_WgTq, m_WuTq, m_dABq_k, m_dABq_st;
   CUtensorMap m_Ys_st16;  // NVFP4: Ys stores in 16-column boxes
+  // block-scaled weight gradients: the backward's operands transposed and
+  // quantised along the tokens, [rows, Rpm] (dY^T, X^T: d rows; [dA|dB]^T: 2F;
+  // (w h)^T: F), with their scale atoms (K = Rpm)
+  uint8_t *dYTq = nullptr, *dYTs = nullptr, *XTq = nullptr, *XTs = nullptr, *dABTq = nullptr, *dABTs = nullptr,
+          *wHTq = nullptr, *wHTs = nullptr;
+  CUtensorMap m_dYTq, m_XTq, m_dABTq, m_wHTq;
   // NVFP4 (prec == MOE_NVFP4) reuses the block-scaled buffers above with
   // packed E2M1 values and a scale per 16; its fp32 tensor scales: [0] Wg and
   // Wu together, [1] Wd
@@ -491,7 +497,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   }
   for (int kind = 0; kind < 6; ++kind) {
     err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
-    if (err == cudaSuccess && kind < 4 && c.prec != MOE_BF16) err = prepare_gemm_mx(kind, c.prec == MOE_NVFP4);
+    if (err == cudaSuccess && c.prec != MOE_BF16) err = prepare_gemm_mx(kind, c.prec == MOE_NVFP4);
     if (err == cudaSuccess) p->pair_grid[kind] = kind < 2 ? gemm_pair_grid_fwd(kind) : gemm_pair_grid_bwd(kind);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -594,6 +600,16 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_xtq = m; m += align256(qb(t_pad * c.d));
     const size_t o_xts = m; m += align256(sb(t_pad * c.d));
     const size_t o_nvs = m; m += 256;
+    // transposed, token-wise quantised weight-gradient operands; 4 KB of slack
+    // after each scale buffer covers an NVFP4 half stage's unused atoms
+    const size_t o_dytq = m; m += align256(qb((size_t)c.d * R));
+    const size_t o_dyts = m; m += align256(sb((size_t)c.d * R)) + 4096;
+    const size_t o_xtrq = m; m += align256(qb((size_t)c.d * R));
+    const size_t o_xtrs = m; m += align256(sb((size_t)c.d * R)) + 4096;
+    const size_t o_dabtq = m; m += align256(qb((size_t)2 * c.F * R));
+    const size_t o_dabts = m; m += align256(sb((size_t)2 * c.F * R)) + 4096;
+    const size_t o_whtq = m; m += align256(qb((size_t)c.F * R));
+    const size_t o_whts = m; m += align256(sb((size_t)c.F * R)) + 4096;
     const bool dump = (c.debug_flags & MOE_DEBUG_DUMP_QUANT) != 0;
     const size_t o_dbh = m; m += dump ? align256((size_t)R * c.F * 4) : 0;
     const size_t o_dbd = m; m += dump ? align256((size_t)R * 2 * c.F * 4) : 0;
@@ -615,6 +631,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->ring_xq = mb + o_rxq; p->ring_xs = mb + o_rxs; p->ring_hq = mb + o_rhq; p->ring_hs = mb + o_rhs;
     p->Xtq = mb + o_xtq; p->Xts = mb + o_xts;
     p->nv_scale = reinterpret_cast<float*>(mb + o_nvs);
+    p->dYTq = mb + o_dytq; p->dYTs = mb + o_dyts; p->XTq = mb + o_xtrq; p->XTs = mb + o_xtrs;
+    p->dABTq = mb + o_dabtq; p->dABTs = mb + o_dabts; p->wHTq = mb + o_whtq; p->wHTs = mb + o_whts;
     if (dump) {
       p->dbg_h = reinterpret_cast<float*>(mb + o_dbh);
       p->dbg_dab = reinterpret_cast<float*>(mb + o_dbd);
@@ -629,7 +647,10 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
          map_fp8_kmajor(&p->m_WuTq, p->WuTq, qb(c.F), Ed, BN) &&
          map_fp8_kmajor(&p->m_dABq_k, p->dABq, qb(2 * c.F), R) &&
          map_fp8_store(&p->m_dABq_st, p->dABq, qb(2 * c.F), R, qbox) &&
-         (!nv || map_store16(&p->m_Ys_st16, p->Ys, c.d, R));
+         (!nv || map_store16(&p->m_Ys_st16, p->Ys, c.d, R)) &&
+         map_fp8_kmajor(&p->m_dYTq, p->dYTq, qb(R), c.d) && map_fp8_kmajor(&p->m_XTq, p->XTq, qb(R), c.d, BN) &&
+         map_fp8_kmajor(&p->m_dABTq, p->dABTq, qb(R), 2 * c.F) &&
+         map_fp8_kmajor(&p->m_wHTq, p->wHTq, qb(R), c.F, BN);
     if (ok && !nv)
       ok = map_fp8_kmajor(&p->m_ring_xq, p->ring_xq, c.d, ring_rows) &&
            map_fp8_kmajor(&p->m_ring_hq, p->ring_hq, c.F, ring_rows) &&
@@ -1026,6 +1047,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(saved) + L.ab);
 
   const bool ep = c.ep_ranks >= 2;
+  err = cudaSuccess;  // block-scaled plans gather no bf16 rows here (their dgrad and wgrad operands are quantised)
   if (ep) {  // pull reverse-combine: each expert rank pulls the dY and X rows of its pairs
     EpArgs ea = ep_args(p, rp, T);
     ea.X = reinterpret_cast<const uint4*>(X);
@@ -1033,7 +1055,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     ea.Xg = static_cast<uint4*>(p->Xg);
     ea.dYg = static_cast<uint4*>(p->dYg);
     err = timed_launch(p, "ep_pull_reverse_combine", st, [&] { return launch_ep_pull(ea, st); });
-  } else {
+  } else if (c.prec == MOE_BF16) {
     // X's sorted rows are still in Xg when this is the backward of the plan's
     // last forward, which ran the separate schedule: gather dY alone then
     const bool xg_current = p->xg_X == X && p->xg_saved == saved && p->xg_T == T;
@@ -1149,6 +1171,59 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
                                 rgrid, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: router gradient launch");
+  }
+  if (mx) {
+    // block-scaled weight gradients: dY, X, dA|dB and w h transposed and
+    // quantised along the tokens (tensor scale 1 for NVFP4), rows past the
+    // ones in use skipped; then dWd = dY^T (w h) and [dWg; dWu] = [dA|dB]^T X
+    // with K = each expert's tokens
+    const int qgrid = p->num_sms * 8;
+    const int Rq = (int)p->Rpm;
+    auto transpose = [&](const void* src, int cols, uint8_t* q, uint8_t* sf) {
+      return nv ? launch_nv_quant_transpose(src, 1, Rq, cols, nullptr, q, sf, qgrid, st, rp.totals)
+                : launch_quant_transpose(src, 1, Rq, cols, q, sf, qgrid, st, rp.totals);
+    };
+    err = timed_launch(p, "quant_wgrad_tokens", st, [&] {
+      // dY and X straight from the token tensors: gathered, transposed, quantised
+      return launch_gather_transpose_q(nv, dY, X, rp.perm_src, rp.totals, c.k, Rq, c.d, p->dYTq, p->dYTs, p->XTq,
+                                       p->XTs, qgrid, st);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient token quantisation launch");
+    err = timed_launch(p, "quant_wgrad_operands", st, [&] {
+      cudaError_t e = transpose(p->dAB, 2 * c.F, p->dABTq, p->dABTs);
+      if (e == cudaSuccess) e = transpose(p->wH, c.F, p->wHTq, p->wHTs);
+      return e;
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient operand quantisation launch");
+    MxArgs w;
+    memset(&w, 0, sizeof(w));
+    w.poff = rp.poff;
+    w.mtile_off = rp.mtile_off;
+    w.status = p->status;
+    w.timeout_ns = (uint64_t)c.wait_timeout_ns;
+    w.E = c.E;
+    w.d = c.d;
+    w.F = c.F;
+    w.Kcap = Rq;
+    MxArgs v = w;
+    w.mapA = p->m_dYTq;
+    w.mapB0 = p->m_wHTq;
+    w.sfA = p->dYTs;
+    w.sfB0 = p->wHTs;
+    w.mapO0 = p->m_dWd_st;
+    err = timed_launch(p, nv ? "gemm_nv_wgrad_down" : "gemm_mx_wgrad_down", st,
+                       [&] { return launch_gemm_mx(kWgradD, w, p->num_sms, st, nv); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled dWd GEMM launch");
+    v.mapA = p->m_dABTq;
+    v.mapB0 = p->m_XTq;
+    v.sfA = p->dABTs;
+    v.sfB0 = p->XTs;
+    v.mapO0 = p->m_dWg_st;
+    v.mapO1 = p->m_dWu_st;
+    err = timed_launch(p, nv ? "gemm_nv_wgrad_gate_up" : "gemm_mx_wgrad_gate_up", st,
+                       [&] { return launch_gemm_mx(kWgradGU, v, p->num_sms, st, nv); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled dWg/dWu GEMM launch");
+    return MOE_OK;
   }
   {
     GemmArgs a = base_args(p, rp);

@@ -1,5 +1,6 @@
 // gemm_mx.cu -- launchers of the block-scaled expert GEMMs (gemm_mx.cuh):
-// MXFP8 and NVFP4 variants of the up, down, bwd-u and bwd-x kinds.
+// MXFP8 and NVFP4 variants of the up, down, bwd-u, bwd-x and weight-gradient
+// kinds.
 #include "gemm_mx.cuh"
 #include "kernels.h"
 
@@ -22,6 +23,8 @@ static cudaError_t launch_kind(int kind, const MxArgs& a, int grid, cudaStream_t
     case kUp: return launch_mx_one<kUp, NV>(a, grid, st);
     case kDown: return launch_mx_one<kDown, NV>(a, grid, st);
     case kBwdU: return launch_mx_one<kBwdU, NV>(a, grid, st);
+    case kWgradD: return launch_mx_one<kWgradD, NV>(a, grid, st);
+    case kWgradGU: return launch_mx_one<kWgradGU, NV>(a, grid, st);
     default: return launch_mx_one<kBwdX, NV>(a, grid, st);
   }
 }
@@ -31,6 +34,8 @@ static cudaError_t prepare_kind(int kind) {
     case kUp: return prepare_mx_one<kUp, NV>();
     case kDown: return prepare_mx_one<kDown, NV>();
     case kBwdU: return prepare_mx_one<kBwdU, NV>();
+    case kWgradD: return prepare_mx_one<kWgradD, NV>();
+    case kWgradGU: return prepare_mx_one<kWgradGU, NV>();
     default: return prepare_mx_one<kBwdX, NV>();
   }
 }

@@ -47,9 +47,10 @@ struct MxTraits {
   // bf16 outputs go out 16 columns at a time through one 1 KB buffer per
   // warp (half16); its bwd-u kind releases TMEM only after its stores, so it
   // keeps three stages and the roomier staging.
+  static constexpr bool wgrad = (KIND == kWgradD || KIND == kWgradGU);
   static constexpr bool seq = !NV;
-  static constexpr bool half16 = NV && KIND != kBwdU;
-  static constexpr int stages = (NV && KIND == kBwdU) ? 3 : 4;
+  static constexpr bool half16 = NV && (KIND == kUp || KIND == kDown || KIND == kBwdX);
+  static constexpr int stages = (NV && (KIND == kBwdU || wgrad)) ? 3 : 4;
   static constexpr int epi_warps = 8;
   static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int kelems = NV ? 256 : 128;         // K values per stage
@@ -91,6 +92,7 @@ struct MxArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int E, d, F;
+  int Kcap;                  // weight-gradient kinds: token capacity of the transposed operands
 };
 
 // One stage: the A and B tiles (TMA; x coordinates in bytes) and their scale
@@ -103,7 +105,21 @@ __device__ __forceinline__ void mx_load_stage(const MxArgs& g, const Tile& t, in
   constexpr uint32_t SFB = TR::sf_rows;
   const int x0 = kb * kMxBK;          // byte coordinate along K
   const int ke = kb * TR::kelems;     // value coordinate along K
-  if (KIND == kUp) {
+  if (KIND == kWgradD || KIND == kWgradGU) {
+    // K = the expert's tokens from its segment start, in the transposed
+    // operands [rows, Kcap]: A = dY^T (kWgradD) or [dA|dB]^T rows, B = (w h)^T
+    // or X^T rows nt*256 ..; everything is an activation (pol_a)
+    const int kt = t.kbase + ke;                  // first token of the stage
+    const int xk = NV ? kt / 2 : kt;              // its byte coordinate
+    const int kg = g.Kcap / TR::atom_k;
+    const int ka = kt / TR::atom_k;
+    const int brow = t.nt * BN;
+    tma_load_2d(sa, &g.mapA, xk, t.row0, bar, pol_a);
+    tma_load_2d(sb, &g.mapB0, xk, brow, bar, pol_a);
+    bulk_load_1d(ssf, g.sfA + ((size_t)(t.row0 >> 7) * kg + ka) * 512, SFB, bar);
+    bulk_load_1d(ssf + SFB, g.sfB0 + ((size_t)(brow >> 7) * kg + ka) * 512, SFB, bar);
+    bulk_load_1d(ssf + 2 * SFB, g.sfB0 + ((size_t)((brow >> 7) + 1) * kg + ka) * 512, SFB, bar);
+  } else if (KIND == kUp) {
     const int kg = g.d / TR::atom_k;  // scale atoms per 128-row block
     tma_load_2d(sa, &g.mapA, x0, t.row0, bar, pol_a);
     const int brow = t.e * g.F + t.nt * 128;
@@ -136,6 +152,23 @@ __device__ __forceinline__ void mx_load_stage(const MxArgs& g, const Tile& t, in
     bulk_load_1d(ssf + SFB, sfb + ((size_t)(brow >> 7) * kgb + kw / TR::atom_k) * 512, SFB, bar);
     bulk_load_1d(ssf + 2 * SFB, sfb + ((size_t)((brow >> 7) + 1) * kgb + kw / TR::atom_k) * 512, SFB, bar);
   }
+}
+
+// K stages of a tile, and how many of the last stage's four MMAs carry K.
+// Weight-gradient kinds take the expert's (128-row aligned) token segment: a
+// stage holds 128 E4M3 or 256 E2M1 tokens, so an NVFP4 segment whose length
+// is an odd multiple of 128 ends on a half stage (two of the four K=64 MMAs);
+// an expert without rows has no stage.
+template <int KIND, bool NV>
+__device__ __forceinline__ int mx_tile_nkb(const MxArgs& g, const Tile& t, int& last_mmas) {
+  using TR = MxTraits<KIND, NV>;
+  last_mmas = 4;
+  if (KIND == kWgradD || KIND == kWgradGU) {
+    const int rows = __ldg(g.poff + t.e + 1) - t.kbase;
+    if (NV && (rows % 256)) last_mmas = 2;
+    return (rows + TR::kelems - 1) / TR::kelems;
+  }
+  return (KIND == kUp || KIND == kBwdU ? g.d : KIND == kDown ? g.F : 2 * g.F) / TR::kelems;
 }
 
 // 32 fp32 -> 32 E4M3 bytes of one row into an unswizzled 32x32-byte staging tile.
@@ -204,7 +237,6 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
   const uint32_t tmem_base = *tmem_slot;
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
   const int ntiles = total_tiles<KIND>(g);
-  const int nkb = (KIND == kUp || KIND == kBwdU ? g.d : KIND == kDown ? g.F : 2 * g.F) / TR::kelems;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -216,6 +248,8 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const Tile t = decode_tile<KIND>(g, tile);
+        int last_mmas;
+        const int nkb = mx_tile_nkb<KIND, NV>(g, t, last_mmas);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kStageBytes + TR::sf_stage);
@@ -240,9 +274,14 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
       uint32_t s = 0, ph = 0, aph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const Tile t = decode_tile<KIND>(g, tile);
+        int last_mmas;
+        const int nkb = mx_tile_nkb<KIND, NV>(g, t, last_mmas);
+        if (nkb == 0) continue;  // an expert without rows: the epilogue writes zeros
         if (!mbar_wait(tempty, aph ^ 1, wc)) break;
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb) {
+          const int nmma = kb == nkb - 1 ? last_mmas : 4;  // MMAs of this stage that carry K
           if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + s * kStageBytes);
@@ -261,6 +300,7 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
+              if (kk >= nmma) break;
               const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
               umma_nvf4(tmem_base, ad, bd, idesc_nvf4(BM, BN), sfa_t + 4 * kk, sfb_t + 8 * kk,
@@ -291,13 +331,17 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
     const int q = warp & 3;            // TMEM lane quadrant
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
     uint8_t* stg = staging_base + (warp - 2) * TR::staging_per_warp;
-    const float gs = NV ? __ldg(g.tsB) : 1.0f;   // weights' tensor scale (NVFP4)
+    const float gs = (NV && g.tsB) ? __ldg(g.tsB) : 1.0f;   // weights' tensor scale (NVFP4)
     const float rc1 = nv_rc(1.0f);               // activations: tensor scale 1
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const Tile t = decode_tile<KIND>(g, tile);
-      if (!mbar_wait(tfull, aph, wc)) break;
-      tc_fence_after();
+      int last_mmas;
+      const bool has_acc = mx_tile_nkb<KIND, NV>(g, t, last_mmas) > 0;
+      if (has_acc) {
+        if (!mbar_wait(tfull, aph, wc)) break;
+        tc_fence_after();
+      }
       const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16);
       const int rowq = t.row0 + 32 * q;
       if (KIND == kBwdU) {
@@ -448,15 +492,22 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
         tmem_ld32(tb + half * 64 + 32, acc[1]);
         tmem_ld32(tb + 128 + half * 64, acc[2]);
         tmem_ld32(tb + 128 + half * 64 + 32, acc[3]);
-      } else {
+      } else if (has_acc) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tb + half * 128 + c * 32, acc[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c][i] = 0u;   // dW of an expert without rows
       }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-      aph ^= 1;
+      if (has_acc) {
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);
+        aph ^= 1;
+      }
       if (KIND == kUp) {
         uint32_t sfw = 0;
 #pragma unroll
@@ -561,6 +612,17 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
           *reinterpret_cast<uint16_t*>(g.sfO + sf_atom_offset(r, kb, g.F / 32)) = (uint16_t)sfw;
         }
       } else {
+        // output rows: kDown / kBwdX the sorted rows; weight gradients the
+        // expert's dW rows (kWgradGU: rows below F are dWg, the rest dWu)
+        const CUtensorMap* om = &g.mapO0;
+        int orow = rowq;
+        if (KIND == kWgradD) {
+          orow = t.e * g.d + t.row0 + 32 * q;
+        } else if (KIND == kWgradGU) {
+          const bool up = t.row0 >= g.F;
+          om = up ? &g.mapO1 : &g.mapO0;
+          orow = t.e * g.F + (up ? t.row0 - g.F : t.row0) + 32 * q;
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float v[32];
@@ -587,7 +649,7 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&g.mapO0, stg, t.nt * BN + half * 128 + c * 32, rowq);
+            tma_store_2d(om, stg, t.nt * BN + half * 128 + c * 32, orow);
             bulk_commit();
           }
         }

@@ -88,14 +88,23 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, int grid, cud
 
 // MXFP8 (mx_quant.cu, gemm_mx.cu)
 cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st);
+// a_used (device, may be null): tiles whose first A row is at or past *a_used are skipped
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
-                                   cudaStream_t st);
+                                   cudaStream_t st, const int32_t* a_used = nullptr);
+// Block-scaled weight gradients (wgrad_quant.cu): the sorted rows of two
+// token tensors, transposed and quantised along the sorted rows (A = row
+// capacity, B = columns): out[c, r] = Q(src[perm_src[r] / k, c]).
+cudaError_t launch_gather_transpose_q(bool nv, const void* X0, const void* X1, const int32_t* perm_src,
+                                      const int32_t* totals, int k, int A, int B, void* q0, void* sf0, void* q1,
+                                      void* sf1, int grid, cudaStream_t st);
 // Sorted rows <- token-quantised rows (E4M3 or packed E2M1 bytes, row_bytes
 // per row, and nblk scale bytes per row in the atom layout).
 cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* totals,
                                  int k, int row_bytes, int nblk, void* q, void* sf, int grid, cudaStream_t st);
 struct MxArgs;
-// kind 0 up, 1 down, 2 bwd-u, 3 bwd-x; nv: the NVFP4 variant (E2M1 operands,
+// kind 0 up, 1 down, 2 bwd-u, 3 bwd-x, 4 wgrad down, 5 wgrad gate/up (K = each
+// expert's tokens, transposed operands quantised along the tokens); nv: the
+// NVFP4 variant (E2M1 operands,
 // E4M3 scales per 16, tensor scales in MxArgs::tsB)
 cudaError_t launch_gemm_mx(int kind, const MxArgs& a, int grid, cudaStream_t st, bool nv = false);
 cudaError_t prepare_gemm_mx(int kind, bool nv = false);
@@ -106,7 +115,7 @@ cudaError_t launch_nv_tensor_scale(const void* a, int64_t na, const void* b, int
 cudaError_t launch_nv_quant_rows(const void* src, int64_t rows, int K, const float* g, void* q, void* sf, int grid,
                                  cudaStream_t st);
 cudaError_t launch_nv_quant_transpose(const void* src, int E, int A, int B, const float* g, void* q, void* sf,
-                                      int grid, cudaStream_t st);
+                                      int grid, cudaStream_t st, const int32_t* a_used = nullptr);
 
 // Ring-buffer forward megakernel (megakernel.cu)
 struct MegaArgs;

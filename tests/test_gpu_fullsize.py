@@ -104,7 +104,7 @@ def test_full_size_sampled_parity(layer, case):
         experts.append(int(np.argmax(counts)))
     for e in experts:
         dwg, dwu, dwd = moe_ref.expert_weight_grads(host["X"], host["logits"], Wg, Wu, Wd, host["dY"], K, e,
-                                                    mx=fmt, wscales=ws)
+                                                    mx=fmt, wscales=ws, stored=fmt is not False)
         for name, ref in (("dWg", dwg), ("dWu", dwu), ("dWd", dwd)):
             err = rel_err(out[name][e], ref)
             assert err <= tol, (e, int(counts[e]), name, err)
