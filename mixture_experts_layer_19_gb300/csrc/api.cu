@@ -498,6 +498,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   for (int kind = 0; kind < 6; ++kind) {
     err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
     if (err == cudaSuccess && c.prec != MOE_BF16) err = prepare_gemm_mx(kind, c.prec == MOE_NVFP4);
+    if (err == cudaSuccess && kind == 0 && c.prec != MOE_BF16) err = prepare_gather_transpose_q(c.prec == MOE_NVFP4);
     if (err == cudaSuccess) p->pair_grid[kind] = kind < 2 ? gemm_pair_grid_fwd(kind) : gemm_pair_grid_bwd(kind);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -1185,8 +1186,9 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     };
     err = timed_launch(p, "quant_wgrad_tokens", st, [&] {
       // dY and X straight from the token tensors: gathered, transposed, quantised
+      // one wave: four CTAs (32 KB of staged tiles each) per SM
       return launch_gather_transpose_q(nv, dY, X, rp.perm_src, rp.totals, c.k, Rq, c.d, p->dYTq, p->dYTs, p->XTq,
-                                       p->XTs, qgrid, st);
+                                       p->XTs, p->num_sms * 4, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient token quantisation launch");
     err = timed_launch(p, "quant_wgrad_operands", st, [&] {
