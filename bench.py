@@ -176,12 +176,12 @@ NCU_TRAFFIC = {
     "workload": WORKLOAD,
     "csrc_sha256": "c598148442bfe6df2b403cf83efa3cce4e286297a77ae318aca90ef713f1aec2",
     "bytes": {
-        "gemm_up_swiglu": 11898674944,
-        "gemm_down": 5725603123,
-        "gemm_bwd_u_swiglu": 6932607437,
-        "gemm_bwd_dx": 11177339136,
-        "gemm_wgrad_down": 8550838579,
-        "gemm_wgrad_gate_up": 16573376614,
+        "gemm_up_swiglu": 11887769753,
+        "gemm_down": 5723498035,
+        "gemm_bwd_u_swiglu": 6945335347,
+        "gemm_bwd_dx": 11188713830,
+        "gemm_wgrad_down": 8508461619,
+        "gemm_wgrad_gate_up": 16134242099,
     },
 }
 
