@@ -226,18 +226,27 @@ moe_status_t moe_nv_quantize(const void* src, int64_t rows, int64_t K, const flo
 moe_status_t moe_nv_quantize_transposed(const void* src, int64_t E, int64_t A, int64_t B, const float* g,
                                         void* q, void* sf, moe_stream_t stream);
 
-/* Block-scaled plans created with MOE_DEBUG_DUMP_QUANT: copy, from the last
- * forward (which = 0: h) or backward (which = 1: dA|dB), the fp32 values the
- * fused epilogue quantised and the bytes it wrote, over the plan's full
- * padded row capacity P (the sorted rows of the routing, each expert's
- * segment padded to 128 rows; rows past the last segment are not written):
- *   vals [P, C] fp32 with C = F (h) or 2F (dA|dB);
+/* Block-scaled plans created with MOE_DEBUG_DUMP_QUANT: copy a quantised
+ * operand of the last forward / backward and the values it was quantised
+ * from, over the plan's full padded row capacity P (the sorted rows of the
+ * routing, each expert's segment padded to 128 rows; rows past the last
+ * segment are not written).
+ * which = 0 (h, forward) or 1 (dA|dB, backward): the fused epilogues'
+ * quantisation along C = F (h) or 2F (dA|dB):
+ *   vals [P, C] fp32 (the values the epilogue quantised);
  *   q    [P, C] E4M3 bytes (MXFP8) or [P, C / 2] packed E2M1 (NVFP4);
  *   sf   scale atoms of the P rows with K = C (moe_mx_quantize /
  *        moe_nv_quantize layout).
+ * which = 2..5: the block-scaled weight gradients' operands, transposed and
+ * quantised along the sorted rows (NVFP4 tensor scale 1): 2 dY^T and 3 X^T
+ * (C = d), 4 [dA|dB]^T (C = 2F), 5 (w h)^T (C = F):
+ *   vals [P, C] fp32: for 4 and 5 the bf16 rows the transposer read, widened
+ *        (must be NULL for 2 and 3, whose rows are the gathered inputs);
+ *   q    [C, P] E4M3 bytes or [C, P / 2] packed E2M1;
+ *   sf   scale atoms of the C rows with K = P.
  * P = moe_plan_padded_rows.  Any pointer may be NULL to skip it.  Synchronous
  * argument errors (MOE_ERR_INVALID_ARG) for a plan without the flag, a BF16
- * plan or another `which`.  Enqueued on `stream`. */
+ * plan, another `which`, or vals with which 2 or 3.  Enqueued on `stream`. */
 moe_status_t moe_debug_quant_dump(moe_plan_t plan, int32_t which, float* vals, void* q, void* sf,
                                   moe_stream_t stream);
 

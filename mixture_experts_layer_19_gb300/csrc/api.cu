@@ -1485,18 +1485,30 @@ moe_status_t moe_debug_quant_dump(moe_plan_t p, int32_t which, float* vals, void
   const moe_config_t& c = p->cfg;
   if (c.prec == MOE_BF16 || !(c.debug_flags & MOE_DEBUG_DUMP_QUANT) || !p->dbg_h)
     return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: needs a block-scaled plan made with MOE_DEBUG_DUMP_QUANT");
-  if (which != 0 && which != 1) return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: which must be 0 (h) or 1 (dA|dB)");
+  if (which < 0 || which > 5)
+    return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: which must be 0 (h), 1 (dA|dB), 2 (dY^T), 3 (X^T), "
+                                     "4 ([dA|dB]^T) or 5 ((w h)^T)");
+  if (vals && (which == 2 || which == 3))
+    return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: dY^T and X^T keep no source values (vals must be NULL)");
   DeviceGuard guard(c.device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool nv = c.prec == MOE_NVFP4;
-  const size_t cols = (size_t)(which == 0 ? c.F : 2 * c.F);
-  const size_t n = (size_t)p->Rpm * cols;
+  const size_t P = (size_t)p->Rpm;
+  // which 0, 1: [P, C] quantised along C; 2..5: [C, P] quantised along the P sorted rows
+  const size_t C = (size_t)(which == 0 || which == 5 ? c.F : which == 1 || which == 4 ? 2 * c.F : c.d);
+  const size_t n = P * C;
+  const void* qsrc[6] = {p->Hq, p->dABq, p->dYTq, p->XTq, p->dABTq, p->wHTq};
+  const void* ssrc[6] = {p->Hs, p->dABs, p->dYTs, p->XTs, p->dABTs, p->wHTs};
   cudaError_t err = cudaSuccess;
-  if (vals) err = cudaMemcpyAsync(vals, which == 0 ? p->dbg_h : p->dbg_dab, n * 4, cudaMemcpyDeviceToDevice, st);
-  if (q && err == cudaSuccess)
-    err = cudaMemcpyAsync(q, which == 0 ? p->Hq : p->dABq, nv ? n / 2 : n, cudaMemcpyDeviceToDevice, st);
+  if (vals) {
+    if (which <= 1)
+      err = cudaMemcpyAsync(vals, which == 0 ? p->dbg_h : p->dbg_dab, n * 4, cudaMemcpyDeviceToDevice, st);
+    else   // the bf16 rows the transposer read, widened
+      err = launch_widen_bf16(which == 4 ? p->dAB : p->wH, vals, (int64_t)n, p->num_sms * 4, st);
+  }
+  if (q && err == cudaSuccess) err = cudaMemcpyAsync(q, qsrc[which], nv ? n / 2 : n, cudaMemcpyDeviceToDevice, st);
   if (sf && err == cudaSuccess)
-    err = cudaMemcpyAsync(sf, which == 0 ? p->Hs : p->dABs, nv ? n / 16 : n / 32, cudaMemcpyDeviceToDevice, st);
+    err = cudaMemcpyAsync(sf, ssrc[which], nv ? n / 16 : n / 32, cudaMemcpyDeviceToDevice, st);
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_debug_quant_dump: copy");
 }
 

@@ -98,6 +98,8 @@ cudaError_t launch_gather_transpose_q(bool nv, const void* X0, const void* X1, c
                                       const int32_t* totals, int k, int A, int B, void* q0, void* sf0, void* q1,
                                       void* sf1, int grid, cudaStream_t st);
 cudaError_t prepare_gather_transpose_q(bool nv);   // its dynamic shared memory size, once
+// dst[i] = src[i] widened from bf16, i < n (debug dumps).
+cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, int grid, cudaStream_t st);
 // Sorted rows <- token-quantised rows (E4M3 or packed E2M1 bytes, row_bytes
 // per row, and nblk scale bytes per row in the atom layout).
 cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* totals,

@@ -136,6 +136,17 @@ cudaError_t launch_gather_transpose_q(bool nv, const void* X0, const void* X1, c
   return cudaGetLastError();
 }
 
+__global__ void __launch_bounds__(256) widen_bf16_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst,
+                                                         int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = __bfloat162float(src[i]);
+}
+
+cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, int grid, cudaStream_t st) {
+  widen_bf16_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), dst, n);
+  return cudaGetLastError();
+}
+
 cudaError_t prepare_gather_transpose_q(bool nv) {
   return cudaFuncSetAttribute(nv ? gather_transpose_q_kernel<true> : gather_transpose_q_kernel<false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);

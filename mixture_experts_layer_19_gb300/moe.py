@@ -28,6 +28,7 @@ MOE_DEBUG_SINGLE_CTA = 0x10
 MOE_DEBUG_MULTI_LAUNCH = 0x20
 MOE_DEBUG_DUMP_QUANT = 0x40
 MOE_DEBUG_STALL_TEST = 0x80
+MOE_ERR_INVALID_ARG = 1
 MOE_ERR_TIMEOUT = 5
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
@@ -301,16 +302,20 @@ class Plan:
         return n.value
 
     def debug_quant_dump(self, which: int, stream=None):
-        """MOE_DEBUG_DUMP_QUANT plans: (fp32 values, quantised bytes, scale atoms)
-        of the fused epilogue quantisation -- which 0: h of the last forward,
-        1: dA|dB of the last backward -- over the padded row capacity."""
+        """MOE_DEBUG_DUMP_QUANT plans: (fp32 values or None, quantised bytes,
+        scale atoms) of one quantised operand over the padded row capacity P.
+        which 0: h of the last forward, 1: dA|dB of the last backward (both
+        [P, C] quantised along C); 2: dY^T, 3: X^T, 4: [dA|dB]^T, 5: (w h)^T of
+        the last backward ([C, P] quantised along P; values [P, C] for 4 and 5,
+        None for 2 and 3)."""
         c = self.cfg
         P = self.padded_rows()
-        cols = c.F if which == 0 else 2 * c.F
+        C = {0: c.F, 1: 2 * c.F, 2: c.d, 3: c.d, 4: 2 * c.F, 5: c.F}.get(which, c.F)
         nv = c.prec == MOE_NVFP4
-        vals = torch.empty((P, cols), dtype=torch.float32, device=self.device)
-        q = torch.empty((P, cols // 2 if nv else cols), dtype=torch.uint8, device=self.device)
-        sf = torch.empty((P * cols // (16 if nv else 32),), dtype=torch.uint8, device=self.device)
+        vals = None if which in (2, 3) else torch.empty((P, C), dtype=torch.float32, device=self.device)
+        shape = (P, C) if which in (0, 1) else (C, P)
+        q = torch.empty((shape[0], shape[1] // 2 if nv else shape[1]), dtype=torch.uint8, device=self.device)
+        sf = torch.empty((P * C // (16 if nv else 32),), dtype=torch.uint8, device=self.device)
         _check(lib().moe_debug_quant_dump(self.handle, which, _ptr(vals), _ptr(q), _ptr(sf), _stream(stream)),
                "moe_debug_quant_dump")
         return vals, q, sf

@@ -59,8 +59,82 @@ def test_fused_epilogue_quantisation_bit_exact(prec, case):
         assert np.array_equal(sf.cpu().numpy()[_atom_offsets(rows, C, blk)], scales), which
 
 
+def _sorted_rows(src, perm, counts, k):
+    """The padded sorted rows of a token tensor: expert segments padded to 128
+    rows, row j of expert e's segment = token perm[offsets[e] + j] // k, the
+    padding rows zero."""
+    rows = int(sum((c + 127) // 128 * 128 for c in counts))
+    out = np.zeros((rows, src.shape[1]))
+    r0 = o = 0
+    for c in counts:
+        out[r0:r0 + c] = src[perm[o:o + c] // k]
+        r0 += (c + 127) // 128 * 128
+        o += c
+    return out
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("case", [(300, 512, 768, 16, 3, 1.5), (200, 256, 512, 8, 2, 0.0)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_weight_gradient_operands_bit_exact(prec, case):
+    """The block-scaled weight gradients' operands, transposed and quantised
+    along the sorted rows: dY^T and X^T (gathered from the token tensors in
+    one pass) against the oracle's quantisation of the sorted rows built here
+    from the inputs and the routing; [dA|dB]^T and (w h)^T against the
+    oracle's quantisation of the bf16 rows they were made from.  Every element
+    byte and scale byte of the rows in use, padding rows included."""
+    T, d, F, E, k, alpha = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=29, alpha=alpha)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, debug_flags=moe.MOE_DEBUG_DUMP_QUANT))
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    r = plan.routing(saved, T)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    counts = r["counts"].cpu().numpy()
+    perm = r["perm_src"].cpu().numpy().astype(np.int64)
+    rows = int(sum((c + 127) // 128 * 128 for c in counts))
+    P = plan.padded_rows()
+    nv = prec == moe.MOE_NVFP4
+    blk = 16 if nv else 32
+    for which, name in ((2, "dY"), (3, "X"), (4, "dAB"), (5, "wH")):
+        vals, q, sf = plan.debug_quant_dump(which)
+        torch.cuda.synchronize()
+        if which in (2, 3):
+            assert vals is None
+            src = _sorted_rows(h[name], perm, counts, k)
+        else:
+            src = vals[:rows].cpu().double().numpy()
+            assert np.abs(src).max() > 0
+        op = src.T                                   # [C, rows]: quantised along the sorted rows
+        C = op.shape[0]
+        if nv:
+            codes, scales = nvfp4.nv_quantize(op, axis=1, g=1.0)
+            got = nvfp4.nv_unpack(q.cpu().numpy()[:, :rows // 2])
+        else:
+            codes, scales = mxfp8.mx_quantize(op, axis=1)
+            got = q.cpu().numpy()[:, :rows]
+        bad = np.argwhere(got != codes)
+        assert bad.size == 0, (name, bad[:5].tolist())
+        atoms = _atom_offsets(C, P, blk)[:, :rows // blk]
+        assert np.array_equal(sf.cpu().numpy()[atoms], scales), name
+
+
 def test_dump_needs_the_flag():
     plan = moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, prec=moe.MOE_NVFP4))
     with pytest.raises(moe.MoEError) as ei:
         plan.debug_quant_dump(0)
     assert ei.value.status == 1
+
+
+def test_dump_rejects_bad_operand_arguments():
+    """which outside 0..5, and source values asked of dY^T or X^T (which keep
+    none), are argument errors that copy nothing."""
+    plan = moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, prec=moe.MOE_MXFP8,
+                               debug_flags=moe.MOE_DEBUG_DUMP_QUANT))
+    buf = torch.zeros(plan.padded_rows() * 256, dtype=torch.float32, device="cuda")
+    for which, vals in ((6, None), (-1, None), (2, buf), (3, buf)):
+        st = moe.lib().moe_debug_quant_dump(plan.handle, which, moe._ptr(vals), None, None, None)
+        assert st == moe.MOE_ERR_INVALID_ARG, which
+    assert torch.count_nonzero(buf).item() == 0
