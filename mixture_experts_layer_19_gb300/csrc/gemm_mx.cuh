@@ -16,6 +16,8 @@
 // 256-column fp32 accumulator plus a 16-column scale slot per stage, so the
 // eight epilogue warps first drain the whole accumulator into registers
 // (128 columns each), release it, and only then do the math and the stores.
+// The u kind, which also reads a|b, parks three of its four 32-column chunks
+// in the 192 TMEM columns left past the scale slots instead.
 // NVFP4 variant (NV = true): the same pipeline over packed E2M1 operands
 // (128 bytes = 256 values of K per stage) with one E4M3 scale per 16 values:
 // a 512-byte scale atom then covers one MMA's K = 64, so a stage brings four
@@ -345,26 +347,26 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
       const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16);
       const int rowq = t.row0 + 32 * q;
       if (KIND == kBwdU) {
-        // u chunk by chunk (the accumulator is released after the last one):
-        // dh = w u, da = dh b s(a)(1 + a(1 - s(a))), db = dh silu(a); outputs
-        // dA|dB and w h in bf16 (weight gradients), dA|dB quantised along F
-        // for the dx GEMM, and the row's <u, h> over this warp's 128 columns.
+        // u in 32-column chunks: dh = w u, da = dh b s(a)(1 + a(1 - s(a))),
+        // db = dh silu(a); outputs dA|dB and w h in bf16 (weight gradients),
+        // dA|dB quantised along F for the dx GEMM, and the row's <u, h> over
+        // this warp's 128 columns.
         const int r = rowq + lane;
         const int src = __ldg(g.perm_src + r);
         const float wr = src >= 0 ? __ldg(g.wts + src) : 0.0f;
         const __nv_bfloat16* abrow = g.ab + (size_t)r * (2 * g.F);
         float dgacc = 0.0f;
         uint32_t sfa[2] = {0u, 0u}, sfb[2] = {0u, 0u};
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ru[32];
-          tmem_ld32(tb + half * 128 + c * 32, ru);
+        // one 32-column chunk c of u, its TMEM load issued into ru: the SwiGLU
+        // backward and the stores; `release` frees the accumulator as soon as
+        // that load has landed
+        auto chunk = [&](int c, uint32_t (&ru)[32], bool release) {
           const int col = t.nt * BN + half * 128 + c * 32;
           float a[32], b[32];
           load_bf16x32(abrow + col, a);
           load_bf16x32(abrow + g.F + col, b);
           tmem_ld_wait();
-          if (c == 3) {
+          if (release) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
               tma_store_2d(&g.mapO2, stg, col, rowq);
               bulk_commit();
             }
-            continue;
+            return;
           }
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
@@ -466,6 +468,42 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             tma_store_2d(&g.mapO1, stg + 3 * kStageChunk, col / qd, rowq);
             tma_store_2d(&g.mapO1, stg + 3 * kStageChunk + TR::qout, (g.F + col) / qd, rowq);
             bulk_commit();
+          }
+        };
+        if constexpr (!NV) {
+          // MXFP8: all four chunks leave the accumulator before any math --
+          // chunks 1-3 into the TMEM columns past the stages' scale slots (96
+          // per column half), chunk 0 into registers -- so the next tile's
+          // MMAs run while this tile's SwiGLU backward and stores do
+          static_assert(NV || BN + TR::stages * TR::sf_cols + 2 * 96 <= 512, "TMEM columns for the u stash");
+          const uint32_t stash = tb + BN + TR::stages * TR::sf_cols + half * 96;
+          uint32_t ru[32];
+#pragma unroll 1
+          for (int c = 1; c < 4; ++c) {
+            tmem_ld32(tb + half * 128 + c * 32, ru);
+            tmem_ld_wait();
+            tmem_st32(stash + (c - 1) * 32, ru);
+            tmem_st_wait();   // ru is reloaded next
+          }
+          tmem_ld32(tb + half * 128, ru);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty);
+          chunk(0, ru, false);
+#pragma unroll 1
+          for (int c = 1; c < 4; ++c) {
+            tmem_ld32(stash + (c - 1) * 32, ru);
+            chunk(c, ru, false);
+          }
+        } else {
+          // NVFP4: its scale slots leave no room to stash, so chunk by chunk,
+          // the accumulator released after the last load
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ru[32];
+            tmem_ld32(tb + half * 128 + c * 32, ru);
+            chunk(c, ru, c == 3);
           }
         }
         aph ^= 1;
