@@ -16,8 +16,9 @@
 // 256-column fp32 accumulator plus a 16-column scale slot per stage, so the
 // eight epilogue warps first drain the whole accumulator into registers
 // (128 columns each), release it, and only then do the math and the stores.
-// The u kind, which also reads a|b, parks three of its four 32-column chunks
-// in the 192 TMEM columns left past the scale slots instead.
+// The u kind, which also reads a|b, parks the last of its four 32-column
+// chunks in the TMEM columns left past the scale slots instead (three for
+// MXFP8; two for NVFP4, whose u kind keeps two stages to make room).
 // NVFP4 variant (NV = true): the same pipeline over packed E2M1 operands
 // (128 bytes = 256 values of K per stage) with one E4M3 scale per 16 values:
 // a 512-byte scale atom then covers one MMA's K = 64, so a stage brings four
@@ -44,15 +45,15 @@ struct MxTraits {
   // MXFP8 keeps four stages in every kind: its multi-output epilogues (up:
   // a, b, h; bwd-u: dA, dB, w h) stage their bf16 tiles one after another
   // through a single buffer (seq), which leaves room for the fourth stage.
-  // NVFP4's 54 KB stages fit three.
-  // NVFP4's 54 KB stages fit four in the up, down and dx kinds when their
+  // NVFP4's 54 KB stages fit three in its weight-gradient kinds and four in the up, down and dx kinds when their
   // bf16 outputs go out 16 columns at a time through one 1 KB buffer per
-  // warp (half16); its bwd-u kind releases TMEM only after its stores, so it
-  // keeps three stages and the roomier staging.
+  // warp (half16).  Its bwd-u kind keeps two stages: their 96 scale columns
+  // leave TMEM room to park half of u, so the accumulator is free before the
+  // SwiGLU backward runs.
   static constexpr bool wgrad = (KIND == kWgradD || KIND == kWgradGU);
   static constexpr bool seq = !NV;
   static constexpr bool half16 = NV && (KIND == kUp || KIND == kDown || KIND == kBwdX);
-  static constexpr int stages = (NV && (KIND == kBwdU || wgrad)) ? 3 : 4;
+  static constexpr int stages = (NV && KIND == kBwdU) ? 2 : (NV && wgrad) ? 3 : 4;
   static constexpr int epi_warps = 8;
   static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int kelems = NV ? 256 : 128;         // K values per stage
@@ -470,40 +471,35 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             bulk_commit();
           }
         };
-        if constexpr (!NV) {
-          // MXFP8: all four chunks leave the accumulator before any math --
-          // chunks 1-3 into the TMEM columns past the stages' scale slots (96
-          // per column half), chunk 0 into registers -- so the next tile's
-          // MMAs run while this tile's SwiGLU backward and stores do
-          static_assert(NV || BN + TR::stages * TR::sf_cols + 2 * 96 <= 512, "TMEM columns for the u stash");
-          const uint32_t stash = tb + BN + TR::stages * TR::sf_cols + half * 96;
-          uint32_t ru[32];
+        {
+          // All four chunks leave the accumulator before any math: the last
+          // kPark of them into the TMEM columns past the stages' scale slots
+          // (kPark * 32 per column half), the others into registers.  The next
+          // tile's MMAs then run while this tile's SwiGLU backward and stores do.
+          constexpr int kPark = NV ? 2 : 3;
+          static_assert(KIND != kBwdU || BN + TR::stages * TR::sf_cols + 2 * 32 * kPark <= 512,
+                        "TMEM columns for the parked u");
+          const uint32_t park = tb + BN + TR::stages * TR::sf_cols + half * 32 * kPark;
+          uint32_t ru0[32], ru1[32];
 #pragma unroll 1
-          for (int c = 1; c < 4; ++c) {
-            tmem_ld32(tb + half * 128 + c * 32, ru);
+          for (int c = 4 - kPark; c < 4; ++c) {
+            tmem_ld32(tb + half * 128 + c * 32, ru0);
             tmem_ld_wait();
-            tmem_st32(stash + (c - 1) * 32, ru);
-            tmem_st_wait();   // ru is reloaded next
+            tmem_st32(park + (c - (4 - kPark)) * 32, ru0);
+            tmem_st_wait();   // ru0 is reloaded next
           }
-          tmem_ld32(tb + half * 128, ru);
+          tmem_ld32(tb + half * 128, ru0);
+          if (kPark == 2) tmem_ld32(tb + half * 128 + 32, ru1);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty);
-          chunk(0, ru, false);
+          chunk(0, ru0, false);
+          if (kPark == 2) chunk(1, ru1, false);
 #pragma unroll 1
-          for (int c = 1; c < 4; ++c) {
-            tmem_ld32(stash + (c - 1) * 32, ru);
-            chunk(c, ru, false);
-          }
-        } else {
-          // NVFP4: its scale slots leave no room to stash, so chunk by chunk,
-          // the accumulator released after the last load
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ru[32];
-            tmem_ld32(tb + half * 128 + c * 32, ru);
-            chunk(c, ru, c == 3);
+          for (int c = 4 - kPark; c < 4; ++c) {
+            tmem_ld32(park + (c - (4 - kPark)) * 32, ru0);
+            chunk(c, ru0, false);
           }
         }
         aph ^= 1;
