@@ -45,9 +45,10 @@ struct MxTraits {
   // MXFP8 keeps four stages in every kind: its multi-output epilogues (up:
   // a, b, h; bwd-u: dA, dB, w h) stage their bf16 tiles one after another
   // through a single buffer (seq), which leaves room for the fourth stage.
-  // NVFP4's 54 KB stages fit three in its weight-gradient kinds and four in the up, down and dx kinds when their
-  // bf16 outputs go out 16 columns at a time through one 1 KB buffer per
-  // warp (half16).  Its bwd-u kind keeps two stages: their 96 scale columns
+  // NVFP4's 54 KB stages fit three in its weight-gradient kinds, and four in
+  // the up, down and dx kinds when their bf16 outputs go out 16 columns at a
+  // time through one 1 KB buffer per warp (half16).  Its bwd-u kind keeps
+  // two stages: their 96 scale columns
   // leave TMEM room to park half of u, so the accumulator is free before the
   // SwiGLU backward runs.
   static constexpr bool wgrad = (KIND == kWgradD || KIND == kWgradGU);
