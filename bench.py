@@ -174,14 +174,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "c598148442bfe6df2b403cf83efa3cce4e286297a77ae318aca90ef713f1aec2",
+    "csrc_sha256": "eb969e379f779f0608579bdbe881c1309e98cb6bb1a7ec41032835e6bfe9e7e6",
     "bytes": {
-        "gemm_up_swiglu": 11887769753,
-        "gemm_down": 5723498035,
-        "gemm_bwd_u_swiglu": 6945335347,
-        "gemm_bwd_dx": 11188713830,
-        "gemm_wgrad_down": 8508461619,
-        "gemm_wgrad_gate_up": 16134242099,
+        "gemm_up_swiglu": 11887223244,
+        "gemm_down": 5726132480,
+        "gemm_bwd_u_swiglu": 6930857011,
+        "gemm_bwd_dx": 11176548352,
+        "gemm_wgrad_down": 8504734566,
+        "gemm_wgrad_gate_up": 16127314483,
     },
 }
 
