@@ -120,9 +120,9 @@ typedef struct moe_plan_s* moe_plan_t;
  * moe_plan_destroy).  Supported: d % 256 == 0, F % 256 == 0, 1 <= k <= 32,
  * k <= E <= 1024, 1 <= T_max <= 2^20, prec MOE_BF16, MOE_MXFP8 or MOE_NVFP4
  * (a block-scaled plan also holds quantised copies of the weights in both
- * orientations: block-scaled forward GEMMs and dgrad GEMMs; its weight
- * gradients are computed from the bf16 operands, since writing dW in bf16
- * bounds those GEMMs; NVFP4 plans run the separate-kernel schedule).  Otherwise
+ * orientations for its block-scaled forward and dgrad GEMMs; its weight
+ * gradients are block-scaled GEMMs on operands quantised along the tokens;
+ * NVFP4 plans run the separate-kernel schedule).  Otherwise
  * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG; allocation failure MOE_ERR_OOM. */
 moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out);
 
@@ -151,7 +151,8 @@ moe_status_t moe_forward(moe_plan_t plan, int64_t T, const void* X, const float*
  *      experts that received no token get zeros)
  *   dg      [T, k] fp32  gradient of the gate weights w (written)
  *   dlogits [T, E] fp32  gradient of the router logits, or NULL to skip
- * Every reduction runs in a fixed order: bitwise deterministic. */
+ * Enqueued on `stream`; every reduction runs in a fixed order: bitwise
+ * deterministic. */
 moe_status_t moe_backward(moe_plan_t plan, int64_t T, const void* dY, const void* X,
                           const void* Wg, const void* Wu, const void* Wd, const void* saved,
                           void* dX, void* dWg, void* dWu, void* dWd, float* dg, float* dlogits,

@@ -338,3 +338,47 @@ def test_backward_reuses_sorted_x_only_for_its_own_forward(flags):
     assert plan.device_status() == 0
     for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
         assert torch.equal(reused[key], regathered[key]), key
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_BF16, moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["bf16", "mxfp8", "nvfp4"])
+def test_idle_experts_get_zero_weight_gradients_over_poisoned_buffers(prec):
+    """Experts that receive no row get exactly zero dWg, dWu and dWd, written
+    over whatever the output buffers held (here NaN), and the experts that
+    do receive rows still match the oracle.  Every token is routed among
+    experts 0-5 of 16, so experts 6-15 are idle."""
+    T, d, F, E, k = 96, 256, 512, 16, 2
+
+    def first_six(logits):
+        out = logits.clone()
+        out[:, 6:] -= 30.0
+        return out
+
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=5, logits_fn=first_six)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec))
+    fmt = {moe.MOE_BF16: False, moe.MOE_MXFP8: "mxfp8", moe.MOE_NVFP4: "nvfp4"}[prec]
+    if fmt:
+        plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    nan = float("nan")
+    out = {
+        "dX": torch.full((T, d), nan, dtype=torch.bfloat16, device="cuda"),
+        "dWg": torch.full((E, F, d), nan, dtype=torch.bfloat16, device="cuda"),
+        "dWu": torch.full((E, F, d), nan, dtype=torch.bfloat16, device="cuda"),
+        "dWd": torch.full((E, d, F), nan, dtype=torch.bfloat16, device="cuda"),
+        "dg": torch.full((T, k), nan, dtype=torch.float32, device="cuda"),
+        "dlogits": torch.full((T, E), nan, dtype=torch.float32, device="cuda"),
+    }
+    plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved, out=out)
+    counts = plan.routing(saved, T)["counts"].cpu().numpy()
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert (counts[6:] == 0).all() and (counts[:6] > 0).all()
+    for name in ("dWg", "dWu", "dWd"):
+        assert torch.count_nonzero(out[name][6:]).item() == 0, name     # NaN counts as nonzero
+        assert not torch.isnan(out[name][:6]).any().item(), name
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k, mx=fmt)
+    gref = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"],
+                            moe_ref.stored_context(ctx) if fmt else ctx)
+    tol = 4e-2 if fmt else BF16_TOL
+    for name in ("dX", "dWg", "dWu", "dWd"):
+        assert rel_err(out[name], gref[name]) <= tol, name
