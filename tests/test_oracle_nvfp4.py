@@ -189,8 +189,9 @@ def test_nvfp4_exact_inputs_only_intermediates_add_error():
     rel = np.abs(Y1 - Y0).max() / np.abs(Y0).max()
     assert 0 < rel < 0.25
     # backward: the weights' other orientation is not exact, so compare with
-    # an explicit emulation: only dY (exact), dA/dB and the re-oriented
-    # weights are quantised; dg and the weight gradients use unquantised h, dY
+    # an explicit emulation: dY (exact), dA/dB and the re-oriented weights are
+    # quantised for dX; dg uses the unquantised u and h; the weight gradients
+    # quantise their operands along the tokens (below)
     g0 = moe_ref.backward(dY, X, L, Wg, Wu, Wd, c0)
     g1 = moe_ref.backward(dY, X, L, Wg, Wu, Wd, c1)
     dX = np.zeros_like(X)
