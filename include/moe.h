@@ -241,7 +241,8 @@ moe_status_t moe_nv_quantize_transposed(const void* src, int64_t E, int64_t A, i
  * which = 2..5: the block-scaled weight gradients' operands, transposed and
  * quantised along the sorted rows (NVFP4 tensor scale 1): 2 dY^T and 3 X^T
  * (C = d), 4 [dA|dB]^T (C = 2F), 5 (w h)^T (C = F):
- *   vals [P, C] fp32: for 4 and 5 the bf16 rows the transposer read, widened
+ *   vals [P, C] fp32: for 4 and 5 the bf16 values the u GEMM's epilogue
+ *        quantised (the plan keeps them in this mode only), widened
  *        (must be NULL for 2 and 3, whose rows are the gathered inputs);
  *   q    [C, P] E4M3 bytes or [C, P / 2] packed E2M1;
  *   sf   scale atoms of the C rows with K = P.

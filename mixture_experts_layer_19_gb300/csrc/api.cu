@@ -1107,6 +1107,13 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     u.dgp = p->dgp;
     u.tsB = nv ? p->nv_scale + 1 : nullptr;
     u.dbg = p->dbg_dab;
+    // the weight gradients' [dA|dB]^T and (w h)^T, quantised along the sorted
+    // rows in the same epilogue
+    u.Kcap = (int)p->Rpm;
+    u.qT0 = p->dABTq;
+    u.sT0 = p->dABTs;
+    u.qT1 = p->wHTq;
+    u.sT1 = p->wHTs;
     err = timed_launch(p, nv ? "gemm_nv_bwd_u_swiglu" : "gemm_mx_bwd_u_swiglu", st,
                        [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st, nv); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled u GEMM launch");
@@ -1174,29 +1181,18 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: router gradient launch");
   }
   if (mx) {
-    // block-scaled weight gradients: dY, X, dA|dB and w h transposed and
-    // quantised along the tokens (tensor scale 1 for NVFP4), rows past the
-    // ones in use skipped; then dWd = dY^T (w h) and [dWg; dWu] = [dA|dB]^T X
-    // with K = each expert's tokens
-    const int qgrid = p->num_sms * 8;
+    // block-scaled weight gradients: dY and X transposed and quantised along
+    // the tokens here ([dA|dB]^T and (w h)^T came from the u GEMM's
+    // epilogue; tensor scale 1 for NVFP4), rows past the ones in use skipped;
+    // then dWd = dY^T (w h) and [dWg; dWu] = [dA|dB]^T X with K = each
+    // expert's tokens
     const int Rq = (int)p->Rpm;
-    auto transpose = [&](const void* src, int cols, uint8_t* q, uint8_t* sf) {
-      return nv ? launch_nv_quant_transpose(src, 1, Rq, cols, nullptr, q, sf, qgrid, st, rp.totals)
-                : launch_quant_transpose(src, 1, Rq, cols, q, sf, qgrid, st, rp.totals);
-    };
     err = timed_launch(p, "quant_wgrad_tokens", st, [&] {
-      // dY and X straight from the token tensors: gathered, transposed, quantised
       // one wave: four CTAs (32 KB of staged tiles each) per SM
       return launch_gather_transpose_q(nv, dY, X, rp.perm_src, rp.totals, c.k, Rq, c.d, p->dYTq, p->dYTs, p->XTq,
                                        p->XTs, p->num_sms * 4, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient token quantisation launch");
-    err = timed_launch(p, "quant_wgrad_operands", st, [&] {
-      cudaError_t e = transpose(p->dAB, 2 * c.F, p->dABTq, p->dABTs);
-      if (e == cudaSuccess) e = transpose(p->wH, c.F, p->wHTq, p->wHTs);
-      return e;
-    });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient operand quantisation launch");
     MxArgs w;
     memset(&w, 0, sizeof(w));
     w.poff = rp.poff;
@@ -1503,7 +1499,7 @@ moe_status_t moe_debug_quant_dump(moe_plan_t p, int32_t which, float* vals, void
   if (vals) {
     if (which <= 1)
       err = cudaMemcpyAsync(vals, which == 0 ? p->dbg_h : p->dbg_dab, n * 4, cudaMemcpyDeviceToDevice, st);
-    else   // the bf16 rows the transposer read, widened
+    else   // the bf16 values the u GEMM's epilogue quantised (stored in this mode), widened
       err = launch_widen_bf16(which == 4 ? p->dAB : p->wH, vals, (int64_t)n, p->num_sms * 4, st);
   }
   if (q && err == cudaSuccess) err = cudaMemcpyAsync(q, qsrc[which], nv ? n / 2 : n, cudaMemcpyDeviceToDevice, st);

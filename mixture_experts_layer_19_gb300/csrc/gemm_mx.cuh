@@ -36,8 +36,9 @@ namespace moe {
 constexpr int kMxBK = 128;  // bytes of K per stage (128 E4M3 or 256 E2M1 values)
 
 // Kinds: kUp, kDown (forward); kBwdU  u = dYq . WdTq^T with the SwiGLU-backward
-// epilogue (dA, dB, w h in bf16 for the weight gradients, dA|dB re-quantised
-// along F for the dx GEMM, <u, h> partials); kBwdX  dx = dABq . [WgTq;WuTq]^T.
+// epilogue (dA|dB re-quantised along F for the dx GEMM; [dA|dB]^T and (w h)^T
+// quantised along the sorted rows for the weight gradients; <u, h> partials);
+// kBwdX  dx = dABq . [WgTq;WuTq]^T.
 // WdTq [E*F, d], WgTq / WuTq [E*d, F] are the weights' backward orientation,
 // quantised along their K (the dgrad GEMMs' K), so every operand is K-major.
 template <int KIND, bool NV = false>
@@ -96,8 +97,45 @@ struct MxArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int E, d, F;
-  int Kcap;                  // weight-gradient kinds: token capacity of the transposed operands
+  int Kcap;                  // weight-gradient kinds and kBwdU: token capacity of the transposed operands
+  // kBwdU: [dA|dB]^T and (w h)^T quantised along the sorted rows (the weight
+  // gradients' operands), [2F, Kcap] and [F, Kcap] with their scale atoms
+  uint8_t* qT0;
+  uint8_t* sT0;
+  uint8_t* qT1;
+  uint8_t* sT1;
 };
+
+// Column `lane` of a staged 32 x 32 bf16 tile (stage_row's layout: 16-byte
+// chunk c of row r at chunk c ^ ((r >> 1) & 3)), quantised along its 32 rows
+// -- sorted rows rowq .. rowq + 31, one MXFP8 block or two NVFP4 blocks
+// (tensor scale 1) -- into row `orow` of a transposed operand qT [C, P] at
+// column rowq, its scale bytes into the atoms of the C rows with K = P.  A
+// warp's 32 lanes read one 64-byte row per step: no bank conflicts.
+template <bool NV>
+__device__ __forceinline__ void store_col_q(const uint8_t* stg, int lane, uint8_t* __restrict__ qT,
+                                            uint8_t* __restrict__ sT, int64_t orow, int rowq, int P, float rc1) {
+  float v[32];
+  const int ch = lane >> 3, el = lane & 7;
+#pragma unroll
+  for (int r = 0; r < 32; ++r)
+    v[r] = __bfloat162float(
+        *reinterpret_cast<const __nv_bfloat16*>(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4) + el * 2));
+  if constexpr (NV) {
+    uint4 o;
+    const uint32_t s2 = nv_encode32(v, rc1, 1.0f, o);
+    *reinterpret_cast<uint4*>(qT + orow * (P / 2) + rowq / 2) = o;
+    *reinterpret_cast<uint16_t*>(sT + sf_atom_offset(orow, rowq / 16, P / 16)) = (uint16_t)s2;
+  } else {
+    const int xe = mx_block_exponent(amax32(v));
+    uint32_t o[8];
+    mx_encode32(v, xe, o);
+    uint4* dq = reinterpret_cast<uint4*>(qT + orow * P + rowq);
+    dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    sT[sf_atom_offset(orow, rowq / 32, P / 32)] = (uint8_t)(xe + 127);
+  }
+}
 
 // One stage: the A and B tiles (TMA; x coordinates in bytes) and their scale
 // atoms (1-D bulk copies).  Atoms of consecutive K groups are adjacent, so the
@@ -350,15 +388,20 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
       const int rowq = t.row0 + 32 * q;
       if (KIND == kBwdU) {
         // u in 32-column chunks: dh = w u, da = dh b s(a)(1 + a(1 - s(a))),
-        // db = dh silu(a); outputs dA|dB and w h in bf16 (weight gradients),
-        // dA|dB quantised along F for the dx GEMM, and the row's <u, h> over
-        // this warp's 128 columns.
+        // db = dh silu(a); outputs dA|dB quantised along F for the dx GEMM,
+        // the bf16 dA, dB and w h staged 32 rows x 32 columns and quantised
+        // column by column along the rows into the weight gradients'
+        // transposed operands, and the row's <u, h> over this warp's 128
+        // columns.
         const int r = rowq + lane;
         const int src = __ldg(g.perm_src + r);
         const float wr = src >= 0 ? __ldg(g.wts + src) : 0.0f;
         const __nv_bfloat16* abrow = g.ab + (size_t)r * (2 * g.F);
         float dgacc = 0.0f;
         uint32_t sfa[2] = {0u, 0u}, sfb[2] = {0u, 0u};
+        // the bf16 dA|dB and w h are read only by the debug dump: the weight
+        // gradients take their quantised transposes, made from the staged tiles
+        const bool keep_bf16 = g.dbg != nullptr;
         // one 32-column chunk c of u, its TMEM load issued into ru: the SwiGLU
         // backward and the stores; `release` frees the accumulator as soon as
         // that load has landed
@@ -413,30 +456,33 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&g.mapO0, stg, col, rowq);
+              if (keep_bf16) tma_store_2d(&g.mapO0, stg, col, rowq);
               tma_store_2d(&g.mapO1, sq, col / qd, rowq);
               bulk_commit();
-              bulk_wait_read<0>();
             }
+            store_col_q<NV>(stg, lane, g.qT0, g.sT0, col + lane, rowq, g.Kcap, rc1);
+            if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
             stage_row(stg, lane, db);
             stage_row_fp8(sq, lane, qb);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&g.mapO0, stg, g.F + col, rowq);
+              if (keep_bf16) tma_store_2d(&g.mapO0, stg, g.F + col, rowq);
               tma_store_2d(&g.mapO1, sq, (g.F + col) / qd, rowq);
               bulk_commit();
-              bulk_wait_read<0>();
             }
+            store_col_q<NV>(stg, lane, g.qT0, g.sT0, g.F + col + lane, rowq, g.Kcap, rc1);
+            if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
             stage_row(stg, lane, wh);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0 && keep_bf16) {
               tma_store_2d(&g.mapO2, stg, col, rowq);
               bulk_commit();
             }
+            store_col_q<NV>(stg, lane, g.qT1, g.sT1, col + lane, rowq, g.Kcap, rc1);
             return;
           }
           if (lane == 0) bulk_wait_read<0>();
@@ -464,13 +510,18 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&g.mapO0, stg, col, rowq);
-            tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
-            tma_store_2d(&g.mapO2, stg + 2 * kStageChunk, col, rowq);
+            if (keep_bf16) {
+              tma_store_2d(&g.mapO0, stg, col, rowq);
+              tma_store_2d(&g.mapO0, stg + kStageChunk, g.F + col, rowq);
+              tma_store_2d(&g.mapO2, stg + 2 * kStageChunk, col, rowq);
+            }
             tma_store_2d(&g.mapO1, stg + 3 * kStageChunk, col / qd, rowq);
             tma_store_2d(&g.mapO1, stg + 3 * kStageChunk + TR::qout, (g.F + col) / qd, rowq);
             bulk_commit();
           }
+          store_col_q<NV>(stg, lane, g.qT0, g.sT0, col + lane, rowq, g.Kcap, rc1);
+          store_col_q<NV>(stg + kStageChunk, lane, g.qT0, g.sT0, g.F + col + lane, rowq, g.Kcap, rc1);
+          store_col_q<NV>(stg + 2 * kStageChunk, lane, g.qT1, g.sT1, col + lane, rowq, g.Kcap, rc1);
         };
         {
           // All four chunks leave the accumulator before any math: the last
