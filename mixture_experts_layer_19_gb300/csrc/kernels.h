@@ -88,9 +88,8 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, int grid, cud
 
 // MXFP8 (mx_quant.cu, gemm_mx.cu)
 cudaError_t launch_quant_rows(const void* src, int64_t rows, int K, void* q, void* sf, int grid, cudaStream_t st);
-// a_used (device, may be null): tiles whose first A row is at or past *a_used are skipped
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
-                                   cudaStream_t st, const int32_t* a_used = nullptr);
+                                   cudaStream_t st);
 // Block-scaled weight gradients (wgrad_quant.cu): the sorted rows of two
 // token tensors, transposed and quantised along the sorted rows (A = row
 // capacity, B = columns): out[c, r] = Q(src[perm_src[r] / k, c]).
@@ -118,7 +117,7 @@ cudaError_t launch_nv_tensor_scale(const void* a, int64_t na, const void* b, int
 cudaError_t launch_nv_quant_rows(const void* src, int64_t rows, int K, const float* g, void* q, void* sf, int grid,
                                  cudaStream_t st);
 cudaError_t launch_nv_quant_transpose(const void* src, int E, int A, int B, const float* g, void* q, void* sf,
-                                      int grid, cudaStream_t st, const int32_t* a_used = nullptr);
+                                      int grid, cudaStream_t st);
 
 // Ring-buffer forward megakernel (megakernel.cu)
 struct MegaArgs;

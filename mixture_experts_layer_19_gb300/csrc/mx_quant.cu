@@ -65,8 +65,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
 // write one 128-byte output row).
 __global__ void __launch_bounds__(256) quant_transpose_kernel(const __nv_bfloat16* __restrict__ src, int E, int A,
                                                               int B, uint8_t* __restrict__ q,
-                                                              uint8_t* __restrict__ sf,
-                                                              const int32_t* __restrict__ a_used) {
+                                                              uint8_t* __restrict__ sf) {
   // tile of 128 A-rows x 64 B-columns.  Loads: 8 threads per row, 16 bytes
   // each, so every row is read as one 128-byte line.  Row r is stored with
   // its columns shifted by 8 * (r / 32) (row stride 88 bf16), which makes the
@@ -80,7 +79,6 @@ __global__ void __launch_bounds__(256) quant_transpose_kernel(const __nv_bfloat1
     const int e = (int)(t / (na * nb));
     const int rem = (int)(t - (int64_t)e * na * nb);
     const int a0 = (rem / nb) * 128, b0 = (rem % nb) * 64;
-    if (a_used && a0 >= __ldg(a_used)) continue;   // past the rows in use (uniform per CTA)
     const int piece = tid & 7;
 #pragma unroll
     for (int pass = 0; pass < 4; ++pass) {
@@ -150,9 +148,9 @@ cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const in
 }
 
 cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q, void* sf, int grid,
-                                   cudaStream_t st, const int32_t* a_used) {
+                                   cudaStream_t st) {
   quant_transpose_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), E, A, B,
-                                               reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf), a_used);
+                                               reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }
 

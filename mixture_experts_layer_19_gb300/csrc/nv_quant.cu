@@ -110,8 +110,7 @@ __global__ void __launch_bounds__(256) nv_quant_rows_kernel(const __nv_bfloat16*
 // output row b0 + i / 4 and the 32 A-elements 32 (i % 4) onwards.
 __global__ void __launch_bounds__(256) nv_quant_transpose_kernel(const __nv_bfloat16* __restrict__ src, int E,
                                                                  int A, int B, const float* __restrict__ gp,
-                                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                                 const int32_t* __restrict__ a_used) {
+                                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
   constexpr int kStride = 88;
   __shared__ __align__(16) __nv_bfloat16 tile[128 * kStride];
   const float g = gp ? __ldg(gp) : 1.0f;
@@ -123,7 +122,6 @@ __global__ void __launch_bounds__(256) nv_quant_transpose_kernel(const __nv_bflo
     const int e = (int)(t / (na * nb));
     const int rem = (int)(t - (int64_t)e * na * nb);
     const int a0 = (rem / nb) * 128, b0 = (rem % nb) * 64;
-    if (a_used && a0 >= __ldg(a_used)) continue;   // past the rows in use (uniform per CTA)
     const int piece = tid & 7;
 #pragma unroll
     for (int pass = 0; pass < 4; ++pass) {
@@ -163,10 +161,9 @@ cudaError_t launch_nv_quant_rows(const void* src, int64_t rows, int K, const flo
 }
 
 cudaError_t launch_nv_quant_transpose(const void* src, int E, int A, int B, const float* g, void* q, void* sf,
-                                      int grid, cudaStream_t st, const int32_t* a_used) {
+                                      int grid, cudaStream_t st) {
   nv_quant_transpose_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), E, A, B, g,
-                                                  reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf),
-                                                  a_used);
+                                                  reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }
 
