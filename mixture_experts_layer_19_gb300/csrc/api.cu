@@ -1072,7 +1072,8 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     // MXFP8 / NVFP4 dgrad: dY quantised along d as it is gathered; u GEMM
     // against Wd^T (quantised along d) with dA|dB re-quantised along F in its
     // epilogue; dx GEMM against [Wg^T; Wu^T] (quantised along F).  The weight
-    // gradients below use the bf16 operands.
+    // gradients below are block-scaled too, on operands quantised along the
+    // tokens.
     err = timed_launch(p, "quant_tokens_dy", st, [&] {
       return nv ? launch_nv_quant_rows(dY, T, c.d, nullptr, p->Xtq, p->Xts, p->num_sms * 8, st)
                 : launch_quant_rows(dY, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
