@@ -46,6 +46,39 @@ def dist_env():
     return ws, rank, local
 
 
+def launch_ranks(args, argv) -> int:
+    """`--gpus N` (N > 1) outside a launcher: start N ranks on this node, one
+    per GPU, with torch.distributed.run on 127.0.0.1 and the same arguments,
+    and return its exit status.  Rank 0 prints the JSON line."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def bench_dry_run(args):
+    """The rank plumbing alone, without a GPU (gloo): each rank times a short
+    host wait of its own length, then barrier and max over ranks as in the
+    timed runs; rank 0 prints the line.  Checks the launcher and the timing
+    exchange on a machine without GPUs."""
+    ws, rank, _ = dist_env()
+    init_dist(ws, "gloo")
+    barrier(ws)
+    t0 = time.perf_counter()
+    time.sleep(0.01 * (1 + rank))
+    el = max_over_ranks((time.perf_counter() - t0) * 1e3, ws, torch.device("cpu"))
+    barrier(ws)
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "n_gpus": ws, "max_rank_ms": round(el, 3),
+                          "config": {"parallelism": f"replicas{ws}"}}), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
 def init_dist(ws: int, backend: str):
     if ws > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group(backend=backend)
@@ -308,7 +341,7 @@ def bench_gpu(args):
         shape["T"] = args.tokens
     T, d, F, E, k = (shape[n] for n in ("T", "d", "F", "E", "k"))
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED + rank, alpha=ALPHA, device=dev)
-    flags = moe.MOE_DEBUG_TIMING | (moe.MOE_DEBUG_SINGLE_CTA if args.single_cta else 0)
+    flags = moe.MOE_DEBUG_TIMING
     plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, device=local, debug_flags=flags))
     saved = plan.new_saved(T)
     Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
@@ -414,11 +447,12 @@ def bench_gpu(args):
         del plan, inp, grads, saved, Y
         torch.cuda.empty_cache()
         out["mxfp8_forward"] = [bench_mx_forward(args, dev, ws, peaks, alpha) for alpha in (0.0, ALPHA)]
+        # the largest configuration (T=32768, tensor-bound) is part of every run
         grid = [(Tm, a) for Tm in (2048, 8192, 32768) for a in (0.0, 1.1, 1.5)] if args.sweep else \
-            [(args.tokens or 8192, ALPHA)]
+            ([(args.tokens, ALPHA)] if args.tokens else [(8192, ALPHA), (32768, ALPHA)])
         out["mxfp8_fwd_bwd"] = [bench_mx_fwd_bwd(args, dev, ws, peaks, Tm, a) for Tm, a in grid]
-        if args.sweep:
-            out["minibatch_sweep"] = bench_minibatch_sweep(args, dev, ws)
+        if not args.tokens:
+            out["mxfp8_minibatch_sweep"] = bench_minibatch_sweep(args, dev, ws)
     if not args.no_nv:
         from mixture_experts_layer_19_gb300 import moe
         if args.no_mx:
@@ -692,44 +726,87 @@ def bench_mx_fwd_bwd(args, dev, ws, peaks, T, alpha, prec=None):
     # quantised weights of the active experts in both orientations, bf16 dW of every expert
     t_hbm = (2 * 3.0 * e_act * F * d * wbytes + 3.0 * E * F * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e3
     ms = el / steps
+    # each expert GEMM against the dense tensor peak of its format (padding-free FLOPs)
+    tag = "nv" if prec == moe.MOE_NVFP4 else "mx"
+    gemm_flops = {"up_swiglu": 4, "down": 2, "bwd_u_swiglu": 2, "bwd_dx": 4, "wgrad_down": 2, "wgrad_gate_up": 4}
+    gemms = {}
+    for kind, mul in gemm_flops.items():
+        name = f"gemm_{tag}_{kind}"
+        if name in kt:
+            g_ms = kt[name][0] / kt[name][1]
+            tf = mul * R * d * F / (g_ms / 1e3) / 1e12
+            gemms[name] = {"ms": round(g_ms, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
+                           "frac": round(tf / tpeak, 4)}
+    g_tot_ms = sum(v["ms"] for v in gemms.values())
+    all_tf = 18.0 * R * d * F / (g_tot_ms / 1e3) / 1e12 if g_tot_ms else 0.0
     res = {"workload": f"moe_layer_fwd_bwd_{fname}_T{T}_zipf{alpha:g}", "T": T, "zipf_alpha": alpha,
            "experts_active": e_act,
            "value": round(ws * T * steps / (el / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_ms": round(max(t_tc, t_hbm), 4),
                               "frac": round(max(t_tc, t_hbm) / ms, 4)},
+           "grouped_gemms": {"peak": round(tpeak, 1), "unit": "TFLOP/s",
+                             "peak_source": peaks["source"] + f" bf16_tflops_sustained x {mult:g}",
+                             "all_six": {"ms": round(g_tot_ms, 4), "achieved": round(all_tf, 1),
+                                         "frac": round(all_tf / tpeak, 4)},
+                             "per_kind": gemms},
            "kernels": {n: round(v[0] / steps, 4) for n, v in sorted(kt.items(), key=lambda x: -x[1][0])}}
     del plan, inp, saved, Y, grads
     torch.cuda.empty_cache()
     return res
 
 
-def bench_minibatch_sweep(args, dev, ws, T=8192, alpha=ALPHA):
-    """BF16 ring-megakernel forward time versus minibatch size (rows per ring
-    slot fill); 0 = the two-wave floor."""
+def bench_minibatch_sweep(args, dev, ws, T=8192, alphas=(0.0, 1.1, 1.5), prec=None,
+                          rows=(512, 1024, 2048, 0, 4096, 8192)):
+    """Layer step time versus the ring pipeline's minibatch size (rows per
+    ring slot fill; 0 = the two-wave floor), forward + backward, for each
+    routing skew: the ring megakernel forward's time and the whole step's."""
     from mixture_experts_layer_19_gb300 import moe
+    prec = moe.MOE_MXFP8 if prec is None else prec
+    fname = {moe.MOE_BF16: "bf16", moe.MOE_MXFP8: "mxfp8", moe.MOE_NVFP4: "nvfp4"}[prec]
     d, F, E, k = SHAPE["d"], SHAPE["F"], SHAPE["E"], SHAPE["k"]
-    inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
     stream = torch.cuda.current_stream(dev)
+    steps = max(3, args.steps // 4)
     out = []
-    for mb in (256, 512, 1024, 2048, 0, 4096, 8192):
-        plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, minibatch_rows=mb, device=dev.index,
-                                   debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL))
-        saved = plan.new_saved(T)
-        Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-        for _ in range(args.warmup):
-            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
-        torch.cuda.synchronize(dev)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        out.append({"minibatch_rows": mb if mb else "two-wave floor", "fwd_ms": round(ev0.elapsed_time(ev1) / args.steps, 4)})
-        del plan, saved, Y
-    del inp
-    torch.cuda.empty_cache()
-    return {"workload": f"bf16 ring-megakernel forward, T={T}, zipf {alpha:g}", "points": out}
+    for alpha in alphas:
+        inp = make_inputs(LayerShape(T, d, F, E, k), seed=SEED, alpha=alpha, device=dev)
+        grads = _alloc_grads(T, d, F, E, k, dev)
+        for mb in rows:
+            plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, minibatch_rows=mb,
+                                       device=dev.index,
+                                       debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL | moe.MOE_DEBUG_TIMING))
+            if prec != moe.MOE_BF16:
+                plan.quantize_weights(inp.Wg, inp.Wu, inp.Wd, stream=stream)
+            saved = plan.new_saved(T)
+            Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+
+            def step():
+                plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+                plan.backward(inp.dY, inp.X, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize(dev)
+            plan.kernel_times()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(steps):
+                step()
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            if plan.device_status() != 0:
+                raise RuntimeError("device status set in the minibatch sweep")
+            kt = plan.kernel_times()
+            mk = [n for n in kt if n.startswith("fwd_megakernel")]
+            info = plan.info()
+            out.append({"zipf_alpha": alpha, "minibatch_rows": mb if mb else "two-wave floor",
+                        "minibatch_tiles": info["minibatch_tiles"],
+                        "step_ms": round(max_over_ranks(ev0.elapsed_time(ev1), ws, dev) / steps, 4),
+                        "megakernel_ms": round(sum(kt[n][0] for n in mk) / steps, 4)})
+            del plan, saved, Y
+        del inp, grads
+        torch.cuda.empty_cache()
+    return {"workload": f"{fname} fwd+bwd with the ring megakernel forward, T={T}, d={d}, F={F}, E={E}, top{k}",
+            "points": out}
 
 
 def bench_e2e(args, plan, inp, Y, saved, grads, stream, dev, ws):
@@ -872,14 +949,22 @@ def main(argv=None):
     ap.add_argument("--no-nv", action="store_true", help="skip the NVFP4 measurements")
     ap.add_argument("--no-ring", action="store_true", help="skip the ring-megakernel forward line")
     ap.add_argument("--no-ep", action="store_true", help="skip the virtual-rank expert-parallel line")
-    ap.add_argument("--single-cta", action="store_true",
-                    help="bf16 GEMMs one CTA per tile (no 2-CTA operand sharing), for comparison")
     ap.add_argument("--sweep", action="store_true",
                     help="MXFP8 fwd+bwd over T in {2048, 8192, 32768} x zipf {0, 1.1, 1.5} and a minibatch sweep")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="start the ranks and exchange timings on the CPU (gloo) without any GPU work")
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args, argv))
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws != args.gpus:
+        ap.error(f"--gpus {args.gpus} but the launcher started {ws} ranks")
+    if args.dry_run:
+        bench_dry_run(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_gpu(args)

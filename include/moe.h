@@ -65,8 +65,7 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_NVFP4 = 2 } moe_precision_t;
 #define MOE_DEBUG_IDENTITY_EXPERTS 0x1u /* experts return their input (y = x); GEMMs skipped */
 #define MOE_DEBUG_TIMING 0x2u           /* bracket each kernel with CUDA events (moe_kernel_times) */
 /* Forward schedule.  By default both precisions run separate kernels
- * (routing, gather, grouped GEMMs over the full sorted buffers, combine): with
- * the paired-CTA GEMMs that is the fastest schedule measured on GB300.
+ * (routing, gather, grouped GEMMs over the full sorted buffers, combine).
  * MOE_DEBUG_RING_MEGAKERNEL selects the ring-buffer megakernel (movers fill a
  * fixed ring of minibatch slots, compute CTAs run the [a|b] and down tiles
  * minibatch by minibatch); for BF16 it is one launch that also routes and
@@ -75,11 +74,6 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_NVFP4 = 2 } moe_precision_t;
  * results. */
 #define MOE_DEBUG_SEPARATE_KERNELS 0x4u /* force separate kernels (overrides the ring flag) */
 #define MOE_DEBUG_RING_MEGAKERNEL 0x8u  /* use the ring-buffer megakernel */
-/* The separate bf16 GEMMs run as 2-CTA clusters whose two CTAs share one
- * operand tile per pipeline stage (TMA multicast), halving its L2 reads; with
- * this flag every GEMM runs one CTA per tile instead.  Results are bitwise
- * identical either way. */
-#define MOE_DEBUG_SINGLE_CTA 0x10u
 /* BF16 ring schedule: routing, layout, the minibatch plan and the combine as
  * separate launches around the ring megakernel instead of inside it. */
 #define MOE_DEBUG_MULTI_LAUNCH 0x20u
@@ -306,12 +300,12 @@ moe_status_t moe_device_status(moe_plan_t plan, moe_stream_t stream, int32_t* st
 moe_status_t moe_kernel_times(moe_plan_t plan, const char** names, double* total_ms,
                               int64_t* launches, int32_t cap, int32_t* n);
 
-/* Launch geometry the plan chose on this device: num_sms, and for each of
- * the six expert GEMM kinds (up, down, bwd u, bwd dx, wgrad down, wgrad
- * gate/up) the grid of its 2-CTA-cluster variant (pair_grid[6]; twice the
- * co-resident clusters, 0 if none), which depends on how the chip's enabled
- * SMs fall into clusters.  Host-only; any pointer may be NULL. */
-moe_status_t moe_plan_info(moe_plan_t plan, int32_t* num_sms, int32_t* pair_grid);
+/* Launch geometry the plan chose on this device: num_sms (the persistent
+ * kernels' grid: one CTA per SM), and the ring pipeline's shape ring[4] =
+ * {mover CTAs, ring slots, minimum minibatch in 128-row tiles (the two-wave
+ * floor or minibatch_rows), largest minibatch in tiles (one slot)}.
+ * Host-only; any pointer may be NULL. */
+moe_status_t moe_plan_info(moe_plan_t plan, int32_t* num_sms, int32_t* ring);
 
 /* Two-wave minibatch floor: the smallest row count m for which a grouped
  * GEMM of output width n_out cut into tile_m x tile_n tiles gives `waves`
@@ -336,11 +330,18 @@ moe_status_t moe_minibatch_floor(int32_t num_sms, int32_t tile_m, int32_t tile_n
  * buffers.  logits [T, E] fp32.  Requires 1 <= k <= 32, k <= E <= 1024.
  *
  * Scratch lives in one fixed 4 MiB device array inside the library, which
- * every GPU that loads the library keeps until the process exits.  A call
- * needs about 4*(2*ceil(T/64)*E + 2*T*k + 128*E) bytes of it; larger calls
- * return MOE_ERR_UNSUPPORTED (see moe_last_error) and enqueue nothing.  The
- * first call on each device looks up the array's device address; make that
- * first call outside any stream capture.  All calls share the array and it
+ * every GPU that loads the library keeps until the process exits.  Under
+ * CUDA's lazy module loading (the default) the 4 MiB is committed when the
+ * library's module first loads on a device, possibly during this entry
+ * point's first call there: a caller whose allocator will reserve the device
+ * memory should make one warm-up call before it does.  A call needs about
+ * 4*(2*ceil(T/64)*E + 2*T*k + 128*E) bytes of the array; larger calls return
+ * MOE_ERR_UNSUPPORTED (see moe_last_error) and enqueue nothing.  Each call
+ * made outside a stream capture looks up the array's device address on the
+ * current device (so a device reset is followed correctly); a call during a
+ * capture uses the address an earlier call looked up, so make the first call
+ * on each device outside any capture (a first call inside one returns
+ * MOE_ERR_INVALID_ARG).  All calls share the array and it
  * keeps the previous call's contents (each call writes every entry it reads,
  * so nothing needs clearing).  Calls that overlap on the GPU -- e.g. on two
  * streams without ordering between them -- race on the array.  Never calls

@@ -182,11 +182,9 @@ struct moe_plan_s {
   // workspace tensor maps
   CUtensorMap m_Xg_k, m_Xg_mn, m_H_k, m_H_st, m_Ys_st, m_dYg_k, m_dYg_mn, m_dAB_k, m_dAB_mn, m_dAB_st, m_wH_mn,
       m_wH_st;
-  CUtensorMap m_Xg_kh, m_H_kh, m_dYg_kh, m_dAB_kh;  // 64-row halves for paired CTAs
-  int pair_grid[6] = {0, 0, 0, 0, 0, 0};          // grid of each paired GEMM kernel (0 = none)
   // caller-pointer tensor maps, re-encoded when a pointer changes
   const void *p_wg = nullptr, *p_wu = nullptr, *p_wd = nullptr;
-  CUtensorMap m_Wg_k, m_Wu_k, m_Wd_k, m_Wg_mn, m_Wu_mn, m_Wd_mn, m_Wd_kh;
+  CUtensorMap m_Wg_k, m_Wu_k, m_Wd_k, m_Wg_mn, m_Wu_mn, m_Wd_mn;
   const void *p_dwg = nullptr, *p_dwu = nullptr, *p_dwd = nullptr;
   CUtensorMap m_dWg_st, m_dWu_st, m_dWd_st;
   // MXFP8 (prec == MOE_MXFP8): E4M3 weights + scale atoms (filled by
@@ -285,24 +283,14 @@ bool ensure_weight_maps(moe_plan_s* p, const void* Wg, const void* Wu, const voi
     p->p_wu = Wu;
   }
   if (Wd != p->p_wd) {
-    if (!map_kmajor(&p->m_Wd_k, Wd, c.F, Ed, BN) || !map_mnmajor(&p->m_Wd_mn, Wd, c.F, Ed) ||
-        !map_kmajor(&p->m_Wd_kh, Wd, c.F, Ed, BN / 2))
-      return false;
+    if (!map_kmajor(&p->m_Wd_k, Wd, c.F, Ed, BN) || !map_mnmajor(&p->m_Wd_mn, Wd, c.F, Ed)) return false;
     p->p_wd = Wd;
   }
   return true;
 }
 
-// Separate GEMMs run as 2-CTA clusters sharing one operand per stage when
-// such clusters can be formed, the debug flag does not forbid it, and the
-// grouped kinds have an even N-tile count (odd last M tiles pair over N).
-bool use_pair(const moe_plan_s* p, int kind) {
-  const moe_config_t& c = p->cfg;
-  if (p->pair_grid[kind] <= 0 || (c.debug_flags & MOE_DEBUG_SINGLE_CTA)) return false;
-  const int nt = kind == kUp ? c.F / 128 : (kind == kDown || kind == kBwdX) ? c.d / BN : kind == kBwdU ? c.F / BN : 2;
-  return nt % 2 == 0;
-}
-int gemm_grid(const moe_plan_s* p, int kind) { return use_pair(p, kind) ? p->pair_grid[kind] : p->num_sms; }
+// Grid of the persistent expert GEMMs: one CTA per SM.
+int gemm_grid(const moe_plan_s* p) { return p->num_sms; }
 
 // Virtual-rank expert parallelism: the argument block shared by its three
 // exchanges (R ranks of G CTAs each).
@@ -487,9 +475,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
             map_store(&p->m_Ys_st, p->Ys, c.d, R) && map_kmajor(&p->m_dYg_k, p->dYg, c.d, R) &&
             map_mnmajor(&p->m_dYg_mn, p->dYg, c.d, R) && map_kmajor(&p->m_dAB_k, p->dAB, 2 * c.F, R) &&
             map_mnmajor(&p->m_dAB_mn, p->dAB, 2 * c.F, R) && map_store(&p->m_dAB_st, p->dAB, 2 * c.F, R) &&
-            map_mnmajor(&p->m_wH_mn, p->wH, c.F, R) && map_store(&p->m_wH_st, p->wH, c.F, R) &&
-            map_kmajor(&p->m_Xg_kh, p->Xg, c.d, R, BM / 2) && map_kmajor(&p->m_H_kh, p->H, c.F, R, BM / 2) &&
-            map_kmajor(&p->m_dYg_kh, p->dYg, c.d, R, BM / 2) && map_kmajor(&p->m_dAB_kh, p->dAB, 2 * c.F, R, BM / 2);
+            map_mnmajor(&p->m_wH_mn, p->wH, c.F, R) && map_store(&p->m_wH_st, p->wH, c.F, R);
   if (!ok) {
     cudaFree(p->ws);
     delete p;
@@ -499,7 +485,6 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     err = kind < 2 ? prepare_gemm_fwd(kind) : prepare_gemm_bwd(kind);
     if (err == cudaSuccess && c.prec != MOE_BF16) err = prepare_gemm_mx(kind, c.prec == MOE_NVFP4);
     if (err == cudaSuccess && kind == 0 && c.prec != MOE_BF16) err = prepare_gather_transpose_q(c.prec == MOE_NVFP4);
-    if (err == cudaSuccess) p->pair_grid[kind] = kind < 2 ? gemm_pair_grid_fwd(kind) : gemm_pair_grid_bwd(kind);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
       delete p;
@@ -711,11 +696,15 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_plan_destroy: cudaFree");
 }
 
-moe_status_t moe_plan_info(moe_plan_t p, int32_t* num_sms, int32_t* pair_grid) {
+moe_status_t moe_plan_info(moe_plan_t p, int32_t* num_sms, int32_t* ring) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_plan_info: null plan");
   if (num_sms) *num_sms = p->num_sms;
-  if (pair_grid)
-    for (int i = 0; i < 6; ++i) pair_grid[i] = p->pair_grid[i];
+  if (ring) {
+    ring[0] = p->movers;
+    ring[1] = p->slots;
+    ring[2] = p->mbt;
+    ring[3] = p->cap;
+  }
   return MOE_OK;
 }
 
@@ -773,22 +762,19 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP dispatch launch");
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_Xg_k;
-    a.mapAh = p->m_Xg_kh;
     a.mapB0 = p->m_Wg_k;
     a.mapB1 = p->m_Wu_k;
     a.mapO0 = m_ab_st;
     a.mapO1 = p->m_H_st;
     err = timed_launch(p, "gemm_up_swiglu", st,
-                       [&] { return launch_gemm_fwd(kUp, a, gemm_grid(p, kUp), use_pair(p, kUp), st); });
+                       [&] { return launch_gemm_fwd(kUp, a, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: up GEMM launch");
     GemmArgs b = base_args(p, rp);
     b.mapA = p->m_H_k;
-    b.mapAh = p->m_H_kh;
     b.mapB0 = p->m_Wd_k;
-    b.mapB0h = p->m_Wd_kh;
     b.mapO0 = p->m_Ys_st;
     err = timed_launch(p, "gemm_down", st,
-                       [&] { return launch_gemm_fwd(kDown, b, gemm_grid(p, kDown), use_pair(p, kDown), st); });
+                       [&] { return launch_gemm_fwd(kDown, b, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: down GEMM launch");
     ea.Ys = static_cast<const uint4*>(p->Ys);
     ea.out = static_cast<uint4*>(Y);
@@ -965,23 +951,20 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   if (!ident) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_Xg_k;
-    a.mapAh = p->m_Xg_kh;
     a.mapB0 = p->m_Wg_k;
     a.mapB1 = p->m_Wu_k;
     a.mapO0 = m_ab_st;
     a.mapO1 = p->m_H_st;
     a.stall = (c.debug_flags & MOE_DEBUG_STALL_TEST) ? 1 : 0;
     err = timed_launch(p, "gemm_up_swiglu", st,
-                       [&] { return launch_gemm_fwd(kUp, a, gemm_grid(p, kUp), use_pair(p, kUp), st); });
+                       [&] { return launch_gemm_fwd(kUp, a, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: up GEMM launch");
     GemmArgs b = base_args(p, rp);
     b.mapA = p->m_H_k;
-    b.mapAh = p->m_H_kh;
     b.mapB0 = p->m_Wd_k;
-    b.mapB0h = p->m_Wd_kh;
     b.mapO0 = p->m_Ys_st;
     err = timed_launch(p, "gemm_down", st,
-                       [&] { return launch_gemm_fwd(kDown, b, gemm_grid(p, kDown), use_pair(p, kDown), st); });
+                       [&] { return launch_gemm_fwd(kDown, b, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: down GEMM launch");
     ys = p->Ys;
   }
@@ -1133,7 +1116,6 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   if (!mx) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dYg_k;
-    a.mapAh = p->m_dYg_kh;
     a.mapB0 = p->m_Wd_mn;
     a.mapO0 = p->m_dAB_st;
     a.mapO1 = p->m_wH_st;
@@ -1142,18 +1124,17 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     a.wts = rp.w;
     a.dgp = p->dgp;
     err = timed_launch(p, "gemm_bwd_u_swiglu", st,
-                       [&] { return launch_gemm_bwd(kBwdU, a, gemm_grid(p, kBwdU), use_pair(p, kBwdU), st); });
+                       [&] { return launch_gemm_bwd(kBwdU, a, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: u GEMM launch");
   }
   if (!mx) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dAB_k;
-    a.mapAh = p->m_dAB_kh;
     a.mapB0 = p->m_Wg_mn;
     a.mapB1 = p->m_Wu_mn;
     a.mapO0 = p->m_Ys_st;
     err = timed_launch(p, "gemm_bwd_dx", st,
-                       [&] { return launch_gemm_bwd(kBwdX, a, gemm_grid(p, kBwdX), use_pair(p, kBwdX), st); });
+                       [&] { return launch_gemm_bwd(kBwdX, a, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dx GEMM launch");
   }
   if (ep) {
@@ -1230,7 +1211,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     a.mapB0 = p->m_wH_mn;
     a.mapO0 = p->m_dWd_st;
     err = timed_launch(p, "gemm_wgrad_down", st,
-                       [&] { return launch_gemm_bwd(kWgradD, a, gemm_grid(p, kWgradD), use_pair(p, kWgradD), st); });
+                       [&] { return launch_gemm_bwd(kWgradD, a, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dWd GEMM launch");
   }
   {
@@ -1240,7 +1221,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     a.mapO0 = p->m_dWg_st;
     a.mapO1 = p->m_dWu_st;
     err = timed_launch(p, "gemm_wgrad_gate_up", st, [&] {
-      return launch_gemm_bwd(kWgradGU, a, gemm_grid(p, kWgradGU), use_pair(p, kWgradGU), st);
+      return launch_gemm_bwd(kWgradGU, a, gemm_grid(p), st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dWg/dWu GEMM launch");
   }

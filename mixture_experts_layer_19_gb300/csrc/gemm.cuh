@@ -10,10 +10,8 @@
 //               -> fused math -> bf16 -> 64-byte-swizzled staging -> TMA store.
 // Two 256-column TMEM accumulators let the epilogue of tile i overlap the
 // main loop of tile i+1.  Tiles are handed out statically (tile = CTA id +
-// j * gridDim.x, or the same over jobs of 2-CTA clusters that share one
-// operand per stage: decode_job, load_stage_pair).  Every tile accumulates
-// its K range in one fixed order, so the result does not depend on
-// scheduling: bitwise deterministic.
+// j * gridDim.x).  Every tile accumulates its K range in one fixed order, so
+// the result does not depend on scheduling: bitwise deterministic.
 //
 // The six contractions of the layer (sorted/padded row space, 128-row expert
 // segments; "rows" are (token, slot) pairs sorted by expert):
@@ -69,8 +67,6 @@ struct GemmArgs {
   CUtensorMap mapO0;   // output stores
   CUtensorMap mapO1;
   CUtensorMap mapO2;
-  CUtensorMap mapAh;   // paired CTAs: A in 64-row halves (K-major A only)
-  CUtensorMap mapB0h;  // paired CTAs, kDown: Wd in 128-row halves
   const int32_t* poff;       // [E+1] padded segment starts (rows)
   const int32_t* mtile_off;  // [E+1] prefix sum of 128-row tiles per expert
   const __nv_bfloat16* ab;   // kBwdU: saved [R, 2F] pre-activations a|b
@@ -89,7 +85,6 @@ struct GemmArgs {
 
 struct Tile {
   int e, mt, nt;   // expert, M tile, N tile
-  int share;       // paired CTAs: 1 = B tile shared (two M tiles), 2 = A tile shared (two N tiles)
   int row0;        // first sorted row (grouped) / first output row inside the expert (wgrad)
   int nkb;         // K slices
   int kbase;       // first sorted row of the K range (wgrad)
@@ -150,7 +145,6 @@ __device__ __forceinline__ Tile decode_tile(const G& g, int tile) {
     t.row0 = t.mt * BM;
     t.nkb = dense_nkb<KIND>(g);
     t.kbase = 0;
-    t.share = 0;
     return t;
   }
   const int NT = n_tiles_n<KIND>(g);
@@ -182,7 +176,6 @@ __device__ __forceinline__ Tile decode_tile(const G& g, int tile) {
     t.kbase = __ldg(g.poff + t.e);
     t.nkb = (__ldg(g.poff + t.e + 1) - t.kbase) / BK;
   }
-  t.share = 0;
   return t;
 }
 
@@ -233,116 +226,6 @@ __device__ __forceinline__ void load_stage(const GemmArgs& g, const Tile& t, int
   }
 }
 
-// Paired CTAs (2-CTA clusters): job `job` of the pair, tile of CTA `rank`.
-// Grouped kinds: expert e owns jobs [mtile_off[e]*NT/2, mtile_off[e+1]*NT/2).
-// Its M tiles are paired (2p, 2p+1) for every N tile (the B tile is shared),
-// ordered (n, p) with p fastest.  An odd last M tile is instead paired with
-// itself over N tiles (2j, 2j+1) (the A tile is shared); NT must be even.
-// Weight-gradient kinds: M tiles (2p, 2p+1) share the B tile, ordered
-// (e, n, p).
-template <int KIND, class G>
-__device__ __forceinline__ Tile decode_job(const G& g, int job, int rank) {
-  Tile t;
-  const int NT = n_tiles_n<KIND>(g);
-  if (KindTraits<KIND>::grouped) {
-    const int half = NT >> 1;
-    const int gidx = job / half;
-    int lo = 0, hi = g.E;  // last e with mtile_off[e] <= gidx
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (__ldg(g.mtile_off + mid) <= gidx) lo = mid; else hi = mid;
-    }
-    t.e = lo;
-    const int m0 = __ldg(g.mtile_off + lo);
-    const int mte = __ldg(g.mtile_off + lo + 1) - m0;
-    const int mp = mte >> 1;
-    const int local = job - m0 * half;
-    if (local < mp * NT) {
-      t.nt = local / mp;
-      t.mt = 2 * (local - t.nt * mp) + rank;
-      t.share = 1;
-    } else {
-      t.mt = mte - 1;
-      t.nt = 2 * (local - mp * NT) + rank;
-      t.share = 2;
-    }
-    t.row0 = __ldg(g.poff + lo) + t.mt * BM;
-    t.nkb = k_blocks_grouped<KIND>(g);
-    t.kbase = 0;
-  } else {
-    const int MP = n_tiles_m_wgrad<KIND>(g) >> 1;
-    const int per = MP * NT;
-    t.e = job / per;
-    const int local = job - t.e * per;
-    t.nt = local / MP;
-    t.mt = 2 * (local - t.nt * MP) + rank;
-    t.share = 1;
-    t.row0 = t.mt * BM;
-    t.kbase = __ldg(g.poff + t.e);
-    t.nkb = (__ldg(g.poff + t.e + 1) - t.kbase) / BK;
-  }
-  return t;
-}
-
-// Paired CTAs: each CTA loads the operand it owns alone and half of the
-// shared one, multicast to both CTAs (same shared-memory offsets), so each
-// stage still receives kStageBytes in every CTA while L2 serves the shared
-// operand once per pair.
-template <int KIND>
-__device__ __forceinline__ void load_stage_pair(const GemmArgs& g, const Tile& t, int kb, int rank, uint8_t* sa,
-                                                uint8_t* sb, uint64_t* bar, uint64_t pol_w, uint64_t pol_a) {
-  constexpr uint16_t kBoth = 0x3;
-  const int k0 = kb * BK;
-  if (KIND == kWgradD || KIND == kWgradGU) {  // M tiles 2p, 2p+1: B shared
-    const int kr = t.kbase + k0;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * 8192, &g.mapA, t.row0 + j * 64, kr, bar, pol_a);
-#pragma unroll
-    for (int j = 2 * rank; j < 2 * rank + 2; ++j)
-      tma_load_2d_mc(sb + j * 8192, &g.mapB0, t.nt * BN + j * 64, kr, bar, kBoth, pol_a);
-    return;
-  }
-  if (t.share == 1) {  // own A, half of the shared B
-    tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
-    if (KIND == kUp) {
-      tma_load_2d_mc(sb + rank * (kBBytes / 2), rank ? &g.mapB1 : &g.mapB0, k0, t.e * g.F + t.nt * 128, bar,
-                     kBoth, pol_w);
-    } else if (KIND == kDown) {
-      tma_load_2d_mc(sb + rank * (kBBytes / 2), &g.mapB0h, k0, t.e * g.d + t.nt * BN + rank * 128, bar, kBoth,
-                     pol_w);
-    } else if (KIND == kBwdU) {
-#pragma unroll
-      for (int j = 2 * rank; j < 2 * rank + 2; ++j)
-        tma_load_2d_mc(sb + j * 8192, &g.mapB0, t.nt * BN + j * 64, t.e * g.d + k0, bar, kBoth, pol_w);
-    } else {  // kBwdX
-      const bool up = k0 >= g.F;
-      const CUtensorMap* mb = up ? &g.mapB1 : &g.mapB0;
-      const int krow = t.e * g.F + (up ? k0 - g.F : k0);
-#pragma unroll
-      for (int j = 2 * rank; j < 2 * rank + 2; ++j)
-        tma_load_2d_mc(sb + j * 8192, mb, t.nt * BN + j * 64, krow, bar, kBoth, pol_w);
-    }
-  } else {  // one M tile, N tiles 2j and 2j+1: half of the shared A, own B
-    tma_load_2d_mc(sa + rank * (kABytes / 2), &g.mapAh, k0, t.row0 + rank * 64, bar, kBoth, pol_a);
-    if (KIND == kUp) {
-      tma_load_2d(sb, &g.mapB0, k0, t.e * g.F + t.nt * 128, bar, pol_w);
-      tma_load_2d(sb + kBBytes / 2, &g.mapB1, k0, t.e * g.F + t.nt * 128, bar, pol_w);
-    } else if (KIND == kDown) {
-      tma_load_2d(sb, &g.mapB0, k0, t.e * g.d + t.nt * BN, bar, pol_w);
-    } else if (KIND == kBwdU) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        tma_load_2d(sb + j * 8192, &g.mapB0, t.nt * BN + j * 64, t.e * g.d + k0, bar, pol_w);
-    } else {
-      const bool up = k0 >= g.F;
-      const CUtensorMap* mb = up ? &g.mapB1 : &g.mapB0;
-      const int krow = t.e * g.F + (up ? k0 - g.F : k0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, mb, t.nt * BN + j * 64, krow, bar, pol_w);
-    }
-  }
-}
-
 // ----------------------------------------------------------------------------
 // Epilogue helpers.
 // ----------------------------------------------------------------------------
@@ -382,9 +265,7 @@ __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + __ex
 // ----------------------------------------------------------------------------
 // The kernel.
 // ----------------------------------------------------------------------------
-// PAIR: launched as 2-CTA clusters; the CTAs of a cluster run the jobs of
-// decode_job in lockstep and share one operand per stage (load_stage_pair).
-template <int KIND, bool PAIR>
+template <int KIND>
 __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(const __grid_constant__ GemmArgs g) {
   using TR = KindTraits<KIND>;
   extern __shared__ uint8_t smem_raw[];
@@ -405,7 +286,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);  // paired: both CTAs' MMAs release a stage
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -428,13 +309,10 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
-  // static schedule: work item w -> tile (single CTA) or job (pair)
-  const int ntiles = total_tiles<KIND>(g);
-  const int rank = PAIR ? (int)cluster_ctarank() : 0;
-  const int w0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int wstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int nwork = PAIR ? ntiles / 2 : ntiles;
-  if (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any multicast
+  // static schedule: tile w = blockIdx.x + j * gridDim.x
+  const int nwork = total_tiles<KIND>(g);
+  const int w0 = (int)blockIdx.x;
+  const int wstep = (int)gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -451,25 +329,14 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
       uint32_t issued_mask = 0, last_par = 0;
       bool ok = true;
       for (int w = w0; w < nwork && ok && !g.stall; w += wstep) {
-        const Tile t = PAIR ? decode_job<KIND>(g, w, rank) : decode_tile<KIND>(g, w);
+        const Tile t = decode_tile<KIND>(g, w);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           uint8_t* sa = stage_base + s * kStageBytes;
-          if (PAIR)
-            load_stage_pair<KIND>(g, t, kb, rank, sa, sa + kABytes, &full[s], pol_w, pol_a);
-          else
-            load_stage<KIND>(g, t, kb, sa, sa + kABytes, &full[s], pol_w, pol_a);
+          load_stage<KIND>(g, t, kb, sa, sa + kABytes, &full[s], pol_w, pol_a);
           issued_mask |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
-          if (++s == kStages) { s = 0; ph ^= 1; }
-        }
-      }
-      if (PAIR && ok && !g.stall) {
-        // the peer's last commits arrive on these barriers: they must land
-        // before this CTA may exit
-        for (int i = 0; i < kStages; ++i) {
-          if (!mbar_wait(&empty[s], ph ^ 1, wc)) break;
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
       }
@@ -491,7 +358,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
       uint32_t s = 0, ph = 0, acc = 0, aph = 0;
       bool ok = true;
       for (int w = w0; w < nwork && ok; w += wstep) {
-        const Tile t = PAIR ? decode_job<KIND>(g, w, rank) : decode_tile<KIND>(g, w);
+        const Tile t = decode_tile<KIND>(g, w);
         if (t.nkb == 0) continue;
         if (!mbar_wait(&tempty[acc], aph ^ 1, wc)) break;
         tc_fence_after();
@@ -507,10 +374,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
             const uint64_t bd = TR::b_mn ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (PAIR)
-            umma_commit_mc(&empty[s], 0x3);
-          else
-            umma_commit(&empty[s]);
+          umma_commit(&empty[s]);
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
@@ -526,7 +390,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
     uint32_t acc = 0, aph = 0;
     int chunk_ctr = 0;
     for (int w = w0; w < nwork; w += wstep) {
-      const Tile t = PAIR ? decode_job<KIND>(g, w, rank) : decode_tile<KIND>(g, w);
+      const Tile t = decode_tile<KIND>(g, w);
       const bool has_acc = t.nkb > 0;
       if (has_acc) {
         if (!mbar_wait(&tfull[acc], aph, wc)) break;
@@ -711,7 +575,6 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
   }
 
   __syncthreads();
-  if (PAIR) cluster_sync_all();  // neither CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
@@ -720,56 +583,15 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
 
 // ---------------------------------------------------------------- host side
 template <int KIND>
-cudaError_t gemm_launch(const GemmArgs& a, int grid, bool pair, cudaStream_t st) {
-  if (!pair) {
-    gemm_kernel<KIND, false><<<grid, KindTraits<KIND>::threads, KindTraits<KIND>::smem_bytes, st>>>(a);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(KindTraits<KIND>::threads);
-  cfg.dynamicSmemBytes = KindTraits<KIND>::smem_bytes;
-  cfg.stream = st;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, true>, a);
+cudaError_t gemm_launch(const GemmArgs& a, int grid, cudaStream_t st) {
+  gemm_kernel<KIND><<<grid, KindTraits<KIND>::threads, KindTraits<KIND>::smem_bytes, st>>>(a);
+  return cudaGetLastError();
 }
 
 template <int KIND>
 cudaError_t gemm_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       KindTraits<KIND>::smem_bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_kernel<KIND, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               KindTraits<KIND>::smem_bytes);
-}
-
-// Grid of the paired kernel: two CTAs per co-resident 2-CTA cluster (0 when
-// clusters of this kernel cannot be formed).
-template <int KIND>
-int gemm_pair_grid() {
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(KindTraits<KIND>::threads);
-  cfg.dynamicSmemBytes = KindTraits<KIND>::smem_bytes;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, true>, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  return 2 * n;
 }
 
 }  // namespace moe

@@ -11,12 +11,12 @@
 
 namespace moe {
 
-cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st) {
+cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, cudaStream_t st) {
   switch (kind) {
-    case kBwdU: return gemm_launch<kBwdU>(a, grid, pair, st);
-    case kBwdX: return gemm_launch<kBwdX>(a, grid, pair, st);
-    case kWgradD: return gemm_launch<kWgradD>(a, grid, pair, st);
-    default: return gemm_launch<kWgradGU>(a, grid, pair, st);
+    case kBwdU: return gemm_launch<kBwdU>(a, grid, st);
+    case kBwdX: return gemm_launch<kBwdX>(a, grid, st);
+    case kWgradD: return gemm_launch<kWgradD>(a, grid, st);
+    default: return gemm_launch<kWgradGU>(a, grid, st);
   }
 }
 cudaError_t prepare_gemm_bwd(int kind) {
@@ -27,13 +27,4 @@ cudaError_t prepare_gemm_bwd(int kind) {
     default: return gemm_prepare<kWgradGU>();
   }
 }
-int gemm_pair_grid_bwd(int kind) {
-  switch (kind) {
-    case kBwdU: return gemm_pair_grid<kBwdU>();
-    case kBwdX: return gemm_pair_grid<kBwdX>();
-    case kWgradD: return gemm_pair_grid<kWgradD>();
-    default: return gemm_pair_grid<kWgradGU>();
-  }
-}
-
 }  // namespace moe

@@ -8,10 +8,9 @@
 
 namespace moe {
 
-cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st) {
-  return kind == kUp ? gemm_launch<kUp>(a, grid, pair, st) : gemm_launch<kDown>(a, grid, pair, st);
+cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, cudaStream_t st) {
+  return kind == kUp ? gemm_launch<kUp>(a, grid, st) : gemm_launch<kDown>(a, grid, st);
 }
 cudaError_t prepare_gemm_fwd(int kind) { return kind == kUp ? gemm_prepare<kUp>() : gemm_prepare<kDown>(); }
-int gemm_pair_grid_fwd(int kind) { return kind == kUp ? gemm_pair_grid<kUp>() : gemm_pair_grid<kDown>(); }
 
 }  // namespace moe

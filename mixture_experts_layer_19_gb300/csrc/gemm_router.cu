@@ -25,9 +25,9 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, int grid, cud
 
 cudaError_t launch_gemm_router(int kind, const GemmArgs& a, int grid, cudaStream_t st) {
   switch (kind) {
-    case kRouter: return gemm_launch<kRouter>(a, grid, false, st);
-    case kRouterDX: return gemm_launch<kRouterDX>(a, grid, false, st);
-    default: return gemm_launch<kRouterDW>(a, grid, false, st);
+    case kRouter: return gemm_launch<kRouter>(a, grid, st);
+    case kRouterDX: return gemm_launch<kRouterDX>(a, grid, st);
+    default: return gemm_launch<kRouterDW>(a, grid, st);
   }
 }
 

@@ -41,15 +41,10 @@ cudaError_t launch_unpad_routing(const RoutingPtrs& rp, int R, int32_t* perm_out
 struct GemmArgs;
 // kind: 0 up (+SwiGLU), 1 down (gemm_fwd.cu); 2 bwd-u (+SwiGLU backward), 3 bwd-x, 4 wgrad down,
 // 5 wgrad gate/up (gemm_bwd.cu).  prepare_* raises the dynamic shared-memory limit.
-// pair: launch the 2-CTA-cluster variant (grid = gemm_pair_grid_*(kind), which
-// is 0 when such clusters cannot be formed); it needs an even tile count
-// along N for the grouped kinds.
-cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st);
+cudaError_t launch_gemm_fwd(int kind, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_gemm_fwd(int kind);
-int gemm_pair_grid_fwd(int kind);
-cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, bool pair, cudaStream_t st);
+cudaError_t launch_gemm_bwd(int kind, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_gemm_bwd(int kind);
-int gemm_pair_grid_bwd(int kind);
 // Expert parallelism over R virtual ranks on one GPU (ep.cu).  Cooperative
 // launches of R * G CTAs; ctr holds 3R + 1 flags, zero between launches.
 struct EpArgs {

@@ -1,8 +1,7 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers with bounded
 // waits, TMA (cp.async.bulk.tensor) loads/stores, and tcgen05 (TMEM alloc,
-// UMMA issue/commit, TMEM loads).  The multicast forms (TMA loads and UMMA
-// commits to both CTAs of a 2-CTA cluster) serve the paired bf16 GEMMs; they
-// only address this GPU's own memory.
+// UMMA issue/commit, TMEM loads).  Every copy and commit addresses the
+// issuing CTA's own shared memory and this GPU's own global memory.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -29,17 +28,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster (aligned: all threads of the CTA
-// execute it together).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -176,17 +164,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// 2-D tiled load multicast to every CTA of cta_mask: the box lands at the
-// same shared-memory offset in each, and each CTA's mbarrier at the offset of
-// `bar` receives the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, int32_t x, int32_t y,
-                                               uint64_t* bar, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
 // L2 prefetch of one 2-D box (no shared-memory destination, no completion
 // event): warms L2 ahead of the tma_load_2d of the same box.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y, uint64_t policy) {
@@ -286,14 +263,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
-// Commit whose arrival lands on the mbarrier at the same shared-memory offset
-// in every CTA of cta_mask (cluster multicast).
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(smem_u32(bar)), "h"(cta_mask)
-               : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

@@ -12,7 +12,11 @@
 // one file-scope device array instead.
 //
 // The array is kNoAllocScratchInts int32 (4 MiB) and every GPU that loads this
-// library keeps it until the process exits.  All calls share it and it keeps
+// library keeps it until the process exits.  With CUDA's lazy module loading
+// (the default) the array is committed when the module first loads on a
+// device, which can be this entry point's first call there; a caller whose
+// allocator reserves the device afterwards should make one warm-up call
+// first.  All calls share it and it keeps
 // the last call's contents; no entry is read before the same call writes it,
 // so nothing needs clearing between calls.  Calls that overlap on the GPU
 // (e.g. on two streams) race on it and must be serialised by the caller.
@@ -37,10 +41,13 @@ std::mutex g_scratch_mu;
 
 // Device address of g_route_scratch on `dev` (the current device).  In host
 // code the symbol is only a host-side stand-in, so the address is looked up
-// once per device and cached.
-cudaError_t scratch_for_device(int dev, int32_t** out) {
+// with the device current.  It is looked up again on every call made outside
+// a stream capture (a device reset reloads the module, which may move the
+// array); during a capture the address cached by an earlier call is used, so
+// the first call on a device must come before any capture.
+cudaError_t scratch_for_device(int dev, bool capturing, int32_t** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || !capturing) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess) return e;
@@ -87,8 +94,19 @@ extern "C" moe_status_t moe_route_noalloc(int64_t T, int32_t E, int32_t k, const
     set_error_detail("moe_route_noalloc: no usable current device");
     return MOE_ERR_CUDA;
   }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((err = cudaStreamIsCapturing(st, &cap)) != cudaSuccess) {
+    set_error_detail((std::string("moe_route_noalloc: cudaStreamIsCapturing: ") + cudaGetErrorString(err)).c_str());
+    return MOE_ERR_CUDA;
+  }
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  if (capturing && !g_scratch_addr[dev]) {
+    set_error_detail("moe_route_noalloc: the first call on a device must come before any stream capture");
+    return MOE_ERR_INVALID_ARG;
+  }
   int32_t* base = nullptr;
-  if ((err = scratch_for_device(dev, &base)) != cudaSuccess) {
+  if ((err = scratch_for_device(dev, capturing, &base)) != cudaSuccess) {
     set_error_detail((std::string("moe_route_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(err)).c_str());
     return MOE_ERR_CUDA;
   }
@@ -105,7 +123,9 @@ extern "C" moe_status_t moe_route_noalloc(int64_t T, int32_t E, int32_t k, const
   rp.totals = p;     p += round256(4);
   rp.dest = p;       p += round256(R);
   rp.perm_src = p;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // a launch error read below belongs to these launches, not to earlier work
+  // on this thread that left an error pending
+  (void)cudaGetLastError();
   if ((err = launch_router(logits, Ti, E, k, chunk_hist, rp, st)) != cudaSuccess ||
       (err = launch_scan(Ti, E, chunk_hist, chunk_base, rp, st)) != cudaSuccess ||
       (err = launch_permute(Ti, E, k, chunk_base, rp, st)) != cudaSuccess ||

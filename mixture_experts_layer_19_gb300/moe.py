@@ -24,7 +24,6 @@ MOE_DEBUG_IDENTITY_EXPERTS = 0x1
 MOE_DEBUG_TIMING = 0x2
 MOE_DEBUG_SEPARATE_KERNELS = 0x4
 MOE_DEBUG_RING_MEGAKERNEL = 0x8
-MOE_DEBUG_SINGLE_CTA = 0x10
 MOE_DEBUG_MULTI_LAUNCH = 0x20
 MOE_DEBUG_DUMP_QUANT = 0x40
 MOE_DEBUG_STALL_TEST = 0x80
@@ -332,11 +331,13 @@ class Plan:
         return st.value
 
     def info(self):
-        """Launch geometry: {"num_sms": n, "pair_grid": [6 grids of the paired GEMM kinds]}."""
+        """Launch geometry: {"num_sms": n, "movers": .., "ring_slots": .., "minibatch_tiles": ..,
+        "slot_tiles": ..} (the ring pipeline's shape, in 128-row tiles)."""
         n = ctypes.c_int32()
-        grids = (ctypes.c_int32 * 6)()
-        _check(lib().moe_plan_info(self.handle, ctypes.byref(n), grids), "moe_plan_info")
-        return {"num_sms": n.value, "pair_grid": list(grids)}
+        ring = (ctypes.c_int32 * 4)()
+        _check(lib().moe_plan_info(self.handle, ctypes.byref(n), ring), "moe_plan_info")
+        return {"num_sms": n.value, "movers": ring[0], "ring_slots": ring[1], "minibatch_tiles": ring[2],
+                "slot_tiles": ring[3]}
 
     def router_forward(self, X, Wr, logits=None, stream=None):
         """logits = X Wr^T (fp32) on the tensor cores."""

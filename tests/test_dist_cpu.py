@@ -6,8 +6,11 @@ pieces (barrier, max-over-ranks) and that sharding tokens across ranks is
 exact: concatenated per-rank outputs equal the single-batch oracle, and the
 weight gradients summed in rank order equal the single-batch ones.
 """
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import numpy as np
 import torch
@@ -75,3 +78,19 @@ def test_two_gloo_ranks():
     assert m == 2.5
     assert yerr == 0.0
     assert dwerr < 1e-13
+
+
+def test_bench_launches_its_own_ranks():
+    """`bench.py --gpus 2` outside any launcher starts two ranks itself
+    (torch.distributed.run on 127.0.0.1); the dry run exchanges their timings
+    over gloo and rank 0 alone prints one line with the max over ranks."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--dry-run"],
+                       capture_output=True, text=True, timeout=240, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2 and out["config"]["parallelism"] == "replicas2"
+    assert out["max_rank_ms"] >= 20.0          # rank 1 waits 20 ms, rank 0 10 ms: the max is taken

@@ -16,8 +16,8 @@ from tests.util import BF16_TOL, cpu_and_gpu_inputs, rel_err
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("flags", [0, moe.MOE_DEBUG_SINGLE_CTA], ids=["paired", "single_cta"])
-def test_stalled_producer_times_out_and_context_survives(flags):
+def test_stalled_producer_times_out_and_context_survives():
+    flags = 0
     T, d, F, E, k = 256, 512, 512, 8, 2
     g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=3)
     timeout_ns = 50_000_000

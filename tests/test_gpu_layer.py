@@ -167,23 +167,22 @@ def test_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers
 
 @pytest.mark.parametrize("case", [(700, 512, 512, 24, 4, 1.1), (300, 768, 768, 16, 3, 1.5), (64, 256, 512, 8, 2, 0.0)],
                          ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
-def test_paired_gemms_match_single_cta_bitwise(case):
-    """2-CTA clusters that share one operand tile per stage (B over two M tiles
-    of an expert, or A over two N tiles of an odd last M tile; the weight
-    gradients pair M tiles) compute every tile exactly as one CTA does.
-    d=768 / F=768 give odd N-tile counts, where those GEMMs stay single-CTA."""
+def test_schedules_match_bitwise_fwd_bwd(case):
+    """The default schedule, the separate kernels and the ring megakernel
+    compute every tile in the same fixed K order, so the whole forward and
+    backward agree bit for bit.  d=768 / F=768 give odd N-tile counts."""
     T, d, F, E, k, alpha = case
     g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=43, alpha=alpha)
-    pair = _plan(T, d, F, E, k)
-    one = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SINGLE_CTA)
+    dflt = _plan(T, d, F, E, k)
+    sep = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_SEPARATE_KERNELS)
     ring = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_RING_MEGAKERNEL)
     outs = []
-    for p in (pair, one, ring):
+    for p in (dflt, sep, ring):
         Y, s = p.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
         gr = p.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], s)
         outs.append((Y, gr))
     torch.cuda.synchronize()
-    assert all(p.device_status() == 0 for p in (pair, one, ring))
+    assert all(p.device_status() == 0 for p in (dflt, sep, ring))
     for Y, gr in outs[1:]:
         assert torch.equal(outs[0][0], Y)
         for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
@@ -319,8 +318,7 @@ def test_maximum_experts_and_top_k(prec):
             assert torch.equal(Y2, Y), flags
 
 
-@pytest.mark.parametrize("flags", [0, moe.MOE_DEBUG_SINGLE_CTA], ids=["paired", "single_cta"])
-def test_backward_reuses_sorted_x_only_for_its_own_forward(flags):
+def test_backward_reuses_sorted_x_only_for_its_own_forward():
     """The backward of the plan's last (separate-schedule) forward reads X's
     sorted rows left by that forward; after another forward on the plan it
     gathers them again.  Both must give the same gradients bit for bit."""
@@ -328,7 +326,7 @@ def test_backward_reuses_sorted_x_only_for_its_own_forward(flags):
     gA, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=41, alpha=1.1)
     gB, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=42, alpha=0.0)
     W = (gA["Wg"], gA["Wu"], gA["Wd"])
-    plan = _plan(T, d, F, E, k, flags)
+    plan = _plan(T, d, F, E, k, moe.MOE_DEBUG_SEPARATE_KERNELS)
     _, sA = plan.forward(gA["X"], gA["logits"], *W)
     reused = plan.backward(gA["dY"], gA["X"], *W, sA)
     _, sA2 = plan.forward(gA["X"], gA["logits"], *W)

@@ -19,7 +19,7 @@ import torch
 
 from mixture_experts_layer_19_gb300 import moe
 from oracle import moe_ref, mxfp8, nvfp4
-from tests.util import cpu_and_gpu_inputs, rel_err
+from tests.util import cpu_and_gpu_inputs, rel_err, rel_err_norm
 
 pytestmark = pytest.mark.gpu
 NV_TOL = 4e-2
@@ -147,6 +147,36 @@ def test_nvfp4_backward_parity(case):
     gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], moe_ref.stored_context(ctx))
     errs = {key: rel_err(out[key], gr[key]) for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")}
     assert all(v <= NV_TOL for v in errs.values()), errs
+    # the gradient of the plain quantised layer (a|b never rounded to bf16),
+    # normwise: E2M1 has one mantissa bit, so a code that flips between the two
+    # contexts moves single elements of dX and dW by a large step
+    gu = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    errs_u = {key: rel_err_norm(out[key], gu[key]) for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")}
+    assert all(v <= NV_TOL for v in errs_u.values()), errs_u
+
+
+@pytest.mark.parametrize("alpha", [0.0, 1.1, 1.5])
+def test_nvfp4_bitwise_deterministic_over_10_runs(alpha):
+    """Ten forward + backward runs give bitwise identical outputs, gradients
+    and routing buffers, for each routing skew."""
+    T, d, F, E, k = 512, 512, 512, 16, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=5, alpha=alpha)
+    plan = _nv_plan(T, d, F, E, k)
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    ref = None
+    for _ in range(10):
+        Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+        out = plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+        r = plan.routing(saved, T)
+        cur = [Y.clone()] + [out[n].clone() for n in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")] + \
+              [r[n].clone() for n in ("idx", "w", "perm_src", "dest")]
+        if ref is None:
+            ref = cur
+        else:
+            for a, b in zip(ref, cur):
+                assert torch.equal(a, b)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
 
 
 def test_nvfp4_bitwise_deterministic_and_empty_experts():

@@ -6,15 +6,18 @@ cannot create a plan, because moe_plan allocates.  This entry point keeps its
 scratch in a fixed array inside the library instead.  The test calls it
 through the C ABI twice in a row, with different shapes so the second call
 runs over the first call's leftovers, and checks both results against the
-routing moe_forward stores (read back with moe_get_routing).  Collected last
-on purpose.
+CPU oracle's routing and layout (bit-exact ids, counts, offsets, permutation
+and destinations; weights within 1e-6) and against the routing moe_forward
+stores (read back with moe_get_routing).  Collected last on purpose.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 from mixture_experts_layer_19_gb300 import moe
+from oracle import moe_ref
 from tests.util import cpu_and_gpu_inputs
 
 pytestmark = pytest.mark.gpu
@@ -46,12 +49,18 @@ def _plan_routing(T, d, E, k, X, logits):
 
 def test_noalloc_routing_matches_plan_routing_two_calls():
     for (T, d, E, k, alpha) in [(1000, 256, 32, 4, 1.1), (300, 256, 16, 2, 0.0)]:
-        g, _ = cpu_and_gpu_inputs(T, d, 256, E, k, seed=T, alpha=alpha)
+        g, h = cpu_and_gpu_inputs(T, d, 256, E, k, seed=T, alpha=alpha)
         got = _noalloc_routing(T, E, k, g["logits"])
         ref = _plan_routing(T, d, E, k, g["X"], g["logits"])
         torch.cuda.synchronize()
+        idx_o, w_o = moe_ref.route(h["logits"], k)
+        lay = moe_ref.layout(idx_o, E)
+        oracle = {"idx": idx_o, "counts": lay["counts"], "offsets": lay["offsets"],
+                  "perm_src": lay["perm_src"], "dest": lay["dest"]}
         for key in ("idx", "counts", "offsets", "perm_src", "dest"):
+            assert np.array_equal(got[key].cpu().numpy(), oracle[key]), key
             assert torch.equal(got[key], ref[key]), key
+        assert np.abs(got["w"].cpu().numpy() - w_o).max() <= 1e-6
         assert (got["w"] - ref["w"]).abs().max().item() <= 1e-6
 
 

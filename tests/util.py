@@ -16,6 +16,17 @@ def rel_err(gpu, ref):
     return float(np.abs(gpu - ref).max() / denom)
 
 
+def rel_err_norm(gpu, ref):
+    """Normwise relative error ||gpu - oracle||_2 / ||oracle||_2: the aggregate
+    drift of a whole tensor, insensitive to a single element whose quantised
+    code flips at a rounding boundary."""
+    gpu = to_f64(gpu) if isinstance(gpu, torch.Tensor) else np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    denom = np.linalg.norm(ref.ravel())
+    diff = np.linalg.norm((gpu - ref).ravel())
+    return float(diff if denom == 0 else diff / denom)
+
+
 def cpu_and_gpu_inputs(T, d, F, E, k, seed=0, alpha=0.0, logits_fn=None):
     inp = make_inputs(LayerShape(T, d, F, E, k), seed=seed, alpha=alpha, device="cpu")
     if logits_fn is not None:
