@@ -98,7 +98,9 @@ typedef struct {
   int32_t prec;           /* moe_precision_t (MOE_MXFP8 / MOE_NVFP4 need moe_quantize_weights) */
   int32_t minibatch_rows; /* rows per ring slot; 0 = two-wave floor (moe_minibatch_floor) */
   int32_t ring_slots;     /* ring buffer slots; 0 = default */
-  int32_t mover_ctas;     /* CTAs that gather (data movers); 0 = default */
+  int32_t mover_ctas;     /* CTAs given over to gathering rows into the ring (data movers);
+                             0 = default: the BF16 ring gathers with two extra warps of every
+                             compute CTA, the MXFP8 ring with 8 mover CTAs */
   int64_t wait_timeout_ns;/* bound on every device-side wait; 0 = 2e9 (2 s) */
   uint32_t debug_flags;   /* MOE_DEBUG_* */
   int32_t device;         /* CUDA device ordinal the plan binds to */
@@ -302,7 +304,8 @@ moe_status_t moe_kernel_times(moe_plan_t plan, const char** names, double* total
 
 /* Launch geometry the plan chose on this device: num_sms (the persistent
  * kernels' grid: one CTA per SM), and the ring pipeline's shape ring[4] =
- * {mover CTAs, ring slots, minimum minibatch in 128-row tiles (the two-wave
+ * {mover CTAs (0: mover warps inside the compute CTAs), ring slots, minimum
+ * minibatch in 128-row tiles (the two-wave
  * floor or minibatch_rows), largest minibatch in tiles (one slot)}.
  * Host-only; any pointer may be NULL. */
 moe_status_t moe_plan_info(moe_plan_t plan, int32_t* num_sms, int32_t* ring);

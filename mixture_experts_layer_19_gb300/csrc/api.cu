@@ -228,6 +228,7 @@ struct moe_plan_s {
   int* counters = nullptr;  // claim | gathered[NM] | mb_done[NM] | g1_done[NM]
   int32_t *mb_start = nullptr, *phase_start = nullptr, *n_mb = nullptr;
   int movers = 0, slots = 0, mbt = 0, cap = 0, nm_max = 0;
+  int mx_movers = 0;   // mover CTAs of the MXFP8 ring megakernel
   CUtensorMap m_ring_x, m_ring_h, m_ring_h_st;
   // one-launch forward: per-(token, 256-column block) arrival counts of the
   // in-kernel combine; grid-barrier arrivals and CTA exits (zero between launches)
@@ -494,15 +495,19 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   {
     // ring token buffer: `slots` slots of `cap` 128-row tiles; minibatches of
     // at least `mbt` tiles (the two-wave floor over the compute SMs)
-    p->movers = c.mover_ctas > 0 ? c.mover_ctas : 8;
+    // BF16: 0 mover CTAs by default (two mover warps in every compute CTA);
+    // the MXFP8 ring keeps dedicated mover CTAs
+    p->movers = c.mover_ctas > 0 ? c.mover_ctas : 0;
+    p->mx_movers = c.mover_ctas > 0 ? c.mover_ctas : 8;
     p->slots = c.ring_slots > 0 ? c.ring_slots : 4;
-    if (p->movers >= p->num_sms - 1 || p->slots < 2) {
+    if (p->mx_movers >= p->num_sms - 1 || p->slots < 2) {
       cudaFree(p->ws);
       delete p;
       return fail(MOE_ERR_INVALID_ARG, "moe_plan: need 2 <= ring_slots and mover_ctas < SM count - 1");
     }
     int64_t mb_rows = c.minibatch_rows;
-    if (mb_rows <= 0) moe_minibatch_floor(p->num_sms - p->movers, BM, 128, c.F, 2, &mb_rows);
+    if (mb_rows <= 0)
+      moe_minibatch_floor(p->num_sms - (c.prec == MOE_BF16 ? p->movers : p->mx_movers), BM, 128, c.F, 2, &mb_rows);
     p->mbt = (int)std::max<int64_t>(1, (mb_rows + BM - 1) / BM);
     p->cap = 2 * p->mbt;
     p->nm_max = (int)(p->Rpm / BM);
@@ -700,7 +705,7 @@ moe_status_t moe_plan_info(moe_plan_t p, int32_t* num_sms, int32_t* ring) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "moe_plan_info: null plan");
   if (num_sms) *num_sms = p->num_sms;
   if (ring) {
-    ring[0] = p->movers;
+    ring[0] = p->cfg.prec == MOE_BF16 ? p->movers : p->mx_movers;
     ring[1] = p->slots;
     ring[2] = p->mbt;
     ring[3] = p->cap;
@@ -860,7 +865,7 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     m.d = c.d;
     m.F = c.F;
     m.k = c.k;
-    m.movers = p->movers;
+    m.movers = p->mx_movers;
     m.slots = p->slots;
     m.slot_rows = p->cap * BM;
     err = timed_launch(p, "fwd_megakernel_mx", st, [&] { return launch_fwd_megakernel_mx(m, p->num_sms, st); });

@@ -40,20 +40,32 @@
 namespace moe {
 
 constexpr int kQueue = 4;          // tiles in flight between producer and consumers
-constexpr int kMegaThreads = 192;  // warp 0 producer, warp 1 MMA, warps 2..5 epilogue
-constexpr int kMegaStaging = 3 * kStageChunk;  // per epilogue warp
-constexpr int kMegaSmem = kStages * kStageBytes + 4 * kMegaStaging + 1024 + 512;
+// warp 0 claimer + producer, warp 1 MMA, warps 2..9 epilogue, warps 10..11
+// movers (when the ring has no dedicated mover CTAs).  A G1 tile's
+// SwiGLU epilogue (three stores per element) runs on warps 2..5, one per TMEM
+// lane quarter; a G2 tile's plain store is split over all eight, two per lane
+// quarter, each on half of the columns (the store-bound kind gets the most
+// store bandwidth, as in the separate down GEMM).
+constexpr int kMegaThreads = 384;
+constexpr int kMoverWarps = 2;              // mover warps of a compute CTA (warps 10, 11)
+constexpr int kMegaStagingA = 3 * kStageChunk;  // warps 2..5: a, b, h (G1); double buffer (G2)
+constexpr int kMegaStagingB = kStageChunk;      // warps 6..9: one buffer (G2 only)
+constexpr int kMegaSmem = kStages * kStageBytes + 4 * kMegaStagingA + 4 * kMegaStagingB + 1024 + 512;
+static_assert(kMegaSmem <= 232448, "shared memory per CTA");
+constexpr int kG1Warps = 4, kG2Warps = 8;   // epilogue warps that finish one G1 / G2 tile
 
 // One thread: cut the 128-row tiles into minibatches on expert boundaries
 // (>= mbt tiles when possible, <= cap tiles always; an expert larger than cap
 // is split into cap-sized pieces) and lay out the claim order's phase
 // boundaries.
-__device__ void cut_minibatches(const int32_t* mtile_off, int E, int mbt, int cap, int nt1, int nt2,
+// tiles[e]: the expert's 128-row tiles (shared memory, so the serial walk
+// does not wait on global loads).
+__device__ void cut_minibatches(const int* tiles, int E, int mbt, int cap, int nt1, int nt2,
                                 int32_t* mb_start, int32_t* phase_start, int32_t* n_mb) {
   int nb = 0, cur = 0, g = 0;
   mb_start[0] = 0;
   for (int e = 0; e < E; ++e) {
-    int t = mtile_off[e + 1] - mtile_off[e];
+    int t = tiles[e];
     while (t > 0) {
       if (cur + t <= cap) {
         cur += t;
@@ -100,24 +112,49 @@ __global__ void __launch_bounds__(1024) plan_minibatches_kernel(const int32_t* _
                                                                   int counters_len, int* counters,
                                                                   int32_t* mb_start, int32_t* phase_start,
                                                                   int32_t* n_mb) {
+  __shared__ int tiles[1024];
   for (int i = threadIdx.x; i < counters_len; i += blockDim.x) counters[i] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) tiles[e] = mtile_off[e + 1] - mtile_off[e];
+  __syncthreads();
   if (threadIdx.x != 0) return;
-  cut_minibatches(mtile_off, E, mbt, cap, nt1, nt2, mb_start, phase_start, n_mb);
+  cut_minibatches(tiles, E, mbt, cap, nt1, nt2, mb_start, phase_start, n_mb);
 }
 
 // ----------------------------------------------------------------------------
-// Mover CTA: pull minibatch rows into their ring slot (warp per row).
+// Mover CTA: pull minibatch rows into their ring slot.  Token rows travel as
+// whole-row bulk copies (cp.async.bulk) through shared-memory buffers: warps
+// 0..kMoverPipes-1 each run one pipeline (its lane 0 keeps up to nbuf - 1 row
+// loads in flight, storing each row into the slot as it lands); the other
+// warps write the slot's padding rows as zeros with plain stores.
 // ----------------------------------------------------------------------------
-__device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag) {
+constexpr int kMoverPipes = 3;
+constexpr int kMoverBufMax = 5;   // buffers per pipeline at most
+
+__device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag, uint8_t* buf_base, uint64_t* mbar) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int nvec = g.d / 8;
+  const uint32_t row_bytes = (uint32_t)g.d * 2;
   const int nt1 = g.F / 128, nt2 = g.d / BN;
+  // buffers per pipeline: the stage ring and staging area (kMegaSmem less the
+  // barrier block) hold kMoverPipes * nbuf rows
+  const int nbuf = min(kMoverBufMax, (int)((kStages * kStageBytes + 4 * kMegaStagingA + 4 * kMegaStagingB) /
+                                           (row_bytes * kMoverPipes)));
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
+  const bool pipe = warp < kMoverPipes && lane == 0;
+  uint8_t* bufs = buf_base + (size_t)warp * nbuf * row_bytes;
+  uint64_t* bar = mbar + warp * kMoverBufMax;
+  uint32_t phase = 0;   // bit b: parity of buffer b's next completion
+  if (pipe)
+    for (int b = 0; b < nbuf; ++b) mbar_init(&bar[b], 1);
+  fence_mbar_init();
+  __syncthreads();
+  const int npipes = g.movers * kMoverPipes, pid = blockIdx.x * kMoverPipes + warp;
+  const int nzw = g.movers * (nwarps - kMoverPipes), zid = blockIdx.x * (nwarps - kMoverPipes) + (warp - kMoverPipes);
   for (int mb = 0; mb < nmb; ++mb) {
     if (threadIdx.x == 0 && mb >= g.slots) {
       const int prev = mb - g.slots;
-      const int target = 4 * (g.mb_start[prev + 1] - g.mb_start[prev]) * (nt1 + nt2);
+      const int target = (g.mb_start[prev + 1] - g.mb_start[prev]) * (kG1Warps * nt1 + kG2Warps * nt2);
       wait_counter_geq(g.mb_done + prev, target, wc);
     }
     __syncthreads();
@@ -125,18 +162,116 @@ __device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag) {
     const int row_base = g.mb_start[mb] * BM;
     const int nrows = (g.mb_start[mb + 1] - g.mb_start[mb]) * BM;
     const size_t slot_base = (size_t)(mb % g.slots) * g.slot_rows;
-    for (int i = blockIdx.x * nwarps + warp; i < nrows; i += g.movers * nwarps) {
-      const int src = g.perm_src[row_base + i];
-      uint4* dst = g.ring_x + (slot_base + i) * nvec;
-      if (src < 0) {
-        for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-      } else {
-        const uint4* s = g.X + (size_t)(src / g.k) * nvec;
-        for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(s + v);
+    if (pipe) {
+      // step j stores this pipeline's row j - (nbuf - 1) (if any) and loads its
+      // row j into buffer j % nbuf; that buffer's previous row was stored one
+      // step earlier, so at most one younger store may still be reading
+      int ld_i = pid, st_i = pid;          // next candidate row (slot-relative) to load / store
+      int dst[kMoverBufMax];
+      bool ok = true;
+      for (int j = 0;; ++j) {
+        const int s = j - (nbuf - 1);
+        bool any = false;
+        if (s >= 0) {
+          while (st_i < nrows && g.perm_src[row_base + st_i] < 0) st_i += npipes;
+          if (st_i < nrows) {
+            const int b = s % nbuf;
+            if (!mbar_wait(&bar[b], (phase >> b) & 1u, wc)) { ok = false; break; }
+            phase ^= 1u << b;
+            bulk_store_1d(g.ring_x + (slot_base + dst[b]) * nvec, bufs + (size_t)b * row_bytes, row_bytes);
+            bulk_commit();
+            st_i += npipes;
+            any = true;
+          }
+        }
+        while (ld_i < nrows && g.perm_src[row_base + ld_i] < 0) ld_i += npipes;
+        if (ld_i < nrows) {
+          const int b = j % nbuf;
+          bulk_wait_read<1>();
+          const int src = g.perm_src[row_base + ld_i];
+          dst[b] = ld_i;
+          mbar_arrive_expect_tx(&bar[b], row_bytes);
+          bulk_load_1d(bufs + (size_t)b * row_bytes, g.X + (size_t)(src / g.k) * nvec, row_bytes, &bar[b]);
+          ld_i += npipes;
+          any = true;
+        }
+        if (!any && s >= 0) break;
+      }
+      if (!ok) {
+        // abort: let every issued load land before the CTA may exit
+        for (int b = 0; b < nbuf; ++b)
+          for (uint64_t t0 = globaltimer_ns(); !mbar_try_wait(&bar[b], (phase >> b) & 1u);)
+            if (globaltimer_ns() - t0 > 50000000ull) break;
+      }
+      bulk_wait<0>();   // the slot rows are written, not only read out of shared memory
+    } else if (warp >= kMoverPipes) {
+      for (int i = zid; i < nrows; i += nzw) {
+        if (g.perm_src[row_base + i] >= 0) continue;
+        uint4* d = g.ring_x + (slot_base + i) * nvec;
+        for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
       }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+      __threadfence();
+      fence_proxy_async_global();
+      red_release_gpu_add(g.gathered + mb, 1);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// The default: no mover CTAs; warps 10..11 of every compute CTA pull the rows
+// (the pull-dispatch residue), so every SM also computes.  Mover warp w of
+// CTA c copies the minibatch's rows i = (2c + w) + j * 2 * gridDim.x, each
+// row by the whole warp with kCopyUnroll 16-byte loads in flight per lane;
+// padding rows are written as zeros.
+// ----------------------------------------------------------------------------
+constexpr int kCopyUnroll = 8;
+
+__device__ void mover_warps(const MegaArgs& g, int nmb, int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = g.d / 8;
+  const int nt1 = g.F / 128, nt2 = g.d / BN;
+  WaitCtl wc{g.status, abort_flag, g.timeout_ns};
+  const int nw = gridDim.x * kMoverWarps, wid = blockIdx.x * kMoverWarps + (warp - 10);
+  for (int mb = 0; mb < nmb; ++mb) {
+    if (mb >= g.slots) {
+      int ok = 1;
+      if (lane == 0) {
+        const int prev = mb - g.slots;
+        const int target = (g.mb_start[prev + 1] - g.mb_start[prev]) * (kG1Warps * nt1 + kG2Warps * nt2);
+        ok = wait_counter_geq(g.mb_done + prev, target, wc) ? 1 : 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    }
+    const int row_base = g.mb_start[mb] * BM;
+    const int nrows = (g.mb_start[mb + 1] - g.mb_start[mb]) * BM;
+    const size_t slot_base = (size_t)(mb % g.slots) * g.slot_rows;
+    for (int i = wid; i < nrows; i += nw) {
+      const int src = g.perm_src[row_base + i];
+      uint4* dst = g.ring_x + (slot_base + i) * nvec;
+      if (src < 0) {
+        for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const uint4* sp = g.X + (size_t)(src / g.k) * nvec;
+      for (int v0 = 0; v0 < nvec; v0 += 32 * kCopyUnroll) {
+        uint4 r[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) r[u] = __ldg(sp + v);
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) dst[v] = r[u];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
       __threadfence();
       fence_proxy_async_global();
       red_release_gpu_add(g.gathered + mb, 1);
@@ -198,8 +333,11 @@ __device__ bool route_in_kernel(const MegaArgs& g, int* scratch, const WaitCtl& 
   // S2a + minibatch plan (one CTA)
   if (blockIdx.x == 0) {
     scan_experts(g.chunk_hist, g.chunk_base, nch, g.E, g.rp, scratch);
+    int* tiles = scratch + g.E;    // scan_experts leaves the counts in scratch[0, E)
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) tiles[e] = (scratch[e] + BM - 1) / BM;
+    __syncthreads();
     if (threadIdx.x == 0)
-      cut_minibatches(g.rp.mtile_off, g.E, g.mbt, g.cap, g.F / 128, nt2, g.mb_start, g.phase_start, g.n_mb);
+      cut_minibatches(tiles, g.E, g.mbt, g.cap, g.F / 128, nt2, g.mb_start, g.phase_start, g.n_mb);
   }
   if (!grid_sync(g, 2, wc, flag)) return false;
   // S2b: one warp per chunk
@@ -223,7 +361,9 @@ __device__ __forceinline__ void combine_arrivals(const MegaArgs& g, int srow, in
   if (src >= 0) {
     t = src / g.k;
     __threadfence();
-    last = atom_add_acq_rel_gpu(g.tok_cnt + (size_t)t * nt2 + nt, 1) == g.k - 1;
+    // two warps store each row's 256-column block (one half each): the
+    // block is complete at 2k arrivals
+    last = atom_add_acq_rel_gpu(g.tok_cnt + (size_t)t * nt2 + nt, 1) == 2 * g.k - 1;
   }
   unsigned m = __ballot_sync(0xffffffffu, last);
   const int nvec = g.d / 8;
@@ -282,7 +422,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
   uint8_t* staging_base = smem + kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(staging_base + 4 * kMegaStaging);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging_base + 4 * kMegaStagingA + 4 * kMegaStagingB);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -306,7 +446,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
   }
   const int nmb = *g.n_mb;
   if ((int)blockIdx.x < g.movers) {
-    mover_loop(g, nmb, abort_flag);
+    mover_loop(g, nmb, abort_flag, stage_base, bars);
     if (FUSED) {
       __syncthreads();
       if (threadIdx.x == 0) fused_exit(g);
@@ -320,11 +460,11 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kG2Warps);   // every epilogue warp arrives once per tile
     }
     for (int q = 0; q < kQueue; ++q) {
       mbar_init(&qfull[q], 1);
-      mbar_init(&qempty[q], 5);  // MMA thread + 4 epilogue warps
+      mbar_init(&qempty[q], 1 + kG2Warps);  // MMA thread + 8 epilogue warps
     }
     fence_mbar_init();
   }
@@ -339,25 +479,35 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
   const int nt1 = g.F / 128;
   const int total = g.phase_start[2 * nmb];
+  // a minibatch is gathered once every mover CTA, or every mover warp, has
+  // signalled it
+  const int gathered_target = g.movers > 0 ? g.movers : (int)gridDim.x * kMoverWarps;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------- claimer + producer
-      const uint64_t pol_w = policy_evict_first();
+      // weights evict_last: the M tiles of a minibatch re-read each weight
+      // tile, from CTAs that claim them at slightly different times
+      const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_a = policy_evict_last();
       uint32_t s = 0, ph = 0, qi = 0, qph = 0, issued_mask = 0, last_par = 0;
       bool ok = true;
+      // the next claim is taken while the current item's stages load, and
+      // decoded right after them, so neither sits between two items' stages
+      int c = atomicAdd(g.claim, 1);
+      Item nxt;
+      nxt.kind = -1;
+      if (c < total) nxt = decode_claim(g, nmb, c);
       while (ok) {
-        const int c = atomicAdd(g.claim, 1);
-        Item it;
-        if (c >= total) {
-          it.kind = -1;
-        } else {
-          it = decode_claim(g, nmb, c);
-          ok = it.kind == 0 ? wait_counter_geq(g.gathered + it.mb, g.movers, wc)
-                            : wait_counter_geq(g.g1_done + it.gt, 4 * nt1, wc);
+        Item it = nxt;
+        const int c_next = c < total ? atomicAdd(g.claim, 1) : total;
+        if (c < total) {
+          ok = it.kind == 0 ? wait_counter_geq(g.gathered + it.mb, gathered_target, wc)
+                            : wait_counter_geq(g.g1_done + it.gt, kG1Warps * nt1, wc);
           fence_proxy_async_global();
           if (!ok) it.kind = -1;
+        } else {
+          it.kind = -1;
         }
         if (!mbar_wait(&qempty[qi], qph ^ 1, wc)) break;
         queue[qi] = it;
@@ -383,6 +533,8 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
           last_par = (last_par & ~(1u << s)) | (ph << s);
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
+        c = c_next;
+        if (c < total) nxt = decode_claim(g, nmb, c);
       }
       if (!ok) {
         for (int st = 0; st < kStages; ++st) {
@@ -427,10 +579,16 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
         if (acc == 0) aph ^= 1;
       }
     }
+  } else if (warp >= 10) {
+    // ------------------------------------------------- movers (no mover CTAs)
+    if (g.movers == 0) mover_warps(g, nmb, abort_flag);
   } else {
     // ------------------------------------------------- epilogue
-    const int q = warp & 3;
-    uint8_t* stg = staging_base + (warp - 2) * kMegaStaging;
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const bool g1_warp = warp < 2 + kG1Warps;  // warps 2..5 also run the SwiGLU epilogue
+    const int c0 = ((warp - 2) >> 2) * 4;      // G2: this warp's four 32-column chunks
+    uint8_t* stg = g1_warp ? staging_base + (warp - 2) * kMegaStagingA
+                           : staging_base + kG1Warps * kMegaStagingA + (warp - 2 - kG1Warps) * kMegaStagingB;
     uint32_t acc = 0, aph = 0, qi = 0, qph = 0;
     int chunk_ctr = 0;
     for (;;) {
@@ -445,7 +603,12 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN;
       const int srow = it.gt * BM + 32 * q;        // sorted padded row of this warp's slab
       const int rrow = it.ring_row0 + 32 * q;      // ring row of this warp's slab
-      if (it.kind == 0) {
+      if (it.kind == 0 && !g1_warp) {
+        // a G1 tile is drained by warps 2..5; the others only release it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else if (it.kind == 0) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ra[32], rb[32];
@@ -481,11 +644,11 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c0; c < c0 + 4; ++c) {
           uint32_t rv[32];
           tmem_ld32(tbase + c * 32, rv);
           tmem_ld_wait();
-          if (c == 7) {
+          if (c == c0 + 3) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -493,8 +656,13 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rv[i]);
-          uint8_t* buf = stg + (chunk_ctr & 1) * kStageChunk;
-          if (lane == 0) bulk_wait_read<1>();
+          uint8_t* buf = stg;
+          if (g1_warp) {                 // double buffer
+            buf += (chunk_ctr & 1) * kStageChunk;
+            if (lane == 0) bulk_wait_read<1>();
+          } else if (lane == 0) {
+            bulk_wait_read<0>();
+          }
           __syncwarp();
           stage_row(buf, lane, v);
           fence_proxy_async_smem();
@@ -508,12 +676,25 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1;
-      // results visible before the hand-off counters move
-      if (lane == 0) {
-        bulk_wait<0>();
-        fence_proxy_async_global();
-        if (it.kind == 0) red_release_gpu_add(g.g1_done + it.gt, 1);
-        red_release_gpu_add(g.mb_done + it.mb, 1);
+      // hand-off counters.  A G1 tile's h rows must be complete before a G2
+      // tile reads them, and a G2 tile's y rows before the in-kernel combine
+      // reads them; a ring slot is free once every tile of its minibatch has
+      // been drained (their MMAs have read the slot).
+      if (it.kind == 0 && g1_warp) {
+        if (lane == 0) {
+          bulk_wait<0>();
+          fence_proxy_async_global();
+          red_release_gpu_add(g.g1_done + it.gt, 1);
+          red_release_gpu_add(g.mb_done + it.mb, 1);
+        }
+      } else if (it.kind == 1) {
+        if (lane == 0) {
+          if (FUSED) {
+            bulk_wait<0>();
+            fence_proxy_async_global();
+          }
+          red_release_gpu_add(g.mb_done + it.mb, 1);
+        }
       }
       __syncwarp();
       if (FUSED && it.kind == 1) combine_arrivals(g, srow, it.nt, lane);

@@ -297,6 +297,13 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// 1-D bulk copy shared -> global (bulk-group completion; 16-byte aligned
+// addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 // Descriptor of a 32-row x 16-byte shared-memory block without swizzle (one
 // scale-factor atom): 8-row core matrices of 128 contiguous bytes.
 __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr) {

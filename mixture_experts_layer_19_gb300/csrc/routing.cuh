@@ -88,9 +88,17 @@ __device__ __forceinline__ void scan_experts(const int32_t* chunk_hist, int32_t*
                                              const RoutingPtrs& rp, int* s_cnt) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int cnt = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      chunk_base[(size_t)c * E + e] = cnt;
-      cnt += chunk_hist[(size_t)c * E + e];
+    // eight chunk counts loaded before any running sum is stored, so the
+    // loads overlap instead of each waiting behind the previous store
+    for (int c0 = 0; c0 < nchunks; c0 += 8) {
+      int h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h[u] = c0 + u < nchunks ? chunk_hist[(size_t)(c0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < nchunks) chunk_base[(size_t)(c0 + u) * E + e] = cnt;
+        cnt += h[u];
+      }
     }
     s_cnt[e] = cnt;
   }
