@@ -224,15 +224,16 @@ struct moe_plan_s {
   // ring-buffer forward megakernel (BF16): ring slots of X and h rows, GPU-local
   // hand-off counters, minibatch table
   void* ring_ws = nullptr;
-  void *ring_x = nullptr, *ring_h = nullptr;
+  void* ring_h = nullptr;   // BF16 ring: slots of h rows (X rows go to their sorted rows in Xg)
   int* counters = nullptr;  // claim | gathered[NM] | mb_done[NM] | g1_done[NM]
   int32_t *mb_start = nullptr, *phase_start = nullptr, *n_mb = nullptr;
   int movers = 0, slots = 0, mbt = 0, cap = 0, nm_max = 0;
   int mx_movers = 0;   // mover CTAs of the MXFP8 ring megakernel
-  CUtensorMap m_ring_x, m_ring_h, m_ring_h_st;
+  CUtensorMap m_ring_h, m_ring_h_st;
   // one-launch forward: per-(token, 256-column block) arrival counts of the
   // in-kernel combine; grid-barrier arrivals and CTA exits (zero between launches)
   int* tok_cnt = nullptr;
+  int* tok_u = nullptr;   // backward megakernel: <u, h> partials stored per token
   unsigned long long* gbar = nullptr;
   // router GEMM backward: dlogits in bf16 [T_max, E]
   void* dlg_bf16 = nullptr;
@@ -324,7 +325,7 @@ MegaArgs mega_args(moe_plan_s* p, const RoutingPtrs& rp, const void* X, const CU
   const moe_config_t& c = p->cfg;
   MegaArgs m;
   memset(&m, 0, sizeof(m));
-  m.mapXr = p->m_ring_x;
+  m.mapXr = p->m_Xg_k;
   m.mapWg = p->m_Wg_k;
   m.mapWu = p->m_Wu_k;
   m.mapWd = p->m_Wd_k;
@@ -333,7 +334,7 @@ MegaArgs mega_args(moe_plan_s* p, const RoutingPtrs& rp, const void* X, const CU
   m.mapABSt = m_ab_st;
   m.mapYsSt = p->m_Ys_st;
   m.X = reinterpret_cast<const uint4*>(X);
-  m.ring_x = reinterpret_cast<uint4*>(p->ring_x);
+  m.xg = reinterpret_cast<uint4*>(p->Xg);
   m.perm_src = rp.perm_src;
   m.mtile_off = rp.mtile_off;
   m.mb_start = p->mb_start;
@@ -513,7 +514,6 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->nm_max = (int)(p->Rpm / BM);
     const size_t slot_rows = (size_t)p->cap * BM;
     size_t m = 0;
-    const size_t o_rx = m; m += align256(p->slots * slot_rows * c.d * 2);
     const size_t o_rh = m; m += align256(p->slots * slot_rows * c.F * 2);
     const size_t o_ct = m; m += align256((1 + 3 * (size_t)p->nm_max) * 4);
     const size_t o_mb = m; m += align256(((size_t)p->nm_max + 1) * 4);
@@ -521,6 +521,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     const size_t o_nm = m; m += 256;
     const size_t o_gb = m; m += 256;
     const size_t o_tc = m; m += align256((size_t)c.T_max * (c.d / BN) * 4);
+    const size_t o_tu = m; m += align256((size_t)c.T_max * 4);
     err = cudaMalloc(&p->ring_ws, m);
     if (err != cudaSuccess) {
       cudaFree(p->ws);
@@ -528,7 +529,6 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
       return fail(MOE_ERR_OOM, std::string("moe_plan: cudaMalloc of ring buffer failed: ") + cudaGetErrorString(err));
     }
     char* rb = static_cast<char*>(p->ring_ws);
-    p->ring_x = rb + o_rx;
     p->ring_h = rb + o_rh;
     p->counters = reinterpret_cast<int*>(rb + o_ct);
     p->mb_start = reinterpret_cast<int32_t*>(rb + o_mb);
@@ -536,6 +536,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     p->n_mb = reinterpret_cast<int32_t*>(rb + o_nm);
     p->gbar = reinterpret_cast<unsigned long long*>(rb + o_gb);
     p->tok_cnt = reinterpret_cast<int*>(rb + o_tc);
+    p->tok_u = reinterpret_cast<int*>(rb + o_tu);
     err = cudaMemset(p->gbar, 0, 2 * sizeof(unsigned long long));
     if (err != cudaSuccess) {
       cudaFree(p->ring_ws);
@@ -544,9 +545,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
       return cuda_fail(err, "moe_plan: cudaMemset of the grid-barrier counter");
     }
     const uint64_t ring_rows = p->slots * slot_rows;
-    ok = map_kmajor(&p->m_ring_x, p->ring_x, c.d, ring_rows) && map_kmajor(&p->m_ring_h, p->ring_h, c.F, ring_rows) &&
-         map_store(&p->m_ring_h_st, p->ring_h, c.F, ring_rows);
+    ok = map_kmajor(&p->m_ring_h, p->ring_h, c.F, ring_rows) && map_store(&p->m_ring_h_st, p->ring_h, c.F, ring_rows);
     err = prepare_fwd_megakernel();
+    if (err == cudaSuccess) err = prepare_bwd_megakernel();
     if (!ok || err != cudaSuccess) {
       cudaFree(p->ring_ws);
       cudaFree(p->ws);
@@ -807,6 +808,9 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     m.cap = p->cap;
     err = timed_launch(p, "fwd_megakernel", st, [&] { return launch_fwd_megakernel(m, p->num_sms, true, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: one-launch megakernel launch");
+    p->xg_X = X;   // the movers left X's sorted rows in Xg
+    p->xg_saved = saved;
+    p->xg_T = T;
     return MOE_OK;
   }
   err = timed_launch(p, "router_topk_hist", st,
@@ -946,6 +950,9 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     err = timed_launch(p, "combine", st,
                        [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: combine launch");
+    p->xg_X = X;
+    p->xg_saved = saved;
+    p->xg_T = T;
     return MOE_OK;
   }
   err = timed_launch(p, "gather", st, [&] {
@@ -1036,6 +1043,9 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(saved) + L.ab);
 
   const bool ep = c.ep_ranks >= 2;
+  // BF16 ring schedule: the backward's expert part as one persistent launch
+  const bool ring_bwd = !ep && c.prec == MOE_BF16 && (c.debug_flags & MOE_DEBUG_RING_MEGAKERNEL) &&
+                        !(c.debug_flags & MOE_DEBUG_SEPARATE_KERNELS);
   err = cudaSuccess;  // block-scaled plans gather no bf16 rows here (their dgrad and wgrad operands are quantised)
   if (ep) {  // pull reverse-combine: each expert rank pulls the dY and X rows of its pairs
     EpArgs ea = ep_args(p, rp, T);
@@ -1044,6 +1054,59 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     ea.Xg = static_cast<uint4*>(p->Xg);
     ea.dYg = static_cast<uint4*>(p->dYg);
     err = timed_launch(p, "ep_pull_reverse_combine", st, [&] { return launch_ep_pull(ea, st); });
+  } else if (ring_bwd) {
+    // B1-B4 and B6 in one persistent launch: movers pull the dY rows (and the
+    // X rows unless the plan's last forward left them in place), u GEMM +
+    // SwiGLU backward and dx GEMM tiles minibatch by minibatch, the dX sums
+    // and the router gradient as their last inputs land
+    const bool xg_current = p->xg_X == X && p->xg_saved == saved && p->xg_T == T;
+    BwdMegaArgs m;
+    memset(&m, 0, sizeof(m));
+    m.mapU_A = p->m_dYg_k;
+    m.mapU_B = p->m_Wd_mn;
+    m.mapX_A = p->m_dAB_k;
+    m.mapX_Bg = p->m_Wg_mn;
+    m.mapX_Bu = p->m_Wu_mn;
+    m.mapDabSt = p->m_dAB_st;
+    m.mapWhSt = p->m_wH_st;
+    m.mapYsSt = p->m_Ys_st;
+    m.dY = reinterpret_cast<const uint4*>(dY);
+    m.X = reinterpret_cast<const uint4*>(X);
+    m.dYg = static_cast<uint4*>(p->dYg);
+    m.Xg = xg_current ? nullptr : static_cast<uint4*>(p->Xg);
+    m.ab = ab;
+    m.rp = rp;
+    m.dgp = p->dgp;
+    m.dg = dg;
+    m.dlogits = dlogits;
+    m.Ys = static_cast<const uint4*>(p->Ys);
+    m.dX = static_cast<uint4*>(dX);
+    m.mtile_off = rp.mtile_off;
+    m.mb_start = p->mb_start;
+    m.phase_start = p->phase_start;
+    m.n_mb = p->n_mb;
+    m.counters = p->counters;
+    m.counters_len = 1 + 2 * p->nm_max;
+    m.tok_dx = p->tok_cnt;
+    m.tok_u = p->tok_u;
+    m.gbar = p->gbar;
+    m.status = p->status;
+    m.timeout_ns = (uint64_t)c.wait_timeout_ns;
+    m.E = c.E;
+    m.d = c.d;
+    m.F = c.F;
+    m.k = c.k;
+    m.T = Ti;
+    m.mbt = p->mbt;
+    m.cap = p->cap;
+    m.nm_max = p->nm_max;
+    m.slots = 1;
+    m.slot_rows = 0;
+    err = timed_launch(p, "bwd_megakernel", st, [&] { return launch_bwd_megakernel(m, p->num_sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: backward megakernel launch");
+    p->xg_X = X;   // the sorted X rows are in place now
+    p->xg_saved = saved;
+    p->xg_T = T;
   } else if (c.prec == MOE_BF16) {
     // X's sorted rows are still in Xg when this is the backward of the plan's
     // last forward, which ran the separate schedule: gather dY alone then
@@ -1118,7 +1181,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
                        [&] { return launch_gemm_mx(kBwdX, x, p->num_sms, st, nv); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled dx GEMM launch");
   }
-  if (!mx) {
+  if (!mx && !ring_bwd) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dYg_k;
     a.mapB0 = p->m_Wd_mn;
@@ -1132,7 +1195,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
                        [&] { return launch_gemm_bwd(kBwdU, a, gemm_grid(p), st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: u GEMM launch");
   }
-  if (!mx) {
+  if (!mx && !ring_bwd) {
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_dAB_k;
     a.mapB0 = p->m_Wg_mn;
@@ -1154,7 +1217,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     ea.dlogits = dlogits;
     err = timed_launch(p, "ep_push_reverse_dispatch", st, [&] { return launch_ep_push(ea, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: EP reverse-dispatch launch");
-  } else {
+  } else if (!ring_bwd) {
     const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
     err = timed_launch(p, "reduce_dx", st,
                        [&] { return launch_combine(p->Ys, rp.dest, nullptr, Ti, c.k, c.d, dX, cgrid, st); });

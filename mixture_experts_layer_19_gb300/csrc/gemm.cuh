@@ -244,6 +244,16 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const float* v
   }
 }
 
+// The same for 32 values already packed as 16 bf16 pairs.
+__device__ __forceinline__ void stage_row_packed(uint8_t* buf, int lane, const uint32_t* p) {
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 q = make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+    *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ sw) << 4)) = q;
+  }
+}
+
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll

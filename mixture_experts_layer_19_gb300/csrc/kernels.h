@@ -121,6 +121,11 @@ cudaError_t launch_plan_minibatches(const int32_t* mtile_off, int E, int mbt, in
                                     int32_t* n_mb, cudaStream_t st);
 cudaError_t launch_fwd_megakernel(const MegaArgs& a, int grid, bool fused, cudaStream_t st);  // fused: one-launch forward
 cudaError_t prepare_fwd_megakernel();
+// Backward megakernel (megakernel_bwd.cu): B1-B4 and B6 of the BF16 layer in
+// one cooperative launch over the saved layout (grid = one CTA per SM).
+struct BwdMegaArgs;
+cudaError_t launch_bwd_megakernel(const BwdMegaArgs& a, int grid, cudaStream_t st);
+cudaError_t prepare_bwd_megakernel();
 struct MegaMxArgs;
 cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_fwd_megakernel_mx();

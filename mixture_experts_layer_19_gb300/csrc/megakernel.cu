@@ -15,8 +15,10 @@
 //    side of minibatch i overlaps the dispatch of minibatch i+1, with no CPU
 //    in the loop and no allocation inside the layer.
 //
-// Here (one GPU): mover CTAs pull the routed token rows of minibatch i into
-// ring slot i % S (the local form of pull dispatch).  Compute CTAs claim tiles
+// Here (one GPU): movers pull the routed token rows of minibatch i into their
+// sorted rows (the local form of pull dispatch; the backward's weight
+// gradients read the same rows, so they are not recycled), and ring slot
+// i % S holds the minibatch's h rows between its two GEMMs.  Compute CTAs claim tiles
 // from one global order -- G1(0), G1(1), G2(0), G1(2), G2(1), ... -- where
 // G1(i) are the [a|b] = x [Wg;Wu]^T + SwiGLU tiles of minibatch i (h goes back
 // into the slot, a|b to the saved context) and G2(i) the y = h Wd^T tiles (y to
@@ -53,54 +55,6 @@ constexpr int kMegaStagingB = kStageChunk;      // warps 6..9: one buffer (G2 on
 constexpr int kMegaSmem = kStages * kStageBytes + 4 * kMegaStagingA + 4 * kMegaStagingB + 1024 + 512;
 static_assert(kMegaSmem <= 232448, "shared memory per CTA");
 constexpr int kG1Warps = 4, kG2Warps = 8;   // epilogue warps that finish one G1 / G2 tile
-
-// One thread: cut the 128-row tiles into minibatches on expert boundaries
-// (>= mbt tiles when possible, <= cap tiles always; an expert larger than cap
-// is split into cap-sized pieces) and lay out the claim order's phase
-// boundaries.
-// tiles[e]: the expert's 128-row tiles (shared memory, so the serial walk
-// does not wait on global loads).
-__device__ void cut_minibatches(const int* tiles, int E, int mbt, int cap, int nt1, int nt2,
-                                int32_t* mb_start, int32_t* phase_start, int32_t* n_mb) {
-  int nb = 0, cur = 0, g = 0;
-  mb_start[0] = 0;
-  for (int e = 0; e < E; ++e) {
-    int t = tiles[e];
-    while (t > 0) {
-      if (cur + t <= cap) {
-        cur += t;
-        g += t;
-        t = 0;
-        if (cur >= mbt) {
-          mb_start[++nb] = g;
-          cur = 0;
-        }
-      } else if (cur > 0) {
-        mb_start[++nb] = g;
-        cur = 0;
-      } else {
-        g += cap;
-        t -= cap;
-        mb_start[++nb] = g;
-      }
-    }
-  }
-  if (cur > 0) mb_start[++nb] = g;
-  *n_mb = nb;
-  // phases: G1(0), [G1(i), G2(i-1)] for i = 1..nb-1, G2(nb-1)
-  int acc = 0, p = 0;
-  phase_start[p++] = 0;
-  for (int i = 0; i <= nb; ++i) {
-    if (i < nb) {  // G1(i)
-      acc += (mb_start[i + 1] - mb_start[i]) * nt1;
-      phase_start[p++] = acc;
-    }
-    if (i >= 1) {  // G2(i-1)
-      acc += (mb_start[i] - mb_start[i - 1]) * nt2;
-      phase_start[p++] = acc;
-    }
-  }
-}
 
 // ----------------------------------------------------------------------------
 // Plan: zero the counters, cut minibatches on expert boundaries (>= mbt tiles
@@ -152,16 +106,11 @@ __device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag, uint8_t*
   const int npipes = g.movers * kMoverPipes, pid = blockIdx.x * kMoverPipes + warp;
   const int nzw = g.movers * (nwarps - kMoverPipes), zid = blockIdx.x * (nwarps - kMoverPipes) + (warp - kMoverPipes);
   for (int mb = 0; mb < nmb; ++mb) {
-    if (threadIdx.x == 0 && mb >= g.slots) {
-      const int prev = mb - g.slots;
-      const int target = (g.mb_start[prev + 1] - g.mb_start[prev]) * (kG1Warps * nt1 + kG2Warps * nt2);
-      wait_counter_geq(g.mb_done + prev, target, wc);
-    }
     __syncthreads();
     if (*abort_flag) return;
     const int row_base = g.mb_start[mb] * BM;
     const int nrows = (g.mb_start[mb + 1] - g.mb_start[mb]) * BM;
-    const size_t slot_base = (size_t)(mb % g.slots) * g.slot_rows;
+    const size_t slot_base = (size_t)row_base;   // sorted rows of the minibatch
     if (pipe) {
       // step j stores this pipeline's row j - (nbuf - 1) (if any) and loads its
       // row j into buffer j % nbuf; that buffer's previous row was stored one
@@ -178,7 +127,7 @@ __device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag, uint8_t*
             const int b = s % nbuf;
             if (!mbar_wait(&bar[b], (phase >> b) & 1u, wc)) { ok = false; break; }
             phase ^= 1u << b;
-            bulk_store_1d(g.ring_x + (slot_base + dst[b]) * nvec, bufs + (size_t)b * row_bytes, row_bytes);
+            bulk_store_1d(g.xg + (slot_base + dst[b]) * nvec, bufs + (size_t)b * row_bytes, row_bytes);
             bulk_commit();
             st_i += npipes;
             any = true;
@@ -207,7 +156,7 @@ __device__ void mover_loop(const MegaArgs& g, int nmb, int* abort_flag, uint8_t*
     } else if (warp >= kMoverPipes) {
       for (int i = zid; i < nrows; i += nzw) {
         if (g.perm_src[row_base + i] >= 0) continue;
-        uint4* d = g.ring_x + (slot_base + i) * nvec;
+        uint4* d = g.xg + (slot_base + i) * nvec;
         for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
       }
     }
@@ -236,21 +185,12 @@ __device__ void mover_warps(const MegaArgs& g, int nmb, int* abort_flag) {
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
   const int nw = gridDim.x * kMoverWarps, wid = blockIdx.x * kMoverWarps + (warp - 10);
   for (int mb = 0; mb < nmb; ++mb) {
-    if (mb >= g.slots) {
-      int ok = 1;
-      if (lane == 0) {
-        const int prev = mb - g.slots;
-        const int target = (g.mb_start[prev + 1] - g.mb_start[prev]) * (kG1Warps * nt1 + kG2Warps * nt2);
-        ok = wait_counter_geq(g.mb_done + prev, target, wc) ? 1 : 0;
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-    }
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return;
     const int row_base = g.mb_start[mb] * BM;
     const int nrows = (g.mb_start[mb + 1] - g.mb_start[mb]) * BM;
-    const size_t slot_base = (size_t)(mb % g.slots) * g.slot_rows;
     for (int i = wid; i < nrows; i += nw) {
       const int src = g.perm_src[row_base + i];
-      uint4* dst = g.ring_x + (slot_base + i) * nvec;
+      uint4* dst = g.xg + (size_t)(row_base + i) * nvec;
       if (src < 0) {
         for (int v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
         continue;
@@ -477,7 +417,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   WaitCtl wc{g.status, abort_flag, g.timeout_ns};
-  const int nt1 = g.F / 128;
+  const int nt1 = g.F / 128, nt2 = g.d / BN;
   const int total = g.phase_start[2 * nmb];
   // a minibatch is gathered once every mover CTA, or every mover warp, has
   // signalled it
@@ -494,6 +434,8 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
       bool ok = true;
       // the next claim is taken while the current item's stages load, and
       // decoded right after them, so neither sits between two items' stages
+      // the next claim is taken while the current item's stages load, and
+      // decoded right after them, so neither sits between two items' stages
       int c = atomicAdd(g.claim, 1);
       Item nxt;
       nxt.kind = -1;
@@ -502,8 +444,19 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
         Item it = nxt;
         const int c_next = c < total ? atomicAdd(g.claim, 1) : total;
         if (c < total) {
-          ok = it.kind == 0 ? wait_counter_geq(g.gathered + it.mb, gathered_target, wc)
-                            : wait_counter_geq(g.g1_done + it.gt, kG1Warps * nt1, wc);
+          if (it.kind == 0) {
+            // the minibatch's X rows are gathered, and its ring slot's h rows
+            // have been read by every G2 tile of minibatch mb - slots
+            ok = wait_counter_geq(g.gathered + it.mb, gathered_target, wc);
+            if (ok && it.mb >= g.slots) {
+              const int prev = it.mb - g.slots;
+              ok = wait_counter_geq(g.mb_done + prev,
+                                    (g.mb_start[prev + 1] - g.mb_start[prev]) * (kG1Warps * nt1 + kG2Warps * nt2),
+                                    wc);
+            }
+          } else {
+            ok = wait_counter_geq(g.g1_done + it.gt, kG1Warps * nt1, wc);
+          }
           fence_proxy_async_global();
           if (!ok) it.kind = -1;
         } else {
@@ -522,7 +475,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) fwd_megakernel(const __grid_c
           uint8_t* sb = sa + kABytes;
           const int k0 = kb * BK;
           if (it.kind == 0) {
-            tma_load_2d(sa, &g.mapXr, k0, it.ring_row0, &full[s], pol_a);
+            tma_load_2d(sa, &g.mapXr, k0, it.gt * BM, &full[s], pol_a);
             tma_load_2d(sb, &g.mapWg, k0, it.e * g.F + it.nt * 128, &full[s], pol_w);
             tma_load_2d(sb + kBBytes / 2, &g.mapWu, k0, it.e * g.F + it.nt * 128, &full[s], pol_w);
           } else {

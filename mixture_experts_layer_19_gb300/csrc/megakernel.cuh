@@ -10,7 +10,7 @@
 namespace moe {
 
 struct MegaArgs {
-  CUtensorMap mapXr;    // ring X rows, K-major loads {d, ring rows}, box 64 x 128
+  CUtensorMap mapXr;    // sorted X rows (Xg), K-major loads {d, rows}, box 64 x 128
   CUtensorMap mapWg;    // Wg K-major {d, E*F}, box 64 x 128
   CUtensorMap mapWu;
   CUtensorMap mapWd;    // Wd K-major {F, E*d}, box 64 x 256
@@ -19,7 +19,7 @@ struct MegaArgs {
   CUtensorMap mapABSt;  // saved a|b {2F, rows}, stores
   CUtensorMap mapYsSt;  // sorted y rows {d, rows}, stores
   const uint4* X;       // [T, d] bf16 tokens
-  uint4* ring_x;        // [slots * slot_rows, d] bf16
+  uint4* xg;            // [rows, d] bf16 sorted X rows (the weight gradients read them too)
   const int32_t* perm_src;
   const int32_t* mtile_off;   // [E+1]
   int32_t* mb_start;          // [n_mb+1] first 128-row tile of each minibatch
@@ -54,6 +54,54 @@ struct Item {
 };
 
 #ifdef __CUDACC__
+// One thread: cut the 128-row tiles into minibatches on expert boundaries
+// (>= mbt tiles when possible, <= cap tiles always; an expert larger than cap
+// is split into cap-sized pieces) and lay out the claim order's phase
+// boundaries.
+// tiles[e]: the expert's 128-row tiles (shared memory, so the serial walk
+// does not wait on global loads).
+__device__ __forceinline__ void cut_minibatches(const int* tiles, int E, int mbt, int cap, int nt1, int nt2,
+                                int32_t* mb_start, int32_t* phase_start, int32_t* n_mb) {
+  int nb = 0, cur = 0, g = 0;
+  mb_start[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    int t = tiles[e];
+    while (t > 0) {
+      if (cur + t <= cap) {
+        cur += t;
+        g += t;
+        t = 0;
+        if (cur >= mbt) {
+          mb_start[++nb] = g;
+          cur = 0;
+        }
+      } else if (cur > 0) {
+        mb_start[++nb] = g;
+        cur = 0;
+      } else {
+        g += cap;
+        t -= cap;
+        mb_start[++nb] = g;
+      }
+    }
+  }
+  if (cur > 0) mb_start[++nb] = g;
+  *n_mb = nb;
+  // phases: G1(0), [G1(i), G2(i-1)] for i = 1..nb-1, G2(nb-1)
+  int acc = 0, p = 0;
+  phase_start[p++] = 0;
+  for (int i = 0; i <= nb; ++i) {
+    if (i < nb) {  // G1(i)
+      acc += (mb_start[i + 1] - mb_start[i]) * nt1;
+      phase_start[p++] = acc;
+    }
+    if (i >= 1) {  // G2(i-1)
+      acc += (mb_start[i] - mb_start[i - 1]) * nt2;
+      phase_start[p++] = acc;
+    }
+  }
+}
+
 __device__ __forceinline__ int find_last_le(const int32_t* a, int n, int v) {  // last i in [0,n) with a[i] <= v
   int lo = 0, hi = n;
   while (hi - lo > 1) {
@@ -88,6 +136,43 @@ __device__ __forceinline__ Item decode_claim(const A& g, int nmb, int c) {
   return it;
 }
 #endif
+
+// Argument block of the BF16 backward megakernel (megakernel_bwd.cu): the
+// expert FFNs' backward (B1-B4, B6) as one launch over the saved layout.
+struct BwdMegaArgs {
+  CUtensorMap mapU_A;   // dYg K-major {d, rows}, box 64 x 128
+  CUtensorMap mapU_B;   // Wd MN-major {F, E*d}, box 64 x 64
+  CUtensorMap mapX_A;   // dA|dB K-major {2F, rows}, box 64 x 128
+  CUtensorMap mapX_Bg;  // Wg MN-major {d, E*F}, box 64 x 64
+  CUtensorMap mapX_Bu;  // Wu MN-major
+  CUtensorMap mapDabSt; // dA|dB stores {2F, rows}, box 32 x 32
+  CUtensorMap mapWhSt;  // w h stores {F, rows}
+  CUtensorMap mapYsSt;  // dx per sorted row {d, rows}
+  const uint4* dY;      // [T, d] upstream gradient
+  const uint4* X;       // [T, d] tokens
+  uint4* dYg;           // [rows, d] sorted dY rows (written: the weight gradients read them)
+  uint4* Xg;            // [rows, d] sorted X rows, or null when they are already in place
+  const __nv_bfloat16* ab;   // saved a|b [rows, 2F]
+  RoutingPtrs rp;            // saved routing (read only)
+  float* dgp;                // [rows, F/256] partial <u, h>
+  float* dg;                 // [T, k]
+  float* dlogits;            // [T, E] or null
+  const uint4* Ys;           // dx per sorted row, read back by the dX reduce
+  uint4* dX;                 // [T, d]
+  const int32_t* mtile_off;  // = rp.mtile_off
+  int32_t* mb_start;
+  int32_t* phase_start;
+  int32_t* n_mb;
+  int* counters;             // claim | gathered[nm] | u_done[nm]   (zeroed in the kernel)
+  int counters_len;
+  int* tok_dx;               // [T * d/256] dx blocks stored per (token, 256-column block)
+  int* tok_u;                // [T] <u, h> partials stored per token
+  unsigned long long* gbar;  // [2] grid barrier, CTA exits (zero between launches)
+  int32_t* status;
+  uint64_t timeout_ns;
+  int E, d, F, k, T, mbt, cap, nm_max;
+  int slots, slot_rows;      // 1, 0: the sorted buffers are not recycled
+};
 
 // Argument block of the MXFP8 ring megakernel (megakernel_mx.cu): the ring
 // holds E4M3 X and h rows with their scale atoms (rows = ring rows).

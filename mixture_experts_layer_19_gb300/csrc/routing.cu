@@ -193,26 +193,8 @@ __global__ void __launch_bounds__(256) router_grad_kernel(const float* __restric
                                                           float* __restrict__ dlogits) {
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps_total) {
-    float g = 0.0f, wj = 0.0f;
-    int e = 0;
-    if (lane < k) {
-      const int r = dest[(size_t)t * k + lane];
-      for (int n = 0; n < ntu; ++n) g += dgp[(size_t)r * ntu + n];
-      wj = w[(size_t)t * k + lane];
-      e = idx[(size_t)t * k + lane];
-      dg[(size_t)t * k + lane] = g;
-    }
-    float s = wj * g;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (dlogits) {
-      float* row = dlogits + (size_t)t * E;
-      for (int i = lane; i < E; i += 32) row[i] = 0.0f;
-      __syncwarp();
-      if (lane < k) row[e] = wj * (g - s);
-    }
-  }
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps_total)
+    router_grad_token(dgp, dest, idx, w, t, k, E, ntu, dg, dlogits, lane);
 }
 
 // -----------------------------------------------------------------------------

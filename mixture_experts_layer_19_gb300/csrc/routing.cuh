@@ -159,6 +159,33 @@ __device__ __forceinline__ void permute_chunk(const int32_t* chunk_base, int T, 
   __syncwarp();
 }
 
+// B6 for token t, one warp: dg[t,j] = sum over the ntu N tiles of the
+// partial <u, h> of pair j's sorted row (tile order), then
+// dlogits[t, idx[t,j]] = w_j (dg_j - sum_i w_i dg_i) (warp-tree sum), zero
+// elsewhere; dlogits may be null.
+__device__ __forceinline__ void router_grad_token(const float* dgp, const int32_t* dest, const int32_t* idx,
+                                                  const float* w, int t, int k, int E, int ntu, float* dg,
+                                                  float* dlogits, int lane) {
+  float g = 0.0f, wj = 0.0f;
+  int e = 0;
+  if (lane < k) {
+    const int r = dest[(size_t)t * k + lane];
+    for (int n = 0; n < ntu; ++n) g += dgp[(size_t)r * ntu + n];
+    wj = w[(size_t)t * k + lane];
+    e = idx[(size_t)t * k + lane];
+    dg[(size_t)t * k + lane] = g;
+  }
+  float s = wj * g;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (dlogits) {
+    float* row = dlogits + (size_t)t * E;
+    for (int i = lane; i < E; i += 32) row[i] = 0.0f;
+    __syncwarp();
+    if (lane < k) row[e] = wj * (g - s);
+  }
+}
+
 // S7 for token t, 8 columns starting at vector i (16 bytes): fp32 fmaf chain
 // over the slots j = 0..k-1 (weights w, or 1 when w is null), one bf16
 // rounding.  NC: the slot rows were written before this kernel started
