@@ -356,6 +356,48 @@ MegaArgs mega_args(moe_plan_s* p, const RoutingPtrs& rp, const void* X, const CU
   return m;
 }
 
+// Argument block of the MXFP8 ring megakernel (both forms).
+MegaMxArgs mx_mega_args(moe_plan_s* p, const RoutingPtrs& rp, const CUtensorMap& m_ab_st) {
+  const moe_config_t& c = p->cfg;
+  MegaMxArgs m;
+  memset(&m, 0, sizeof(m));
+  m.mapXr = p->m_ring_xq;
+  m.mapWg = p->m_Wgq;
+  m.mapWu = p->m_Wuq;
+  m.mapWd = p->m_Wdq;
+  m.mapHr = p->m_ring_hq;
+  m.mapHrSt = p->m_ring_hq_st;
+  m.mapABSt = m_ab_st;
+  m.mapYsSt = p->m_Ys_st;
+  m.xq = p->Xtq;
+  m.xs = p->Xts;
+  m.ring_xq = p->ring_xq;
+  m.ring_xs = p->ring_xs;
+  m.ring_hs = p->ring_hs;
+  m.wgs = p->Wgs;
+  m.wus = p->Wus;
+  m.wds = p->Wds;
+  m.perm_src = rp.perm_src;
+  m.mtile_off = rp.mtile_off;
+  m.mb_start = p->mb_start;
+  m.phase_start = p->phase_start;
+  m.n_mb = p->n_mb;
+  m.claim = p->counters;
+  m.gathered = p->counters + 1;
+  m.mb_done = p->counters + 1 + p->nm_max;
+  m.g1_done = p->counters + 1 + 2 * p->nm_max;
+  m.status = p->status;
+  m.timeout_ns = (uint64_t)c.wait_timeout_ns;
+  m.E = c.E;
+  m.d = c.d;
+  m.F = c.F;
+  m.k = c.k;
+  m.movers = p->mx_movers;
+  m.slots = p->slots;
+  m.slot_rows = p->cap * BM;
+  return m;
+}
+
 GemmArgs base_args(moe_plan_s* p, const RoutingPtrs& rp) {
   GemmArgs a;
   memset(&a, 0, sizeof(a));
@@ -813,6 +855,34 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     p->xg_T = T;
     return MOE_OK;
   }
+  if (mx && ring && !nv && !(c.debug_flags & MOE_DEBUG_MULTI_LAUNCH)) {
+    // MXFP8 ring schedule, one launch: token quantisation, routing, layout,
+    // ring pipeline and combine in one cooperative persistent kernel
+    MegaMxArgs m = mx_mega_args(p, rp, m_ab_st);
+    m.Xtok = static_cast<const __nv_bfloat16*>(X);
+    m.logits = logits;
+    m.rp = rp;
+    m.chunk_hist = p->chunk_hist;
+    m.chunk_base = p->chunk_base;
+    m.counters = p->counters;
+    m.counters_len = 1 + 3 * p->nm_max;
+    m.Ys = reinterpret_cast<const uint4*>(p->Ys);
+    m.Y = reinterpret_cast<uint4*>(Y);
+    m.tok_cnt = p->tok_cnt;
+    m.gbar = p->gbar;
+    m.T = Ti;
+    m.mbt = p->mbt;
+    m.cap = p->cap;
+    err = timed_launch(p, "fwd_megakernel_mx", st,
+                       [&] { return launch_fwd_megakernel_mx(m, p->num_sms, true, st); });
+    if (err != cudaSuccess) {
+      const std::string why = g_last_error;
+      cuda_fail(err, "moe_forward: MXFP8 one-launch megakernel launch");
+      if (err == cudaErrorCooperativeLaunchTooLarge) g_last_error += " (" + why + ")";
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
   err = timed_launch(p, "router_topk_hist", st,
                      [&] { return launch_router(logits, Ti, c.E, c.k, p->chunk_hist, rp, st); });
   if (err == cudaSuccess)
@@ -836,43 +906,9 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
       return launch_quant_rows(X, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: token quantisation launch");
-    MegaMxArgs m;
-    memset(&m, 0, sizeof(m));
-    m.mapXr = p->m_ring_xq;
-    m.mapWg = p->m_Wgq;
-    m.mapWu = p->m_Wuq;
-    m.mapWd = p->m_Wdq;
-    m.mapHr = p->m_ring_hq;
-    m.mapHrSt = p->m_ring_hq_st;
-    m.mapABSt = m_ab_st;
-    m.mapYsSt = p->m_Ys_st;
-    m.xq = p->Xtq;
-    m.xs = p->Xts;
-    m.ring_xq = p->ring_xq;
-    m.ring_xs = p->ring_xs;
-    m.ring_hs = p->ring_hs;
-    m.wgs = p->Wgs;
-    m.wus = p->Wus;
-    m.wds = p->Wds;
-    m.perm_src = rp.perm_src;
-    m.mtile_off = rp.mtile_off;
-    m.mb_start = p->mb_start;
-    m.phase_start = p->phase_start;
-    m.n_mb = p->n_mb;
-    m.claim = p->counters;
-    m.gathered = p->counters + 1;
-    m.mb_done = p->counters + 1 + p->nm_max;
-    m.g1_done = p->counters + 1 + 2 * p->nm_max;
-    m.status = p->status;
-    m.timeout_ns = (uint64_t)c.wait_timeout_ns;
-    m.E = c.E;
-    m.d = c.d;
-    m.F = c.F;
-    m.k = c.k;
-    m.movers = p->mx_movers;
-    m.slots = p->slots;
-    m.slot_rows = p->cap * BM;
-    err = timed_launch(p, "fwd_megakernel_mx", st, [&] { return launch_fwd_megakernel_mx(m, p->num_sms, st); });
+    const MegaMxArgs m = mx_mega_args(p, rp, m_ab_st);
+    err = timed_launch(p, "fwd_megakernel_mx", st,
+                       [&] { return launch_fwd_megakernel_mx(m, p->num_sms, false, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: MXFP8 megakernel launch");
     const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
     err = timed_launch(p, "combine", st,

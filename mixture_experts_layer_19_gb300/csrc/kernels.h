@@ -127,7 +127,7 @@ struct BwdMegaArgs;
 cudaError_t launch_bwd_megakernel(const BwdMegaArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_bwd_megakernel();
 struct MegaMxArgs;
-cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, bool fused, cudaStream_t st);  // fused: one launch
 cudaError_t prepare_fwd_megakernel_mx();
 
 // Record the detail string moe_last_error() returns on this thread.

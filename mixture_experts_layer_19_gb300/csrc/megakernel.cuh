@@ -185,8 +185,8 @@ struct MegaMxArgs {
   CUtensorMap mapHrSt;  // ring Hq stores, box 32 x 32 bytes
   CUtensorMap mapABSt;  // saved a|b bf16 stores
   CUtensorMap mapYsSt;  // sorted y rows bf16 stores
-  const uint8_t* xq;    // [T, d] E4M3 tokens, quantised once per token along d
-  const uint8_t* xs;    // their scale atoms (rows = tokens, K = d)
+  uint8_t* xq;          // [T, d] E4M3 tokens, quantised once per token along d
+  uint8_t* xs;          // their scale atoms (rows = tokens, K = d)
   uint8_t* ring_xq;     // [ring rows, d] E4M3
   uint8_t* ring_xs;     // scale atoms of ring_xq (K = d)
   uint8_t* ring_hs;     // scale atoms of the ring Hq rows (K = F)
@@ -195,9 +195,9 @@ struct MegaMxArgs {
   const uint8_t* wds;
   const int32_t* perm_src;
   const int32_t* mtile_off;
-  const int32_t* mb_start;
-  const int32_t* phase_start;
-  const int32_t* n_mb;
+  int32_t* mb_start;
+  int32_t* phase_start;
+  int32_t* n_mb;
   int* claim;
   int* gathered;
   int* g1_done;
@@ -205,6 +205,20 @@ struct MegaMxArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int E, d, F, k, movers, slots, slot_rows;
+  // One-launch forward (fwd_megakernel_mx<true>): token quantisation, routing,
+  // minibatch planning and the combine run inside the kernel.
+  const __nv_bfloat16* Xtok;  // [T, d] bf16 tokens (quantised into xq / xs in the kernel)
+  const float* logits;
+  RoutingPtrs rp;
+  int32_t* chunk_hist;
+  int32_t* chunk_base;
+  int* counters;
+  int counters_len;
+  const uint4* Ys;
+  uint4* Y;
+  int* tok_cnt;
+  unsigned long long* gbar;
+  int T, mbt, cap;
 };
 
 }  // namespace moe

@@ -13,9 +13,19 @@
 // straight into the slot; G2 tiles run the block-scaled down GEMM from the
 // slot.  Eight epilogue warps per compute CTA each bump the hand-off counters
 // once per tile (targets are 8 x tiles).
+// FUSED (the one-launch forward): the kernel also quantises the tokens,
+// routes them, lays out the sorted rows and cuts the minibatches (three
+// bounded grid barriers; megakernel_common.cuh) and combines each token's
+// 256-column blocks as their last rows land, so the whole MXFP8 forward is
+// one launch.
 #include "gemm_mx.cuh"
 #include "kernels.h"
 #include "megakernel.cuh"
+#include "megakernel_common.cuh"
+#include "mx.cuh"
+
+#include <cstdio>
+#include <cstring>
 
 namespace moe {
 
@@ -75,6 +85,7 @@ __device__ void mx_mover_loop(const MegaMxArgs& g, int nmb, int* abort_flag) {
   }
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(kMxMegaThreads, 1) fwd_megakernel_mx(const __grid_constant__ MegaMxArgs g) {
   constexpr int S = kMxMegaStages;
   extern __shared__ uint8_t smem_raw[];
@@ -92,13 +103,36 @@ __global__ void __launch_bounds__(kMxMegaThreads, 1) fwd_megakernel_mx(const __g
   Item* queue = reinterpret_cast<Item*>(qempty + kQueueMx);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(queue + kQueueMx);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* sync_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nmb = *g.n_mb;
   if (threadIdx.x == 0) *abort_flag = 0;
   __syncthreads();
+  if (FUSED) {
+    // every token quantised along d once (the quant_rows_kernel arithmetic),
+    // then routing, layout and the minibatch plan
+    const int kblocks = g.d >> 5;
+    const int64_t nblk = (int64_t)g.T * kblocks;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
+      const int64_t r = i / kblocks;
+      const int kb = (int)(i - r * kblocks);
+      float v[32];
+      load_bf16x32_f(g.Xtok + r * g.d + kb * 32, v);
+      quant_block_store(v, g.xq + r * g.d + kb * 32, g.xs + sf_atom_offset(r, kb, kblocks));
+    }
+    WaitCtl wca{g.status, abort_flag, g.timeout_ns};
+    if (!route_in_kernel(g, reinterpret_cast<int*>(stage_base), wca, sync_flag)) {
+      if (threadIdx.x == 0) fused_exit(g);
+      return;
+    }
+  }
+  const int nmb = *g.n_mb;
   if ((int)blockIdx.x < g.movers) {
     mx_mover_loop(g, nmb, abort_flag);
+    if (FUSED) {
+      __syncthreads();
+      if (threadIdx.x == 0) fused_exit(g);
+    }
     return;
   }
   if (threadIdx.x == 0) {
@@ -320,6 +354,7 @@ __global__ void __launch_bounds__(kMxMegaThreads, 1) fwd_megakernel_mx(const __g
         red_release_gpu_add(g.mb_done + it.mb, 1);
       }
       __syncwarp();
+      if (FUSED && it.kind == 1) combine_arrivals(g, srow, it.nt, lane);
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
@@ -330,16 +365,37 @@ __global__ void __launch_bounds__(kMxMegaThreads, 1) fwd_megakernel_mx(const __g
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+  if (FUSED && threadIdx.x == 0) fused_exit(g);
 }
 
-cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, cudaStream_t st) {
+cudaError_t launch_fwd_megakernel_mx(const MegaMxArgs& a, int grid, bool fused, cudaStream_t st) {
   void* args[] = {const_cast<MegaMxArgs*>(&a)};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fwd_megakernel_mx), dim3(grid),
-                                     dim3(kMxMegaThreads), args, kMxMegaSmem, st);
+  const void* fn = fused ? reinterpret_cast<const void*>(fwd_megakernel_mx<true>)
+                         : reinterpret_cast<const void*>(fwd_megakernel_mx<false>);
+  const cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kMxMegaThreads), args, kMxMegaSmem, st);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    // say why the grid cannot be co-resident
+    int per_sm = -1;
+    cudaFuncAttributes fa;
+    memset(&fa, 0, sizeof(fa));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kMxMegaThreads, kMxMegaSmem);
+    cudaFuncGetAttributes(&fa, fn);
+    char buf[256];
+    snprintf(buf, sizeof(buf),
+             "cooperative grid %d: %d CTA(s) per SM fit (registers %d, static smem %zu, dynamic smem %d of max %d, "
+             "local %zu B, max threads %d)",
+             grid, per_sm, fa.numRegs, fa.sharedSizeBytes, kMxMegaSmem, fa.maxDynamicSharedSizeBytes,
+             fa.localSizeBytes, fa.maxThreadsPerBlock);
+    set_error_detail(buf);
+  }
+  return e;
 }
 
 cudaError_t prepare_fwd_megakernel_mx() {
-  return cudaFuncSetAttribute(fwd_megakernel_mx, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxMegaSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(fwd_megakernel_mx<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxMegaSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fwd_megakernel_mx<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxMegaSmem);
 }
 
 }  // namespace moe

@@ -20,31 +20,6 @@
 
 namespace moe {
 
-__device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 q = __ldg(s + c);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-      v[8 * c + 2 * i] = f.x;
-      v[8 * c + 2 * i + 1] = f.y;
-    }
-  }
-}
-
-__device__ __forceinline__ void quant_block_store(const float* v, uint8_t* q, uint8_t* sfp) {
-  const int X = mx_block_exponent(amax32(v));
-  uint32_t o[8];
-  mx_encode32(v, X, o);
-  uint4* dq = reinterpret_cast<uint4*>(q);
-  dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
-  *sfp = (uint8_t)(X + 127);
-}
-
 __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int K,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
   const int kblocks = K >> 5;

@@ -111,15 +111,19 @@ def test_mxfp8_backward_parity(case):
     assert all(v <= MX_TOL for v in errs_u.values()), errs_u
 
 
+@pytest.mark.parametrize("multi", [False, True], ids=["one_launch", "multi_launch"])
 @pytest.mark.parametrize("mb_rows,slots,movers", [(0, 0, 0), (128, 2, 1), (512, 3, 4)])
-def test_mxfp8_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers):
-    """The MXFP8 ring megakernel (movers quantise while they gather; h is
-    re-quantised into the ring slot) must equal the separate-kernel MXFP8
-    schedule bit for bit, forward and backward."""
+def test_mxfp8_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, movers, multi):
+    """The MXFP8 ring megakernel (movers copy the once-quantised token rows
+    into the slot; h is re-quantised into the ring slot) must equal the
+    separate-kernel MXFP8 schedule bit for bit, forward and backward -- as one
+    launch that also quantises, routes and combines, and between separate
+    routing / quantisation / combine launches."""
     T, d, F, E, k = 700, 512, 512, 24, 4
     g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=41, alpha=1.1)
+    flags = moe.MOE_DEBUG_RING_MEGAKERNEL | (moe.MOE_DEBUG_MULTI_LAUNCH if multi else 0)
     ring = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, minibatch_rows=mb_rows,
-                               ring_slots=slots, mover_ctas=movers, debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL))
+                               ring_slots=slots, mover_ctas=movers, debug_flags=flags))
     sep = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8,
                               debug_flags=moe.MOE_DEBUG_SEPARATE_KERNELS))
     for p in (ring, sep):
@@ -133,6 +137,9 @@ def test_mxfp8_ring_megakernel_matches_separate_kernels_bitwise(mb_rows, slots, 
     assert torch.equal(Ya, Yb)
     for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
         assert torch.equal(ga[key], gb[key]), key
+    ra, rb = ring.routing(sa, T), sep.routing(sb, T)
+    for key in ("idx", "w", "counts", "offsets", "perm_src", "dest"):
+        assert torch.equal(ra[key], rb[key]), key
     Yr, _ = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k, mx=True)
     assert rel_err(Ya, Yr) <= MX_TOL
 
