@@ -439,7 +439,7 @@ def bench_gpu(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, k, args.cpu_tokens)
     if not args.no_ring:
-        out["ring_megakernel_forward"] = bench_ring_forward(args, plan, inp, Y, saved, stream, dev, ws)
+        out["ring_pipeline"] = bench_ring(args, plan, inp, Y, saved, grads, stream, dev, ws)
     out["router_gemm"] = bench_router(args, plan, inp, stream, dev, ws, peaks)
     if not args.no_ep:
         out["virtual_rank_ep"] = bench_ep(args, plan, inp, Y, saved, grads, stream, dev, ws)
@@ -451,6 +451,17 @@ def bench_gpu(args):
         grid = [(Tm, a) for Tm in (2048, 8192, 32768) for a in (0.0, 1.1, 1.5)] if args.sweep else \
             ([(args.tokens, ALPHA)] if args.tokens else [(8192, ALPHA), (32768, ALPHA)])
         out["mxfp8_fwd_bwd"] = [bench_mx_fwd_bwd(args, dev, ws, peaks, Tm, a) for Tm, a in grid]
+        big = [m for m in out["mxfp8_fwd_bwd"] if m["T"] == 32768 and m["zipf_alpha"] == ALPHA]
+        if big:
+            m = big[0]
+            gg = m["grouped_gemms"]["all_six"]["frac"]
+            lf = m["layer_roofline"]["frac"]
+            out["largest_config_target"] = {
+                "workload": m["workload"], "grouped_gemms_frac_of_fp8_peak": gg, "layer_frac_of_roofline": lf,
+                "layer_bound": m["layer_roofline"]["bound"], "targets": {"grouped_gemms": 0.6, "layer": 0.5},
+                "met": bool(gg >= 0.6 and lf >= 0.5),
+                "note": "the six block-scaled expert GEMMs' padding-free FLOPs over their summed device time, "
+                        "against 2 x the measured sustained bf16 peak"}
         if not args.tokens:
             out["mxfp8_minibatch_sweep"] = bench_minibatch_sweep(args, dev, ws)
     if not args.no_nv:
@@ -538,39 +549,56 @@ def bench_router(args, plan, inp, stream, dev, ws, peaks):
     return res
 
 
-def bench_ring_forward(args, plan_sep, inp, Y, saved, stream, dev, ws):
-    """Forward-only time of the three bf16 forward schedules on the headline
-    workload: separate kernels (the default), the ring megakernel as one
-    launch (routing and combine inside), and the ring megakernel between
-    separate routing / combine launches.  All are bitwise identical."""
+def bench_ring(args, plan_sep, inp, Y, saved, grads, stream, dev, ws):
+    """The bf16 schedules on the headline workload, forward alone and the
+    whole fwd+bwd step: separate kernels (the default), the ring pipeline as
+    one launch per direction (forward megakernel with routing and combine
+    inside; backward megakernel with the dY gather, u and dx GEMMs, dX sums
+    and router gradient inside; the weight gradients after it), and the ring
+    forward between separate routing / combine launches.  All are bitwise
+    identical to one another."""
     from mixture_experts_layer_19_gb300 import moe
     c = plan_sep.cfg
     res = {}
     schedules = (("separate", plan_sep), ("ring_one_launch", None), ("ring_multi_launch", None))
     flag_of = {"ring_one_launch": moe.MOE_DEBUG_RING_MEGAKERNEL,
                "ring_multi_launch": moe.MOE_DEBUG_RING_MEGAKERNEL | moe.MOE_DEBUG_MULTI_LAUNCH}
+    steps = max(3, args.steps // 2)
+
+    def timed(plan, fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        plan.kernel_times()
+        barrier(ws)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if plan.device_status() != 0:
+            raise RuntimeError("device status set in the ring measurement")
+        kt = plan.kernel_times()
+        return round(max_over_ranks(ev0.elapsed_time(ev1), ws, dev) / steps, 4), \
+            {n: round(v[0] / steps, 4) for n, v in sorted(kt.items(), key=lambda x: -x[1][0])}
+
     for name, plan in schedules:
         own = plan is None
         if own:
             plan = moe.Plan(moe.Config(T_max=c.T_max, d=c.d, F=c.F, E=c.E, k=c.k, device=dev.index,
                                        debug_flags=flag_of[name] | moe.MOE_DEBUG_TIMING))
-        for _ in range(args.warmup):
+
+        def fwd():
             plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
-        torch.cuda.synchronize(dev)
-        plan.kernel_times()
-        steps = max(3, args.steps // 2)
-        barrier(ws)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(steps):
-            plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        if plan.device_status() != 0:
-            raise RuntimeError(f"device status set in the {name} forward")
-        kt = plan.kernel_times()
-        res[name] = {"fwd_ms": round(max_over_ranks(ev0.elapsed_time(ev1), ws, dev) / steps, 4),
-                     "kernels": {n: round(v[0] / steps, 4) for n, v in kt.items()}}
+
+        def step():
+            fwd()
+            plan.backward(inp.dY, inp.X, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+
+        f_ms, f_k = timed(plan, fwd)
+        s_ms, s_k = timed(plan, step)
+        res[name] = {"fwd_ms": f_ms, "fwd_kernels": f_k, "fwd_bwd_ms": s_ms, "fwd_bwd_kernels": s_k}
         if own:
             del plan
     return res
@@ -947,7 +975,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiler captures on a smaller layer)")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurements")
     ap.add_argument("--no-nv", action="store_true", help="skip the NVFP4 measurements")
-    ap.add_argument("--no-ring", action="store_true", help="skip the ring-megakernel forward line")
+    ap.add_argument("--no-ring", action="store_true", help="skip the ring-pipeline line (forward and fwd+bwd)")
     ap.add_argument("--no-ep", action="store_true", help="skip the virtual-rank expert-parallel line")
     ap.add_argument("--sweep", action="store_true",
                     help="MXFP8 fwd+bwd over T in {2048, 8192, 32768} x zipf {0, 1.1, 1.5} and a minibatch sweep")
