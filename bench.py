@@ -207,14 +207,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "eb969e379f779f0608579bdbe881c1309e98cb6bb1a7ec41032835e6bfe9e7e6",
+    "csrc_sha256": "0488d5b73a4384318b35dbaf11c8a09795f6efa19595a613a3f3de703adf4165",
     "bytes": {
-        "gemm_up_swiglu": 11887223244,
-        "gemm_down": 5726132480,
-        "gemm_bwd_u_swiglu": 6930857011,
-        "gemm_bwd_dx": 11176548352,
-        "gemm_wgrad_down": 8504734566,
-        "gemm_wgrad_gate_up": 16127314483,
+        "gemm_up_swiglu": 11576141670,
+        "gemm_down": 5643801446,
+        "gemm_bwd_u_swiglu": 6876249088,
+        "gemm_bwd_dx": 10763954278,
+        "gemm_wgrad_down": 8503758336,
+        "gemm_wgrad_gate_up": 16146945280,
     },
 }
 
