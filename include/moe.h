@@ -104,9 +104,10 @@ typedef struct {
   int64_t wait_timeout_ns;/* bound on every device-side wait; 0 = 2e9 (2 s) */
   uint32_t debug_flags;   /* MOE_DEBUG_* */
   int32_t device;         /* CUDA device ordinal the plan binds to */
-  int32_t ep_ranks;       /* >= 2: BF16 layer as expert parallelism over this many virtual
+  int32_t ep_ranks;       /* >= 2: the layer as expert parallelism over this many virtual
                              ranks on the one GPU (pull dispatch, push combine, pull reverse-
-                             combine, push reverse-dispatch); must divide E; 0 or 1 = off */
+                             combine, push reverse-dispatch; block-scaled plans quantise the
+                             pulled bf16 rows); must divide E; 0 or 1 = off */
 } moe_config_t;
 
 typedef struct moe_plan_s* moe_plan_t;

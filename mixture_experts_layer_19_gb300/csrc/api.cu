@@ -307,7 +307,7 @@ EpArgs ep_args(moe_plan_s* p, const RoutingPtrs& rp, int64_t T) {
   a.F = c.F;
   a.E = c.E;
   a.k = c.k;
-  a.ntu = c.F / BN;
+  a.ntu = c.prec == MOE_BF16 ? c.F / BN : c.F / 128;   // <u, h> partials per row of the u GEMM kind
   a.nch = route_chunks((int)T);
   a.rp = rp;
   a.chunk_hist = p->chunk_hist;
@@ -411,6 +411,112 @@ GemmArgs base_args(moe_plan_s* p, const RoutingPtrs& rp) {
   return a;
 }
 
+// Quantise the plan's whole sorted-row capacity of bf16 rows along d into the
+// block-scaled sorted operand (Xq / Xs): MXFP8, or NVFP4 with tensor scale 1.
+// Rows past the last expert segment are never read by a GEMM tile.
+cudaError_t launch_quant_sorted(moe_plan_s* p, const void* rows, cudaStream_t st) {
+  const moe_config_t& c = p->cfg;
+  return c.prec == MOE_NVFP4 ? launch_nv_quant_rows(rows, p->Rpm, c.d, nullptr, p->Xq, p->Xs, p->num_sms * 8, st)
+                             : launch_quant_rows(rows, p->Rpm, c.d, p->Xq, p->Xs, p->num_sms * 8, st);
+}
+
+// Block-scaled (MXFP8 / NVFP4) forward expert GEMMs over the plan's sorted,
+// quantised X rows (Xq / Xs): [a|b] GEMM + SwiGLU with h re-quantised along F
+// in its epilogue, then the down GEMM into Ys.
+cudaError_t launch_block_scaled_fwd_gemms(moe_plan_s* p, const RoutingPtrs& rp, const CUtensorMap& m_ab_st,
+                                          const CUtensorMap& m_ab_st16, cudaStream_t st) {
+  const moe_config_t& c = p->cfg;
+  const bool nv = c.prec == MOE_NVFP4;
+  MxArgs a;
+  memset(&a, 0, sizeof(a));
+  a.poff = rp.poff;
+  a.mtile_off = rp.mtile_off;
+  a.status = p->status;
+  a.timeout_ns = (uint64_t)c.wait_timeout_ns;
+  a.E = c.E;
+  a.d = c.d;
+  a.F = c.F;
+  MxArgs b = a;
+  a.mapA = p->m_Xq;
+  a.mapB0 = p->m_Wgq;
+  a.mapB1 = p->m_Wuq;
+  a.mapO0 = nv ? m_ab_st16 : m_ab_st;
+  a.mapO1 = p->m_Hq_st;
+  a.sfA = p->Xs;
+  a.sfB0 = p->Wgs;
+  a.sfB1 = p->Wus;
+  a.sfO = p->Hs;
+  a.tsB = nv ? p->nv_scale : nullptr;
+  a.dbg = p->dbg_h;
+  cudaError_t err = timed_launch(p, nv ? "gemm_nv_up_swiglu" : "gemm_mx_up_swiglu", st,
+                     [&] { return launch_gemm_mx(kUp, a, p->num_sms, st, nv); });
+  if (err != cudaSuccess) return err;
+  b.mapA = p->m_Hq_k;
+  b.mapB0 = p->m_Wdq;
+  b.mapO0 = nv ? p->m_Ys_st16 : p->m_Ys_st;
+  b.sfA = p->Hs;
+  b.sfB0 = p->Wds;
+  b.tsB = nv ? p->nv_scale + 1 : nullptr;
+  err = timed_launch(p, nv ? "gemm_nv_down" : "gemm_mx_down", st,
+                     [&] { return launch_gemm_mx(kDown, b, p->num_sms, st, nv); });
+  return err;
+}
+
+// Block-scaled dgrad GEMMs over the plan's sorted, quantised dY rows (Xq /
+// Xs): u GEMM against Wd^T with the SwiGLU-backward epilogue (dA|dB
+// re-quantised along F, and the weight gradients' [dA|dB]^T and (w h)^T
+// quantised along the rows), then the dx GEMM into Ys.
+cudaError_t launch_block_scaled_dgrad_gemms(moe_plan_s* p, const RoutingPtrs& rp, const __nv_bfloat16* ab,
+                                            cudaStream_t st) {
+  const moe_config_t& c = p->cfg;
+  const bool nv = c.prec == MOE_NVFP4;
+  MxArgs u;
+  memset(&u, 0, sizeof(u));
+  u.poff = rp.poff;
+  u.mtile_off = rp.mtile_off;
+  u.status = p->status;
+  u.timeout_ns = (uint64_t)c.wait_timeout_ns;
+  u.E = c.E;
+  u.d = c.d;
+  u.F = c.F;
+  MxArgs x = u;
+  u.mapA = p->m_Xq;
+  u.mapB0 = p->m_WdTq;
+  u.mapO0 = p->m_dAB_st;
+  u.mapO1 = p->m_dABq_st;
+  u.mapO2 = p->m_wH_st;
+  u.sfA = p->Xs;
+  u.sfB0 = p->WdTs;
+  u.sfO = p->dABs;
+  u.ab = ab;
+  u.perm_src = rp.perm_src;
+  u.wts = rp.w;
+  u.dgp = p->dgp;
+  u.tsB = nv ? p->nv_scale + 1 : nullptr;
+  u.dbg = p->dbg_dab;
+  // the weight gradients' [dA|dB]^T and (w h)^T, quantised along the sorted
+  // rows in the same epilogue
+  u.Kcap = (int)p->Rpm;
+  u.qT0 = p->dABTq;
+  u.sT0 = p->dABTs;
+  u.qT1 = p->wHTq;
+  u.sT1 = p->wHTs;
+  cudaError_t err = timed_launch(p, nv ? "gemm_nv_bwd_u_swiglu" : "gemm_mx_bwd_u_swiglu", st,
+                     [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st, nv); });
+  if (err != cudaSuccess) return err;
+  x.mapA = p->m_dABq_k;
+  x.mapB0 = p->m_WgTq;
+  x.mapB1 = p->m_WuTq;
+  x.mapO0 = nv ? p->m_Ys_st16 : p->m_Ys_st;
+  x.sfA = p->dABs;
+  x.sfB0 = p->WgTs;
+  x.sfB1 = p->WuTs;
+  x.tsB = nv ? p->nv_scale : nullptr;
+  err = timed_launch(p, nv ? "gemm_nv_bwd_dx" : "gemm_mx_bwd_dx", st,
+                     [&] { return launch_gemm_mx(kBwdX, x, p->num_sms, st, nv); });
+  return err;
+}
+
 }  // namespace
 
 void moe::set_error_detail(const char* msg) { g_last_error = msg ? msg : ""; }
@@ -457,9 +563,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
     return fail(MOE_ERR_UNSUPPORTED, "moe_plan: weight tensor too large");
   if (c.ep_ranks < 0 || c.ep_ranks > 64)
     return fail(MOE_ERR_INVALID_ARG, "moe_plan: ep_ranks must be in [0, 64]");
-  if (c.ep_ranks >= 2 && (c.E % c.ep_ranks != 0 || c.prec != MOE_BF16 || (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)))
-    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: virtual-rank expert parallelism needs a BF16 plan, ep_ranks dividing "
-                                     "E, and real experts");
+  if (c.ep_ranks >= 2 && (c.E % c.ep_ranks != 0 || (c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_plan: virtual-rank expert parallelism needs ep_ranks dividing E and real "
+                                     "experts");
   if (!encode_fn()) return fail(MOE_ERR_CUDA, "moe_plan: cuTensorMapEncodeTiled unavailable");
 
   DeviceGuard guard(c.device);
@@ -702,7 +808,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   if (err == cudaSuccess) err = prepare_gemm_router();
   if (err == cudaSuccess && c.ep_ranks >= 2) {
     const size_t pairs = (size_t)c.T_max * c.k;
-    const size_t o_slot = 0, o_dgs = align256(pairs * c.d * 2), o_ctr = o_dgs + align256(pairs * (c.F / BN) * 4);
+    // <u, h> partials per pair: F/256 (bf16 u GEMM) or F/128 (block-scaled)
+    const size_t ntu = c.prec == MOE_BF16 ? c.F / BN : c.F / 128;
+    const size_t o_slot = 0, o_dgs = align256(pairs * c.d * 2), o_ctr = o_dgs + align256(pairs * ntu * 4);
     err = cudaMalloc(&p->ep_ws, o_ctr + 4096);
     if (err == cudaSuccess) {
       char* eb = static_cast<char*>(p->ep_ws);
@@ -808,6 +916,20 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     ea.Xg = static_cast<uint4*>(p->Xg);
     err = timed_launch(p, "ep_pull_dispatch", st, [&] { return launch_ep_dispatch(ea, st); });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP dispatch launch");
+    if (mx) {
+      // block-scaled experts: each rank quantises the bf16 rows it pulled
+      // along d -- the bytes of quantising each token once and copying them,
+      // as the single-GPU schedule does -- then the block-scaled GEMMs
+      err = timed_launch(p, "quant_pulled_rows", st, [&] { return launch_quant_sorted(p, p->Xg, st); });
+      if (err == cudaSuccess) err = launch_block_scaled_fwd_gemms(p, rp, m_ab_st, m_ab_st16, st);
+      if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP block-scaled GEMM launch");
+      ea.Ys = static_cast<const uint4*>(p->Ys);
+      ea.out = static_cast<uint4*>(Y);
+      ea.w_out = rp.w;
+      err = timed_launch(p, "ep_push_combine", st, [&] { return launch_ep_push(ea, st); });
+      if (err != cudaSuccess) return cuda_fail(err, "moe_forward: EP combine launch");
+      return MOE_OK;
+    }
     GemmArgs a = base_args(p, rp);
     a.mapA = p->m_Xg_k;
     a.mapB0 = p->m_Wg_k;
@@ -931,39 +1053,8 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
                                     nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
       });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
-    MxArgs a;
-    memset(&a, 0, sizeof(a));
-    a.poff = rp.poff;
-    a.mtile_off = rp.mtile_off;
-    a.status = p->status;
-    a.timeout_ns = (uint64_t)c.wait_timeout_ns;
-    a.E = c.E;
-    a.d = c.d;
-    a.F = c.F;
-    MxArgs b = a;
-    a.mapA = p->m_Xq;
-    a.mapB0 = p->m_Wgq;
-    a.mapB1 = p->m_Wuq;
-    a.mapO0 = nv ? m_ab_st16 : m_ab_st;
-    a.mapO1 = p->m_Hq_st;
-    a.sfA = p->Xs;
-    a.sfB0 = p->Wgs;
-    a.sfB1 = p->Wus;
-    a.sfO = p->Hs;
-    a.tsB = nv ? p->nv_scale : nullptr;
-    a.dbg = p->dbg_h;
-    err = timed_launch(p, nv ? "gemm_nv_up_swiglu" : "gemm_mx_up_swiglu", st,
-                       [&] { return launch_gemm_mx(kUp, a, p->num_sms, st, nv); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled up GEMM launch");
-    b.mapA = p->m_Hq_k;
-    b.mapB0 = p->m_Wdq;
-    b.mapO0 = nv ? p->m_Ys_st16 : p->m_Ys_st;
-    b.sfA = p->Hs;
-    b.sfB0 = p->Wds;
-    b.tsB = nv ? p->nv_scale + 1 : nullptr;
-    err = timed_launch(p, nv ? "gemm_nv_down" : "gemm_mx_down", st,
-                       [&] { return launch_gemm_mx(kDown, b, p->num_sms, st, nv); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled down GEMM launch");
+    err = launch_block_scaled_fwd_gemms(p, rp, m_ab_st, m_ab_st16, st);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled GEMM launch");
     const int cgrid = (int)std::min<int64_t>(T, (int64_t)p->num_sms * 16);
     err = timed_launch(p, "combine", st,
                        [&] { return launch_combine(p->Ys, rp.dest, rp.w, Ti, c.k, c.d, Y, cgrid, st); });
@@ -1155,7 +1246,12 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
   if (err != cudaSuccess) return cuda_fail(err, "moe_backward: gather launch");
   const bool mx = c.prec != MOE_BF16;  // block-scaled dgrad GEMMs
   const bool nv = c.prec == MOE_NVFP4;
-  if (mx) {
+  if (mx && ep) {
+    // the dY rows each expert rank pulled, quantised along d in place of the
+    // per-token quantisation and copy (the same bytes)
+    err = timed_launch(p, "quant_pulled_rows_dy", st, [&] { return launch_quant_sorted(p, p->dYg, st); });
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: EP dY quantisation launch");
+  } else if (mx) {
     // MXFP8 / NVFP4 dgrad: dY quantised along d as it is gathered; u GEMM
     // against Wd^T (quantised along d) with dA|dB re-quantised along F in its
     // epilogue; dx GEMM against [Wg^T; Wu^T] (quantised along F).  The weight
@@ -1171,51 +1267,10 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
                                     nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
       });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dY gather launch");
-    MxArgs u;
-    memset(&u, 0, sizeof(u));
-    u.poff = rp.poff;
-    u.mtile_off = rp.mtile_off;
-    u.status = p->status;
-    u.timeout_ns = (uint64_t)c.wait_timeout_ns;
-    u.E = c.E;
-    u.d = c.d;
-    u.F = c.F;
-    MxArgs x = u;
-    u.mapA = p->m_Xq;
-    u.mapB0 = p->m_WdTq;
-    u.mapO0 = p->m_dAB_st;
-    u.mapO1 = p->m_dABq_st;
-    u.mapO2 = p->m_wH_st;
-    u.sfA = p->Xs;
-    u.sfB0 = p->WdTs;
-    u.sfO = p->dABs;
-    u.ab = ab;
-    u.perm_src = rp.perm_src;
-    u.wts = rp.w;
-    u.dgp = p->dgp;
-    u.tsB = nv ? p->nv_scale + 1 : nullptr;
-    u.dbg = p->dbg_dab;
-    // the weight gradients' [dA|dB]^T and (w h)^T, quantised along the sorted
-    // rows in the same epilogue
-    u.Kcap = (int)p->Rpm;
-    u.qT0 = p->dABTq;
-    u.sT0 = p->dABTs;
-    u.qT1 = p->wHTq;
-    u.sT1 = p->wHTs;
-    err = timed_launch(p, nv ? "gemm_nv_bwd_u_swiglu" : "gemm_mx_bwd_u_swiglu", st,
-                       [&] { return launch_gemm_mx(kBwdU, u, p->num_sms, st, nv); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled u GEMM launch");
-    x.mapA = p->m_dABq_k;
-    x.mapB0 = p->m_WgTq;
-    x.mapB1 = p->m_WuTq;
-    x.mapO0 = nv ? p->m_Ys_st16 : p->m_Ys_st;
-    x.sfA = p->dABs;
-    x.sfB0 = p->WgTs;
-    x.sfB1 = p->WuTs;
-    x.tsB = nv ? p->nv_scale : nullptr;
-    err = timed_launch(p, nv ? "gemm_nv_bwd_dx" : "gemm_mx_bwd_dx", st,
-                       [&] { return launch_gemm_mx(kBwdX, x, p->num_sms, st, nv); });
-    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled dx GEMM launch");
+  }
+  if (mx) {
+    err = launch_block_scaled_dgrad_gemms(p, rp, ab, st);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_backward: block-scaled dgrad GEMM launch");
   }
   if (!mx && !ring_bwd) {
     GemmArgs a = base_args(p, rp);
