@@ -312,10 +312,13 @@ def test_maximum_experts_and_top_k(prec):
     if prec == moe.MOE_BF16:
         for flags in (moe.MOE_DEBUG_RING_MEGAKERNEL, moe.MOE_DEBUG_RING_MEGAKERNEL | moe.MOE_DEBUG_MULTI_LAUNCH):
             other = _plan(T, d, F, E, k, flags)
-            Y2, _ = other.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+            Y2, s2 = other.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+            out2 = other.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], s2)
             torch.cuda.synchronize()
             assert other.device_status() == 0
             assert torch.equal(Y2, Y), flags
+            for key in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits"):
+                assert torch.equal(out2[key], out[key]), (flags, key)
 
 
 def test_backward_reuses_sorted_x_only_for_its_own_forward():
@@ -380,3 +383,95 @@ def test_idle_experts_get_zero_weight_gradients_over_poisoned_buffers(prec):
     tol = 4e-2 if fmt else BF16_TOL
     for name in ("dX", "dWg", "dWu", "dWd"):
         assert rel_err(out[name], gref[name]) <= tol, name
+
+
+def _ring_vs_separate(T, d, F, E, k, g, h, dlogits=True):
+    """Forward + backward of the one-launch ring schedule (both megakernels)
+    against the separate kernels, bit for bit, and the oracle."""
+    ring = _plan(T, d, F, E, k, moe.MOE_DEBUG_RING_MEGAKERNEL)
+    sep = _plan(T, d, F, E, k, moe.MOE_DEBUG_SEPARATE_KERNELS)
+    res = []
+    for p in (ring, sep):
+        Y, s = p.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+        out = {
+            "dX": torch.empty((T, d), dtype=torch.bfloat16, device="cuda"),
+            "dWg": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+            "dWu": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+            "dWd": torch.empty((E, d, F), dtype=torch.bfloat16, device="cuda"),
+            "dg": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+            "dlogits": torch.empty((T, E), dtype=torch.float32, device="cuda") if dlogits else None,
+        }
+        p.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], s, out=out)
+        res.append((Y, out))
+    torch.cuda.synchronize()
+    assert ring.device_status() == 0 and sep.device_status() == 0
+    assert torch.equal(res[0][0], res[1][0])
+    keys = ("dX", "dWg", "dWu", "dWd", "dg") + (("dlogits",) if dlogits else ())
+    for key in keys:
+        assert torch.equal(res[0][1][key], res[1][1][key]), key
+    Yr, ctx = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
+    gr = moe_ref.backward(h["dY"], h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], ctx)
+    assert rel_err(res[0][0], Yr) <= BF16_TOL
+    for key in keys:
+        assert rel_err(res[0][1][key], gr[key]) <= BF16_TOL, key
+
+
+@pytest.mark.parametrize("case", [(1, 256, 256, 8, 2), (3, 256, 512, 4, 4), (129, 512, 256, 16, 3),
+                                  (200, 256, 256, 1024, 32)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d" % c)
+def test_ring_backward_megakernel_edge_cases(case):
+    """The one-launch forward and backward megakernels at the edges: a single
+    token, k = E, a ragged token count, and the largest routing (E = 1024,
+    k = 32, most experts with one row each, padded to a 128-row tile)."""
+    T, d, F, E, k = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=70 + T, alpha=1.1)
+    _ring_vs_separate(T, d, F, E, k, g, h)
+
+
+def test_ring_backward_megakernel_degenerate_routing_without_dlogits():
+    """Every token routed to the same two experts (all others idle), and a
+    backward that skips dlogits: the in-kernel router gradient writes dg alone."""
+    T, d, F, E, k = 300, 256, 256, 12, 2
+    bias = torch.zeros(E)
+    bias[5], bias[9] = 40.0, 30.0
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=71, logits_fn=lambda L: L + bias[None, :])
+    _ring_vs_separate(T, d, F, E, k, g, h, dlogits=False)
+
+
+def test_ring_forward_and_backward_replay_from_a_cuda_graph():
+    """A captured one-launch forward and backward replay correctly: both
+    megakernels reset their grid barrier and zero their own counters."""
+    T, d, F, E, k = 300, 256, 512, 16, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=49, alpha=1.1)
+    plan = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_RING_MEGAKERNEL)
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    out = {"dX": torch.empty((T, d), dtype=torch.bfloat16, device="cuda"),
+           "dWg": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+           "dWu": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+           "dWd": torch.empty((E, d, F), dtype=torch.bfloat16, device="cuda"),
+           "dg": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+           "dlogits": torch.empty((T, E), dtype=torch.float32, device="cuda")}
+    stream = torch.cuda.Stream()
+
+    def step():
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+        plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    ref = {"Y": Y.clone(), **{n: v.clone() for n, v in out.items()}}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(3):
+        Y.zero_()
+        for v in out.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert torch.equal(Y, ref["Y"])
+        for n, v in out.items():
+            assert torch.equal(v, ref[n]), n
