@@ -1329,9 +1329,9 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     // expert's tokens
     const int Rq = (int)p->Rpm;
     err = timed_launch(p, "quant_wgrad_tokens", st, [&] {
-      // one wave: four CTAs (32 KB of staged tiles each) per SM
+      // one wave: two CTAs (three 32 KB stages each) per SM
       return launch_gather_transpose_q(nv, dY, X, rp.perm_src, rp.totals, c.k, Rq, c.d, p->dYTq, p->dYTs, p->XTq,
-                                       p->XTs, p->num_sms * 4, st);
+                                       p->XTs, p->status, (uint64_t)c.wait_timeout_ns, p->num_sms * 2, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient token quantisation launch");
     MxArgs w;

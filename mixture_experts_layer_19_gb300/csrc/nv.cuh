@@ -36,10 +36,9 @@ __device__ __forceinline__ float e4m3_value(uint8_t s) {
 
 // Quantise 16 floats (one block): returns the E4M3 scale byte and writes the
 // 8 packed E2M1 bytes (little-endian) into out.
-__device__ __forceinline__ uint8_t nv_encode16(const float* v, float rc, float g, uint2& out) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+// amax: the block's largest magnitude, max over i of fabsf(v[i]) (fmaxf
+// order, NaN ignored), computed by the caller.
+__device__ __forceinline__ uint8_t nv_encode16_amax(const float* v, float amax, float rc, float g, uint2& out) {
   const uint8_t s = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(amax, rc), __NV_SATFINITE, __NV_E4M3);
   const float sv = e4m3_value(s);
   if (sv == 0.0f) {
@@ -56,6 +55,14 @@ __device__ __forceinline__ uint8_t nv_encode16(const float* v, float rc, float g
   }
   out = make_uint2(w[0], w[1]);
   return s;
+}
+
+// The same with the block's amax taken here.
+__device__ __forceinline__ uint8_t nv_encode16(const float* v, float rc, float g, uint2& out) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  return nv_encode16_amax(v, amax, rc, g, out);
 }
 
 // 32 floats -> 16 packed bytes (two blocks); returns the two scale bytes
