@@ -219,3 +219,53 @@ def test_stored_context_sampled_form_matches_full_form():
         dwg, dwu, dwd = moe_ref.expert_weight_grads(X, L, Wg, Wu, Wd, dY, k, e, mx=mx, stored=True)
         for name, got in (("dWg", dwg), ("dWu", dwu), ("dWd", dwd)):
             assert np.allclose(got, g[name][e], rtol=1e-12, atol=1e-12), (mx, name)
+
+
+def test_weight_gradient_quantisation_axis_hand_pins():
+    """The block-scaled weight gradients quantise every operand along the
+    expert's rows (the tokens), and dA, dB, w h from their bf16 values.  The
+    expected sums below are worked out by hand from the formats' definitions
+    (OCP MX: E8M0 scale 2^(floor(log2 amax) - 8) for E4M3, round to nearest
+    even; NVFP4: E4M3 scale of amax / 6, E2M1 elements {0, 0.5, 1, 1.5, 2, 3,
+    4, 6}), not from the oracle's code; quantising along the features, or
+    skipping the bf16 step, gives different numbers."""
+    # MXFP8, one 32-row block.  dy column 0: 448 then 31 x 2^-10.  Along the
+    # rows amax = 448 = 1.75 * 2^8 sets scale 2^0, and 2^-10 is exactly half of
+    # E4M3's smallest subnormal 2^-9: the tie goes to the even code, 0.  Column
+    # 1 (32 x 2^-10) has scale 2^-18 and is exact.  Along the features each of
+    # rows 1..31 would keep its 2^-10 (column 0 would sum to 448 + 31 * 2^-10).
+    n = 32
+    dy = np.full((n, 2), 2.0 ** -10)
+    dy[0, 0] = 448.0
+    ones = np.ones((n, 1))
+    # da column 0: 448, then 1.0625 + 2^-12, then zeros.  bf16 rounds
+    # 1.0625 + 2^-12 to 1.0625 (its spacing at 1 is 2^-7), the E4M3 midpoint
+    # of 1 and 1.125, which ties to the even code, 1.0; without the bf16 step
+    # the value lies above the midpoint and becomes 1.125.
+    da = np.zeros((n, 1))
+    da[0, 0] = 448.0
+    da[1, 0] = 1.0625 + 2.0 ** -12
+    dWd, dWg, dWu = moe_ref._weight_grads(dy, ones, ones, da, da, "mxfp8")
+    assert dWd.shape == (2, 1) and dWg.shape == (1, 1)
+    assert dWd[0, 0] == 448.0
+    assert dWd[1, 0] == 32 * 2.0 ** -10
+    assert dWg[0, 0] == 449.0 and dWu[0, 0] == 449.0
+    # w h takes the same bf16 step (dy = ones)
+    dWd2, _, _ = moe_ref._weight_grads(ones, ones, da, da, da, "mxfp8")
+    assert dWd2[0, 0] == 449.0
+    # NVFP4 (activations: tensor scale 1), one 16-row block.  Column 0: 6, then
+    # 15 x 0.25: the scale is E4M3(6 / 6) = 1, and 0.25 is the midpoint of the
+    # E2M1 codes 0 and 0.5, so it ties to 0.  Column 1 (16 x 0.25): amax / 6 =
+    # 0.041666... lies between the E4M3 values 1.25 * 2^-5 and 1.375 * 2^-5 and
+    # rounds to the nearer, 0.04296875; 0.25 / 0.04296875 = 5.818... rounds to
+    # the code 6, so each row dequantises to 6 * 0.04296875 = 0.2578125.
+    # The other operand is 16 x 6, exact with scale E4M3(6 / 6) = 1 (a column
+    # of ones is not: its scale E4M3(1 / 6) = 0.171875 makes each 1 read
+    # 6 * 0.171875 = 1.03125).
+    m = 16
+    dy4 = np.full((m, 2), 0.25)
+    dy4[0, 0] = 6.0
+    six = np.full((m, 1), 6.0)
+    dWd4, _, _ = moe_ref._weight_grads(dy4, six, six, six, six, "nvfp4")
+    assert dWd4[0, 0] == 6.0 * 6.0
+    assert dWd4[1, 0] == 16 * 0.2578125 * 6.0
