@@ -207,14 +207,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "0488d5b73a4384318b35dbaf11c8a09795f6efa19595a613a3f3de703adf4165",
+    "csrc_sha256": "9df5ccc4e13f84ff55a6fe836e874824a352db104d99079025421dcc4d845b86",
     "bytes": {
-        "gemm_up_swiglu": 11576141670,
-        "gemm_down": 5643801446,
-        "gemm_bwd_u_swiglu": 6876249088,
-        "gemm_bwd_dx": 10763954278,
-        "gemm_wgrad_down": 8503758336,
-        "gemm_wgrad_gate_up": 16146945280,
+        "gemm_up_swiglu": 11563515238,
+        "gemm_down": 5640832051,
+        "gemm_bwd_u_swiglu": 6875002010,
+        "gemm_bwd_dx": 10710400768,
+        "gemm_wgrad_down": 8508768870,
+        "gemm_wgrad_gate_up": 16121603072,
     },
 }
 

@@ -50,7 +50,11 @@ struct KindTraits {
   static constexpr bool grouped = (KIND <= kBwdX);          // tiles follow expert segments
   static constexpr bool dense = (KIND >= kRouter);          // plain M x N tiles (router GEMM)
   static constexpr int n_out = (KIND == kUp || KIND == kBwdU) ? 3 : 1;
-  static constexpr int n_buf = (n_out == 3) ? 1 : 2;
+  // staging buffers per epilogue warp: the weight gradients keep one, so each
+  // warp has at most one dW store reading shared memory (measured: more dW
+  // store bytes in flight slow the operand loads more than they gain)
+  static constexpr bool wgrad = (KIND == kWgradD || KIND == kWgradGU);
+  static constexpr int n_buf = (n_out == 3 || wgrad) ? 1 : 2;
   // single-output epilogues are store-bound (weight gradients write 64 KB per
   // tile): two warps per TMEM lane quadrant, each taking half of the columns
   static constexpr int epi_warps = (n_out == 1) ? 8 : 4;
@@ -561,8 +565,11 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
-          uint8_t* buf = stg + (chunk_ctr & 1) * kStageChunk;
-          if (lane == 0) bulk_wait_read<1>();
+          uint8_t* buf = stg + (TR::n_buf == 2 ? (chunk_ctr & 1) : 0) * kStageChunk;
+          if (lane == 0) {
+            if constexpr (TR::n_buf == 2) bulk_wait_read<1>();
+            else bulk_wait_read<0>();
+          }
           __syncwarp();
           stage_row(buf, lane, v);
           fence_proxy_async_smem();

@@ -729,7 +729,15 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
             }
             continue;
           }
-          if (lane == 0) bulk_wait_read<0>();
+          if (lane == 0) {
+            // MXFP8 weight gradients: the warp's previous dW store has left
+            // for global memory, not only been read out of shared memory
+            // (measured: throttling the dW stores this way lets the operand
+            // loads through; 3.83 -> 3.41 ms for gate/up at T=8192.  NVFP4,
+            // with three stages, loses with it)
+            if constexpr (TR::wgrad && !NV) bulk_wait<0>();
+            else bulk_wait_read<0>();
+          }
           __syncwarp();
           stage_row(stg, lane, v);
           fence_proxy_async_smem();
