@@ -83,10 +83,12 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_NVFP4 = 2 } moe_precision_t;
  * kernels (the ring megakernel keeps no copy). */
 #define MOE_DEBUG_DUMP_QUANT 0x40u
 /* Fault-injection test hook (tests only): in the separate-kernel BF16
- * forward, the up GEMM's producer issues no loads, so its consumers' bounded
- * waits expire after wait_timeout_ns.  The kernel then exits cleanly (TMEM
- * freed, nothing in flight), the status word reads MOE_ERR_TIMEOUT at the next
- * moe_device_status, and the CUDA context stays usable.  Y is not valid. */
+ * forward, the up GEMM's producer issues no loads, and in a block-scaled
+ * backward the weight gradients' token pass copies no rows, so the waiting
+ * warps' bounded waits expire after wait_timeout_ns.  The kernel then exits
+ * cleanly (TMEM freed, nothing in flight), the status word reads
+ * MOE_ERR_TIMEOUT at the next moe_device_status, and the CUDA context stays
+ * usable.  Y (forward) or the weight gradients (backward) are not valid. */
 #define MOE_DEBUG_STALL_TEST 0x80u
 
 typedef struct {

@@ -1331,7 +1331,8 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     err = timed_launch(p, "quant_wgrad_tokens", st, [&] {
       // one wave: two CTAs (three 32 KB stages each) per SM
       return launch_gather_transpose_q(nv, dY, X, rp.perm_src, rp.totals, c.k, Rq, c.d, p->dYTq, p->dYTs, p->XTq,
-                                       p->XTs, p->status, (uint64_t)c.wait_timeout_ns, p->num_sms * 2, st);
+                                       p->XTs, p->status, (uint64_t)c.wait_timeout_ns,
+                                       (c.debug_flags & MOE_DEBUG_STALL_TEST) ? 1 : 0, p->num_sms * 2, st);
     });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: weight-gradient token quantisation launch");
     MxArgs w;

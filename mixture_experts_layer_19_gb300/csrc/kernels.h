@@ -88,11 +88,12 @@ cudaError_t launch_quant_transpose(const void* src, int E, int A, int B, void* q
 // Block-scaled weight gradients (wgrad_quant.cu): the sorted rows of two
 // token tensors, transposed and quantised along the sorted rows (A = row
 // capacity, B = columns): out[c, r] = Q(src[perm_src[r] / k, c]).  Waits
-// are bounded by timeout_ns (kStatusTimeout into status); grid: two CTAs
-// per SM.
+// are bounded by timeout_ns (kStatusTimeout into status); stall != 0 (test
+// hook) keeps the producer warps from copying anything; grid: two CTAs per SM.
 cudaError_t launch_gather_transpose_q(bool nv, const void* X0, const void* X1, const int32_t* perm_src,
                                       const int32_t* totals, int k, int A, int B, void* q0, void* sf0, void* q1,
-                                      void* sf1, int32_t* status, uint64_t timeout_ns, int grid, cudaStream_t st);
+                                      void* sf1, int32_t* status, uint64_t timeout_ns, int stall, int grid,
+                                      cudaStream_t st);
 cudaError_t prepare_gather_transpose_q(bool nv);   // its dynamic shared memory size, once
 // dst[i] = src[i] widened from bf16, i < n (debug dumps).
 cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, int grid, cudaStream_t st);

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kGtThreads, 2) gather_transpose_q_kernel(
     const __nv_bfloat16* __restrict__ X0, const __nv_bfloat16* __restrict__ X1, const int32_t* __restrict__ perm_src,
     const int32_t* __restrict__ totals, int k, uint32_t kmag, int A, int B, uint8_t* __restrict__ q0,
     uint8_t* __restrict__ sf0, uint8_t* __restrict__ q1, uint8_t* __restrict__ sf1, int32_t* status,
-    uint64_t timeout_ns) {
+    uint64_t timeout_ns, int stall) {
   extern __shared__ __align__(128) unsigned char gt_smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(gt_smem + kGtStages * kGtStageBytes);
   uint64_t* empty = full + kGtStages;
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kGtThreads, 2) gather_transpose_q_kernel(
   __syncthreads();
   const WaitCtl wc{status, abort_flag, timeout_ns};
   if (warp >= kGtQuantWarps) {
+    if (stall) return;   // test hook: no copies, so the quantising warps' waits expire
     constexpr int R = 128 / kGtProdWarps;   // rows per producer warp
     const int r0 = (warp - kGtQuantWarps) * R;
     int i = 0;
@@ -214,7 +215,8 @@ __global__ void __launch_bounds__(kGtThreads, 2) gather_transpose_q_kernel(
 
 cudaError_t launch_gather_transpose_q(bool nv, const void* X0, const void* X1, const int32_t* perm_src,
                                       const int32_t* totals, int k, int A, int B, void* q0, void* sf0, void* q1,
-                                      void* sf1, int32_t* status, uint64_t timeout_ns, int grid, cudaStream_t st) {
+                                      void* sf1, int32_t* status, uint64_t timeout_ns, int stall, int grid,
+                                      cudaStream_t st) {
   auto x0 = reinterpret_cast<const __nv_bfloat16*>(X0);
   auto x1 = reinterpret_cast<const __nv_bfloat16*>(X1);
   auto o0 = reinterpret_cast<uint8_t*>(q0);
@@ -226,7 +228,7 @@ cudaError_t launch_gather_transpose_q(bool nv, const void* X0, const void* X1, c
                             : 0u;
   auto kern = nv ? gather_transpose_q_kernel<true> : gather_transpose_q_kernel<false>;
   kern<<<grid, kGtThreads, kGtSmem, st>>>(x0, x1, perm_src, totals, k, kmag, A, B, o0, s0, o1, s1, status,
-                                          timeout_ns);
+                                          timeout_ns, stall);
   return cudaGetLastError();
 }
 

@@ -38,3 +38,35 @@ def test_stalled_producer_times_out_and_context_survives():
     assert ok.device_status() == 0
     Yr, _ = moe_ref.forward(h["X"], h["logits"], h["Wg"], h["Wu"], h["Wd"], k)
     assert rel_err(Y, Yr) <= BF16_TOL
+
+
+def test_stalled_token_pass_times_out_and_context_survives():
+    """The block-scaled weight gradients' token pass (a producer / quantiser
+    ring in shared memory): with the producers stalled, the quantising warps'
+    waits on the ring expire, the backward records MOE_ERR_TIMEOUT, and the
+    next plan's backward runs cleanly and repeats bit for bit."""
+    T, d, F, E, k = 256, 512, 512, 8, 2
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=5)
+    dY = g["dY"]
+    stalled = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8, wait_timeout_ns=50_000_000,
+                                  debug_flags=moe.MOE_DEBUG_STALL_TEST))
+    stalled.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    Y, saved = stalled.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    assert stalled.device_status() == 0            # the forward has no stall hook in block-scaled plans
+    t0 = time.perf_counter()
+    stalled.backward(dY, g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert stalled.device_status() == moe.MOE_ERR_TIMEOUT
+    assert elapsed < 2.0, elapsed
+    ok = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8))
+    ok.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    _, saved2 = ok.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    g1 = ok.backward(dY, g["X"], g["Wg"], g["Wu"], g["Wd"], saved2)
+    g2 = ok.backward(dY, g["X"], g["Wg"], g["Wu"], g["Wd"], saved2)
+    torch.cuda.synchronize()
+    assert ok.device_status() == 0
+    for name in ("dWg", "dWu", "dWd", "dX"):
+        assert torch.isfinite(g1[name].float()).all()
+        assert torch.equal(g1[name], g2[name]), name
