@@ -74,7 +74,10 @@ def _sorted_rows(src, perm, counts, k):
 
 
 @pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
-@pytest.mark.parametrize("case", [(300, 512, 768, 16, 3, 1.5), (200, 256, 512, 8, 2, 0.0)],
+@pytest.mark.parametrize("case", [(300, 512, 768, 16, 3, 1.5), (200, 256, 512, 8, 2, 0.0),
+                                  # one token, k = 1 (the plain-division row lookup); k = 8 over 32
+                                  # experts, most of them empty, 12 column blocks
+                                  (1, 256, 512, 4, 1, 0.0), (64, 768, 512, 32, 8, 1.1)],
                          ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
 def test_weight_gradient_operands_bit_exact(prec, case):
     """The block-scaled weight gradients' operands, transposed and quantised
