@@ -1083,7 +1083,8 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     return MOE_OK;
   }
   err = timed_launch(p, "gather", st, [&] {
-    return launch_gather(X, nullptr, rp.perm_src, rp.totals, c.k, c.d, p->Xg, nullptr, p->num_sms * 8, st);
+    return launch_gather(X, nullptr, rp.perm_src, rp.dest, rp.totals, (int)T, c.k, c.d, p->Xg, nullptr,
+                         p->num_sms * 8, st);
   });
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
   const void* ys = p->Xg;
@@ -1239,7 +1240,7 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     // last forward, which ran the separate schedule: gather dY alone then
     const bool xg_current = p->xg_X == X && p->xg_saved == saved && p->xg_T == T;
     err = timed_launch(p, "gather_bwd", st, [&] {
-      return launch_gather(dY, xg_current ? nullptr : X, rp.perm_src, rp.totals, c.k, c.d, p->dYg,
+      return launch_gather(dY, xg_current ? nullptr : X, rp.perm_src, rp.dest, rp.totals, Ti, c.k, c.d, p->dYg,
                            xg_current ? nullptr : p->Xg, p->num_sms * 8, st);
     });
   }

@@ -29,8 +29,10 @@ cudaError_t launch_router(const float* logits, int T, int E, int k, int32_t* chu
 cudaError_t launch_scan(int T, int E, const int32_t* chunk_hist, int32_t* chunk_base, const RoutingPtrs& rp,
                         cudaStream_t st);
 cudaError_t launch_permute(int T, int E, int k, const int32_t* chunk_base, const RoutingPtrs& rp, cudaStream_t st);
-cudaError_t launch_gather(const void* X0, const void* X1, const int32_t* perm_src, const int32_t* totals, int k,
-                          int d, void* G0, void* G1, int grid, cudaStream_t st);
+// Sorted rows G[r] = X[perm_src[r] / k] (X1 / G1 optional), written token by
+// token through dest; padding rows (perm_src < 0) zeroed.
+cudaError_t launch_gather(const void* X0, const void* X1, const int32_t* perm_src, const int32_t* dest,
+                          const int32_t* totals, int T, int k, int d, void* G0, void* G1, int grid, cudaStream_t st);
 cudaError_t launch_combine(const void* S, const int32_t* dest, const float* w, int T, int k, int d, void* Y,
                            int grid, cudaStream_t st);
 cudaError_t launch_router_grad(const float* dgp, const int32_t* dest, const int32_t* idx, const float* w, int T,

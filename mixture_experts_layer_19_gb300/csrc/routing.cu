@@ -120,49 +120,60 @@ __global__ void __launch_bounds__(32) permute_kernel(const int32_t* __restrict__
   permute_chunk(chunk_base, T, E, k, blockIdx.x, rp, cursor, threadIdx.x);
 }
 
-// -----------------------------------------------------------------------------
-// S4 (pull dispatch residue): sorted row r <- token row X[perm_src[r] / k];
-// padding rows are zero.  One warp per row, 16-byte vectors.  With two
-// sources (backward) the same rows of a second tensor are gathered too.
-// -----------------------------------------------------------------------------
+// S4 / B1: the sorted rows of one or two token tensors (G[r] = X[perm_src[r] /
+// k]), walked by token so that each token's row is read from HBM once: work
+// item (t, part) reads a quarter of token t's row (four 16-byte loads in
+// flight per lane and source) and writes it to the token's k sorted rows
+// dest[t k + j].  A second sweep zeroes the rows with perm_src < 0 (the
+// padding at the end of each expert's segment).  X1 / G1 may be null.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ X0, const uint4* __restrict__ X1,
                                                      const int32_t* __restrict__ perm_src,
-                                                     const int32_t* __restrict__ totals, int k, int d,
+                                                     const int32_t* __restrict__ dest,
+                                                     const int32_t* __restrict__ totals, int T, int k, int d,
                                                      uint4* __restrict__ G0, uint4* __restrict__ G1) {
-  const int rows = totals[0];
-  const int nvec = d / 8;
+  constexpr int kParts = 4;
+  const int nvec = d / 8, pvec = nvec / kParts;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps_total) {
-    const int src = perm_src[r];
+  for (int item = gw; item < T * kParts; item += warps_total) {
+    const int t = item / kParts, c0 = (item - t * kParts) * pvec;
+    const int dl = lane < k ? __ldg(dest + (size_t)t * k + lane) : 0;
+    const uint4* x0 = X0 + (size_t)t * nvec;
+    const uint4* x1 = X1 ? X1 + (size_t)t * nvec : nullptr;
+    // every lane runs the same trips (the shuffles below take the whole
+    // warp); only the loads and stores are guarded
+    for (int i0 = c0; i0 < c0 + pvec; i0 += 128) {
+      const int i = i0 + lane;
+      uint4 a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i + 32 * u < c0 + pvec) {
+          a[u] = __ldg(x0 + i + 32 * u);
+          if (G1) b[u] = __ldg(x1 + i + 32 * u);
+        }
+      for (int j = 0; j < k; ++j) {
+        const size_t r = (size_t)__shfl_sync(0xffffffffu, dl, j);
+        uint4* g0 = G0 + r * nvec;
+        uint4* g1 = G1 ? G1 + r * nvec : nullptr;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i + 32 * u < c0 + pvec) {
+            g0[i + 32 * u] = a[u];
+            if (G1) g1[i + 32 * u] = b[u];
+          }
+      }
+    }
+  }
+  const int rows = totals[0];
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int r = gw; r < rows; r += warps_total) {
+    if (__ldg(perm_src + r) >= 0) continue;
     uint4* g0 = G0 + (size_t)r * nvec;
     uint4* g1 = G1 ? G1 + (size_t)r * nvec : nullptr;
-    if (src < 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int i = lane; i < nvec; i += 32) {
-        g0[i] = z;
-        if (g1) g1[i] = z;
-      }
-    } else {
-      // four 16-byte loads in flight per lane and source
-      const size_t t = (size_t)(src / k);
-      const uint4* x0 = X0 + t * nvec;
-      const uint4* x1 = X1 ? X1 + t * nvec : nullptr;
-      for (int i = lane; i < nvec; i += 128) {
-        uint4 a[4], b[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (i + 32 * u < nvec) {
-            a[u] = __ldg(x0 + i + 32 * u);
-            if (g1) b[u] = __ldg(x1 + i + 32 * u);
-          }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (i + 32 * u < nvec) {
-            g0[i + 32 * u] = a[u];
-            if (g1) g1[i + 32 * u] = b[u];
-          }
-      }
+    for (int i = lane; i < nvec; i += 32) {
+      g0[i] = z;
+      if (G1) g1[i] = z;
     }
   }
 }
@@ -228,10 +239,10 @@ cudaError_t launch_permute(int T, int E, int k, const int32_t* chunk_base, const
 
 int route_chunks(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
 
-cudaError_t launch_gather(const void* X0, const void* X1, const int32_t* perm_src, const int32_t* totals, int k,
-                          int d, void* G0, void* G1, int grid, cudaStream_t st) {
+cudaError_t launch_gather(const void* X0, const void* X1, const int32_t* perm_src, const int32_t* dest,
+                          const int32_t* totals, int T, int k, int d, void* G0, void* G1, int grid, cudaStream_t st) {
   gather_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(X0), reinterpret_cast<const uint4*>(X1),
-                                      perm_src, totals, k, d, reinterpret_cast<uint4*>(G0),
+                                      perm_src, dest, totals, T, k, d, reinterpret_cast<uint4*>(G0),
                                       reinterpret_cast<uint4*>(G1));
   return cudaGetLastError();
 }
