@@ -1049,8 +1049,8 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
     });
     if (err == cudaSuccess)
       err = timed_launch(p, "gather_quant", st, [&] {
-        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.totals, c.k, nv ? c.d / 2 : c.d,
-                                    nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
+        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.dest, rp.totals, (int)T, c.k,
+                                    nv ? c.d / 2 : c.d, nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
       });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
     err = launch_block_scaled_fwd_gemms(p, rp, m_ab_st, m_ab_st16, st);
@@ -1264,8 +1264,8 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     });
     if (err == cudaSuccess)
       err = timed_launch(p, "gather_quant_dy", st, [&] {
-        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.totals, c.k, nv ? c.d / 2 : c.d,
-                                    nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
+        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.dest, rp.totals, (int)T, c.k,
+                                    nv ? c.d / 2 : c.d, nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
       });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dY gather launch");
   }

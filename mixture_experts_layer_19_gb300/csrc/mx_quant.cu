@@ -78,47 +78,69 @@ __global__ void __launch_bounds__(256) quant_transpose_kernel(const __nv_bfloat1
 // word), from the token-quantised copy (one quantisation per token, made by
 // quant_rows_kernel / nv_quant_rows_kernel) into the sorted rows' atoms;
 // padding rows get zero bytes and zero scales.  Same bytes as quantising each
-// routed row.  One warp per row; nblk = scale blocks per row (a multiple of 4).
+// routed row.  nblk = scale blocks per row (a multiple of 4).
 __global__ void __launch_bounds__(256) gather_rows_q_kernel(const uint8_t* __restrict__ q_tok,
                                                             const uint8_t* __restrict__ sf_tok,
                                                             const int32_t* __restrict__ perm_src,
-                                                            const int32_t* __restrict__ totals, int k, int row_bytes,
-                                                            int nblk, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
-  const int rows = totals[0];
+                                                            const int32_t* __restrict__ dest,
+                                                            const int32_t* __restrict__ totals, int T, int k,
+                                                            int row_bytes, int nblk, uint8_t* __restrict__ q,
+                                                            uint8_t* __restrict__ sf) {
+  // walked by token: work item (t, part) reads a quarter of token t's codes
+  // and scale words once and writes them to the token's k sorted rows
+  // dest[t k + j]; then the padding rows (perm_src < 0) are zeroed
+  constexpr int kParts = 4;
   const int nvec = row_bytes / 16;
   const int nwords = nblk / 4;
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
-  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps_total) {
-    const int src = perm_src[r];
-    uint4* dq = reinterpret_cast<uint4*>(q + (size_t)r * row_bytes);
-    if (src < 0) {
-      for (int i = lane; i < nvec; i += 32) dq[i] = make_uint4(0, 0, 0, 0);
-      for (int w = lane; w < nwords; w += 32) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) = 0u;
-      continue;
-    }
-    const int64_t t = src / k;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int item = gw; item < T * kParts; item += warps_total) {
+    const int t = item / kParts, part = item - t * kParts;
+    const int v0 = part * nvec / kParts, v1 = (part + 1) * nvec / kParts;
+    const int w0 = part * nwords / kParts, w1 = (part + 1) * nwords / kParts;
+    const int dl = lane < k ? __ldg(dest + (size_t)t * k + lane) : 0;
     const uint4* sq = reinterpret_cast<const uint4*>(q_tok + (size_t)t * row_bytes);
-    for (int i = lane; i < nvec; i += 128) {
+    // every lane runs the same trips (the shuffles take the whole warp)
+    for (int i0 = v0; i0 < v1; i0 += 128) {
+      const int i = i0 + lane;
       uint4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (i + 32 * u < nvec) v[u] = __ldg(sq + i + 32 * u);
+        if (i + 32 * u < v1) v[u] = __ldg(sq + i + 32 * u);
+      for (int j = 0; j < k; ++j) {
+        uint4* dq = reinterpret_cast<uint4*>(q + (size_t)__shfl_sync(0xffffffffu, dl, j) * row_bytes);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i + 32 * u < nvec) dq[i + 32 * u] = v[u];
+        for (int u = 0; u < 4; ++u)
+          if (i + 32 * u < v1) dq[i + 32 * u] = v[u];
+      }
     }
-    for (int w = lane; w < nwords; w += 32)
-      *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) =
-          __ldg(reinterpret_cast<const uint32_t*>(sf_tok + sf_atom_offset(t, 4 * w, nblk)));
+    for (int w00 = w0; w00 < w1; w00 += 32) {
+      const int w = w00 + lane;
+      const uint32_t sw =
+          w < w1 ? __ldg(reinterpret_cast<const uint32_t*>(sf_tok + sf_atom_offset(t, 4 * w, nblk))) : 0u;
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, dl, j);
+        if (w < w1) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) = sw;
+      }
+    }
+  }
+  const int rows = totals[0];
+  for (int r = gw; r < rows; r += warps_total) {
+    if (__ldg(perm_src + r) >= 0) continue;
+    uint4* dq = reinterpret_cast<uint4*>(q + (size_t)r * row_bytes);
+    for (int i = lane; i < nvec; i += 32) dq[i] = make_uint4(0, 0, 0, 0);
+    for (int w = lane; w < nwords; w += 32) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) = 0u;
   }
 }
 
-cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* totals,
-                                 int k, int row_bytes, int nblk, void* q, void* sf, int grid, cudaStream_t st) {
+cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* dest,
+                                 const int32_t* totals, int T, int k, int row_bytes, int nblk, void* q, void* sf,
+                                 int grid, cudaStream_t st) {
   gather_rows_q_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(q_tok),
-                                             reinterpret_cast<const uint8_t*>(sf_tok), perm_src, totals, k, row_bytes,
-                                             nblk, reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
+                                             reinterpret_cast<const uint8_t*>(sf_tok), perm_src, dest, totals, T, k,
+                                             row_bytes, nblk, reinterpret_cast<uint8_t*>(q),
+                                             reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }
 
