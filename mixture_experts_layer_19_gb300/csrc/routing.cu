@@ -22,7 +22,7 @@
 
 namespace moe {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 512;   // 16 warps: four tokens of a 64-token chunk each
 
 // -----------------------------------------------------------------------------
 // S1: one warp per token (route_token, routing.cuh); the block also
