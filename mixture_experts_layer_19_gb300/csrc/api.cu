@@ -237,6 +237,7 @@ struct moe_plan_s {
   unsigned long long* gbar = nullptr;
   // router GEMM backward: dlogits in bf16 [T_max, E]
   void* dlg_bf16 = nullptr;
+  float* router_part = nullptr;   // split-K partial sums of the router GEMMs
   // virtual-rank expert parallelism (ep_ranks >= 2): home slots of the pushed
   // rows [T_max * k, d] bf16, of the pushed <u, h> partials, and the flags
   void* ep_ws = nullptr;
@@ -247,6 +248,16 @@ struct moe_plan_s {
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
 };
+
+namespace {
+// K splits for a router GEMM with `tiles` output tiles and nkb K blocks: enough
+// to fill about one wave of the SMs, at most kRouterMaxSplit and nkb.
+constexpr int kRouterMaxSplit = 8;
+int router_splits(const moe_plan_s* p, int64_t tiles, int64_t nkb) {
+  if (tiles >= p->num_sms) return 1;
+  return (int)std::max<int64_t>(1, std::min<int64_t>({p->num_sms / tiles, nkb, (int64_t)kRouterMaxSplit}));
+}
+}  // namespace
 
 namespace {
 
@@ -805,6 +816,16 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   }
   // router GEMM backward: dlogits rounded to bf16 for the tensor cores
   err = cudaMalloc(&p->dlg_bf16, (size_t)std::max<int64_t>(1, c.T_max) * c.E * 2);
+  if (err == cudaSuccess) {
+    // split-K partials: the logits GEMM splits only while S * ceil(T/128) <=
+    // SMs (so S * T <= 128 * SMs) and S <= 8; the dWr GEMM at most its
+    // largest split of E x d
+    const int64_t fwd = std::min<int64_t>(128 * (int64_t)p->num_sms, kRouterMaxSplit * std::max<int64_t>(1, c.T_max)) *
+                        c.E;
+    const int64_t tiles_w = ((c.E + BM - 1) / BM) * (c.d / BN);
+    const int64_t dw = (int64_t)router_splits(p, tiles_w, kRouterMaxSplit) * c.E * c.d;
+    err = cudaMalloc(&p->router_part, (size_t)std::max(fwd, dw) * sizeof(float));
+  }
   if (err == cudaSuccess) err = prepare_gemm_router();
   if (err == cudaSuccess && c.ep_ranks >= 2) {
     const size_t pairs = (size_t)c.T_max * c.k;
@@ -824,6 +845,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out) {
   if (err != cudaSuccess) {
     if (p->ep_ws) cudaFree(p->ep_ws);
     if (p->dlg_bf16) cudaFree(p->dlg_bf16);
+    if (p->router_part) cudaFree(p->router_part);
     if (p->mx_ws) cudaFree(p->mx_ws);
     if (p->ring_ws) cudaFree(p->ring_ws);
     cudaFree(p->ws);
@@ -846,6 +868,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   if (p->mx_ws) cudaFree(p->mx_ws);
   if (p->ring_ws) cudaFree(p->ring_ws);
   if (p->dlg_bf16) cudaFree(p->dlg_bf16);
+  if (p->router_part) cudaFree(p->router_part);
   if (p->ep_ws) cudaFree(p->ep_ws);
   cudaError_t err = cudaFree(p->ws);
   delete p;
@@ -1454,10 +1477,16 @@ moe_status_t moe_router_forward(moe_plan_t p, int64_t T, const void* X, const vo
   GemmArgs a = router_args(p, T);
   if (!map_kmajor(&a.mapA, X, c.d, T) || !map_kmajor(&a.mapB0, Wr, c.d, c.E, BN))
     return fail(MOE_ERR_CUDA, "moe_router_forward: tensor maps");
-  a.out_f32 = logits;
   const int64_t tiles = ((T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
+  const int S = router_splits(p, tiles, (c.d + BK - 1) / BK);
+  a.out_f32 = S > 1 ? p->router_part : logits;
+  a.ksplit = S;
   cudaError_t err = timed_launch(p, "gemm_router", st,
-                                 [&] { return launch_gemm_router(kRouter, a, router_grid(p, tiles), st); });
+                                 [&] { return launch_gemm_router(kRouter, a, router_grid(p, tiles * S), st); });
+  if (err == cudaSuccess && S > 1)
+    err = timed_launch(p, "router_split_sum", st, [&] {
+      return launch_split_sum(p->router_part, S, T * c.E, logits, nullptr, p->num_sms * 4, st);
+    });
   if (err != cudaSuccess) return cuda_fail(err, "moe_router_forward: launch");
   return MOE_OK;
 }
@@ -1488,8 +1517,15 @@ moe_status_t moe_router_backward(moe_plan_t p, int64_t T, const void* X, const v
                      [&] { return launch_gemm_router(kRouterDX, x, router_grid(p, tx), st); });
   if (err != cudaSuccess) return cuda_fail(err, "moe_router_backward: dX launch");
   const int64_t tw = ((c.E + BM - 1) / BM) * (c.d / BN);
+  const int Sw = router_splits(p, tw, (T + BK - 1) / BK);
+  w.ksplit = Sw;
+  w.part_f32 = p->router_part;
   err = timed_launch(p, "gemm_router_dw", st,
-                     [&] { return launch_gemm_router(kRouterDW, w, router_grid(p, tw), st); });
+                     [&] { return launch_gemm_router(kRouterDW, w, router_grid(p, tw * Sw), st); });
+  if (err == cudaSuccess && Sw > 1)
+    err = timed_launch(p, "router_dw_split_sum", st, [&] {
+      return launch_split_sum(p->router_part, Sw, (int64_t)c.E * c.d, nullptr, dWr, p->num_sms * 4, st);
+    });
   if (err != cudaSuccess) return cuda_fail(err, "moe_router_backward: dWr launch");
   return MOE_OK;
 }

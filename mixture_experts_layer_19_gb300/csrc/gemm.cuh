@@ -77,7 +77,9 @@ struct GemmArgs {
   const int32_t* perm_src;   // kBwdU: flat pair of each sorted row (-1 = padding)
   const float* wts;          // kBwdU: gate weights [T*k]
   float* dgp;                // kBwdU: [R, F/256] partial <u, h> per N tile
-  float* out_f32;            // kRouter: logits [T, E]
+  float* out_f32;            // kRouter: logits [T, E] (with ksplit > 1: partials [ksplit, T, E])
+  float* part_f32;           // kRouterDW with ksplit > 1: fp32 partials [ksplit, E, d]
+  int ksplit;                // router kinds kRouter / kRouterDW: K range split over this many tiles (0 / 1: none)
   __nv_bfloat16* io_bf16;    // kRouterDX: dX [T, d], read and written
   int32_t* status;
   uint64_t timeout_ns;
@@ -91,7 +93,8 @@ struct Tile {
   int e, mt, nt;   // expert, M tile, N tile
   int row0;        // first sorted row (grouped) / first output row inside the expert (wgrad)
   int nkb;         // K slices
-  int kbase;       // first sorted row of the K range (wgrad)
+  int kbase;       // first sorted row of the K range (wgrad); first K of the split (router kinds)
+  int split;       // router kinds: which K split this tile's partial sums belong to
 };
 
 // The helpers below take any argument struct with E, d, F, poff, mtile_off
@@ -133,7 +136,7 @@ __device__ __forceinline__ int dense_nkb(const G& g) {
 
 template <int KIND, class G>
 __device__ __forceinline__ int total_tiles(const G& g) {
-  if constexpr (KindTraits<KIND>::dense) return dense_mt<KIND>(g) * dense_nt<KIND>(g);
+  if constexpr (KindTraits<KIND>::dense) return dense_mt<KIND>(g) * dense_nt<KIND>(g) * max(1, g.ksplit);
   if (KindTraits<KIND>::grouped) return g.mtile_off[g.E] * n_tiles_n<KIND>(g);
   return g.E * n_tiles_m_wgrad<KIND>(g) * n_tiles_n<KIND>(g);
 }
@@ -141,14 +144,19 @@ __device__ __forceinline__ int total_tiles(const G& g) {
 template <int KIND, class G>
 __device__ __forceinline__ Tile decode_tile(const G& g, int tile) {
   Tile t;
-  if constexpr (KindTraits<KIND>::dense) {  // (n, m) with m fastest
-    const int MT = dense_mt<KIND>(g);
+  t.split = 0;
+  if constexpr (KindTraits<KIND>::dense) {  // (split, n, m) with m fastest, split slowest
+    const int MT = dense_mt<KIND>(g), NT = dense_nt<KIND>(g);
+    const int S = max(1, g.ksplit);
+    t.split = tile / (MT * NT);
+    const int local = tile - t.split * MT * NT;
     t.e = 0;
-    t.nt = tile / MT;
-    t.mt = tile - t.nt * MT;
+    t.nt = local / MT;
+    t.mt = local - t.nt * MT;
     t.row0 = t.mt * BM;
-    t.nkb = dense_nkb<KIND>(g);
-    t.kbase = 0;
+    const int nkb = dense_nkb<KIND>(g), base = nkb / S, rem = nkb % S;
+    t.nkb = base + (t.split < rem ? 1 : 0);
+    t.kbase = (t.split * base + min(t.split, rem)) * BK;
     return t;
   }
   const int NT = n_tiles_n<KIND>(g);
@@ -189,7 +197,7 @@ __device__ __forceinline__ Tile decode_tile(const G& g, int tile) {
 template <int KIND>
 __device__ __forceinline__ void load_stage(const GemmArgs& g, const Tile& t, int kb, uint8_t* sa, uint8_t* sb,
                                            uint64_t* bar, uint64_t pol_w, uint64_t pol_a) {
-  const int k0 = kb * BK;
+  const int k0 = kb * BK + (KindTraits<KIND>::dense ? t.kbase : 0);
   if (KIND == kUp) {
     tma_load_2d(sa, &g.mapA, k0, t.row0, bar, pol_a);
     tma_load_2d(sb, &g.mapB0, k0, t.e * g.F + t.nt * 128, bar, pol_w);
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
           const int col0 = t.nt * BN + c * 32;
           if (row < g.T) {
             if (KIND == kRouter) {
-              float4* dst = reinterpret_cast<float4*>(g.out_f32 + (size_t)row * g.E + col0);
+              float4* dst = reinterpret_cast<float4*>(g.out_f32 + ((size_t)t.split * g.T + row) * g.E + col0);
               const int nv = min(32, g.E - col0) / 4;  // E % 8 == 0: whole 16-byte vectors
               for (int v = 0; v < nv; ++v)
                 dst[v] = make_float4(__uint_as_float(rv[4 * v]), __uint_as_float(rv[4 * v + 1]),
@@ -564,6 +572,19 @@ __global__ void __launch_bounds__(KindTraits<KIND>::threads, 1) gemm_kernel(cons
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+          if constexpr (KIND == kRouterDW) {
+            if (g.ksplit > 1) {
+              // split K: this split's fp32 partial sums, one row per lane
+              if (rowq + lane < g.E) {
+                float4* dst = reinterpret_cast<float4*>(g.part_f32 + ((size_t)t.split * g.E + rowq + lane) * g.d +
+                                                        t.nt * BN + c * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4) dst[v4] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+              }
+              ++chunk_ctr;
+              continue;
+            }
           }
           uint8_t* buf = stg + (TR::n_buf == 2 ? (chunk_ctr & 1) : 0) * kStageChunk;
           if (lane == 0) {

@@ -79,6 +79,10 @@ cudaError_t launch_ep_push(const EpArgs& a, cudaStream_t st);
 cudaError_t prepare_ep();
 
 // Router GEMM (gemm_router.cu): kind 6 logits, 7 dX += dlogits Wr, 8 dWr.
+// out = sum over s < S of part[s] (n values each, n % 4 == 0), in split order,
+// into out_f32 or (out_f32 null) rounded once into bf16 out_bf16.
+cudaError_t launch_split_sum(const float* part, int S, int64_t n, float* out_f32, void* out_bf16, int grid,
+                             cudaStream_t st);
 cudaError_t launch_gemm_router(int kind, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t prepare_gemm_router();
 cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, int grid, cudaStream_t st);
