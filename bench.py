@@ -207,14 +207,14 @@ def layer_roofline(shape, peaks, e_act: int):
 # sources makes measured_traffic() report null until a new capture is taken.
 NCU_TRAFFIC = {
     "workload": WORKLOAD,
-    "csrc_sha256": "9df5ccc4e13f84ff55a6fe836e874824a352db104d99079025421dcc4d845b86",
+    "csrc_sha256": "2b67d396b0083f3c8f356e821589e1ebb991c02e7b1f81df11974171b3cbe150",
     "bytes": {
-        "gemm_up_swiglu": 11563515238,
-        "gemm_down": 5640832051,
-        "gemm_bwd_u_swiglu": 6875002010,
-        "gemm_bwd_dx": 10710400768,
-        "gemm_wgrad_down": 8508768870,
-        "gemm_wgrad_gate_up": 16121603072,
+        "gemm_up_swiglu": 11549616282,
+        "gemm_down": 5641070285,
+        "gemm_bwd_u_swiglu": 6876470170,
+        "gemm_bwd_dx": 10699051725,
+        "gemm_wgrad_down": 8508401101,
+        "gemm_wgrad_gate_up": 16121594010,
     },
 }
 
