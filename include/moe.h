@@ -275,10 +275,12 @@ moe_status_t moe_get_routing(moe_plan_t plan, int64_t T, const void* saved, int3
  *   X      [T, d]  bf16 device, row-major (the same tokens moe_forward takes)
  *   Wr     [E, d]  bf16 device, row-major ([out, in] convention)
  *   logits [T, E]  fp32 device, written (the input moe_forward takes)
- * fp32 accumulation on the tensor cores.  Needs E % 8 == 0
- * (MOE_ERR_UNSUPPORTED otherwise); T <= T_max; all pointers 16-byte aligned
- * (MOE_ERR_INVALID_ARG otherwise, nothing enqueued).  T = 0 is a no-op.
- * Enqueued on `stream`. */
+ * fp32 accumulation on the tensor cores; when T/128 tiles leave SMs idle,
+ * the K range (d) is split over up to 8 tiles whose fp32 partials (plan
+ * workspace) are summed in split order, so the result is deterministic for
+ * a given T.  Needs E % 8 == 0 (MOE_ERR_UNSUPPORTED otherwise); T <= T_max;
+ * all pointers 16-byte aligned (MOE_ERR_INVALID_ARG otherwise, nothing
+ * enqueued).  T = 0 is a no-op.  Enqueued on `stream`. */
 moe_status_t moe_router_forward(moe_plan_t plan, int64_t T, const void* X, const void* Wr, float* logits,
                                 moe_stream_t stream);
 
@@ -287,7 +289,9 @@ moe_status_t moe_router_forward(moe_plan_t plan, int64_t T, const void* X, const
  *               one bf16 rounding), so passing moe_backward's dX gives the
  *               token gradient through both the experts and the router;
  *   dWr [E, d]  bf16 device, written: dWr = dlogits^T X, reduced over the T
- *               tokens in one fixed order (bitwise deterministic).
+ *               tokens in one fixed order (bitwise deterministic; split over
+ *               up to 8 token ranges summed in range order when its
+ *               E/128 x d/256 tiles leave SMs idle).
  * dlogits is rounded to bf16 for the tensor cores (into plan workspace).
  * Same shape, alignment and error rules as moe_router_forward; with T = 0,
  * dWr is zeroed and the other pointers are not used. */
