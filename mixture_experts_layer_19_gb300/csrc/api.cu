@@ -1064,17 +1064,12 @@ moe_status_t moe_forward(moe_plan_t p, int64_t T, const void* X, const float* lo
   if (mx) {
     // MXFP8 / NVFP4: gather + quantise X along d, block-scaled [a|b] GEMM with
     // SwiGLU and h re-quantised along F in its epilogue, block-scaled down GEMM.
-    // each token quantised once, then its bytes and scale words copied into
-    // the sorted rows (the same bytes as quantising every routed row)
-    err = timed_launch(p, "quant_tokens", st, [&] {
-      return nv ? launch_nv_quant_rows(X, T, c.d, nullptr, p->Xtq, p->Xts, p->num_sms * 8, st)
-                : launch_quant_rows(X, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
+    // each token quantised once and its codes and scale words stored straight
+    // into its k sorted rows (the same bytes as quantising every routed row)
+    err = timed_launch(p, "quant_scatter", st, [&] {
+      return launch_quant_scatter_rows(nv, X, rp.perm_src, rp.dest, rp.totals, (int)T, c.k, c.d, p->Xq, p->Xs,
+                                       p->num_sms * 8, st);
     });
-    if (err == cudaSuccess)
-      err = timed_launch(p, "gather_quant", st, [&] {
-        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.dest, rp.totals, (int)T, c.k,
-                                    nv ? c.d / 2 : c.d, nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
-      });
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: gather launch");
     err = launch_block_scaled_fwd_gemms(p, rp, m_ab_st, m_ab_st16, st);
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward: block-scaled GEMM launch");
@@ -1281,15 +1276,10 @@ moe_status_t moe_backward(moe_plan_t p, int64_t T, const void* dY, const void* X
     // epilogue; dx GEMM against [Wg^T; Wu^T] (quantised along F).  The weight
     // gradients below are block-scaled too, on operands quantised along the
     // tokens.
-    err = timed_launch(p, "quant_tokens_dy", st, [&] {
-      return nv ? launch_nv_quant_rows(dY, T, c.d, nullptr, p->Xtq, p->Xts, p->num_sms * 8, st)
-                : launch_quant_rows(dY, T, c.d, p->Xtq, p->Xts, p->num_sms * 8, st);
+    err = timed_launch(p, "quant_scatter_dy", st, [&] {
+      return launch_quant_scatter_rows(nv, dY, rp.perm_src, rp.dest, rp.totals, (int)T, c.k, c.d, p->Xq, p->Xs,
+                                       p->num_sms * 8, st);
     });
-    if (err == cudaSuccess)
-      err = timed_launch(p, "gather_quant_dy", st, [&] {
-        return launch_gather_rows_q(p->Xtq, p->Xts, rp.perm_src, rp.dest, rp.totals, (int)T, c.k,
-                                    nv ? c.d / 2 : c.d, nv ? c.d / 16 : c.d / 32, p->Xq, p->Xs, p->num_sms * 8, st);
-      });
     if (err != cudaSuccess) return cuda_fail(err, "moe_backward: dY gather launch");
   }
   if (mx) {

@@ -105,9 +105,12 @@ cudaError_t prepare_gather_transpose_q(bool nv);   // its dynamic shared memory 
 cudaError_t launch_widen_bf16(const void* src, float* dst, int64_t n, int grid, cudaStream_t st);
 // Sorted rows <- token-quantised rows (E4M3 or packed E2M1 bytes, row_bytes
 // per row, and nblk scale bytes per row in the atom layout).
-cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* dest,
-                                 const int32_t* totals, int T, int k, int row_bytes, int nblk, void* q, void* sf,
-                                 int grid, cudaStream_t st);
+// Block-scaled sorted rows straight from the bf16 token rows: each token
+// quantised along d once (MXFP8, or NVFP4 with tensor scale 1) and written to
+// its k sorted rows through dest; padding rows (perm_src < 0) zeroed.
+cudaError_t launch_quant_scatter_rows(bool nv, const void* src, const int32_t* perm_src, const int32_t* dest,
+                                      const int32_t* totals, int T, int k, int d, void* q, void* sf, int grid,
+                                      cudaStream_t st);
 struct MxArgs;
 // kind 0 up, 1 down, 2 bwd-u, 3 bwd-x, 4 wgrad down, 5 wgrad gate/up (K = each
 // expert's tokens, transposed operands quantised along the tokens); nv: the

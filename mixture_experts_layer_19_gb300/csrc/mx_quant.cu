@@ -3,13 +3,11 @@
 //  * quant_rows_kernel: a bf16 row-major [rows, K] matrix -> E4M3 [rows, K] +
 //    scale atoms, blocks of 32 along K (the expert weights once per optimiser
 //    step, and the public moe_mx_quantize utility).
-//    The same kernel quantises the tokens (X, or dY in the backward) once per
-//    token for the dispatch (MXFP8 activation quantisation inside the
-//    dispatch datapath: kucoin page "Cursor's MoK réalise une amélioration des
-//    performances de 2,37x sur NVIDIA GB300 NVL72", section 02).
-//  * gather_rows_q_kernel: sorted row r <- the quantised row of token
-//    perm_src[r] / k, element bytes and scale words; padding rows -> zero
-//    bytes and zero scales (MXFP8 and NVFP4 rows alike).
+//    The same kernel quantises the tokens (X) once per token for the ring
+//    megakernel's movers.
+//  * quant_scatter_rows_kernel: each token row quantised once (MXFP8, or
+//    NVFP4 with tensor scale 1) and stored into its k sorted rows; padding
+//    rows -> zero bytes and zero scales.
 // Quantisers: one thread per 32-element block: 64 contiguous input bytes, 32
 // output bytes.
 #include <cuda_bf16.h>
@@ -17,6 +15,7 @@
 
 #include "kernels.h"
 #include "mx.cuh"
+#include "nv.cuh"
 
 namespace moe {
 
@@ -73,74 +72,95 @@ __global__ void __launch_bounds__(256) quant_transpose_kernel(const __nv_bfloat1
   }
 }
 
-// Sorted row r <- the quantised row of token perm_src[r] / k: its
-// row_bytes element bytes and its scale words (4 blocks = 4 bytes per atom
-// word), from the token-quantised copy (one quantisation per token, made by
-// quant_rows_kernel / nv_quant_rows_kernel) into the sorted rows' atoms;
-// padding rows get zero bytes and zero scales.  Same bytes as quantising each
-// routed row.  nblk = scale blocks per row (a multiple of 4).
-__global__ void __launch_bounds__(256) gather_rows_q_kernel(const uint8_t* __restrict__ q_tok,
-                                                            const uint8_t* __restrict__ sf_tok,
-                                                            const int32_t* __restrict__ perm_src,
-                                                            const int32_t* __restrict__ dest,
-                                                            const int32_t* __restrict__ totals, int T, int k,
-                                                            int row_bytes, int nblk, uint8_t* __restrict__ q,
-                                                            uint8_t* __restrict__ sf) {
-  // walked by token: work item (t, part) reads a quarter of token t's codes
-  // and scale words once and writes them to the token's k sorted rows
-  // dest[t k + j]; then the padding rows (perm_src < 0) are zeroed
-  constexpr int kParts = 4;
-  const int nvec = row_bytes / 16;
-  const int nwords = nblk / 4;
+// S4 / B1 block-scaled: each token row (X, or dY in the backward) quantised
+// along d once and written straight into its k sorted rows -- the same bytes
+// and scale words as quantising every routed row (activation quantisation
+// inside the dispatch: kucoin page "Cursor's MoK réalise une amélioration des
+// performances de 2,37x sur NVIDIA GB300 NVL72", section 02).  Thread i of the grid-wide
+// sweep takes block i of the token-major order (token t, 32-value block kb):
+// it loads the 32 bf16 values, encodes them (MXFP8: E4M3 + one E8M0 scale;
+// NVFP4: E2M1 + two E4M3 scales, tensor scale 1) and stores the codes to row
+// dest[t k + j] for every slot j; four (MXFP8) or two (NVFP4) neighbouring
+// lanes pack their scale bytes into one 4-byte atom word first.  The padding
+// rows (perm_src < 0) get zero codes and scales.  d % 256 == 0, so the lanes
+// that pack one word always hold the same token.
+template <bool NV>
+__global__ void __launch_bounds__(256) quant_scatter_rows_kernel(const __nv_bfloat16* __restrict__ src,
+                                                                 const int32_t* __restrict__ perm_src,
+                                                                 const int32_t* __restrict__ dest,
+                                                                 const int32_t* __restrict__ totals, int T, int k,
+                                                                 int d, uint8_t* __restrict__ q,
+                                                                 uint8_t* __restrict__ sf) {
+  const int kb32 = d / 32;                      // 32-value blocks per row
+  const int row_bytes = NV ? d / 2 : d;
+  const int nblk = NV ? d / 16 : d / 32;        // scale blocks per row
+  const int64_t total = (int64_t)T * kb32;
   const int lane = threadIdx.x & 31;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  for (int item = gw; item < T * kParts; item += warps_total) {
-    const int t = item / kParts, part = item - t * kParts;
-    const int v0 = part * nvec / kParts, v1 = (part + 1) * nvec / kParts;
-    const int w0 = part * nwords / kParts, w1 = (part + 1) * nwords / kParts;
-    const int dl = lane < k ? __ldg(dest + (size_t)t * k + lane) : 0;
-    const uint4* sq = reinterpret_cast<const uint4*>(q_tok + (size_t)t * row_bytes);
-    // every lane runs the same trips (the shuffles take the whole warp)
-    for (int i0 = v0; i0 < v1; i0 += 128) {
-      const int i = i0 + lane;
-      uint4 v[4];
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const float rc1 = nv_rc(1.0f);
+  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < total;
+       base += warps_total * 32) {
+    const int64_t i = base + lane;
+    const bool valid = i < total;
+    const int t = valid ? (int)(i / kb32) : 0;
+    const int kb = valid ? (int)(i - (int64_t)t * kb32) : 0;
+    float v[32];
+    if (valid) load_bf16x32_f(src + (size_t)t * d + kb * 32, v);
+    else
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i + 32 * u < v1) v[u] = __ldg(sq + i + 32 * u);
-      for (int j = 0; j < k; ++j) {
-        uint4* dq = reinterpret_cast<uint4*>(q + (size_t)__shfl_sync(0xffffffffu, dl, j) * row_bytes);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (i + 32 * u < v1) dq[i + 32 * u] = v[u];
-      }
+      for (int m = 0; m < 32; ++m) v[m] = 0.0f;
+    uint4 c0, c1;
+    uint32_t sword;   // this lane's scale bytes, packed with its neighbours' below
+    if constexpr (NV) {
+      const uint32_t s2 = nv_encode32(v, rc1, 1.0f, c0);
+      c1 = make_uint4(0, 0, 0, 0);
+      const uint32_t o2 = __shfl_down_sync(0xffffffffu, s2, 1);
+      sword = s2 | (o2 << 16);                  // valid in even lanes: blocks 2 kb .. 2 kb + 3
+    } else {
+      const int xe = mx_block_exponent(amax32(v));
+      uint32_t o[8];
+      mx_encode32(v, xe, o);
+      c0 = make_uint4(o[0], o[1], o[2], o[3]);
+      c1 = make_uint4(o[4], o[5], o[6], o[7]);
+      uint32_t b = (uint32_t)(xe + 127);
+      b |= __shfl_down_sync(0xffffffffu, b, 1) << 8;
+      b |= __shfl_down_sync(0xffffffffu, b, 2) << 16;
+      sword = b;                                // valid in lanes 4n: blocks kb .. kb + 3
     }
-    for (int w00 = w0; w00 < w1; w00 += 32) {
-      const int w = w00 + lane;
-      const uint32_t sw =
-          w < w1 ? __ldg(reinterpret_cast<const uint32_t*>(sf_tok + sf_atom_offset(t, 4 * w, nblk))) : 0u;
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, dl, j);
-        if (w < w1) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) = sw;
+    const bool word_lane = NV ? (lane & 1) == 0 : (lane & 3) == 0;
+    if (!valid) continue;
+    for (int j = 0; j < k; ++j) {
+      const int r = __ldg(dest + (size_t)t * k + j);
+      uint8_t* dq = q + (size_t)r * row_bytes;
+      if constexpr (NV) {
+        *reinterpret_cast<uint4*>(dq + kb * 16) = c0;
+        if (word_lane) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 2 * kb, nblk)) = sword;
+      } else {
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dq + kb * 32), "r"(c0.x),
+                     "r"(c0.y), "r"(c0.z), "r"(c0.w), "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w)
+                     : "memory");
+        if (word_lane) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, kb, nblk)) = sword;
       }
     }
   }
+  // padding rows: zero codes and scales
   const int rows = totals[0];
-  for (int r = gw; r < rows; r += warps_total) {
+  const int nvec = row_bytes / 16, nwords = nblk / 4;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int r = gw; r < rows; r += (int)warps_total) {
     if (__ldg(perm_src + r) >= 0) continue;
     uint4* dq = reinterpret_cast<uint4*>(q + (size_t)r * row_bytes);
-    for (int i = lane; i < nvec; i += 32) dq[i] = make_uint4(0, 0, 0, 0);
+    for (int x = lane; x < nvec; x += 32) dq[x] = make_uint4(0, 0, 0, 0);
     for (int w = lane; w < nwords; w += 32) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(r, 4 * w, nblk)) = 0u;
   }
 }
 
-cudaError_t launch_gather_rows_q(const void* q_tok, const void* sf_tok, const int32_t* perm_src, const int32_t* dest,
-                                 const int32_t* totals, int T, int k, int row_bytes, int nblk, void* q, void* sf,
-                                 int grid, cudaStream_t st) {
-  gather_rows_q_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(q_tok),
-                                             reinterpret_cast<const uint8_t*>(sf_tok), perm_src, dest, totals, T, k,
-                                             row_bytes, nblk, reinterpret_cast<uint8_t*>(q),
-                                             reinterpret_cast<uint8_t*>(sf));
+cudaError_t launch_quant_scatter_rows(bool nv, const void* src, const int32_t* perm_src, const int32_t* dest,
+                                      const int32_t* totals, int T, int k, int d, void* q, void* sf, int grid,
+                                      cudaStream_t st) {
+  auto kern = nv ? quant_scatter_rows_kernel<true> : quant_scatter_rows_kernel<false>;
+  kern<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), perm_src, dest, totals, T, k, d,
+                             reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }
 

@@ -5,8 +5,8 @@
 //    share one scale), 1 for an all-zero tensor;
 //  * nv_quant_rows_kernel: a bf16 row-major [rows, K] matrix -> packed E2M1
 //    [rows, K / 2] + scale atoms, blocks of 16 along K;
-//    (also the tokens, X or dY, once per token with tensor scale 1, before
-//    gather_rows_q_kernel copies them into the sorted rows);
+//    (the tokens, X or dY, use tensor scale 1 and are quantised straight
+//    into their sorted rows by quant_scatter_rows_kernel in mx_quant.cu);
 //  * nv_quant_transpose_kernel: a weight's backward orientation, quantised
 //    along its other axis.
 // One thread per 32 elements: 64 input bytes, 16 output bytes, 2 scale bytes.
