@@ -125,7 +125,11 @@ typedef struct moe_plan_s* moe_plan_t;
  * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG; allocation failure MOE_ERR_OOM. */
 moe_status_t moe_plan(const moe_config_t* cfg, moe_plan_t* out);
 
-/* Free the plan's workspace (synchronises its device first). NULL is a no-op. */
+/* Free the plan's workspace (synchronises its device first). NULL is a no-op.
+ * Not while any stream of the device is being captured into a CUDA graph: the
+ * device synchronisation and the frees would invalidate that capture (the
+ * Python binding defers a plan closed or collected during a capture to its
+ * next plan creation or close outside one). */
 moe_status_t moe_plan_destroy(moe_plan_t plan);
 
 /* Bytes of the caller-owned "saved" context a forward of T tokens writes and
@@ -245,9 +249,14 @@ moe_status_t moe_nv_quantize_transposed(const void* src, int64_t E, int64_t A, i
  *        (must be NULL for 2 and 3, whose rows are the gathered inputs);
  *   q    [C, P] E4M3 bytes or [C, P / 2] packed E2M1;
  *   sf   scale atoms of the C rows with K = P.
+ * which = 6: the dispatch's quantised sorted rows of the last call on the
+ * separate-kernel schedule (X after moe_forward, dY after moe_backward;
+ * quantised along d, NVFP4 tensor scale 1, padding rows zero):
+ *   q    [P, d] E4M3 bytes or [P, d / 2] packed E2M1;
+ *   sf   scale atoms of the P rows with K = d;  vals must be NULL.
  * P = moe_plan_padded_rows.  Any pointer may be NULL to skip it.  Synchronous
  * argument errors (MOE_ERR_INVALID_ARG) for a plan without the flag, a BF16
- * plan, another `which`, or vals with which 2 or 3.  Enqueued on `stream`. */
+ * plan, another `which`, or vals with which 2, 3 or 6.  Enqueued on `stream`. */
 moe_status_t moe_debug_quant_dump(moe_plan_t plan, int32_t which, float* vals, void* q, void* sf,
                                   moe_stream_t stream);
 

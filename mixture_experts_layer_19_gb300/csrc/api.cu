@@ -1650,20 +1650,21 @@ moe_status_t moe_debug_quant_dump(moe_plan_t p, int32_t which, float* vals, void
   const moe_config_t& c = p->cfg;
   if (c.prec == MOE_BF16 || !(c.debug_flags & MOE_DEBUG_DUMP_QUANT) || !p->dbg_h)
     return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: needs a block-scaled plan made with MOE_DEBUG_DUMP_QUANT");
-  if (which < 0 || which > 5)
+  if (which < 0 || which > 6)
     return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: which must be 0 (h), 1 (dA|dB), 2 (dY^T), 3 (X^T), "
-                                     "4 ([dA|dB]^T) or 5 ((w h)^T)");
-  if (vals && (which == 2 || which == 3))
-    return fail(MOE_ERR_INVALID_ARG, "moe_debug_quant_dump: dY^T and X^T keep no source values (vals must be NULL)");
+                                     "4 ([dA|dB]^T), 5 ((w h)^T) or 6 (dispatched rows)");
+  if (vals && (which == 2 || which == 3 || which == 6))
+    return fail(MOE_ERR_INVALID_ARG,
+                "moe_debug_quant_dump: dY^T, X^T and the dispatched rows keep no source values (vals must be NULL)");
   DeviceGuard guard(c.device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool nv = c.prec == MOE_NVFP4;
   const size_t P = (size_t)p->Rpm;
-  // which 0, 1: [P, C] quantised along C; 2..5: [C, P] quantised along the P sorted rows
+  // which 0, 1, 6: [P, C] quantised along C; 2..5: [C, P] quantised along the P sorted rows
   const size_t C = (size_t)(which == 0 || which == 5 ? c.F : which == 1 || which == 4 ? 2 * c.F : c.d);
   const size_t n = P * C;
-  const void* qsrc[6] = {p->Hq, p->dABq, p->dYTq, p->XTq, p->dABTq, p->wHTq};
-  const void* ssrc[6] = {p->Hs, p->dABs, p->dYTs, p->XTs, p->dABTs, p->wHTs};
+  const void* qsrc[7] = {p->Hq, p->dABq, p->dYTq, p->XTq, p->dABTq, p->wHTq, p->Xq};
+  const void* ssrc[7] = {p->Hs, p->dABs, p->dYTs, p->XTs, p->dABTs, p->wHTs, p->Xs};
   cudaError_t err = cudaSuccess;
   if (vals) {
     if (which <= 1)

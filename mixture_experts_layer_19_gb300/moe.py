@@ -215,10 +215,31 @@ class Config:
                             self.device, self.ep_ranks)
 
 
+# Plans whose destruction came while the current stream was being captured
+# into a CUDA graph (typically the garbage collector reaching an unreferenced
+# plan inside a capture).  moe_plan_destroy synchronises the device and frees
+# memory, which would invalidate the capture, so these handles are destroyed
+# at the next Plan creation or close made outside a capture.
+_deferred_destroy: list = []
+
+
+def _capturing() -> bool:
+    try:
+        return torch.cuda.is_current_stream_capturing()
+    except Exception:
+        return False
+
+
+def _destroy_deferred() -> None:
+    while _deferred_destroy and not _capturing():
+        lib().moe_plan_destroy(_deferred_destroy.pop())
+
+
 class Plan:
     """One moe_plan_t: owns the device workspace for tokens T <= T_max."""
 
     def __init__(self, cfg: Config):
+        _destroy_deferred()
         self.cfg = cfg
         self._c = cfg.to_c()
         h = ctypes.c_void_p()
@@ -227,9 +248,14 @@ class Plan:
         self.device = torch.device("cuda", cfg.device)
 
     def close(self):
-        if self.handle:
-            lib().moe_plan_destroy(self.handle)
-            self.handle = None
+        h = getattr(self, "handle", None)
+        self.handle = None
+        if h:
+            if _capturing():
+                _deferred_destroy.append(h)
+            else:
+                lib().moe_plan_destroy(h)
+        _destroy_deferred()
 
     def __del__(self):
         try:
@@ -306,13 +332,15 @@ class Plan:
         which 0: h of the last forward, 1: dA|dB of the last backward (both
         [P, C] quantised along C); 2: dY^T, 3: X^T, 4: [dA|dB]^T, 5: (w h)^T of
         the last backward ([C, P] quantised along P; values [P, C] for 4 and 5,
-        None for 2 and 3)."""
+        None for 2 and 3); 6: the dispatch's quantised sorted rows of the last
+        call (X after forward, dY after backward; [P, d] quantised along d,
+        values None)."""
         c = self.cfg
         P = self.padded_rows()
-        C = {0: c.F, 1: 2 * c.F, 2: c.d, 3: c.d, 4: 2 * c.F, 5: c.F}.get(which, c.F)
+        C = {0: c.F, 1: 2 * c.F, 2: c.d, 3: c.d, 4: 2 * c.F, 5: c.F, 6: c.d}.get(which, c.F)
         nv = c.prec == MOE_NVFP4
-        vals = None if which in (2, 3) else torch.empty((P, C), dtype=torch.float32, device=self.device)
-        shape = (P, C) if which in (0, 1) else (C, P)
+        vals = None if which in (2, 3, 6) else torch.empty((P, C), dtype=torch.float32, device=self.device)
+        shape = (P, C) if which in (0, 1, 6) else (C, P)
         q = torch.empty((shape[0], shape[1] // 2 if nv else shape[1]), dtype=torch.uint8, device=self.device)
         sf = torch.empty((P * C // (16 if nv else 32),), dtype=torch.uint8, device=self.device)
         _check(lib().moe_debug_quant_dump(self.handle, which, _ptr(vals), _ptr(q), _ptr(sf), _stream(stream)),

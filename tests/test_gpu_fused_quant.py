@@ -5,7 +5,10 @@ quantise -- h in the forward's up GEMM (along F), dA|dB in the backward's u
 GEMM (along 2F) -- next to the bytes they wrote.  Re-quantising the GPU's own
 fp32 values with the oracle's codec (OCP MX for MXFP8; E2M1 with E4M3 scales
 per 16 and tensor scale 1 for NVFP4) must reproduce every element byte and
-every scale byte, padding rows included.
+every scale byte, padding rows included.  The same holds for the operands
+quantised outside the GEMMs (the dispatch's sorted rows, the weight
+gradients' transposed operands), checked against the oracle's quantisation of
+rows built here from the inputs and the routing.
 """
 import numpy as np
 import pytest
@@ -124,6 +127,46 @@ def test_weight_gradient_operands_bit_exact(prec, case):
         assert np.array_equal(sf.cpu().numpy()[atoms], scales), name
 
 
+@pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("case", [(300, 512, 768, 16, 3, 1.5), (200, 256, 512, 8, 2, 0.0),
+                                  (1, 256, 512, 4, 1, 0.0), (64, 768, 512, 32, 8, 1.1)],
+                         ids=lambda c: "T%d_d%d_F%d_E%d_k%d_a%g" % c)
+def test_dispatched_rows_bit_exact(prec, case):
+    """The dispatch's quantised sorted rows (each token quantised along d once
+    and stored into its k sorted rows): X after the forward, dY after the
+    backward, against the oracle's quantisation of the sorted rows built here
+    from the inputs and the routing.  Every element byte and scale byte of the
+    rows in use, padding rows (zero codes, zero scales) included."""
+    T, d, F, E, k, alpha = case
+    g, h = cpu_and_gpu_inputs(T, d, F, E, k, seed=31, alpha=alpha)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, debug_flags=moe.MOE_DEBUG_DUMP_QUANT))
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    nv = prec == moe.MOE_NVFP4
+    blk = 16 if nv else 32
+    Y, saved = plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    r = plan.routing(saved, T)
+    counts = r["counts"].cpu().numpy()
+    perm = r["perm_src"].cpu().numpy().astype(np.int64)
+    rows = int(sum((c + 127) // 128 * 128 for c in counts))
+    for name in ("X", "dY"):
+        if name == "dY":
+            plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+        vals, q, sf = plan.debug_quant_dump(6)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert vals is None
+        src = _sorted_rows(h[name], perm, counts, k)
+        if nv:
+            codes, scales = nvfp4.nv_quantize(src, axis=1, g=1.0)
+            got = nvfp4.nv_unpack(q[:rows].cpu().numpy())
+        else:
+            codes, scales = mxfp8.mx_quantize(src, axis=1)
+            got = q[:rows].cpu().numpy()
+        bad = np.argwhere(got != codes)
+        assert bad.size == 0, (name, bad[:5].tolist())
+        assert np.array_equal(sf.cpu().numpy()[_atom_offsets(rows, d, blk)], scales), name
+
+
 def test_dump_needs_the_flag():
     plan = moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, prec=moe.MOE_NVFP4))
     with pytest.raises(moe.MoEError) as ei:
@@ -132,12 +175,13 @@ def test_dump_needs_the_flag():
 
 
 def test_dump_rejects_bad_operand_arguments():
-    """which outside 0..5, and source values asked of dY^T or X^T (which keep
-    none), are argument errors that copy nothing."""
+    """which outside 0..6, and source values asked of dY^T, X^T or the
+    dispatched rows (which keep none), are argument errors that copy
+    nothing."""
     plan = moe.Plan(moe.Config(T_max=64, d=256, F=256, E=4, k=2, prec=moe.MOE_MXFP8,
                                debug_flags=moe.MOE_DEBUG_DUMP_QUANT))
     buf = torch.zeros(plan.padded_rows() * 256, dtype=torch.float32, device="cuda")
-    for which, vals in ((6, None), (-1, None), (2, buf), (3, buf)):
+    for which, vals in ((7, None), (-1, None), (2, buf), (3, buf), (6, buf)):
         st = moe.lib().moe_debug_quant_dump(plan.handle, which, moe._ptr(vals), None, None, None)
         assert st == moe.MOE_ERR_INVALID_ARG, which
     assert torch.count_nonzero(buf).item() == 0

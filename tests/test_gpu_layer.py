@@ -1,6 +1,8 @@
 """GPU parity of the fused MoE layer against the fp64 CPU oracle, through
 the C ABI.  Routing, histograms and the permutation are compared bit for
 bit; floating-point outputs within max|err| / max|ref| <= 2e-2 (bf16)."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -246,6 +248,43 @@ def test_forward_replays_from_a_cuda_graph(flags):
         torch.cuda.synchronize()
         assert plan.device_status() == 0
         assert torch.equal(Y, ref)
+
+
+def test_plan_collected_during_a_capture_is_destroyed_afterwards():
+    """The garbage collector may reach an unreferenced plan while a CUDA graph
+    is being captured.  Destroying it then (device synchronise, frees) would
+    invalidate the capture, so the binding defers it: the capture and its
+    replays succeed, and the next plan creation destroys the deferred one."""
+    T, d, F, E, k = 300, 256, 512, 16, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=49, alpha=1.1)
+    plan = _plan(T, d, F, E, k, flags=moe.MOE_DEBUG_RING_MEGAKERNEL)
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+    stream.synchronize()
+    ref = Y.clone()
+    gc.collect()                      # earlier garbage goes outside the capture
+    gc.disable()
+    try:
+        doomed = [_plan(64, 256, 256, 4, 2)]
+        doomed.append(doomed)         # reachable only through a reference cycle
+        del doomed
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            gc.collect()              # the collector runs inside the capture
+            plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+    finally:
+        gc.enable()
+    assert len(moe._deferred_destroy) == 1
+    Y.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert torch.equal(Y, ref)
+    _plan(64, 256, 256, 4, 2).close()
+    assert len(moe._deferred_destroy) == 0
 
 
 def test_ring_config_is_validated():
