@@ -250,6 +250,57 @@ def test_forward_replays_from_a_cuda_graph(flags):
         assert torch.equal(Y, ref)
 
 
+@pytest.mark.parametrize("prec", [moe.MOE_BF16, moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["bf16", "mxfp8", "nvfp4"])
+def test_training_step_with_router_replays_from_a_cuda_graph(prec):
+    """A whole training step of the layer -- router GEMM (split over K), layer
+    forward, layer backward, router backward into dX -- captured once and
+    replayed: every output bitwise equal to the eager step's, for each
+    precision's default schedule."""
+    T, d, F, E, k = 300, 256, 512, 16, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=50, alpha=1.1)
+    gen = torch.Generator().manual_seed(51)
+    Wr = (torch.randn((E, d), generator=gen) / d ** 0.5).to(torch.bfloat16).cuda()
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec))
+    if prec != moe.MOE_BF16:
+        plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    saved = plan.new_saved(T)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    dWr = torch.empty((E, d), dtype=torch.bfloat16, device="cuda")
+    out = {"dX": torch.empty((T, d), dtype=torch.bfloat16, device="cuda"),
+           "dWg": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+           "dWu": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+           "dWd": torch.empty((E, d, F), dtype=torch.bfloat16, device="cuda"),
+           "dg": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+           "dlogits": torch.empty((T, E), dtype=torch.float32, device="cuda")}
+    stream = torch.cuda.Stream()
+
+    def step():
+        plan.router_forward(g["X"], Wr, logits=logits, stream=stream)
+        plan.forward(g["X"], logits, g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+        plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved, out=out, stream=stream)
+        plan.router_backward(g["X"], Wr, out["dlogits"], out["dX"], dWr=dWr, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    assert plan.device_status() == 0
+    bufs = {"logits": logits, "Y": Y, "dWr": dWr, **out}
+    ref = {n: v.clone() for n, v in bufs.items()}
+    assert torch.count_nonzero(ref["dWr"]).item() > 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(2):
+        for v in bufs.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        for n, v in bufs.items():
+            assert torch.equal(v, ref[n]), n
+
+
 def test_plan_collected_during_a_capture_is_destroyed_afterwards():
     """The garbage collector may reach an unreferenced plan while a CUDA graph
     is being captured.  Destroying it then (device synchronise, frees) would
