@@ -283,8 +283,12 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
   if (warp == 0) {
     if (lane == 0) {
       // weight tiles are re-read by every M tile of their expert: evict_last,
-      // as in the bf16 grouped GEMMs
+      // as in the bf16 grouped GEMMs.  MXFP8: an expert with a single M tile
+      // reads its weight tiles once, so they go evict_first and leave L2 to
+      // the re-read activation rows (the four grouped kinds 0.04-0.07 ms
+      // faster per fwd+bwd step at T=8192, E=256; neutral for bf16 and NVFP4).
       const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_once = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
       uint32_t s = 0, ph = 0, issued_mask = 0, last_par = 0;
       bool ok = true;
@@ -292,11 +296,15 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
         const Tile t = decode_tile<KIND>(g, tile);
         int last_mmas;
         const int nkb = mx_tile_nkb<KIND, NV>(g, t, last_mmas);
+        bool once = false;
+        if constexpr (!NV && KindTraits<KIND>::grouped)
+          once = __ldg(g.mtile_off + t.e + 1) - __ldg(g.mtile_off + t.e) == 1;
+        const uint64_t pw = once ? pol_once : pol_w;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kStageBytes + TR::sf_stage);
           uint8_t* sa = stage_base + s * kStageBytes;
-          mx_load_stage<KIND, NV>(g, t, kb, sa, sa + kABytes, sf_base + s * TR::sf_stage, &full[s], pol_w, pol_a);
+          mx_load_stage<KIND, NV>(g, t, kb, sa, sa + kABytes, sf_base + s * TR::sf_stage, &full[s], pw, pol_a);
           issued_mask |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
           if (++s == S) { s = 0; ph ^= 1; }
