@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(MxTraits<KIND, NV>::threads, 1) gemm_mx_kernel
       // as in the bf16 grouped GEMMs.  MXFP8: an expert with a single M tile
       // reads its weight tiles once, so they go evict_first and leave L2 to
       // the re-read activation rows (the four grouped kinds 0.04-0.07 ms
-      // faster per fwd+bwd step at T=8192, E=256; neutral for bf16 and NVFP4).
+      // faster per fwd+bwd step at T=8192, E=256; neutral for bf16, and the
+      // NVFP4 u kind got slower).
       const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_once = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
