@@ -86,3 +86,46 @@ def test_product_path_has_no_cpu_fallback():
         moe.load_library("/nonexistent/libmoe.so")
     src = open(os.path.join(ROOT, "mixture_experts_layer_19_gb300", "moe.py"), encoding="utf-8").read()
     assert "oracle" not in src.replace("no fallback", "")
+
+
+class _FakeLib:
+    """Stands in for libmoe.so: records which plan handles were destroyed."""
+
+    def __init__(self):
+        self.destroyed = []
+
+    def moe_plan_destroy(self, handle):
+        self.destroyed.append(handle)
+        return 0
+
+
+def test_plan_destroyed_during_a_capture_is_deferred(monkeypatch):
+    """Host logic of the binding: a plan closed (or collected) while the
+    current stream is being captured is queued, not destroyed -- destroying
+    synchronises the device and would invalidate the capture -- and the queue
+    is emptied by the next close made outside a capture, oldest or newest
+    alike, each handle exactly once."""
+    from mixture_experts_layer_19_gb300 import moe
+    fake = _FakeLib()
+    monkeypatch.setattr(moe, "lib", lambda: fake)
+    monkeypatch.setattr(moe, "_deferred_destroy", [])
+    capturing = {"on": True}
+    monkeypatch.setattr(moe, "_capturing", lambda: capturing["on"])
+
+    def plan_with(handle):
+        p = object.__new__(moe.Plan)     # no device: only the handle matters here
+        p.handle = handle
+        return p
+
+    a, b, c = plan_with(11), plan_with(12), plan_with(13)
+    a.close()
+    b.__del__()                          # what the garbage collector calls
+    assert fake.destroyed == [] and sorted(moe._deferred_destroy) == [11, 12]
+    assert a.handle is None and b.handle is None
+    a.close()                            # closing twice queues nothing more
+    assert sorted(moe._deferred_destroy) == [11, 12]
+    capturing["on"] = False
+    c.close()
+    assert sorted(fake.destroyed) == [11, 12, 13] and moe._deferred_destroy == []
+    c.close()
+    assert sorted(fake.destroyed) == [11, 12, 13]
