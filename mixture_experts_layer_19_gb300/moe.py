@@ -114,8 +114,22 @@ def _check(status: int, where: str):
 def _ptr(t: Optional[torch.Tensor]):
     if t is None:
         return None
-    assert t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors"
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError("tensors must be contiguous CUDA tensors")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _expect(t: Optional[torch.Tensor], name: str, shape, dtype, optional: bool = False) -> None:
+    """The C ABI takes untyped pointers, so the binding checks what the header
+    fixes for each tensor (dtype, shape) before passing it on."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
 def _stream(stream: Optional[torch.cuda.Stream] = None):
@@ -271,8 +285,19 @@ class Plan:
     def new_saved(self, T: int) -> torch.Tensor:
         return torch.empty(self.saved_bytes(T), dtype=torch.uint8, device=self.device)
 
+    def _expect_weights(self, Wg, Wu, Wd):
+        c = self.cfg
+        optional = bool(c.debug_flags & MOE_DEBUG_IDENTITY_EXPERTS)
+        _expect(Wg, "Wg", (c.E, c.F, c.d), torch.bfloat16, optional)
+        _expect(Wu, "Wu", (c.E, c.F, c.d), torch.bfloat16, optional)
+        _expect(Wd, "Wd", (c.E, c.d, c.F), torch.bfloat16, optional)
+
     def forward(self, X, logits, Wg, Wu, Wd, Y=None, saved=None, stream=None):
-        T = X.shape[0]
+        T, c = X.shape[0], self.cfg
+        _expect(X, "X", (T, c.d), torch.bfloat16)
+        _expect(logits, "logits", (T, c.E), torch.float32)
+        self._expect_weights(Wg, Wu, Wd)
+        _expect(Y, "Y", (T, c.d), torch.bfloat16, optional=True)
         if Y is None:
             Y = torch.empty((T, self.cfg.d), dtype=torch.bfloat16, device=self.device)
         if saved is None:
@@ -284,6 +309,15 @@ class Plan:
     def backward(self, dY, X, Wg, Wu, Wd, saved, out=None, want_dlogits=True, stream=None):
         T, c = X.shape[0], self.cfg
         dev = self.device
+        _expect(X, "X", (T, c.d), torch.bfloat16)
+        _expect(dY, "dY", (T, c.d), torch.bfloat16)
+        self._expect_weights(Wg, Wu, Wd)
+        if out is not None:
+            for name, shape, dtype in (("dX", (T, c.d), torch.bfloat16), ("dWg", (c.E, c.F, c.d), torch.bfloat16),
+                                       ("dWu", (c.E, c.F, c.d), torch.bfloat16),
+                                       ("dWd", (c.E, c.d, c.F), torch.bfloat16), ("dg", (T, c.k), torch.float32)):
+                _expect(out.get(name), f"out[{name!r}]", shape, dtype)
+            _expect(out.get("dlogits"), "out['dlogits']", (T, c.E), torch.float32, optional=True)
         if out is None:
             out = {
                 "dX": torch.empty((T, c.d), dtype=torch.bfloat16, device=dev),
@@ -317,6 +351,7 @@ class Plan:
 
     def quantize_weights(self, Wg, Wu, Wd, stream=None):
         """MXFP8 / NVFP4 plans: fill the plan's quantised weight copies (once per weight update)."""
+        self._expect_weights(Wg, Wu, Wd)
         _check(lib().moe_quantize_weights(self.handle, _ptr(Wg), _ptr(Wu), _ptr(Wd), _stream(stream)),
                "moe_quantize_weights")
 
@@ -369,7 +404,10 @@ class Plan:
 
     def router_forward(self, X, Wr, logits=None, stream=None):
         """logits = X Wr^T (fp32) on the tensor cores."""
-        T = X.shape[0]
+        T, c = X.shape[0], self.cfg
+        _expect(X, "X", (T, c.d), torch.bfloat16)
+        _expect(Wr, "Wr", (c.E, c.d), torch.bfloat16)
+        _expect(logits, "logits", (T, c.E), torch.float32, optional=True)
         if logits is None:
             logits = torch.empty((T, self.cfg.E), dtype=torch.float32, device=self.device)
         _check(lib().moe_router_forward(self.handle, T, _ptr(X), _ptr(Wr), _ptr(logits), _stream(stream)),
@@ -378,6 +416,12 @@ class Plan:
 
     def router_backward(self, X, Wr, dlogits, dX, dWr=None, stream=None):
         """dX += dlogits Wr (in place); returns dWr = dlogits^T X."""
+        T, c = X.shape[0], self.cfg
+        _expect(X, "X", (T, c.d), torch.bfloat16)
+        _expect(Wr, "Wr", (c.E, c.d), torch.bfloat16)
+        _expect(dlogits, "dlogits", (T, c.E), torch.float32)
+        _expect(dX, "dX", (T, c.d), torch.bfloat16)
+        _expect(dWr, "dWr", (c.E, c.d), torch.bfloat16, optional=True)
         if dWr is None:
             dWr = torch.empty((self.cfg.E, self.cfg.d), dtype=torch.bfloat16, device=self.device)
         _check(lib().moe_router_backward(self.handle, X.shape[0], _ptr(X), _ptr(Wr), _ptr(dlogits), _ptr(dX),

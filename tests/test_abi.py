@@ -129,3 +129,41 @@ def test_plan_destroyed_during_a_capture_is_deferred(monkeypatch):
     assert sorted(fake.destroyed) == [11, 12, 13] and moe._deferred_destroy == []
     c.close()
     assert sorted(fake.destroyed) == [11, 12, 13]
+
+
+def test_binding_rejects_wrong_dtypes_and_shapes_before_the_abi(monkeypatch):
+    """The C ABI takes untyped pointers, so the binding checks each tensor's
+    dtype and shape against the plan's config and raises ValueError before
+    any library call (CPU tensors suffice: the checks come first)."""
+    import torch
+    from mixture_experts_layer_19_gb300 import moe
+
+    class NoCalls:
+        def __getattr__(self, name):
+            raise AssertionError(f"library called: {name}")
+
+    monkeypatch.setattr(moe, "lib", lambda: NoCalls())
+    plan = object.__new__(moe.Plan)
+    plan.cfg = moe.Config(T_max=8, d=256, F=512, E=4, k=2)
+    plan.handle = None
+    plan.device = torch.device("cpu")
+    T, d, F, E = 8, 256, 512, 4
+    X = torch.zeros((T, d), dtype=torch.bfloat16)
+    L = torch.zeros((T, E), dtype=torch.float32)
+    W = torch.zeros((E, F, d), dtype=torch.bfloat16)
+    Wd = torch.zeros((E, d, F), dtype=torch.bfloat16)
+    cases = [
+        lambda: plan.forward(X.float(), L, W, W, Wd),                 # X must be bf16
+        lambda: plan.forward(X, L.to(torch.bfloat16), W, W, Wd),      # logits must be fp32
+        lambda: plan.forward(X, L[:, :3], W, W, Wd),                  # logits [T, E]
+        lambda: plan.forward(X, L, Wd, W, Wd),                        # Wg is [E, F, d], not [E, d, F]
+        lambda: plan.forward(X, L, W, W, W[:, :, :128]),              # Wd [E, d, F]
+        lambda: plan.forward(X, L, None, W, Wd),                      # weights required
+        lambda: plan.backward(X[:4], X, W, W, Wd, None),              # dY rows = X rows
+        lambda: plan.router_forward(X, torch.zeros((E + 1, d), dtype=torch.bfloat16)),
+        lambda: plan.router_backward(X, torch.zeros((E, d), dtype=torch.bfloat16), L, X.float()),
+        lambda: plan.quantize_weights(W, W.float(), Wd),
+    ]
+    for call in cases:
+        with pytest.raises(ValueError):
+            call()
