@@ -292,6 +292,17 @@ class Plan:
         _expect(Wu, "Wu", (c.E, c.F, c.d), torch.bfloat16, optional)
         _expect(Wd, "Wd", (c.E, c.d, c.F), torch.bfloat16, optional)
 
+    def _expect_saved(self, saved, T: int):
+        """The saved context is written (forward) and read (backward) through an
+        untyped pointer: it must hold moe_saved_bytes(T) bytes."""
+        if saved is None:
+            raise ValueError("saved is required")
+        if saved.dtype != torch.uint8:
+            raise ValueError(f"saved: dtype {saved.dtype}, expected torch.uint8 (from new_saved)")
+        need = self.saved_bytes(T)
+        if saved.numel() < need:
+            raise ValueError(f"saved: {saved.numel()} bytes, the context of T={T} needs {need}")
+
     def forward(self, X, logits, Wg, Wu, Wd, Y=None, saved=None, stream=None):
         T, c = X.shape[0], self.cfg
         _expect(X, "X", (T, c.d), torch.bfloat16)
@@ -302,6 +313,8 @@ class Plan:
             Y = torch.empty((T, self.cfg.d), dtype=torch.bfloat16, device=self.device)
         if saved is None:
             saved = self.new_saved(T)
+        else:
+            self._expect_saved(saved, T)
         _check(lib().moe_forward(self.handle, T, _ptr(X), _ptr(logits), _ptr(Wg), _ptr(Wu), _ptr(Wd),
                                  _ptr(Y), _ptr(saved), _stream(stream)), "moe_forward")
         return Y, saved
@@ -318,6 +331,7 @@ class Plan:
                                        ("dWd", (c.E, c.d, c.F), torch.bfloat16), ("dg", (T, c.k), torch.float32)):
                 _expect(out.get(name), f"out[{name!r}]", shape, dtype)
             _expect(out.get("dlogits"), "out['dlogits']", (T, c.E), torch.float32, optional=True)
+        self._expect_saved(saved, T)
         if out is None:
             out = {
                 "dX": torch.empty((T, c.d), dtype=torch.bfloat16, device=dev),
@@ -335,6 +349,7 @@ class Plan:
 
     def routing(self, saved, T, stream=None):
         c, dev = self.cfg, self.device
+        self._expect_saved(saved, T)
         R = T * c.k
         out = {
             "idx": torch.empty((T, c.k), dtype=torch.int32, device=dev),

@@ -160,6 +160,8 @@ def test_binding_rejects_wrong_dtypes_and_shapes_before_the_abi(monkeypatch):
         lambda: plan.forward(X, L, W, W, W[:, :, :128]),              # Wd [E, d, F]
         lambda: plan.forward(X, L, None, W, Wd),                      # weights required
         lambda: plan.backward(X[:4], X, W, W, Wd, None),              # dY rows = X rows
+        lambda: plan.backward(X, X, W, W, Wd, None),                  # the saved context is required
+        lambda: plan.backward(X, X, W, W, Wd, torch.zeros(16)),       # saved is bytes (new_saved)
         lambda: plan.router_forward(X, torch.zeros((E + 1, d), dtype=torch.bfloat16)),
         lambda: plan.router_backward(X, torch.zeros((E, d), dtype=torch.bfloat16), L, X.float()),
         lambda: plan.quantize_weights(W, W.float(), Wd),

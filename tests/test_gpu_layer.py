@@ -372,6 +372,9 @@ def test_argument_errors_are_synchronous():
     Xmis = bad[: g["X"].numel()].view(T, d)
     with pytest.raises(moe.MoEError):
         plan.forward(Xmis, g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    small = torch.empty(plan.saved_bytes(T) - 1, dtype=torch.uint8, device=g["X"].device)
+    with pytest.raises(ValueError):   # a context too small for T is refused before any launch
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], saved=small)
     assert plan.device_status() == 0
 
 
