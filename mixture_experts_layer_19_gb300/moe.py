@@ -456,7 +456,8 @@ class Plan:
 class _MoEFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, plan: Plan, X, logits, Wg, Wu, Wd):
-        Y, saved = plan.forward(X.contiguous(), logits.contiguous(), Wg, Wu, Wd)
+        X = X.contiguous()
+        Y, saved = plan.forward(X, logits.contiguous(), Wg, Wu, Wd)
         ctx.plan = plan
         ctx.save_for_backward(X, Wg, Wu, Wd, saved)
         return Y
@@ -490,27 +491,45 @@ class _RoutedMoEFunction(torch.autograd.Function):
 
 
 class MoELayer(torch.nn.Module):
-    """Fused MoE layer over bf16 expert weights; router logits are an input."""
+    """Fused MoE layer over bf16 expert weights; router logits are an input.
 
-    def __init__(self, d: int, F: int, E: int, k: int, T_max: int, device=0, debug_flags: int = 0):
+    prec = MOE_BF16, MOE_MXFP8 or MOE_NVFP4.  A block-scaled layer quantises
+    its weights again whenever they changed since the last quantisation (an
+    optimiser step, a copy_ or a load_state_dict bumps the parameters'
+    version counters), before the forward that first sees the change."""
+
+    def __init__(self, d: int, F: int, E: int, k: int, T_max: int, device=0, debug_flags: int = 0,
+                 prec: int = MOE_BF16):
         super().__init__()
         dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
-        self.plan = Plan(Config(T_max=T_max, d=d, F=F, E=E, k=k, device=dev.index or 0,
+        self.plan = Plan(Config(T_max=T_max, d=d, F=F, E=E, k=k, prec=prec, device=dev.index or 0,
                                 debug_flags=debug_flags))
         self.Wg = torch.nn.Parameter(torch.empty((E, F, d), dtype=torch.bfloat16, device=dev))
         self.Wu = torch.nn.Parameter(torch.empty((E, F, d), dtype=torch.bfloat16, device=dev))
         self.Wd = torch.nn.Parameter(torch.empty((E, d, F), dtype=torch.bfloat16, device=dev))
+        self._quantized_key = None
+
+    def _sync_quantized_weights(self):
+        if self.plan.cfg.prec == MOE_BF16:
+            return
+        key = tuple((w.data_ptr(), w._version) for w in (self.Wg, self.Wu, self.Wd))
+        if key != self._quantized_key:
+            self.plan.quantize_weights(self.Wg.detach(), self.Wu.detach(), self.Wd.detach())
+            self._quantized_key = key
 
     def forward(self, X, logits):
+        self._sync_quantized_weights()
         return _MoEFunction.apply(self.plan, X, logits, self.Wg, self.Wu, self.Wd)
 
 
 class RoutedMoELayer(MoELayer):
     """Fused MoE layer with its router: logits = X Wr^T (bf16 Wr [E, d])."""
 
-    def __init__(self, d: int, F: int, E: int, k: int, T_max: int, device=0, debug_flags: int = 0):
-        super().__init__(d, F, E, k, T_max, device=device, debug_flags=debug_flags)
+    def __init__(self, d: int, F: int, E: int, k: int, T_max: int, device=0, debug_flags: int = 0,
+                 prec: int = MOE_BF16):
+        super().__init__(d, F, E, k, T_max, device=device, debug_flags=debug_flags, prec=prec)
         self.Wr = torch.nn.Parameter(torch.empty((E, d), dtype=torch.bfloat16, device=self.Wg.device))
 
     def forward(self, X):
+        self._sync_quantized_weights()
         return _RoutedMoEFunction.apply(self.plan, X, self.Wr, self.Wg, self.Wu, self.Wd)

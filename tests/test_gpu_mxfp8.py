@@ -189,3 +189,35 @@ def test_mx_quantize_transposed_bit_exact(E, A, B):
     codes, scales = mxfp8.mx_quantize(T, axis=1)
     assert np.array_equal(q.cpu().numpy().reshape(E * B, A), codes)
     assert np.array_equal(sf.cpu().numpy()[_atom_offsets(E * B, A)], scales)
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_MXFP8, moe.MOE_NVFP4], ids=["mxfp8", "nvfp4"])
+def test_block_scaled_module_requantises_after_an_update(prec):
+    """MoELayer(prec=...) quantises its weights before its first forward and
+    again after an in-place update (what an optimiser step does): each forward
+    equals, bitwise, a plan given the current weights' quantisation."""
+    T, d, F, E, k = 128, 256, 512, 8, 2
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=61, alpha=1.1)
+    layer = moe.MoELayer(d, F, E, k, T_max=T, prec=prec)
+    with torch.no_grad():
+        for n in ("Wg", "Wu", "Wd"):
+            getattr(layer, n).copy_(g[n])
+    ref = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec))
+
+    def expected():
+        W = [getattr(layer, n).detach() for n in ("Wg", "Wu", "Wd")]
+        ref.quantize_weights(*W)
+        Y, _ = ref.forward(g["X"], g["logits"], *W)
+        return Y
+
+    X = g["X"].clone().requires_grad_(True)
+    Y1 = layer(X, g["logits"])
+    assert torch.equal(Y1, expected())
+    Y1.backward(g["dY"])
+    assert X.grad is not None and all(getattr(layer, n).grad is not None for n in ("Wg", "Wu", "Wd"))
+    torch.optim.SGD(layer.parameters(), lr=0.5).step()   # in-place: the layer must quantise again
+    Y2 = layer(g["X"], g["logits"])
+    assert not torch.equal(Y2, Y1)
+    assert torch.equal(Y2, expected())
+    torch.cuda.synchronize()
+    assert layer.plan.device_status() == 0 and ref.device_status() == 0
