@@ -508,6 +508,17 @@ class MoELayer(torch.nn.Module):
         self.Wu = torch.nn.Parameter(torch.empty((E, F, d), dtype=torch.bfloat16, device=dev))
         self.Wd = torch.nn.Parameter(torch.empty((E, d, F), dtype=torch.bfloat16, device=dev))
         self._quantized_key = None
+        self.reset_parameters()
+
+    def reset_parameters(self):
+        """Each weight ~ N(0, 1/fan_in): fan_in = d for Wg, Wu (and Wr), F for Wd."""
+        c = self.plan.cfg
+        with torch.no_grad():
+            self.Wg.normal_(0.0, c.d ** -0.5)
+            self.Wu.normal_(0.0, c.d ** -0.5)
+            self.Wd.normal_(0.0, c.F ** -0.5)
+            if hasattr(self, "Wr"):
+                self.Wr.normal_(0.0, c.d ** -0.5)
 
     def _sync_quantized_weights(self):
         if self.plan.cfg.prec == MOE_BF16:
@@ -529,6 +540,7 @@ class RoutedMoELayer(MoELayer):
                  prec: int = MOE_BF16):
         super().__init__(d, F, E, k, T_max, device=device, debug_flags=debug_flags, prec=prec)
         self.Wr = torch.nn.Parameter(torch.empty((E, d), dtype=torch.bfloat16, device=self.Wg.device))
+        self.reset_parameters()
 
     def forward(self, X):
         self._sync_quantized_weights()

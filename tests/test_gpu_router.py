@@ -124,3 +124,21 @@ def test_router_edge_cases():
     with pytest.raises(moe.MoEError) as ei:
         odd.router_forward(g["X"], torch.zeros((12, d), dtype=torch.bfloat16, device="cuda"))
     assert ei.value.status == 2
+
+
+def test_routed_layer_initialises_its_weights():
+    """A freshly built layer holds N(0, 1/fan_in) weights (fan_in = d for Wr,
+    Wg, Wu and F for Wd), not uninitialised memory, and runs a step."""
+    T, d, F, E, k = 64, 256, 512, 8, 2
+    layer = moe.RoutedMoELayer(d, F, E, k, T_max=T)
+    for n, fan_in in (("Wr", d), ("Wg", d), ("Wu", d), ("Wd", F)):
+        w = getattr(layer, n).detach().float()
+        assert torch.isfinite(w).all(), n
+        assert abs(w.std().item() * fan_in ** 0.5 - 1.0) < 0.1, n
+        assert abs(w.mean().item()) < 0.1 * fan_in ** -0.5, n
+    X = torch.randn((T, d), device="cuda").to(torch.bfloat16).requires_grad_(True)
+    Y = layer(X)
+    Y.float().sum().backward()
+    torch.cuda.synchronize()
+    assert torch.isfinite(Y.float()).all() and torch.isfinite(X.grad.float()).all()
+    assert layer.plan.device_status() == 0
