@@ -465,7 +465,8 @@ class _MoEFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dY):
         X, Wg, Wu, Wd, saved = ctx.saved_tensors
-        g = ctx.plan.backward(dY.contiguous(), X, Wg, Wu, Wd, saved, want_dlogits=True)
+        want_dlogits = ctx.needs_input_grad[2]   # no dlogits kernel work when logits need no gradient
+        g = ctx.plan.backward(dY.contiguous(), X, Wg, Wu, Wd, saved, want_dlogits=want_dlogits)
         return None, g["dX"], g["dlogits"], g["dWg"], g["dWu"], g["dWd"]
 
 

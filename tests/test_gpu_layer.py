@@ -568,3 +568,33 @@ def test_ring_forward_and_backward_replay_from_a_cuda_graph():
         assert torch.equal(Y, ref["Y"])
         for n, v in out.items():
             assert torch.equal(v, ref[n]), n
+
+
+def test_module_autograd_matches_the_plan_calls():
+    """MoELayer through autograd gives, bitwise, the gradients of the plan's
+    own forward + backward -- dlogits included when the logits require a
+    gradient, and not computed (None) when they do not."""
+    T, d, F, E, k = 200, 256, 512, 8, 2
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=52, alpha=1.1)
+    layer = moe.MoELayer(d, F, E, k, T_max=T)
+    with torch.no_grad():
+        for n in ("Wg", "Wu", "Wd"):
+            getattr(layer, n).copy_(g[n])
+    Y, saved = layer.plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"])
+    ref = layer.plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved)
+    for logits_grad in (True, False):
+        layer.zero_grad(set_to_none=True)
+        X = g["X"].clone().requires_grad_(True)
+        L = g["logits"].clone().requires_grad_(logits_grad)
+        Ym = layer(X, L)
+        Ym.backward(g["dY"])
+        torch.cuda.synchronize()
+        assert torch.equal(Ym, Y)
+        assert torch.equal(X.grad, ref["dX"])
+        for n in ("Wg", "Wu", "Wd"):
+            assert torch.equal(getattr(layer, n).grad, ref["d" + n]), n
+        if logits_grad:
+            assert torch.equal(L.grad, ref["dlogits"])
+        else:
+            assert L.grad is None
+    assert layer.plan.device_status() == 0
