@@ -221,3 +221,32 @@ def test_block_scaled_module_requantises_after_an_update(prec):
     assert torch.equal(Y2, expected())
     torch.cuda.synchronize()
     assert layer.plan.device_status() == 0 and ref.device_status() == 0
+
+
+def test_mxfp8_one_launch_ring_forward_replays_from_a_cuda_graph():
+    """The MXFP8 one-launch forward (token quantisation, routing, layout, ring
+    pipeline and combine in one cooperative kernel) captured once and
+    replayed: its grid barriers and hand-off counters reset themselves, so
+    every replay equals the eager forward bitwise."""
+    T, d, F, E, k = 300, 256, 512, 16, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=62, alpha=1.1)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=moe.MOE_MXFP8,
+                               debug_flags=moe.MOE_DEBUG_RING_MEGAKERNEL))
+    plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+    stream.synchronize()
+    assert plan.device_status() == 0
+    ref = Y.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+    for _ in range(3):
+        Y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert torch.equal(Y, ref)
