@@ -8,7 +8,7 @@ routing, Y, dX, dW, dg, dlogits -- must therefore match it bit for bit, for
 several rank counts, ragged token counts (ranks without tokens), and repeated
 calls (the flags reset themselves).  Block-scaled plans (MXFP8, NVFP4) run
 the same exchanges on bf16 rows and quantise the pulled rows along d, which
-gives the bytes of the single-GPU path's once-per-token quantisation, so they
+gives the bytes of the single-GPU path's dispatch quantisation, so they
 too match their single-GPU path bit for bit."""
 import numpy as np
 import pytest
@@ -88,3 +88,46 @@ def test_virtual_rank_ep_config_is_validated():
         moe.Plan(moe.Config(T_max=64, d=256, F=256, E=8, k=2, ep_ranks=2,
                             debug_flags=moe.MOE_DEBUG_IDENTITY_EXPERTS))
     assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("prec", [moe.MOE_BF16, moe.MOE_MXFP8], ids=["bf16", "mxfp8"])
+def test_virtual_rank_ep_step_replays_from_a_cuda_graph(prec):
+    """A virtual-rank EP forward + backward captured once and replayed: the
+    exchange flags reset at the end of every launch, so each replay equals
+    the eager step bitwise."""
+    T, d, F, E, k, R = 300, 256, 512, 16, 4, 4
+    g, _ = cpu_and_gpu_inputs(T, d, F, E, k, seed=63, alpha=1.1)
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, prec=prec, ep_ranks=R))
+    if prec != moe.MOE_BF16:
+        plan.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    saved = plan.new_saved(T)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    out = {"dX": torch.empty((T, d), dtype=torch.bfloat16, device="cuda"),
+           "dWg": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+           "dWu": torch.empty((E, F, d), dtype=torch.bfloat16, device="cuda"),
+           "dWd": torch.empty((E, d, F), dtype=torch.bfloat16, device="cuda"),
+           "dg": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+           "dlogits": torch.empty((T, E), dtype=torch.float32, device="cuda")}
+    stream = torch.cuda.Stream()
+
+    def step():
+        plan.forward(g["X"], g["logits"], g["Wg"], g["Wu"], g["Wd"], Y=Y, saved=saved, stream=stream)
+        plan.backward(g["dY"], g["X"], g["Wg"], g["Wu"], g["Wd"], saved, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    assert plan.device_status() == 0
+    bufs = {"Y": Y, **out}
+    ref = {n: v.clone() for n, v in bufs.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(2):
+        for v in bufs.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        for n, v in bufs.items():
+            assert torch.equal(v, ref[n]), n
