@@ -143,7 +143,14 @@ moe_status_t moe_saved_bytes(moe_plan_t plan, int64_t T, size_t* bytes);
  *   Wg, Wu [E, F, d] bf16, Wd [E, d, F] bf16
  *   Y      [T, d] bf16      output (written)
  *   saved  moe_saved_bytes(T) bytes, written; pass it unchanged to moe_backward.
- * Enqueued on `stream`; bitwise deterministic for identical inputs. */
+ * Enqueued on `stream`; bitwise deterministic for identical inputs.
+ * Errors, synchronous with nothing enqueued: MOE_ERR_INVALID_ARG for a null
+ * plan or tensor pointer (the weights may be NULL only with
+ * MOE_DEBUG_IDENTITY_EXPERTS), a tensor not 16-byte aligned, `saved` not
+ * 256-byte aligned, T outside [0, T_max], or a block-scaled plan whose
+ * weights were never quantised; MOE_ERR_CUDA when a launch fails.  The
+ * sizes of X, Y and `saved` cannot be checked through these pointers: a
+ * buffer smaller than stated is overrun. */
 moe_status_t moe_forward(moe_plan_t plan, int64_t T, const void* X, const float* logits,
                          const void* Wg, const void* Wu, const void* Wd, void* Y,
                          void* saved, moe_stream_t stream);
@@ -155,7 +162,7 @@ moe_status_t moe_forward(moe_plan_t plan, int64_t T, const void* X, const float*
  *   dg      [T, k] fp32  gradient of the gate weights w (written)
  *   dlogits [T, E] fp32  gradient of the router logits, or NULL to skip
  * Enqueued on `stream`; every reduction runs in a fixed order: bitwise
- * deterministic. */
+ * deterministic.  Errors as for moe_forward (dlogits may be NULL). */
 moe_status_t moe_backward(moe_plan_t plan, int64_t T, const void* dY, const void* X,
                           const void* Wg, const void* Wu, const void* Wd, const void* saved,
                           void* dX, void* dWg, void* dWu, void* dWd, float* dg, float* dlogits,
