@@ -436,6 +436,9 @@ def bench_gpu(args):
         "clocks": clk,
         "e2e": e2e,
     }
+    ref = {"Y": Y.clone(), **{n: v.clone() for n, v in grads.items()}}
+    out["graph_replay"] = bench_graph(args, inp, ref, dev, ws)
+    del ref
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, k, args.cpu_tokens)
     if not args.no_ring:
@@ -511,6 +514,55 @@ def bench_ep(args, plan_one, inp, Y, saved, grads, stream, dev, ws, ranks=8):
            "value": round(ws * inp.X.shape[0] / (ms / 1e3), 1), "unit": "tokens/s",
            "exchange_ms": {n: round(v[0] / steps, 4) for n, v in kt.items() if n.startswith("ep_")}}
     del plan
+    return res
+
+
+def bench_graph(args, inp, ref, dev, ws):
+    """The same fwd+bwd step captured once as a CUDA graph and replayed (a plan
+    without per-kernel timing events, so the graph holds only the layer's
+    kernels); the replayed outputs must equal the eager step's bitwise."""
+    from mixture_experts_layer_19_gb300 import moe
+    T, d = inp.X.shape
+    E, F = inp.Wg.shape[0], inp.Wg.shape[1]
+    k = ref["dg"].shape[1]
+    plan = moe.Plan(moe.Config(T_max=T, d=d, F=F, E=E, k=k, device=dev.index or 0))
+    saved = plan.new_saved(T)
+    Y = torch.empty_like(ref["Y"])
+    grads = {n: torch.empty_like(ref[n]) for n in ("dX", "dWg", "dWu", "dWd", "dg", "dlogits")}
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        plan.forward(inp.X, inp.logits, inp.Wg, inp.Wu, inp.Wd, Y=Y, saved=saved, stream=stream)
+        plan.backward(inp.dY, inp.X, inp.Wg, inp.Wu, inp.Wd, saved, out=grads, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status set during the graph replays")
+    same = torch.equal(Y, ref["Y"]) and all(torch.equal(grads[n], ref[n]) for n in grads)
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+    res = {"ms_per_step": round(elapsed_ms / args.steps, 4),
+           "value": round(ws * T * args.steps / (elapsed_ms / 1e3), 1), "unit": "tokens/s",
+           "bitwise_equal_to_eager": bool(same),
+           "note": "one fwd+bwd step captured once as a CUDA graph (no per-kernel timing events) and replayed"}
+    del graph, plan, saved, Y, grads
+    torch.cuda.empty_cache()
     return res
 
 
