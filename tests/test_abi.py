@@ -37,7 +37,9 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_minibatch_floor_matches_pages(lib):
-    for line in open(GOLDEN_FLOOR, encoding="utf-8"):
+    with open(GOLDEN_FLOOR, encoding="utf-8") as fh:
+        golden_lines = fh.read().splitlines(keepends=True)
+    for line in golden_lines:
         if line.startswith("#") or not line.strip():
             continue
         hidden, ffn, waves, sms, tm, tn, expect = map(int, line.split())

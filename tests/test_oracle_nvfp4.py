@@ -20,7 +20,9 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "nvfp4_spec_examples.
 
 def _golden_cases():
     cases = []
-    for line in open(GOLDEN, encoding="utf-8"):
+    with open(GOLDEN, encoding="utf-8") as fh:
+        golden_lines = fh.read().splitlines(keepends=True)
+    for line in golden_lines:
         if line.startswith("#") or not line.strip():
             continue
         name, g, vals, scale, elems = [f.strip() for f in line.split("|")]

@@ -105,7 +105,9 @@ def test_layout_degenerate_cases():
 
 
 def test_minibatch_floor_golden():
-    for line in open(GOLDEN_FLOOR, encoding="utf-8"):
+    with open(GOLDEN_FLOOR, encoding="utf-8") as fh:
+        golden_lines = fh.read().splitlines(keepends=True)
+    for line in golden_lines:
         if line.startswith("#") or not line.strip():
             continue
         hidden, ffn, waves, sms, tm, tn, expect = map(int, line.split())
