@@ -271,6 +271,13 @@ class Plan:
                 lib().moe_plan_destroy(h)
         _destroy_deferred()
 
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
+
     def __del__(self):
         try:
             self.close()

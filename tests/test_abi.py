@@ -131,6 +131,9 @@ def test_plan_destroyed_during_a_capture_is_deferred(monkeypatch):
     assert sorted(fake.destroyed) == [11, 12, 13] and moe._deferred_destroy == []
     c.close()
     assert sorted(fake.destroyed) == [11, 12, 13]
+    with plan_with(14) as d:             # a plan used as a context manager is closed on exit
+        assert d.handle == 14
+    assert d.handle is None and sorted(fake.destroyed) == [11, 12, 13, 14]
 
 
 def test_binding_rejects_wrong_dtypes_and_shapes_before_the_abi(monkeypatch):
